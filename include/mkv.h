@@ -1,0 +1,202 @@
+/*
+ * mkv.h -- C ABI of the GB300 library for decode attention over a KV cache
+ * compressed along both the sequence and the channel dimension.
+ *
+ * Method: "MosaicKV: Serving Long-Context LLM with Dynamic Two-D KV Cache
+ * Compression" (arXiv 2607.00760), §1 Introduction:
+ *   - "Observation & Method 1" (dynamic two-D compression): KV vectors are
+ *     rotated into an SVD basis, important elements are picked per vector, and
+ *     every fixed-size segment of the cache gets its own compression strategy.
+ *   - "Observation & Method 2" (compressed KV cache management): the sparse KV
+ *     matrix is packed into a dense format in GPU memory and attention runs on
+ *     it, without unpacking, on CUDA cores.
+ *   - prior-work paragraph: query-aware token selection (as in Quest) and a
+ *     shared channel mask (as in ThinK).
+ * The paper gives no interface; these calls follow its problem statement:
+ * compress a prefill cache per KV head, then attend over it at every decode
+ * step.
+ *
+ * Conventions for every call:
+ *   - Pointers named "device" must point to memory of the ctx's CUDA device.
+ *     Host pointers are plain host memory.  No call takes ownership of a
+ *     caller pointer; inputs are read and outputs written in stream order on
+ *     the given stream (they must stay valid until that work has run).
+ *   - Every call returns an mkv_status.  On MKV_ERR_INVALID_ARG and
+ *     MKV_ERR_OOM the ctx is left exactly as it was.  MKV_ERR_CUDA means a
+ *     CUDA runtime call failed (the CUDA error is printed by
+ *     mkv_last_error_string()).
+ *   - A ctx is not thread-safe: calls on one ctx must not overlap.
+ *   - No call allocates or frees memory other than what the ctx owns.
+ *
+ * Stream numbering: stream (b, h) of X in {K, V} is the T x 128 matrix
+ * X[b][h][0:T][0:128].  Query head i belongs to KV head i / g, g = Hq / H.
+ */
+#ifndef MKV_H_
+#define MKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL means the legacy default stream. */
+typedef struct CUstream_st* mkv_stream_t;
+
+typedef enum {
+  MKV_OK = 0,
+  MKV_ERR_INVALID_ARG = 1,  /* bad pointer, size or config value */
+  MKV_ERR_STATE = 2,        /* e.g. mkv_decode before any mkv_compress */
+  MKV_ERR_OOM = 3,          /* device allocation failed or max_pool_bytes exceeded */
+  MKV_ERR_CUDA = 4,         /* a CUDA runtime call failed */
+  MKV_ERR_DEVICE_CHECK = 5, /* a kernel's own bounds check fired */
+  MKV_ERR_TIMEOUT = 6       /* a bounded device-side wait gave up */
+} mkv_status;
+
+/* Per-segment strategies (§1 Observation & Method 1: "dynamic compression
+ * strategy"; the set is this library's reading). */
+enum {
+  MKV_STRATEGY_SM = 0,    /* segment-shared mask of c channels */
+  MKV_STRATEGY_PV = 1,    /* per-vector top-c channels (values + uint8 indices) */
+  MKV_STRATEGY_DENSE = 2  /* all 128 channels */
+};
+
+#define MKV_HEAD_DIM 128
+/* Record CUDA events around every decode kernel; read with mkv_kernel_time. */
+#define MKV_FLAG_KERNEL_TIMING 1u
+
+typedef struct {
+  int32_t batch;          /* B >= 1 */
+  int32_t n_kv_heads;     /* H >= 1 */
+  int32_t n_q_heads;      /* Hq, a multiple of H; Hq / H <= 16 */
+  int32_t head_dim;       /* must be 128 */
+  int64_t max_ctx;        /* largest T that mkv_compress will accept, >= 1 */
+  int32_t segment;        /* S: tokens per segment, 16..256, multiple of 16 */
+  int32_t c;              /* kept channels per vector: 8..128, multiple of 8 */
+  float tau;              /* retained-energy threshold, 0 < tau <= 1 */
+  int32_t top_k;          /* tokens attended per KV head per step, >= 1 */
+  int32_t attn_chunk;     /* selected tokens per split-K attention block; 0 = auto,
+                             else 8..1024 and a multiple of 8 */
+  uint64_t max_pool_bytes;/* cap on the packed cache of one ctx; 0 = no cap */
+  uint32_t flags;         /* MKV_FLAG_* */
+  int32_t device;         /* CUDA device ordinal */
+} mkv_config;
+
+typedef struct mkv_ctx mkv_ctx;  /* one ctx = one attention layer */
+
+/* Packed segment header, 8 bytes, one per segment of every stream.
+ * off16: payload byte offset / 16 from the start of the ctx's packed pool
+ * (in mkv_export: from the start of the exported stream payload). */
+typedef struct {
+  uint32_t off16;
+  uint8_t strategy;
+  uint8_t reserved;  /* 0 */
+  uint16_t rows;     /* tokens in the segment: S, or T mod S for the last one */
+} mkv_segment_header;
+
+typedef struct {
+  int64_t ctx_len;                 /* T of the current cache (0 if none) */
+  int64_t n_segments;              /* per stream */
+  int64_t strategy_count[2][3];    /* [K, V][SM, PV, DENSE] over all streams */
+  uint64_t payload_bytes[2];       /* packed bytes of all K, all V streams */
+  uint64_t header_bytes;           /* bytes of all segment headers */
+  uint64_t uncompressed_bytes;     /* 2 * B * H * T * 128 * 2 */
+  uint64_t pool_capacity;          /* bytes currently allocated for the pool */
+  int64_t decode_calls;
+  int64_t kernel_launches;         /* kernels launched by this ctx since creation */
+} mkv_stats_t;
+
+/* Kernel ids for mkv_kernel_time. */
+enum {
+  MKV_KERNEL_QROT = 0,
+  MKV_KERNEL_SCORE = 1,
+  MKV_KERNEL_TOPK = 2,   /* the four radix-select / compaction launches together */
+  MKV_KERNEL_ATTN = 3,
+  MKV_KERNEL_MERGE = 4,
+  MKV_KERNEL_COUNT = 5
+};
+
+/* Checks a config without touching any GPU.  MKV_OK or MKV_ERR_INVALID_ARG. */
+mkv_status mkv_validate_config(const mkv_config* cfg);
+
+/* Packed bytes of one segment with `rows` tokens (host-only, no GPU):
+ *   SM:    pad16(c) + rows * 2c      (uint8 mask, then fp16 values per row)
+ *   PV:    rows * 2c + pad16(rows*c) (fp16 values per row, then uint8 indices)
+ *   DENSE: rows * 256
+ * Returns 0 for an invalid argument. */
+uint64_t mkv_segment_bytes(int strategy, int rows, int c);
+
+/* Creates a ctx for one layer: validates cfg, then allocates the fixed device
+ * buffers (bases, headers, decode scratch).  The packed pool is allocated by
+ * mkv_compress.  *out receives the ctx (NULL on failure). */
+mkv_status mkv_create(const mkv_config* cfg, mkv_ctx** out);
+
+/* Prefill compression (§1 Observation & Method 1).  For each stream of K and
+ * of V: the SVD basis R (eigenvectors of X^T X, eigenvalues descending, each
+ * column's largest-magnitude entry positive), x~ = x R, per-token top-c
+ * channels by |x~| (ties to the lower channel), per-segment strategy = the
+ * cheapest of {SM, PV, DENSE} whose retained energy fraction is >= tau
+ * (DENSE always allowed; cost ties resolve SM, PV, DENSE), then packing
+ * (values fp16 round-to-nearest-even, channels ascending).
+ *   k, v: device fp16 [B][H][ctx_len][128], contiguous.
+ *   ctx_len: 1 <= ctx_len <= max_ctx.
+ * Replaces any previous cache.  The call blocks once, on `stream`, to read the
+ * packed size back before allocating the pool; the final packing kernel is
+ * still in flight on `stream` when it returns, so k and v must stay valid
+ * until that stream's work has run, and decode must run on the same stream
+ * (or after synchronising with it). */
+mkv_status mkv_compress(mkv_ctx* ctx, const void* k, const void* v, int64_t ctx_len,
+                        mkv_stream_t stream);
+
+/* One decode step over the compressed cache (§1: query-aware token selection
+ * and attention on the packed cache without unpacking).  Per KV head:
+ * q~_i = q_i R_K; s_t = sum over the group of q~_i . k^_t; the min(top_k, T)
+ * tokens with the highest s_t (ties to the lower token index); softmax of
+ * q~_i . k^_t / sqrt(128) over them; o_i = (sum_t p_it v^_t) R_V^T.
+ *   q:   device fp16 [B][Hq][128].
+ *   out: device fp32 [B][Hq][128].
+ *   sel: device int32 [B][H][min(top_k, T)] or NULL; receives the selected
+ *        token ids in ascending order.
+ * Fully asynchronous on `stream`; no host synchronisation, no allocation. */
+mkv_status mkv_decode(mkv_ctx* ctx, const void* q, float* out, int32_t* sel,
+                      mkv_stream_t stream);
+
+/* Frees everything the ctx owns.  NULL is allowed.  Synchronises the device. */
+void mkv_free(mkv_ctx* ctx);
+
+/* Static string for a status code. */
+const char* mkv_status_string(mkv_status s);
+
+/* Text of the last CUDA error seen by this library in the calling thread. */
+const char* mkv_last_error_string(void);
+
+/* Counters of the current cache (synchronous; copies headers to the host). */
+mkv_status mkv_stats(const mkv_ctx* ctx, mkv_stats_t* out);
+
+/* Copies one compressed stream to host buffers (synchronous).
+ *   which: 0 = K, 1 = V.
+ *   basis:   host float[128*128] or NULL; R row-major, R[r*128 + j] = entry r of
+ *            basis vector j.
+ *   eigvals: host float[128] or NULL; descending.
+ *   headers: host mkv_segment_header[n_segments] or NULL; off16 relative to
+ *            the start of this stream's payload.
+ *   payload: host buffer of *payload_bytes bytes or NULL.
+ *   payload_bytes: in/out.  On entry the capacity of `payload` (ignored when
+ *            payload is NULL); on return the stream's payload size.  A payload
+ *            buffer smaller than the stream returns MKV_ERR_INVALID_ARG. */
+mkv_status mkv_export(const mkv_ctx* ctx, int b, int h, int which, float* basis,
+                      float* eigvals, mkv_segment_header* headers, void* payload,
+                      uint64_t* payload_bytes);
+
+/* With MKV_FLAG_KERNEL_TIMING: total device time (ms) and launch count of one
+ * decode kernel id since creation or the last reset (synchronous).  reset != 0
+ * clears the counters after reading them. */
+mkv_status mkv_kernel_time(mkv_ctx* ctx, int kernel_id, double* total_ms,
+                           int64_t* launches, int reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MKV_H_ */

@@ -316,25 +316,35 @@ class DecodeResult:
     logits: np.ndarray      # [g, kk]
 
 
+def rotate_queries(q: np.ndarray, R_K: np.ndarray) -> np.ndarray:
+    """q~_i = q_i R_K for each query head of the group (fp64)."""
+    return np.atleast_2d(np.asarray(q, dtype=np.float64)) @ np.asarray(R_K, dtype=np.float64)
+
+
+def attend(qt: np.ndarray, R_V: np.ndarray, K_hat: np.ndarray, V_hat: np.ndarray,
+           sel: np.ndarray):
+    """Softmax attention of the rotated queries over the selected tokens:
+    logits q~_i . k^_t / sqrt(d), max-subtracted softmax, o~_i = sum_t p_it v^_t
+    in the rotated V basis, o_i = o~_i R_V^T.  Returns (out [g, d], logits)."""
+    d = qt.shape[1]
+    logits = (qt @ K_hat[sel].T) / math.sqrt(d)
+    m = logits.max(axis=1, keepdims=True)
+    p = np.exp(logits - m)
+    p /= p.sum(axis=1, keepdims=True)
+    ot = p @ V_hat[sel]
+    return ot @ np.asarray(R_V, dtype=np.float64).T, logits
+
+
 def decode_stream(q: np.ndarray, R_K: np.ndarray, R_V: np.ndarray,
                   K_hat: np.ndarray, V_hat: np.ndarray, k: int) -> DecodeResult:
     """One decode step for one KV head and its g query heads.
 
     q~_i = q_i R_K; s_t = sum_i q~_i . k^_t (the GQA group's scores summed);
-    Sel = top-k of s; logits q~_i . k^_t / sqrt(d) over Sel; softmax;
-    o~_i = sum_t p_it v^_t (rotated V basis); o_i = o~_i R_V^T."""
-    q = np.atleast_2d(np.asarray(q, dtype=np.float64))
-    d = q.shape[1]
-    qt = q @ np.asarray(R_K, dtype=np.float64)
-    per_head = qt @ K_hat.T                      # [g, T]
-    s = per_head.sum(axis=0)
+    Sel = top-k of s; then `attend` over Sel."""
+    qt = rotate_queries(q, R_K)
+    s = (qt @ K_hat.T).sum(axis=0)
     sel = top_k_tokens(s, k)
-    logits = per_head[:, sel] / math.sqrt(d)
-    m = logits.max(axis=1, keepdims=True)
-    p = np.exp(logits - m)
-    p /= p.sum(axis=1, keepdims=True)
-    ot = p @ V_hat[sel]
-    out = ot @ np.asarray(R_V, dtype=np.float64).T
+    out, logits = attend(qt, R_V, K_hat, V_hat, sel)
     return DecodeResult(scores=s, sel=sel, out=out, logits=logits)
 
 

@@ -1,0 +1,174 @@
+"""Comparison of the CUDA library's results with the CPU oracle.
+
+Rules (the oracle computes in fp64, the library in fp32 arithmetic over fp16
+storage; a decision taken on floating-point values may flip only inside these
+near-tie windows, and every flip is counted):
+  * basis: only unique parts are compared with the oracle's own fp64 basis
+    (eigenvalues, eigenvectors of well-separated eigenvalues); the library's
+    basis is then checked for validity (orthonormal, eigen-residual, order,
+    sign rule), and the steps after it are checked given that basis;
+  * per-token / per-segment channel sets: equal, unless the c-th and (c+1)-th
+    largest energies are within 1e-4 relative;
+  * strategy: equal, unless the deciding fraction is within 1e-5 of tau;
+  * stored fp16 values: equal, or one ulp apart with the fp64 value within
+    1e-5 relative of the rounding midpoint;
+  * selected tokens: equal, unless the token's score is within 1e-4 relative
+    of the k-th score;
+  * attention output: max abs error <= 2e-3.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from oracle import mosaickv as O
+
+NEAR_REL = 1e-4
+TAU_WIN = 1e-5
+MID_REL = 1e-5
+OUT_TOL = 2e-3
+
+
+def _ordered16(a: np.ndarray) -> np.ndarray:
+    u = a.view(np.uint16).astype(np.int64)
+    return np.where(u & 0x8000, -(u & 0x7FFF), u)
+
+
+def _near_tie(sorted_desc: np.ndarray, c: int) -> bool:
+    if c >= len(sorted_desc):
+        return False
+    a, b = sorted_desc[c - 1], sorted_desc[c]
+    return abs(a - b) <= NEAR_REL * max(abs(a), 1e-300)
+
+
+def check_basis(X: np.ndarray, R: np.ndarray, lam: np.ndarray, report: dict):
+    """Validity of a library basis and agreement of its unique part with the
+    oracle's fp64 eigendecomposition."""
+    X64 = X.astype(np.float64)
+    G = X64.T @ X64
+    R64 = R.astype(np.float64)
+    d = R.shape[0]
+    orth = np.abs(R64.T @ R64 - np.eye(d)).max()
+    resid = np.linalg.norm(G @ R64 - R64 * lam.astype(np.float64)) / max(np.linalg.norm(G), 1e-300)
+    lam_o, R_o = O.basis(X)
+    lam_err = np.abs(lam.astype(np.float64) - lam_o).max() / max(lam_o[0], 1e-300)
+    gaps = np.full(d, np.inf)
+    gaps[:-1] = np.minimum(gaps[:-1], lam_o[:-1] - lam_o[1:])
+    gaps[1:] = np.minimum(gaps[1:], lam_o[:-1] - lam_o[1:])
+    sep = gaps / max(lam_o[0], 1e-300) > 1e-3
+    cos = np.abs(np.sum(R64 * R_o, axis=0))
+    report.update(orth=float(orth), resid=float(resid), lam_err=float(lam_err),
+                  sep_cols=int(sep.sum()), min_cos_sep=float(cos[sep].min()) if sep.any() else 1.0)
+    assert orth <= 1e-5, f"basis not orthonormal: {orth}"
+    assert resid <= 1e-5, f"eigen-residual {resid}"
+    assert lam_err <= 1e-5, f"eigenvalues differ from fp64: {lam_err}"
+    assert (np.diff(lam.astype(np.float64)) <= 0).all(), "eigenvalues not descending"
+    if sep.any():
+        assert cos[sep].min() >= 1 - 1e-4, f"separated eigenvectors differ: {cos[sep].min()}"
+    for j in range(d):
+        col = np.abs(R64[:, j])
+        r = int(np.argmax(col))
+        second = np.partition(col, -2)[-2]
+        if col[r] - second > 1e-6:
+            assert R64[r, j] > 0, f"sign rule, column {j}"
+
+
+def compare_compressed(X: np.ndarray, R: np.ndarray, hdr: np.ndarray, payload: bytes,
+                       S: int, c: int, tau: float, report: dict):
+    """Packed stream from the library vs the oracle's steps 2-4 given the
+    library's basis.  Returns the oracle's CompressedStream."""
+    cs = O.compress_stream(X, S, c, tau, R=R.astype(np.float64))
+    buf = np.frombuffer(payload, dtype=np.uint8)
+    q16 = O.to_fp16(cs.Xt)
+    tau32 = float(np.float32(tau))
+    cnt = dict(segments=len(cs.segs), bytes_equal=0, strat_near=0, idx_near=0, ulp_near=0)
+    expect_off = 0
+    for si, (a, b) in enumerate(O.segment_bounds(cs.T, S)):
+        seg = cs.segs[si]
+        h = hdr[si]
+        rows = b - a
+        assert int(h["rows"]) == rows, f"segment {si}: rows"
+        assert int(h["off16"]) * 16 == expect_off, f"segment {si}: offset not the running sum"
+        st = int(h["strategy"])
+        size = O.segment_cost(st, rows, c)
+        expect_off += size
+        gseg = buf[int(h["off16"]) * 16:int(h["off16"]) * 16 + size]
+        assert len(gseg) == size, f"segment {si}: payload truncated"
+        if st != seg.strategy:
+            near = abs(seg.f_sm - tau32) <= TAU_WIN or abs(seg.f_pv - tau32) <= TAU_WIN
+            assert near, (f"segment {si}: strategy {st} vs oracle {seg.strategy} "
+                          f"(f_sm {seg.f_sm:.7f}, f_pv {seg.f_pv:.7f}, tau {tau32})")
+            cnt["strat_near"] += 1
+            continue
+        # the oracle's bytes for this segment
+        one = O.CompressedStream(T=rows, d=cs.d, S=rows, c=c, R=cs.R, lam=None,
+                                 Xt=cs.Xt[a:b], P=cs.P[a:b], segs=[seg])
+        _, obytes = O.pack_stream(one)
+        if gseg.tobytes() == obytes:
+            cnt["bytes_equal"] += 1
+            continue
+        sq = cs.Xt[a:b] ** 2
+        if st == O.DENSE:
+            gv = gseg.view("<f2").reshape(rows, cs.d)
+            _check_vals(gv, q16[a:b], cs.Xt[a:b], cnt, f"segment {si}")
+        elif st == O.SM:
+            gidx = gseg[:c].astype(np.int64)
+            if not np.array_equal(gidx, seg.mask):
+                col = np.sort(sq.sum(axis=0))[::-1]
+                assert _near_tie(col, c), f"segment {si}: shared mask differs"
+                cnt["idx_near"] += 1
+                continue
+            assert not gseg[c:O.pad16(c)].any(), f"segment {si}: nonzero padding"
+            gv = gseg[O.pad16(c):].view("<f2").reshape(rows, c)
+            _check_vals(gv, q16[a:b][:, seg.mask], cs.Xt[a:b][:, seg.mask], cnt, f"segment {si}")
+        else:
+            gv = gseg[:2 * c * rows].view("<f2").reshape(rows, c)
+            gidx = gseg[2 * c * rows:2 * c * rows + c * rows].reshape(rows, c).astype(np.int64)
+            assert not gseg[2 * c * rows + c * rows:].any(), f"segment {si}: nonzero padding"
+            for r in range(rows):
+                P = cs.P[a + r]
+                if not np.array_equal(gidx[r], P):
+                    srt = np.sort(sq[r])[::-1]
+                    assert _near_tie(srt, c), f"segment {si} row {r}: channels differ"
+                    cnt["idx_near"] += 1
+                    continue
+                _check_vals(gv[r:r + 1], q16[a + r:a + r + 1][:, P],
+                            cs.Xt[a + r:a + r + 1][:, P], cnt, f"segment {si} row {r}")
+    for k, v in cnt.items():
+        report[k] = report.get(k, 0) + v
+    return cs
+
+
+def _check_vals(got16, want16, exact, cnt, where):
+    d = np.abs(_ordered16(np.ascontiguousarray(got16)) - _ordered16(np.ascontiguousarray(want16)))
+    assert d.max(initial=0) <= 1, f"{where}: stored values differ by {d.max()} ulp"
+    for idx in zip(*np.nonzero(d)):
+        lo, hi = sorted([float(got16[idx]), float(want16[idx])])
+        mid = 0.5 * (lo + hi)
+        x = float(exact[idx])
+        assert abs(x - mid) <= MID_REL * max(abs(x), 1e-30), f"{where}: 1-ulp difference away from a midpoint"
+        cnt["ulp_near"] += 1
+
+
+def compare_decode(q: np.ndarray, RK: np.ndarray, RV: np.ndarray, K_hat: np.ndarray,
+                   V_hat: np.ndarray, k: int, gsel: np.ndarray, gout: np.ndarray, report: dict):
+    """Library decode vs the oracle's decode over the same packed cache."""
+    r = O.decode_stream(q, RK.astype(np.float64), RV.astype(np.float64), K_hat, V_hat, k)
+    T = K_hat.shape[0]
+    kk = min(k, T)
+    gsel = np.asarray(gsel, dtype=np.int64)
+    assert gsel.shape == (kk,), "selection length"
+    assert (np.diff(gsel) > 0).all(), "selection not strictly ascending"
+    assert gsel.min() >= 0 and gsel.max() < T, "selection out of range"
+    s = r.scores
+    sk = np.sort(s)[::-1][kk - 1]
+    diff = np.setxor1d(gsel, r.sel)
+    for t in diff:
+        assert abs(s[t] - sk) <= NEAR_REL * max(abs(sk), 1e-30), \
+            f"token {t}: selection differs (score {s[t]}, k-th {sk})"
+    report["sel_near"] = report.get("sel_near", 0) + len(diff) // 2
+    qt = O.rotate_queries(q, RK.astype(np.float64))
+    out_o, _ = O.attend(qt, RV.astype(np.float64), K_hat, V_hat, gsel)
+    err = float(np.abs(out_o - gout).max())
+    report["out_err"] = max(report.get("out_err", 0.0), err)
+    assert err <= OUT_TOL, f"attention output error {err}"
+    return r

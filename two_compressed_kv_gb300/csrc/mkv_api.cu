@@ -1,0 +1,496 @@
+// Host side of the C ABI in include/mkv.h: ctx lifetime, argument checks,
+// device buffers, launch order, kernel timing and introspection.
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <utility>
+#include <vector>
+
+#include "mkv_internal.cuh"
+
+using namespace mkv;
+
+namespace {
+
+constexpr int kSMs = 152;          // GB300
+thread_local std::string g_last_error = "no error";
+
+mkv_status cuda_fail(cudaError_t e, const char* what) {
+  char buf[256];
+  snprintf(buf, sizeof(buf), "%s: %s (%d)", what, cudaGetErrorString(e), (int)e);
+  g_last_error = buf;
+  return e == cudaErrorMemoryAllocation ? MKV_ERR_OOM : MKV_ERR_CUDA;
+}
+
+#define CK(call)                                         \
+  do {                                                   \
+    cudaError_t e_ = (call);                             \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #call);  \
+  } while (0)
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct KernelTimer {
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> pending;
+  std::vector<cudaEvent_t> spare;
+  double total_ms = 0.0;
+  int64_t launches = 0;
+};
+
+}  // namespace
+
+struct mkv_ctx {
+  mkv_config cfg;
+  int B = 0, H = 0, Hq = 0, g = 0, BH = 0;
+  int64_t max_seg = 0;
+  int kk_max = 0;
+  int gram_chunks_max = 0;
+  int attn_chunk = 64;
+  int attn_chunks_max = 0;
+  int topk_chunks_max = 0;
+
+  // current cache
+  int64_t T = 0;
+  int n_seg = 0;
+  bool ready = false;
+  int live = 0;                    // which of the double-buffered copies is live
+  float* R[2] = {nullptr, nullptr};
+  float* lam[2] = {nullptr, nullptr};
+  mkv_segment_header* hdr[2] = {nullptr, nullptr};
+  uint8_t* pool = nullptr;
+  uint64_t pool_cap = 0;
+
+  // compression scratch
+  SegInfo* seg = nullptr;
+  float* gram_part = nullptr;
+  unsigned long long* total_dev = nullptr;
+  unsigned long long* total_host = nullptr;
+
+  // decode scratch
+  float* qt = nullptr;
+  float* qbar = nullptr;
+  float* scores = nullptr;
+  uint32_t* hist = nullptr;
+  int2* cnt = nullptr;
+  int2* res = nullptr;
+  int32_t* sel = nullptr;
+  float* part_o = nullptr;
+  float* part_ml = nullptr;
+
+  int64_t decode_calls = 0;
+  int64_t launches = 0;
+  KernelTimer timers[MKV_KERNEL_COUNT];
+};
+
+namespace {
+
+bool timing_on(const mkv_ctx* c) { return (c->cfg.flags & MKV_FLAG_KERNEL_TIMING) != 0u; }
+
+mkv_status resolve_timer(KernelTimer& t, size_t keep) {
+  while (t.pending.size() > keep) {
+    auto ev = t.pending.front();
+    t.pending.erase(t.pending.begin());
+    CK(cudaEventSynchronize(ev.second));
+    float ms = 0.f;
+    CK(cudaEventElapsedTime(&ms, ev.first, ev.second));
+    t.total_ms += ms;
+    t.spare.push_back(ev.first);
+    t.spare.push_back(ev.second);
+  }
+  return MKV_OK;
+}
+
+mkv_status timer_event(KernelTimer& t, cudaEvent_t* ev) {
+  if (!t.spare.empty()) {
+    *ev = t.spare.back();
+    t.spare.pop_back();
+    return MKV_OK;
+  }
+  CK(cudaEventCreate(ev));
+  return MKV_OK;
+}
+
+// Runs `launch` on `st`, bracketed by events when timing is on.
+template <typename F>
+mkv_status timed(mkv_ctx* c, int id, cudaStream_t st, int n_kernels, F launch) {
+  cudaEvent_t a = nullptr, b = nullptr;
+  if (timing_on(c)) {
+    if (c->timers[id].pending.size() >= 4096) {
+      mkv_status s = resolve_timer(c->timers[id], 2048);
+      if (s != MKV_OK) return s;
+    }
+    mkv_status s = timer_event(c->timers[id], &a);
+    if (s != MKV_OK) return s;
+    s = timer_event(c->timers[id], &b);
+    if (s != MKV_OK) return s;
+    CK(cudaEventRecord(a, st));
+  }
+  CK(launch());
+  c->launches += n_kernels;
+  if (timing_on(c)) {
+    CK(cudaEventRecord(b, st));
+    c->timers[id].pending.emplace_back(a, b);
+    c->timers[id].launches += 1;
+  }
+  return MKV_OK;
+}
+
+template <typename T>
+mkv_status dalloc(T** p, size_t n) {
+  *p = nullptr;
+  if (n == 0) n = 1;
+  CK(cudaMalloc(reinterpret_cast<void**>(p), n * sizeof(T)));
+  return MKV_OK;
+}
+
+void release(mkv_ctx* c) {
+  if (!c) return;
+  cudaSetDevice(c->cfg.device);
+  for (int i = 0; i < 2; ++i) {
+    cudaFree(c->R[i]);
+    cudaFree(c->lam[i]);
+    cudaFree(c->hdr[i]);
+  }
+  cudaFree(c->pool);
+  cudaFree(c->seg);
+  cudaFree(c->gram_part);
+  cudaFree(c->total_dev);
+  if (c->total_host) cudaFreeHost(c->total_host);
+  cudaFree(c->qt);
+  cudaFree(c->qbar);
+  cudaFree(c->scores);
+  cudaFree(c->hist);
+  cudaFree(c->cnt);
+  cudaFree(c->res);
+  cudaFree(c->sel);
+  cudaFree(c->part_o);
+  cudaFree(c->part_ml);
+  for (auto& t : c->timers) {
+    for (auto& e : t.pending) {
+      cudaEventDestroy(e.first);
+      cudaEventDestroy(e.second);
+    }
+    for (auto& e : t.spare) cudaEventDestroy(e);
+  }
+  delete c;
+}
+
+int gram_chunks_for(int BH, int64_t T) {
+  const int64_t target = 4 * kSMs;
+  int64_t ch = ceil_div(target, 2 * (int64_t)BH);
+  ch = std::min<int64_t>(ch, std::max<int64_t>(1, ceil_div(T, 256)));
+  return (int)std::max<int64_t>(1, ch);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mkv_status_string(mkv_status s) {
+  switch (s) {
+    case MKV_OK: return "MKV_OK";
+    case MKV_ERR_INVALID_ARG: return "MKV_ERR_INVALID_ARG";
+    case MKV_ERR_STATE: return "MKV_ERR_STATE";
+    case MKV_ERR_OOM: return "MKV_ERR_OOM";
+    case MKV_ERR_CUDA: return "MKV_ERR_CUDA";
+    case MKV_ERR_DEVICE_CHECK: return "MKV_ERR_DEVICE_CHECK";
+    case MKV_ERR_TIMEOUT: return "MKV_ERR_TIMEOUT";
+  }
+  return "MKV_ERR_UNKNOWN";
+}
+
+const char* mkv_last_error_string(void) { return g_last_error.c_str(); }
+
+uint64_t mkv_segment_bytes(int strategy, int rows, int c) {
+  if (rows < 1 || rows > 65535 || c < 1 || c > MKV_HEAD_DIM) return 0;
+  if (strategy < MKV_STRATEGY_SM || strategy > MKV_STRATEGY_DENSE) return 0;
+  return segment_bytes(strategy, rows, c);
+}
+
+mkv_status mkv_validate_config(const mkv_config* cfg) {
+  if (!cfg) return MKV_ERR_INVALID_ARG;
+  const mkv_config& c = *cfg;
+  if (c.batch < 1 || c.n_kv_heads < 1 || c.n_q_heads < 1) return MKV_ERR_INVALID_ARG;
+  if (c.n_q_heads % c.n_kv_heads != 0) return MKV_ERR_INVALID_ARG;
+  if (c.n_q_heads / c.n_kv_heads > MAX_G) return MKV_ERR_INVALID_ARG;
+  if (c.head_dim != MKV_HEAD_DIM) return MKV_ERR_INVALID_ARG;
+  if (c.max_ctx < 1 || c.max_ctx > (int64_t)INT32_MAX) return MKV_ERR_INVALID_ARG;
+  if (c.segment < 16 || c.segment > 256 || c.segment % 16 != 0) return MKV_ERR_INVALID_ARG;
+  if (c.c < 8 || c.c > MKV_HEAD_DIM || c.c % 8 != 0) return MKV_ERR_INVALID_ARG;
+  if (!(c.tau > 0.f && c.tau <= 1.f)) return MKV_ERR_INVALID_ARG;
+  if (c.top_k < 1) return MKV_ERR_INVALID_ARG;
+  if (c.attn_chunk != 0 && (c.attn_chunk < 8 || c.attn_chunk > 1024 || c.attn_chunk % 8 != 0))
+    return MKV_ERR_INVALID_ARG;
+  if (c.flags & ~MKV_FLAG_KERNEL_TIMING) return MKV_ERR_INVALID_ARG;
+  if (c.device < 0) return MKV_ERR_INVALID_ARG;
+  const int64_t streams = (int64_t)c.batch * c.n_kv_heads;
+  if (streams > (1 << 20)) return MKV_ERR_INVALID_ARG;
+  return MKV_OK;
+}
+
+mkv_status mkv_create(const mkv_config* cfg, mkv_ctx** out) {
+  if (!out) return MKV_ERR_INVALID_ARG;
+  *out = nullptr;
+  mkv_status st = mkv_validate_config(cfg);
+  if (st != MKV_OK) return st;
+  int ndev = 0;
+  CK(cudaGetDeviceCount(&ndev));
+  if (cfg->device >= ndev) return MKV_ERR_INVALID_ARG;
+  CK(cudaSetDevice(cfg->device));
+  mkv_ctx* c = new (std::nothrow) mkv_ctx();
+  if (!c) return MKV_ERR_OOM;
+  c->cfg = *cfg;
+  c->B = cfg->batch;
+  c->H = cfg->n_kv_heads;
+  c->Hq = cfg->n_q_heads;
+  c->g = c->Hq / c->H;
+  c->BH = c->B * c->H;
+  c->max_seg = ceil_div(cfg->max_ctx, cfg->segment);
+  c->kk_max = (int)std::min<int64_t>(cfg->top_k, cfg->max_ctx);
+  c->gram_chunks_max = gram_chunks_for(c->BH, cfg->max_ctx);
+  c->attn_chunk = cfg->attn_chunk ? cfg->attn_chunk : 64;
+  c->attn_chunks_max = (int)ceil_div(c->kk_max, c->attn_chunk);
+  c->topk_chunks_max = (int)ceil_div(cfg->max_ctx, TOPK_CHUNK);
+  const size_t BH = c->BH;
+  mkv_status s = MKV_OK;
+#define AL(ptr, n)                         \
+  if (s == MKV_OK) s = dalloc(&(ptr), (n)); \
+  if (s != MKV_OK) {                       \
+    release(c);                            \
+    return s;                              \
+  }
+  for (int i = 0; i < 2; ++i) {
+    AL(c->R[i], 2 * BH * D * D);
+    AL(c->lam[i], 2 * BH * D);
+    AL(c->hdr[i], 2 * BH * (size_t)c->max_seg);
+  }
+  AL(c->seg, 2 * BH * (size_t)c->max_seg);
+  AL(c->gram_part, 2 * BH * (size_t)c->gram_chunks_max * D * D);
+  AL(c->total_dev, 1);
+  AL(c->qt, (size_t)c->B * c->Hq * D);
+  AL(c->qbar, BH * D);
+  AL(c->scores, BH * (size_t)cfg->max_ctx);
+  AL(c->hist, BH * HIST_WORDS);
+  AL(c->cnt, BH * (size_t)c->topk_chunks_max);
+  AL(c->res, BH);
+  AL(c->sel, BH * (size_t)c->kk_max);
+  AL(c->part_o, BH * (size_t)c->attn_chunks_max * c->g * D);
+  AL(c->part_ml, BH * (size_t)c->attn_chunks_max * c->g * 2);
+#undef AL
+  cudaError_t e = cudaMallocHost(reinterpret_cast<void**>(&c->total_host), sizeof(unsigned long long));
+  if (e != cudaSuccess) {
+    release(c);
+    return cuda_fail(e, "cudaMallocHost");
+  }
+  *out = c;
+  return MKV_OK;
+}
+
+void mkv_free(mkv_ctx* ctx) {
+  if (!ctx) return;
+  cudaSetDevice(ctx->cfg.device);
+  cudaDeviceSynchronize();
+  release(ctx);
+}
+
+mkv_status mkv_compress(mkv_ctx* c, const void* k, const void* v, int64_t ctx_len,
+                        mkv_stream_t stream) {
+  if (!c || !k || !v) return MKV_ERR_INVALID_ARG;
+  if (ctx_len < 1 || ctx_len > c->cfg.max_ctx) return MKV_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15u) return MKV_ERR_INVALID_ARG;
+  CK(cudaSetDevice(c->cfg.device));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int stage = 1 - c->live;
+  CompressParams p;
+  memset(&p, 0, sizeof(p));
+  p.X[0] = static_cast<const __half*>(k);
+  p.X[1] = static_cast<const __half*>(v);
+  p.BH = c->BH;
+  p.T = ctx_len;
+  p.S = c->cfg.segment;
+  p.c = c->cfg.c;
+  p.tau = c->cfg.tau;
+  p.n_seg = (int)ceil_div(ctx_len, p.S);
+  p.gram_chunks = std::min(c->gram_chunks_max, gram_chunks_for(c->BH, ctx_len));
+  p.gram_chunk_tokens = ceil_div(ceil_div(ctx_len, p.gram_chunks), TILE_T) * TILE_T;
+  p.gram_chunks = (int)ceil_div(ctx_len, p.gram_chunk_tokens);
+  p.gram_part = c->gram_part;
+  p.R = c->R[stage];
+  p.lam = c->lam[stage];
+  // analyze/pack: about 4 CTAs of 1 per SM per wave, whole segments each
+  const int64_t total_segs = 2 * (int64_t)c->BH * p.n_seg;
+  const int64_t want_ctas = 4 * kSMs;
+  p.segs_per_cta = (int)std::max<int64_t>(1, ceil_div(total_segs, want_ctas));
+  p.ctas_per_stream = (int)ceil_div(p.n_seg, p.segs_per_cta);
+  p.seg = c->seg;
+  p.hdr = c->hdr[stage];
+  p.total = c->total_dev;
+  p.pool = nullptr;
+
+  CK(launch_gram(p, st));
+  CK(launch_eig(p, st));
+  CK(launch_analyze(p, st));
+  CK(launch_scan(p, st));
+  c->launches += 4;
+  CK(cudaMemcpyAsync(c->total_host, c->total_dev, sizeof(unsigned long long),
+                     cudaMemcpyDeviceToHost, st));
+  CK(cudaStreamSynchronize(st));
+  const uint64_t total = *c->total_host;
+  if ((total >> 4) > 0xffffffffull) {
+    g_last_error = "packed cache exceeds 64 GiB per ctx";
+    return MKV_ERR_INVALID_ARG;
+  }
+  if (c->cfg.max_pool_bytes && total > c->cfg.max_pool_bytes) {
+    g_last_error = "packed cache exceeds max_pool_bytes";
+    return MKV_ERR_OOM;
+  }
+  if (total > c->pool_cap) {
+    uint8_t* np = nullptr;
+    cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&np), total);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return cuda_fail(e, "cudaMalloc(pool)");
+    }
+    CK(cudaFree(c->pool));   // synchronises: no decode still reads the old pool
+    c->pool = np;
+    c->pool_cap = total;
+  }
+  p.pool = c->pool;
+  c->ready = false;   // the live headers may no longer match the pool
+  CK(launch_pack(p, st));
+  c->launches += 1;
+  c->live = stage;
+  c->T = ctx_len;
+  c->n_seg = p.n_seg;
+  c->ready = true;
+  return MKV_OK;
+}
+
+mkv_status mkv_decode(mkv_ctx* c, const void* q, float* out, int32_t* sel, mkv_stream_t stream) {
+  if (!c || !q || !out) return MKV_ERR_INVALID_ARG;
+  if (!c->ready) return MKV_ERR_STATE;
+  CK(cudaSetDevice(c->cfg.device));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  DecodeParams p;
+  memset(&p, 0, sizeof(p));
+  p.B = c->B;
+  p.H = c->H;
+  p.Hq = c->Hq;
+  p.g = c->g;
+  p.T = c->T;
+  p.S = c->cfg.segment;
+  p.c = c->cfg.c;
+  p.n_seg = c->n_seg;
+  p.kk = (int)std::min<int64_t>(c->cfg.top_k, c->T);
+  p.q = static_cast<const __half*>(q);
+  p.RK = c->R[c->live];
+  p.RV = c->R[c->live] + (size_t)c->BH * D * D;
+  p.pool = c->pool;
+  p.hdrK = c->hdr[c->live];
+  p.hdrV = c->hdr[c->live] + (size_t)c->BH * c->n_seg;
+  p.qt = c->qt;
+  p.qbar = c->qbar;
+  p.scores = c->scores;
+  p.hist = c->hist;
+  p.cnt = c->cnt;
+  p.res = c->res;
+  p.topk_chunks = (int)ceil_div(c->T, TOPK_CHUNK);
+  p.sel = c->sel;
+  p.sel_user = sel;
+  // score: whole segments per CTA, ~8 segments per warp
+  p.score_segs_per_cta = 64;
+  p.score_ctas_per_stream = (int)ceil_div(c->n_seg, p.score_segs_per_cta);
+  p.attn_chunk = c->attn_chunk;
+  p.attn_chunks = (int)ceil_div(p.kk, p.attn_chunk);
+  p.part_o = c->part_o;
+  p.part_ml = c->part_ml;
+  p.out = out;
+  mkv_status s;
+  if ((s = timed(c, MKV_KERNEL_QROT, st, 1, [&] { return launch_qrot(p, st); })) != MKV_OK) return s;
+  if ((s = timed(c, MKV_KERNEL_SCORE, st, 1, [&] { return launch_score(p, st); })) != MKV_OK) return s;
+  if ((s = timed(c, MKV_KERNEL_TOPK, st, 4, [&] { return launch_topk(p, st); })) != MKV_OK) return s;
+  if ((s = timed(c, MKV_KERNEL_ATTN, st, 1, [&] { return launch_attn(p, st); })) != MKV_OK) return s;
+  if ((s = timed(c, MKV_KERNEL_MERGE, st, 1, [&] { return launch_merge(p, st); })) != MKV_OK) return s;
+  c->decode_calls += 1;
+  return MKV_OK;
+}
+
+mkv_status mkv_stats(const mkv_ctx* c, mkv_stats_t* out) {
+  if (!c || !out) return MKV_ERR_INVALID_ARG;
+  memset(out, 0, sizeof(*out));
+  out->pool_capacity = c->pool_cap;
+  out->decode_calls = c->decode_calls;
+  out->kernel_launches = c->launches;
+  if (!c->ready) return MKV_OK;
+  CK(cudaSetDevice(c->cfg.device));
+  const size_t n = 2 * (size_t)c->BH * c->n_seg;
+  std::vector<mkv_segment_header> h(n);
+  CK(cudaMemcpy(h.data(), c->hdr[c->live], n * sizeof(mkv_segment_header), cudaMemcpyDeviceToHost));
+  out->ctx_len = c->T;
+  out->n_segments = c->n_seg;
+  for (size_t i = 0; i < n; ++i) {
+    const int x = (int)(i / ((size_t)c->BH * c->n_seg));
+    const int st = h[i].strategy;
+    if (st >= 0 && st < 3) out->strategy_count[x][st] += 1;
+    out->payload_bytes[x] += segment_bytes(st, h[i].rows, c->cfg.c);
+  }
+  out->header_bytes = n * sizeof(mkv_segment_header);
+  out->uncompressed_bytes = 2ull * c->BH * (uint64_t)c->T * D * 2ull;
+  return MKV_OK;
+}
+
+mkv_status mkv_export(const mkv_ctx* c, int b, int h, int which, float* basis, float* eigvals,
+                      mkv_segment_header* headers, void* payload, uint64_t* payload_bytes) {
+  if (!c || !payload_bytes) return MKV_ERR_INVALID_ARG;
+  if (b < 0 || b >= c->B || h < 0 || h >= c->H || which < 0 || which > 1) return MKV_ERR_INVALID_ARG;
+  if (!c->ready) return MKV_ERR_STATE;
+  CK(cudaSetDevice(c->cfg.device));
+  CK(cudaDeviceSynchronize());
+  const size_t sx = (size_t)which * c->BH + (size_t)b * c->H + h;
+  if (basis)
+    CK(cudaMemcpy(basis, c->R[c->live] + sx * D * D, D * D * sizeof(float), cudaMemcpyDeviceToHost));
+  if (eigvals)
+    CK(cudaMemcpy(eigvals, c->lam[c->live] + sx * D, D * sizeof(float), cudaMemcpyDeviceToHost));
+  std::vector<mkv_segment_header> hd(c->n_seg);
+  CK(cudaMemcpy(hd.data(), c->hdr[c->live] + sx * c->n_seg, c->n_seg * sizeof(mkv_segment_header),
+                cudaMemcpyDeviceToHost));
+  const uint64_t first = (uint64_t)hd[0].off16 * 16u;
+  const mkv_segment_header& last = hd[c->n_seg - 1];
+  const uint64_t end = (uint64_t)last.off16 * 16u + segment_bytes(last.strategy, last.rows, c->cfg.c);
+  const uint64_t bytes = end - first;
+  if (payload) {
+    if (*payload_bytes < bytes) {
+      *payload_bytes = bytes;
+      return MKV_ERR_INVALID_ARG;
+    }
+    CK(cudaMemcpy(payload, c->pool + first, bytes, cudaMemcpyDeviceToHost));
+  }
+  *payload_bytes = bytes;
+  if (headers) {
+    for (int i = 0; i < c->n_seg; ++i) {
+      headers[i] = hd[i];
+      headers[i].off16 = hd[i].off16 - (uint32_t)(first >> 4);
+    }
+  }
+  return MKV_OK;
+}
+
+mkv_status mkv_kernel_time(mkv_ctx* c, int kernel_id, double* total_ms, int64_t* launches,
+                           int reset) {
+  if (!c || kernel_id < 0 || kernel_id >= MKV_KERNEL_COUNT) return MKV_ERR_INVALID_ARG;
+  CK(cudaSetDevice(c->cfg.device));
+  KernelTimer& t = c->timers[kernel_id];
+  mkv_status s = resolve_timer(t, 0);
+  if (s != MKV_OK) return s;
+  if (total_ms) *total_ms = t.total_ms;
+  if (launches) *launches = t.launches;
+  if (reset) {
+    t.total_ms = 0.0;
+    t.launches = 0;
+  }
+  return MKV_OK;
+}
+
+}  // extern "C"
