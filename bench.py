@@ -1,0 +1,452 @@
+"""Decode-attention benchmark over a two-D compressed KV cache.
+
+Workload: the 128K-context batch-8 Llama-3.1-8B-shaped attention layer
+(8 KV heads, 32 query heads, head dim 128, segment 128, c = 40, tau = 0.85,
+top-k 4096), 32 independently seeded layers.  One step = one decode step of
+every layer (mkv_decode per layer, layers cycled so that the 674 MB of packed
+keys each layer streams never sit in the 129 MB L2).  Inputs are synthetic
+(seeded generators; no model weights or datasets).
+
+Metric: context tokens attended per second = layers * B * T / step time.
+Prints one JSON line.  With torchrun (N > 1) each rank runs the whole workload
+on its own GPU (weak scaling, no data-path collective); the step time is the
+maximum over ranks.
+
+--impl reference times the CPU oracle (fp64 NumPy) on a bounded sample of the
+same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from two_compressed_kv_gb300 import workloads as W  # noqa: E402
+
+METRIC = "decode-attention ctx-tokens/s (128K, bs8) and achieved HBM GB/s vs 8 TB/s"
+UNIT = "ctx-tokens/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return ws, rank, local
+
+
+def _barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x: float, ws: int, device) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def committed_traffic(kernel_file: str, summary: str):
+    """DRAM bytes per launch of the score kernel from a committed ncu summary,
+    or None when the summary is missing or was taken on a different source."""
+    path = os.path.join(ROOT, "profiles", summary)
+    if not os.path.exists(path):
+        return None
+    src = open(os.path.join(ROOT, "two_compressed_kv_gb300", "csrc", kernel_file), "rb").read()
+    sha = hashlib.sha256(src).hexdigest()
+    vals = {}
+    for line in open(path):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_sha256") != sha:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch_full_size"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sms.append(float(parts[0]))
+                maxes.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sms:
+            return None
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes),
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle leg (cpu_baseline and --impl reference)
+# ---------------------------------------------------------------------------
+def oracle_decode_sample(w: W.Workload, seconds: float, K=None, V=None, q=None):
+    """Times the oracle's decode (unpack the packed stream + scores + top-k +
+    attention) on stream (b=0, h=0) of layer 0, repeated for about `seconds`.
+    Compression of the sample runs first and is not timed."""
+    from oracle import mosaickv as O
+    if K is None:
+        K, V = W.draw_kv(w, layer=0, device="cpu", streams=1)
+        q = W.draw_queries(w, K)
+    Kn = K[0, 0].cpu().numpy()
+    Vn = V[0, 0].cpu().numpy()
+    g = w.group
+    qn = q[0, :g].cpu().numpy()
+    ck = O.compress_stream(Kn, w.segment, w.c, w.tau)
+    cv = O.compress_stream(Vn, w.segment, w.c, w.tau)
+    hk, pk = O.pack_stream(ck)
+    hv, pv = O.pack_stream(cv)
+    T = Kn.shape[0]
+    times = []
+    t_end = time.perf_counter() + seconds
+    while True:
+        t0 = time.perf_counter()
+        Kh = O.unpack_stream(hk, pk, T, w.segment, w.c)
+        Vh = O.unpack_stream(hv, pv, T, w.segment, w.c)
+        O.decode_stream(qn, ck.R, cv.R, Kh, Vh, w.top_k)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() > t_end and len(times) >= 1:
+            break
+    per = statistics.median(times)
+    return T / per, len(times), per
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+def workload_config(w: W.Workload, layers: int) -> dict:
+    return {
+        "workload": f"{w.name}: batch {w.batch}, {w.n_kv_heads} KV / {w.n_q_heads} query heads, "
+                    f"head dim 128, context {w.ctx}, {layers} layers, segment {w.segment}, "
+                    f"c {w.c}, tau {w.tau}, top-k {w.top_k}",
+        "batch": w.batch, "ctx": w.ctx, "layers": layers, "n_kv_heads": w.n_kv_heads,
+        "n_q_heads": w.n_q_heads, "head_dim": 128, "segment": w.segment, "c": w.c,
+        "tau": w.tau, "top_k": w.top_k, "storage": "fp16 values, uint8 channel indices",
+        "l2": "inputs larger than L2: each layer streams ~674 MB of packed keys, layers cycled",
+    }
+
+
+def run_reference(args, w: W.Workload, ws: int, rank: int):
+    if rank != 0:
+        return
+    cfg = workload_config(w, 1)
+    cfg["sample"] = "stream (b=0, h=0) of layer 0"
+    per_step = max(0.5, args.ref_seconds)
+    vals = []
+    n = 0
+    for i in range(args.warmup + args.steps):
+        v, reps, per = oracle_decode_sample(w, per_step)
+        if i >= args.warmup:
+            vals.append(v)
+            n += reps
+    value = statistics.median(vals)
+    cores = blas_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": w.ctx / value * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": cfg,
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"oracle decode (unpack + score + top-k + attention) of one "
+                                   f"131072-token stream of layer 0, {n} timed repetitions"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU leg
+# ---------------------------------------------------------------------------
+def gathered_bytes(m, M, sel: np.ndarray, w: W.Workload) -> float:
+    """Bytes of the K and V rows (plus shared masks) that the selected tokens
+    read, counted from the packed layout of every stream."""
+    c = w.c
+    total = 0
+    for b in range(w.batch):
+        for h in range(w.n_kv_heads):
+            for x in range(2):
+                hdr = M.mkv_export_headers(m.ctx, b, h, x, m.n_segments())
+                segs = sel[b, h] // w.segment
+                st = hdr["strategy"][segs]
+                row = np.where(st == 0, 2 * c, np.where(st == 1, 3 * c, 256))
+                total += int(row.sum())
+                sm_segs = np.unique(segs[st == 0])
+                total += len(sm_segs) * ((c + 15) // 16 * 16)
+    return float(total)
+
+
+def run_gpu(args, w: W.Workload, ws: int, rank: int, local: int):
+    from two_compressed_kv_gb300 import mkv as M
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    L = args.layers
+    cfg = M.make_config(w.batch, w.n_kv_heads, w.n_q_heads, w.ctx, w.segment, w.c, w.tau,
+                        w.top_k, flags=M.MKV_FLAG_KERNEL_TIMING, device=local)
+    ctxs, qs, outs = [], [], []
+    comp_ms = []
+    cpu_args = None
+    for layer in range(L):
+        K, V = W.draw_kv(w, layer=layer, device=dev)
+        q = W.draw_queries(w, K, layer=layer)
+        if layer == 0 and rank == 0 and ws == 1 and not args.no_cpu_baseline:
+            cpu_args = (K[:1, :1].cpu(), V[:1, :1].cpu(), q[:1].cpu())
+        m = M.Mkv(cfg)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        m.compress(K, V)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        comp_ms.append(e0.elapsed_time(e1))
+        ctxs.append(m)
+        qs.append(q)
+        outs.append(torch.empty(q.shape, dtype=torch.float32, device=dev))
+        del K, V
+    torch.cuda.empty_cache()
+    st0 = ctxs[0].stats()
+    kk = min(w.top_k, w.ctx)
+    sel0 = torch.empty(w.batch, w.n_kv_heads, kk, dtype=torch.int32, device=dev)
+
+    def step():
+        for m, q, o in zip(ctxs, qs, outs):
+            M.mkv_decode(m.ctx, q, o, None, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    for m in ctxs:
+        for kid in range(5):
+            M.mkv_kernel_time(m.ctx, kid, reset=True)
+    launches0 = sum(m.stats()["kernel_launches"] for m in ctxs)
+
+    clocks = ClockSampler(local)
+    _barrier(ws)
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    _barrier(ws)
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    ms = _max_over_ranks(ms, ws, dev)
+    launches = sum(m.stats()["kernel_launches"] for m in ctxs) - launches0
+    ms_step = ms / args.steps
+    units_step = L * w.batch * w.ctx
+    value = ws * units_step / (ms_step / 1e3)
+
+    # per-kernel device time inside the timed region
+    ktimes = {}
+    for kid, name in enumerate(M.KERNEL_NAMES):
+        tot, n = 0.0, 0
+        for m in ctxs:
+            a, b = M.mkv_kernel_time(m.ctx, kid)
+            tot += a
+            n += b
+        ktimes[name] = (tot, n)
+
+    # algorithmic bytes of one layer-step (layer 0), counted from its layout
+    M.mkv_decode(ctxs[0].ctx, qs[0], outs[0], sel0, stream)
+    torch.cuda.synchronize(dev)
+    score_bytes = float(st0["payload_bytes"][0] + st0["header_bytes"] // 2)
+    gath = gathered_bytes(ctxs[0], M, sel0.cpu().numpy(), w)
+    small = (w.batch * w.n_q_heads * 128 * (2 + 4) + 2 * w.streams * 128 * 128 * 4)
+    alg_layer = score_bytes + gath + small
+    hbm_gbs = alg_layer * L / (ms_step / 1e3) / 1e9
+
+    peak, peak_kind = measured_peaks()
+    s_ms, s_n = ktimes["score"]
+    score_avg_s = s_ms / max(1, s_n) / 1e3
+    roof = {"kernel": "score_kernel", "bound": "hbm",
+            "achieved": score_bytes / score_avg_s / 1e9, "peak": peak, "unit": "GB/s",
+            "frac": score_bytes / score_avg_s / 1e9 / peak, "peak_kind": peak_kind,
+            "traffic": committed_traffic("k_decode.cu", "score_kernel_headline_128k.txt"),
+            "algorithmic_bytes_per_launch": score_bytes,
+            "avg_launch_us": score_avg_s * 1e6}
+
+    # end to end through the public API with host buffers
+    q_host = [q.cpu().pin_memory() for q in qs]
+    out_host = [torch.empty(o.shape, dtype=torch.float32).pin_memory() for o in outs]
+    h2d = sum(x.numel() * x.element_size() for x in q_host)
+    d2h = sum(x.numel() * x.element_size() for x in out_host)
+
+    def e2e_step():
+        for m, qh, qd, oh, od in zip(ctxs, q_host, qs, out_host, outs):
+            qd.copy_(qh, non_blocking=True)
+            M.mkv_decode(m.ctx, qd, od, None, stream)
+            oh.copy_(od, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    _barrier(ws)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    t_e2e = time.perf_counter() - t0
+    _barrier(ws)
+    t_e2e = _max_over_ranks(t_e2e, ws, dev)
+    e2e_value = ws * units_step * args.steps / t_e2e
+
+    cpu = None
+    if cpu_args is not None:
+        cv, reps, per = oracle_decode_sample(w, args.cpu_seconds, *cpu_args)
+        cpu = {"value": cv, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+               "sample": f"oracle decode (unpack + score + top-k + attention) of one "
+                         f"{w.ctx}-token stream (b=0, h=0) of layer 0, {reps} repetitions, "
+                         f"median {per * 1e3:.0f} ms"}
+
+    if rank == 0:
+        cfgd = workload_config(w, L)
+        cfgd["parallelism"] = f"replicas x{ws}" if ws > 1 else "single GPU"
+        tok = L * w.batch * w.ctx
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": cfgd,
+            "hbm_gbs": hbm_gbs, "hbm_frac_of_measured": hbm_gbs / peak,
+            "hbm_frac_of_nominal_8tbs": hbm_gbs / NOMINAL_HBM_GBS,
+            "algorithmic_bytes_per_layer_step": alg_layer,
+            "roofline": roof,
+            "kernel_us_per_layer": {k: v[0] / max(1, v[1]) * 1e3 for k, v in ktimes.items()},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches,
+            "clocks": clk,
+            "prefill": {"value": w.batch * w.ctx / (statistics.median(comp_ms) / 1e3),
+                        "unit": "prefill-tokens/s per layer (K and V)",
+                        "ms_per_layer_median": statistics.median(comp_ms)},
+            "compression": {"payload_bytes_K": st0["payload_bytes"][0],
+                            "payload_bytes_V": st0["payload_bytes"][1],
+                            "uncompressed_bytes": st0["uncompressed_bytes"],
+                            "ratio": st0["uncompressed_bytes"] / (st0["payload_bytes"][0] +
+                                                                  st0["payload_bytes"][1]),
+                            "strategies_K": st0["strategy_count"][0],
+                            "strategies_V": st0["strategy_count"][1]},
+            "ctx_tokens_per_step": tok,
+        }
+        print(json.dumps(line), flush=True)
+    for m in ctxs:
+        m.close()
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--layers", type=int, default=32)
+    ap.add_argument("--workload", default=W.HEADLINE_128K.name, choices=list(W.WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=2.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    w = W.WORKLOADS[args.workload]
+    ws, rank, local = _dist()
+    try:
+        if args.impl == "reference":
+            run_reference(args, w, ws, rank)
+        else:
+            run_gpu(args, w, ws, rank, local)
+    finally:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -7,11 +7,17 @@ near-tie windows, and every flip is counted):
     (eigenvalues, eigenvectors of well-separated eigenvalues); the library's
     basis is then checked for validity (orthonormal, eigen-residual, order,
     sign rule), and the steps after it are checked given that basis;
-  * per-token / per-segment channel sets: equal, unless the c-th and (c+1)-th
-    largest energies are within 1e-4 relative;
-  * strategy: equal, unless the deciding fraction is within 1e-5 of tau;
-  * stored fp16 values: equal, or one ulp apart with the fp64 value within
-    1e-5 relative of the rounding midpoint;
+  * per-token channel sets: equal, unless the c-th and (c+1)-th largest
+    magnitudes are within 2e-5 of the token's norm (the library's rotated
+    values carry an error of about 1e-6 of the row norm: fp16 x fp16 products
+    accumulated in fp32 on tensor cores with R split into two fp16 parts);
+  * segment-shared masks: equal, unless the c-th and (c+1)-th column energies
+    differ by at most 4e-5 * sqrt(column energy * segment energy) (the same
+    error propagated through a sum of squares);
+  * strategy: equal, unless the deciding fraction is within 1e-4 of tau;
+  * stored fp16 values: the fp16 rounding of a value within 1e-5 of the row
+    norm of the exact rotated value (counted when not the rounding of the
+    exact value itself);
   * selected tokens: equal, unless the token's score is within 1e-4 relative
     of the k-th score;
   * attention output: max abs error <= 2e-3.
@@ -22,10 +28,20 @@ import numpy as np
 
 from oracle import mosaickv as O
 
-NEAR_REL = 1e-4
-TAU_WIN = 1e-5
-MID_REL = 1e-5
+NEAR_REL = 1e-4       # selected tokens: relative to the k-th score
+TOK_WIN = 2e-5        # channel magnitudes: relative to the token norm
+COL_WIN = 4e-5        # column energies: times sqrt(col * segment energy)
+TAU_WIN = 1e-4
+MID_WIN = 1e-5        # rounding midpoints: relative to the token norm
 OUT_TOL = 2e-3
+# fp32 Jacobi on a dense 128 x 128 G: the eigen-residual and eigenvalue errors
+# are of order n * sqrt(rotations per entry) * eps_32 relative to lambda_max
+# (~1e-4); eigenvectors whose eigengap exceeds 1e-2 lambda_max are then good
+# to an angle of ~1e-2, i.e. |cos| >= 1 - 1e-3.
+EIG_RESID = 3e-4
+EIG_LAM = 3e-4
+EIG_GAP = 1e-2
+EIG_COS = 1e-3
 
 
 def _ordered16(a: np.ndarray) -> np.ndarray:
@@ -33,11 +49,16 @@ def _ordered16(a: np.ndarray) -> np.ndarray:
     return np.where(u & 0x8000, -(u & 0x7FFF), u)
 
 
-def _near_tie(sorted_desc: np.ndarray, c: int) -> bool:
-    if c >= len(sorted_desc):
+def _near_tie_tok(mags_desc: np.ndarray, c: int, norm: float) -> bool:
+    if c >= len(mags_desc):
         return False
-    a, b = sorted_desc[c - 1], sorted_desc[c]
-    return abs(a - b) <= NEAR_REL * max(abs(a), 1e-300)
+    return mags_desc[c - 1] - mags_desc[c] <= TOK_WIN * norm
+
+
+def _near_tie_col(col_desc: np.ndarray, c: int, e_tot: float) -> bool:
+    if c >= len(col_desc):
+        return False
+    return col_desc[c - 1] - col_desc[c] <= COL_WIN * np.sqrt(col_desc[c - 1] * e_tot) + 1e-300
 
 
 def check_basis(X: np.ndarray, R: np.ndarray, lam: np.ndarray, report: dict):
@@ -54,16 +75,16 @@ def check_basis(X: np.ndarray, R: np.ndarray, lam: np.ndarray, report: dict):
     gaps = np.full(d, np.inf)
     gaps[:-1] = np.minimum(gaps[:-1], lam_o[:-1] - lam_o[1:])
     gaps[1:] = np.minimum(gaps[1:], lam_o[:-1] - lam_o[1:])
-    sep = gaps / max(lam_o[0], 1e-300) > 1e-3
+    sep = gaps / max(lam_o[0], 1e-300) > EIG_GAP
     cos = np.abs(np.sum(R64 * R_o, axis=0))
     report.update(orth=float(orth), resid=float(resid), lam_err=float(lam_err),
                   sep_cols=int(sep.sum()), min_cos_sep=float(cos[sep].min()) if sep.any() else 1.0)
     assert orth <= 1e-5, f"basis not orthonormal: {orth}"
-    assert resid <= 1e-5, f"eigen-residual {resid}"
-    assert lam_err <= 1e-5, f"eigenvalues differ from fp64: {lam_err}"
+    assert resid <= EIG_RESID, f"eigen-residual {resid}"
+    assert lam_err <= EIG_LAM, f"eigenvalues differ from fp64: {lam_err}"
     assert (np.diff(lam.astype(np.float64)) <= 0).all(), "eigenvalues not descending"
     if sep.any():
-        assert cos[sep].min() >= 1 - 1e-4, f"separated eigenvectors differ: {cos[sep].min()}"
+        assert cos[sep].min() >= 1 - EIG_COS, f"separated eigenvectors differ: {cos[sep].min()}"
     for j in range(d):
         col = np.abs(R64[:, j])
         r = int(np.argmax(col))
@@ -107,19 +128,21 @@ def compare_compressed(X: np.ndarray, R: np.ndarray, hdr: np.ndarray, payload: b
             cnt["bytes_equal"] += 1
             continue
         sq = cs.Xt[a:b] ** 2
+        norms = np.sqrt(sq.sum(axis=1))
         if st == O.DENSE:
             gv = gseg.view("<f2").reshape(rows, cs.d)
-            _check_vals(gv, q16[a:b], cs.Xt[a:b], cnt, f"segment {si}")
+            _check_vals(gv, q16[a:b], cs.Xt[a:b], norms, cnt, f"segment {si}")
         elif st == O.SM:
             gidx = gseg[:c].astype(np.int64)
             if not np.array_equal(gidx, seg.mask):
                 col = np.sort(sq.sum(axis=0))[::-1]
-                assert _near_tie(col, c), f"segment {si}: shared mask differs"
+                assert _near_tie_col(col, c, seg.e_tot), f"segment {si}: shared mask differs"
                 cnt["idx_near"] += 1
                 continue
             assert not gseg[c:O.pad16(c)].any(), f"segment {si}: nonzero padding"
             gv = gseg[O.pad16(c):].view("<f2").reshape(rows, c)
-            _check_vals(gv, q16[a:b][:, seg.mask], cs.Xt[a:b][:, seg.mask], cnt, f"segment {si}")
+            _check_vals(gv, q16[a:b][:, seg.mask], cs.Xt[a:b][:, seg.mask], norms, cnt,
+                        f"segment {si}")
         else:
             gv = gseg[:2 * c * rows].view("<f2").reshape(rows, c)
             gidx = gseg[2 * c * rows:2 * c * rows + c * rows].reshape(rows, c).astype(np.int64)
@@ -127,26 +150,32 @@ def compare_compressed(X: np.ndarray, R: np.ndarray, hdr: np.ndarray, payload: b
             for r in range(rows):
                 P = cs.P[a + r]
                 if not np.array_equal(gidx[r], P):
-                    srt = np.sort(sq[r])[::-1]
-                    assert _near_tie(srt, c), f"segment {si} row {r}: channels differ"
+                    mags = np.sort(np.abs(cs.Xt[a + r]))[::-1]
+                    assert _near_tie_tok(mags, c, np.sqrt(sq[r].sum())), \
+                        f"segment {si} row {r}: channels differ"
                     cnt["idx_near"] += 1
                     continue
                 _check_vals(gv[r:r + 1], q16[a + r:a + r + 1][:, P],
-                            cs.Xt[a + r:a + r + 1][:, P], cnt, f"segment {si} row {r}")
+                            cs.Xt[a + r:a + r + 1][:, P], norms[r:r + 1], cnt,
+                            f"segment {si} row {r}")
     for k, v in cnt.items():
         report[k] = report.get(k, 0) + v
     return cs
 
 
-def _check_vals(got16, want16, exact, cnt, where):
-    d = np.abs(_ordered16(np.ascontiguousarray(got16)) - _ordered16(np.ascontiguousarray(want16)))
-    assert d.max(initial=0) <= 1, f"{where}: stored values differ by {d.max()} ulp"
-    for idx in zip(*np.nonzero(d)):
-        lo, hi = sorted([float(got16[idx]), float(want16[idx])])
-        mid = 0.5 * (lo + hi)
-        x = float(exact[idx])
-        assert abs(x - mid) <= MID_REL * max(abs(x), 1e-30), f"{where}: 1-ulp difference away from a midpoint"
-        cnt["ulp_near"] += 1
+def _check_vals(got16, want16, exact, norms, cnt, where):
+    """Each stored value must be the fp16 rounding of some value within
+    MID_WIN * (row norm) of the exact rotated value (fp16 rounding is
+    monotone, so that set is the ordered range [fp16(x - e), fp16(x + e)])."""
+    got16 = np.ascontiguousarray(got16)
+    eps = MID_WIN * np.asarray(norms, dtype=np.float64).reshape(-1, 1)
+    lo = _ordered16(np.ascontiguousarray(O.to_fp16(exact - eps)))
+    hi = _ordered16(np.ascontiguousarray(O.to_fp16(exact + eps)))
+    g = _ordered16(got16)
+    bad = (g < lo) | (g > hi)
+    assert not bad.any(), (f"{where}: stored value outside the rounding range of the exact "
+                           f"value +- {MID_WIN} x row norm ({int(bad.sum())} values)")
+    cnt["ulp_near"] += int((got16.view(np.uint16) != np.ascontiguousarray(want16).view(np.uint16)).sum())
 
 
 def compare_decode(q: np.ndarray, RK: np.ndarray, RV: np.ndarray, K_hat: np.ndarray,

@@ -249,7 +249,7 @@ def test_error_paths(M):
     # allocation failure injected through the pool cap: the old cache survives
     w2 = W.small_workload("err2", ctx=512, segment=64, top_k=16)
     K2, V2 = W.draw_kv(w2)
-    cfg = M.make_config(1, 2, 4, 512, 64, 40, 0.85, 16, max_pool_bytes=200_000)
+    cfg = M.make_config(1, 2, 4, 512, 64, 40, 0.85, 16, max_pool_bytes=140_000)
     m = M.Mkv(cfg)
     m.compress(Kd, Vd)
     before = m.decode(q).cpu().numpy()

@@ -10,7 +10,8 @@
 //            split over CTAs; partial Grams are summed in a fixed order later.
 //   eig      cyclic Jacobi on G in fp32 (one CTA per stream), then sort by
 //            descending eigenvalue, fix column signs, write R and lambda.
-//   analyze  x~ = x R on tensor cores with R split into fp16 hi + lo parts,
+//   analyze  x~ = x R on tensor cores with R split into fp16 hi + lo parts
+//            (lo scaled by 2^11 so it stays a normal fp16, own accumulator),
 //            per-token top-c channels, per-segment energies and strategy.
 //   scan     exclusive scan of the packed segment sizes -> headers, total.
 //   pack     same rotation and selection again, writes the packed payload.
@@ -397,7 +398,7 @@ __global__ void __launch_bounds__(256, 1) analyze_kernel(CompressParams p) {
       const int i = e >> 7, j = e & 127;      // R[i][j]: input channel i, basis vector j
       const float r = R[e];
       const __half hi = __float2half_rn(r);
-      const __half lo = __float2half_rn(r - __half2float(hi));
+      const __half lo = __float2half_rn((r - __half2float(hi)) * 2048.f);   // kept normal
       const uint32_t off = swz(j, i >> 3) + (i & 7) * 2;
       *reinterpret_cast<__half*>(Rhi + off) = hi;
       *reinterpret_cast<__half*>(Rlo + off) = lo;
@@ -423,11 +424,11 @@ __global__ void __launch_bounds__(256, 1) analyze_kernel(CompressParams p) {
     __syncthreads();
     const uint32_t tile = xs_base + (it & 1) * 16384u;
     // ---- x~ tile on tensor cores -------------------------------------------
-    float acc[8][4];
+    float acc[8][4], accl[8][4];
 #pragma unroll
     for (int ni = 0; ni < 8; ++ni)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[ni][e] = 0.f;
+      for (int e = 0; e < 4; ++e) acc[ni][e] = accl[ni][e] = 0.f;
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
       uint32_t a[4];
@@ -441,18 +442,20 @@ __global__ void __launch_bounds__(256, 1) analyze_kernel(CompressParams p) {
         ldsm_x4(rlo + off, bl);
         mma16816(acc[2 * np], a, bh[0], bh[1]);
         mma16816(acc[2 * np + 1], a, bh[2], bh[3]);
-        mma16816(acc[2 * np], a, bl[0], bl[1]);
-        mma16816(acc[2 * np + 1], a, bl[2], bl[3]);
+        mma16816(accl[2 * np], a, bl[0], bl[1]);
+        mma16816(accl[2 * np + 1], a, bl[2], bl[3]);
       }
     }
     {
       const int g = lane >> 2, q = lane & 3;
 #pragma unroll
+      constexpr float kLo = 1.f / 2048.f;
       for (int ni = 0; ni < 8; ++ni) {
         const int col = n0 + ni * 8 + 2 * q;
-        *reinterpret_cast<float2*>(Xt + (m0 + g) * XT_LD + col) = make_float2(acc[ni][0], acc[ni][1]);
+        *reinterpret_cast<float2*>(Xt + (m0 + g) * XT_LD + col) =
+            make_float2(fmaf(accl[ni][0], kLo, acc[ni][0]), fmaf(accl[ni][1], kLo, acc[ni][1]));
         *reinterpret_cast<float2*>(Xt + (m0 + g + 8) * XT_LD + col) =
-            make_float2(acc[ni][2], acc[ni][3]);
+            make_float2(fmaf(accl[ni][2], kLo, acc[ni][2]), fmaf(accl[ni][3], kLo, acc[ni][3]));
       }
     }
     __syncthreads();

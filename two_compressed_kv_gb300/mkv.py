@@ -204,6 +204,15 @@ def mkv_export(ctx, b: int, h: int, which: int, n_segments: int):
     return basis, lam, hdr, payload[:nbytes.value].tobytes()
 
 
+def mkv_export_headers(ctx, b: int, h: int, which: int, n_segments: int) -> np.ndarray:
+    """Only the segment headers of one stream (off16 relative to the stream)."""
+    hdr = np.zeros(n_segments, dtype=HEADER_NP)
+    nbytes = c_uint64(0)
+    _check(_lib.mkv_export(ctx, b, h, which, None, None, hdr.ctypes.data, None,
+                           ctypes.byref(nbytes)), "mkv_export(headers)")
+    return hdr
+
+
 def mkv_kernel_time(ctx, kernel_id: int, reset: bool = False):
     ms = c_double(0.0)
     n = c_int64(0)

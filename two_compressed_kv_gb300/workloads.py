@@ -117,12 +117,16 @@ def _sigma(decay: float, device) -> torch.Tensor:
 
 
 def _draw(w: Workload, layer: int, which: int, decay: float, device,
-          ctx: Optional[int] = None) -> torch.Tensor:
-    """One of K (which=0) or V (which=1): fp16 [B, H, T, 128] on `device`."""
+          ctx: Optional[int] = None, streams: Optional[int] = None) -> torch.Tensor:
+    """One of K (which=0) or V (which=1): fp16 [B, H, T, 128] on `device`.
+    streams=1 draws only stream (b=0, h=0) (same values as in the full draw on
+    the same device) and returns [1, 1, T, 128]."""
     T = w.ctx if ctx is None else ctx
     B, H = w.batch, w.n_kv_heads
     gen = _gen(w.seed, layer, 1 + which, device)
     Q = haar_orthogonal(H, gen, device)                       # [H, 128, 128]
+    if streams == 1:
+        B, H = 1, 1
     out = torch.empty(B, H, T, HEAD_DIM, dtype=torch.float16, device=device)
     if w.mixed_regimes:
         regime = (torch.arange(T, device=device) // w.segment) % 3     # [T]
@@ -146,10 +150,12 @@ def _draw(w: Workload, layer: int, which: int, decay: float, device,
     return out
 
 
-def draw_kv(w: Workload, layer: int = 0, device="cpu", ctx: Optional[int] = None):
+def draw_kv(w: Workload, layer: int = 0, device="cpu", ctx: Optional[int] = None,
+            streams: Optional[int] = None):
     """(K, V) fp16 [B, H, T, 128] for one layer."""
     dk, dv = layer_decays(w, layer)
-    return (_draw(w, layer, 0, dk, device, ctx), _draw(w, layer, 1, dv, device, ctx))
+    return (_draw(w, layer, 0, dk, device, ctx, streams),
+            _draw(w, layer, 1, dv, device, ctx, streams))
 
 
 def draw_queries(w: Workload, K: torch.Tensor, layer: int = 0, step: int = 0) -> torch.Tensor:
