@@ -111,7 +111,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -294,31 +294,70 @@ def run_gpu(args, w: W.Workload, ws: int, rank: int, local: int):
     sel0 = torch.empty(w.batch, w.n_kv_heads, kk, dtype=torch.int32, device=dev)
 
     def step():
+        # the binding launches on torch's current stream: the capture stream
+        # while a graph is being captured
         for m, q, o in zip(ctxs, qs, outs):
-            M.mkv_decode(m.ctx, q, o, None, stream)
+            M.mkv_decode(m.ctx, q, o, None, None)
 
-    for _ in range(args.warmup):
-        step()
+    # One CUDA graph per step (all layers): replays have no host launch gaps.
+    # Each graph owns its own timing events; the timed graphs are captured
+    # after the warm-up timers were reset, so every event pair is read only
+    # after the graph holding it has run.
+    def capture(n):
+        out = []
+        for _ in range(n):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                step()
+            out.append(g)
+        torch.cuda.synchronize(dev)
+        return out
+
+    l0 = sum(m.stats()["kernel_launches"] for m in ctxs)
+    step()
+    torch.cuda.synchronize(dev)
+    per_step_launches = sum(m.stats()["kernel_launches"] for m in ctxs) - l0
+    use_graph = not args.no_graph
+    warm = capture(args.warmup) if use_graph else []
+    for i in range(args.warmup):
+        warm[i].replay() if use_graph else step()
     torch.cuda.synchronize(dev)
     for m in ctxs:
         for kid in range(5):
             M.mkv_kernel_time(m.ctx, kid, reset=True)
+    timed = capture(args.steps) if use_graph else []
+    if use_graph:              # re-warm after the capture pause
+        timed[0].replay()
+        timed[min(1, args.steps - 1)].replay()
+        torch.cuda.synchronize(dev)
     launches0 = sum(m.stats()["kernel_launches"] for m in ctxs)
+
+    def run(i):
+        if use_graph:
+            timed[i].replay()
+        else:
+            step()
 
     clocks = ClockSampler(local)
     _barrier(ws)
     torch.cuda.synchronize(dev)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
-    for _ in range(args.steps):
-        step()
+    for i in range(args.steps):
+        run(i)
     ev1.record(stream)
     torch.cuda.synchronize(dev)
     _barrier(ws)
     clk = clocks.stop()
+    for m in ctxs:
+        if M.mkv_check_device(m.ctx) != M.MKV_OK:
+            raise RuntimeError("a device-side wait gave up during the timed region")
     ms = ev0.elapsed_time(ev1)
     ms = _max_over_ranks(ms, ws, dev)
-    launches = sum(m.stats()["kernel_launches"] for m in ctxs) - launches0
+    if use_graph:   # kernels are counted when captured: one step's worth per graph
+        launches = per_step_launches * args.steps
+    else:
+        launches = sum(m.stats()["kernel_launches"] for m in ctxs) - launches0
     ms_step = ms / args.steps
     units_step = L * w.batch * w.ctx
     value = ws * units_step / (ms_step / 1e3)
@@ -403,6 +442,7 @@ def run_gpu(args, w: W.Workload, ws: int, rank: int, local: int):
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": launches,
+            "cuda_graph": use_graph,
             "clocks": clk,
             "prefill": {"value": w.batch * w.ctx / (statistics.median(comp_ms) / 1e3),
                         "unit": "prefill-tokens/s per layer (K and V)",
@@ -424,7 +464,7 @@ def run_gpu(args, w: W.Workload, ws: int, rank: int, local: int):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--layers", type=int, default=32)
@@ -432,10 +472,15 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=2.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--batch", type=int, default=0, help="override the batch (profiling runs)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
     w = W.WORKLOADS[args.workload]
+    if args.batch:
+        import dataclasses
+        w = dataclasses.replace(w, batch=args.batch, name=f"{w.name}-batch{args.batch}")
     ws, rank, local = _dist()
     try:
         if args.impl == "reference":

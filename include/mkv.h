@@ -76,8 +76,10 @@ typedef struct {
   int32_t c;              /* kept channels per vector: 8..128, multiple of 8 */
   float tau;              /* retained-energy threshold, 0 < tau <= 1 */
   int32_t top_k;          /* tokens attended per KV head per step, >= 1 */
-  int32_t attn_chunk;     /* selected tokens per split-K attention block; 0 = auto,
-                             else 8..1024 and a multiple of 8 */
+  int32_t attn_chunk;     /* selected tokens per split-K attention block; 0 = auto
+                             (128), else 8..128 and a multiple of 8.  With
+                             g = Hq / H, ceil(min(top_k, max_ctx) / 128) * g must
+                             not exceed 12288 (mkv_create: MKV_ERR_INVALID_ARG) */
   uint64_t max_pool_bytes;/* cap on the packed cache of one ctx; 0 = no cap */
   uint32_t flags;         /* MKV_FLAG_* */
   int32_t device;         /* CUDA device ordinal */
@@ -111,7 +113,7 @@ typedef struct {
 enum {
   MKV_KERNEL_QROT = 0,
   MKV_KERNEL_SCORE = 1,
-  MKV_KERNEL_TOPK = 2,   /* the four radix-select / compaction launches together */
+  MKV_KERNEL_TOPK = 2,   /* the two selection launches together */
   MKV_KERNEL_ATTN = 3,
   MKV_KERNEL_MERGE = 4,
   MKV_KERNEL_COUNT = 5
@@ -188,6 +190,14 @@ mkv_status mkv_stats(const mkv_ctx* ctx, mkv_stats_t* out);
 mkv_status mkv_export(const mkv_ctx* ctx, int b, int h, int which, float* basis,
                       float* eigvals, mkv_segment_header* headers, void* payload,
                       uint64_t* payload_bytes);
+
+/* Waits for all work on the ctx's device, then reports whether a kernel of
+ * this ctx gave up a bounded device-side wait since the last check
+ * (MKV_ERR_TIMEOUT; the word is then cleared) or MKV_OK.  Kernels never spin
+ * without a bound: a wait that exceeds about two seconds sets the word,
+ * abandons the rest of its work (the outputs of that call are undefined) and
+ * returns. */
+mkv_status mkv_check_device(mkv_ctx* ctx);
 
 /* With MKV_FLAG_KERNEL_TIMING: total device time (ms) and launch count of one
  * decode kernel id since creation or the last reset (synchronous).  reset != 0

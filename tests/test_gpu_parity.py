@@ -201,7 +201,7 @@ def test_split_count_invariance(M):
     K, V = W.draw_kv(w)
     q = W.draw_queries(w, K)
     outs, sels = [], []
-    for ch in (8, 64, 1000 // 8 * 8, 1024):
+    for ch in (8, 64, 120, 128):
         m, out, sel = run_gpu(M, w, K, V, q, attn_chunk=ch)
         outs.append(out)
         sels.append(sel)
@@ -225,6 +225,7 @@ def test_determinism(M):
     # repeated decode on one ctx is bit-identical too
     o3 = m1.decode(q.to(DEV)).cpu().numpy()
     assert np.array_equal(o1, o3)
+    assert M.mkv_check_device(m1.ctx) == M.MKV_OK
     m1.close()
     m2.close()
 

@@ -117,15 +117,17 @@ def test_basis_invariants_random():
 
 
 def test_basis_recovers_generator_rotation():
-    """K = (Z*M) diag(sigma) Q_h: the leading right singular vectors are the
-    leading rows of Q_h (textbook PCA of a rotated diagonal covariance)."""
-    w = W.small_workload("pin", ctx=16384, n_kv_heads=1, n_q_heads=1)
+    """K = (Z*M) diag(sigma) Q_h: the leading right singular vectors span the
+    leading rows of Q_h (textbook PCA of a rotated diagonal covariance).  The
+    4-dimensional principal subspace is compared (single vectors can swap when
+    two sample eigenvalues are close)."""
+    w = W.small_workload("pin", ctx=65536, n_kv_heads=1, n_q_heads=1)
     K, _ = W.draw_kv(w)
-    gen = W._gen(w.seed, 0, 1, "cpu")
-    Q = W.haar_orthogonal(1, gen, "cpu")[0].double().numpy()
+    Q = W.haar_orthogonal(1, W._gen(w.seed, 0, 11, "cpu"))[0].double().numpy()
     _, R = O.basis(K[0, 0].numpy())
-    for j in range(3):
-        assert abs(float(R[:, j] @ Q[j])) >= 0.98, j
+    P = R[:, :4].T @ Q[:4].T
+    assert (P ** 2).sum() / 4 >= 0.98
+    assert abs(float(R[:, 0] @ Q[0])) >= 0.99
 
 
 # ---------------------------------------------------------------------------

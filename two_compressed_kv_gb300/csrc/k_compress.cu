@@ -448,8 +448,8 @@ __global__ void __launch_bounds__(256, 1) analyze_kernel(CompressParams p) {
     }
     {
       const int g = lane >> 2, q = lane & 3;
-#pragma unroll
       constexpr float kLo = 1.f / 2048.f;
+#pragma unroll
       for (int ni = 0; ni < 8; ++ni) {
         const int col = n0 + ni * 8 + 2 * q;
         *reinterpret_cast<float2*>(Xt + (m0 + g) * XT_LD + col) =

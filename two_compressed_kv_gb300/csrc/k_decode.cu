@@ -4,10 +4,13 @@
 // (prior-work paragraph) and attention computed on the packed dense format
 // with CUDA cores, without unpacking ("Observation & Method 2").
 //
-// Launch order per step: qrot -> score -> topk (4 launches) -> attn -> merge.
-// No kernel waits on another CTA; every cross-CTA combination is either an
-// integer atomic (histograms: order-independent) or a later launch.
+// Launch order per step: qrot -> score -> topk_pass2 -> topk_write -> attn -> merge.
+// No kernel waits on another CTA.  Cross-CTA results are combined with
+// integer atomics (order-independent), "last CTA finishes" tickets, or a
+// later launch; every floating-point sum runs in a fixed order, so a decode is
+// bit-for-bit repeatable.
 #include "mkv_internal.cuh"
+#include "ptx.cuh"
 
 namespace mkv {
 
@@ -23,541 +26,773 @@ __device__ __forceinline__ void h8_to_f(const uint4& raw, float v[8]) {
   const __half2* h = reinterpret_cast<const __half2*>(&raw);
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    float2 f = __half22float2(h[e]);
+    const float2 f = __half22float2(h[e]);
     v[2 * e] = f.x;
     v[2 * e + 1] = f.y;
   }
 }
 
+__device__ __forceinline__ int64_t clamp_t(int32_t t, int64_t T) {
+  return t < 0 ? 0 : (t >= T ? T - 1 : (int64_t)t);
+}
+
+// Block-wide (the first 256 threads compute; every thread must call it): the
+// bin of histogram h[NB] (shared memory) holding the krem-th largest key,
+// counting from the top bin, and how many keys of that bin are still needed.
+// Results land in res[0] (bin) and res[1] (remaining count).
+template <int NB>
+__device__ void find_bin(const uint32_t* h, uint32_t krem, uint32_t* res, uint32_t* sh_warp) {
+  constexpr int PER = NB / 256;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  uint32_t mine = 0, suf = 0;
+  if (t < 256) {
+#pragma unroll
+    for (int i = 0; i < PER; ++i) mine += h[t * PER + i];
+    suf = mine;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t o = __shfl_down_sync(0xffffffffu, suf, off);
+      if (lane + off < 32) suf += o;
+    }
+    if (lane == 0) sh_warp[warp] = suf;
+  }
+  __syncthreads();
+  if (t < 256) {
+    uint32_t above = 0;
+    for (int w = warp + 1; w < 8; ++w) above += sh_warp[w];
+    uint32_t running = above + (suf - mine);
+    for (int i = PER - 1; i >= 0; --i) {
+      const uint32_t c = h[t * PER + i];
+      if (running < krem && krem <= running + c) {
+        res[0] = (uint32_t)(t * PER + i);
+        res[1] = krem - running;
+      }
+      running += c;
+    }
+  }
+  __syncthreads();
+}
+
 // ---------------------------------------------------------------------------
-// qrot: q~_i = q_i R_K for the g query heads of a KV head; q_bar = sum_i q~_i.
-// Also clears the stream's selection histograms for this step.
-// grid: BH, block: 128 (thread j = output channel)
+// qrot: q~_i = q_i R_K for the g query heads of a KV head, q_bar = sum_i q~_i.
+// R_K is staged in shared memory with 16-byte loads.  Also clears the stream's
+// histogram, tickets and candidate counter for this step.
+// grid: BH, block: 512 (column j = tid % 128, heads tid / 128 + 4n), dynamic
+// smem 64 KB
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(128) qrot_kernel(DecodeParams p) {
+constexpr int QR_THREADS = 512;
+
+__global__ void __launch_bounds__(QR_THREADS) qrot_kernel(DecodeParams p) {
+  extern __shared__ __align__(16) float Rs[];   // [128][128]
+  __shared__ float qs[MAX_G][D];
+  __shared__ float psum[4][D];
   const int s = blockIdx.x;
   const int b = s / p.H, h = s % p.H;
-  const int j = threadIdx.x;
-  __shared__ float qs[MAX_G][D];
+  const int tid = threadIdx.x, j = tid & 127, hq = tid >> 7;
+  const float4* R4 = reinterpret_cast<const float4*>(p.RK + (size_t)s * D * D);
+  float4* Rs4 = reinterpret_cast<float4*>(Rs);
+#pragma unroll
+  for (int x = 0; x < D * D / 4 / QR_THREADS; ++x) Rs4[tid + x * QR_THREADS] = __ldg(R4 + tid + x * QR_THREADS);
   const __half* q = p.q + ((size_t)b * p.Hq + (size_t)h * p.g) * D;
-  for (int i = 0; i < p.g; ++i) qs[i][j] = __half2float(q[i * D + j]);
-  uint32_t* hist = p.hist + (size_t)s * HIST_WORDS;
-  for (int x = j; x < HIST_WORDS; x += 128) hist[x] = 0u;
-  __syncthreads();
-  const float* R = p.RK + (size_t)s * D * D;
-  float acc[MAX_G];
-#pragma unroll
-  for (int i = 0; i < MAX_G; ++i) acc[i] = 0.f;
-  for (int r = 0; r < D; ++r) {
-    const float rv = R[r * D + j];
-#pragma unroll
-    for (int i = 0; i < MAX_G; ++i)
-      if (i < p.g) acc[i] = fmaf(qs[i][r], rv, acc[i]);
+  for (int x = tid; x < p.g * D; x += QR_THREADS) qs[x / D][x % D] = __half2float(q[x]);
+  uint4* hz = reinterpret_cast<uint4*>(p.hist + (size_t)s * HIST1);
+  for (int x = tid; x < HIST1 / 4; x += QR_THREADS) hz[x] = make_uint4(0u, 0u, 0u, 0u);
+  if (tid == 0) {
+    p.tick1[s] = 0u;
+    p.tick2[s] = 0u;
+    p.cand_n[s] = 0u;
   }
-  float sum = 0.f;
+  __syncthreads();
   float* qt = p.qt + ((size_t)b * p.Hq + (size_t)h * p.g) * D;
-#pragma unroll
-  for (int i = 0; i < MAX_G; ++i) {
-    if (i < p.g) {
-      qt[i * D + j] = acc[i];
-      sum += acc[i];
-    }
+  float mine = 0.f;
+  for (int i = hq; i < p.g; i += 4) {
+    float acc = 0.f;
+#pragma unroll 8
+    for (int r = 0; r < D; ++r) acc = fmaf(qs[i][r], Rs[r * D + j], acc);
+    qt[i * D + j] = acc;
+    mine += acc;
   }
-  p.qbar[(size_t)s * D + j] = sum;
+  psum[hq][j] = mine;
+  __syncthreads();
+  if (tid < D) p.qbar[(size_t)s * D + j] = ((psum[0][j] + psum[1][j]) + psum[2][j]) + psum[3][j];
 }
 
 // ---------------------------------------------------------------------------
-// score: s_t = q_bar . k^_t for every cached token of a stream, read straight
-// from the packed segments with 16-byte loads.  A warp walks one segment at a
-// time; each lane owns one 16-byte chunk (8 channels) of a row, so a warp
-// covers floor(32 / chunks_per_row) consecutive rows per load and the bytes a
-// warp reads are contiguous.  Also builds the first radix histogram (key bits
-// 31..21) of the stream's scores.
-// grid: (ctas_per_stream, BH), block: 256
+// score: s_t = q_bar . k^_t for every cached token, straight from the packed
+// segments.  Persistent: CTA i streams the flattened K segments
+// [part[i], part[i+1]) (balanced by bytes at compression time).  One producer
+// warp moves runs of whole, contiguous segments into a ring of shared-memory
+// stages with bulk copies (L2 evict-first); 12 consumer warps score rows from
+// shared memory, one 16-byte chunk (8 channels) per lane, a row's chunks
+// summed in channel order by its first lane.  Scores go to global memory with
+// an L2 evict-last hint for the selection passes; the level-1 radix histogram
+// (key bits 31..20) is built on the way, and the CTA that finishes a stream
+// last turns it into the level-1 bin of the k-th largest score.
+// grid: G, block: 13 warps, dynamic smem n_stages * stage_bytes
 // ---------------------------------------------------------------------------
-constexpr int SCORE_WARPS = 8;
-constexpr int SCORE_UNROLL = 4;
+constexpr int SC_CONS = 12;
+constexpr int SC_THREADS = (SC_CONS + 1) * 32;
+constexpr int SC_NSLOT = 2;
+constexpr int SC_MAX_STAGES = 8;
+constexpr int SC_MAX_SEGS = 64;   // segments per stage
+constexpr int SC_STATIC_SMEM = SC_NSLOT * HIST1 * 4 + SC_NSLOT * D * 4 + SC_NSLOT * D * 32 * 4 +
+                               SC_CONS * D * 4 + SC_MAX_STAGES * SC_MAX_SEGS * 8 + 1024;
 
-template <int STRAT>
-__device__ __forceinline__ void score_segment(const uint8_t* base, int rows, int c, int lane,
-                                              const float* qb, const float* qrep,
-                                              const float* qm, float* out, uint32_t* hist) {
-  const int cpr = (STRAT == MKV_STRATEGY_DENSE) ? 16 : (c >> 3);   // 16-B chunks per row
-  const int rpi = 32 / cpr;                                          // rows per warp load
-  const int active = rpi * cpr;
-  const int my_row = lane / cpr;
-  const int my_chunk = lane - my_row * cpr;
-  const uint8_t* vals = base + ((STRAT == MKV_STRATEGY_SM) ? pad16((uint32_t)c) : 0u);
-  const uint8_t* idxs = base + 2u * (uint32_t)c * (uint32_t)rows;    // PV index block
-  for (int r0 = 0; r0 < rows; r0 += rpi * SCORE_UNROLL) {
-    uint4 raw[SCORE_UNROLL];
-    uint2 ix[SCORE_UNROLL];
-    bool ok[SCORE_UNROLL];
-#pragma unroll
-    for (int u = 0; u < SCORE_UNROLL; ++u) {
-      const int row = r0 + u * rpi + my_row;
-      ok[u] = (lane < active) && (row < rows);
-      const uint32_t chunk = (uint32_t)row * cpr + my_chunk;
-      if (ok[u]) {
-        raw[u] = __ldg(reinterpret_cast<const uint4*>(vals) + chunk);
-        if (STRAT == MKV_STRATEGY_PV) ix[u] = __ldg(reinterpret_cast<const uint2*>(idxs) + chunk);
-      } else {
-        raw[u] = make_uint4(0u, 0u, 0u, 0u);
-        ix[u] = make_uint2(0u, 0u);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < SCORE_UNROLL; ++u) {
-      float v[8];
-      h8_to_f(raw[u], v);
-      float part = 0.f;
-      if (STRAT == MKV_STRATEGY_PV) {
-        const uint32_t w0 = ix[u].x, w1 = ix[u].y;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const uint32_t ch = ((e < 4 ? w0 : w1) >> (8 * (e & 3))) & 0x7fu;
-          part = fmaf(v[e], qrep[ch * 32 + lane], part);
-        }
-      } else {
-        const float* qq = (STRAT == MKV_STRATEGY_SM ? qm : qb) + my_chunk * 8;
-        const float4 a = *reinterpret_cast<const float4*>(qq);
-        const float4 b = *reinterpret_cast<const float4*>(qq + 4);
-        part = fmaf(v[0], a.x, part);
-        part = fmaf(v[1], a.y, part);
-        part = fmaf(v[2], a.z, part);
-        part = fmaf(v[3], a.w, part);
-        part = fmaf(v[4], b.x, part);
-        part = fmaf(v[5], b.y, part);
-        part = fmaf(v[6], b.z, part);
-        part = fmaf(v[7], b.w, part);
-      }
-      // the row's leader (chunk 0) adds the row's chunks in channel order
-      float sum = part;
-      for (int off = 1; off < cpr; ++off) {
-        const float o = __shfl_down_sync(0xffffffffu, part, off);
-        if (my_chunk == 0) sum += o;
-      }
-      if (ok[u] && my_chunk == 0) {
-        const int row = r0 + u * rpi + my_row;
-        out[row] = sum;
-        atomicAdd(&hist[f2key(sum) >> 21], 1u);
-      }
-    }
-  }
+// header i of the flattened K segments as two words, or zeros past the end
+__device__ __forceinline__ uint2 load_hdr(const mkv_segment_header* h, int i, int end) {
+  return i < end ? __ldg(reinterpret_cast<const uint2*>(h) + i) : make_uint2(0u, 0u);
 }
 
-__global__ void __launch_bounds__(256) score_kernel(DecodeParams p) {
-  const int s = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __shared__ __align__(16) float qb[D];
-  __shared__ __align__(16) float qrep[D * 32];
-  __shared__ uint32_t hist[HIST1];
-  __shared__ __align__(16) float qm[SCORE_WARPS][D];
-  for (int x = threadIdx.x; x < D; x += blockDim.x) qb[x] = p.qbar[(size_t)s * D + x];
-  for (int x = threadIdx.x; x < HIST1; x += blockDim.x) hist[x] = 0u;
-  __syncthreads();
-  for (int x = threadIdx.x; x < D * 32; x += blockDim.x) qrep[x] = qb[x >> 5];
-  __syncthreads();
-
-  const int seg0 = blockIdx.x * p.score_segs_per_cta;
-  const int seg1 = min(p.n_seg, seg0 + p.score_segs_per_cta);
-  const mkv_segment_header* hdr = p.hdrK + (size_t)s * p.n_seg;
-  float* scores = p.scores + (size_t)s * p.T;
-  for (int sg = seg0 + warp; sg < seg1; sg += SCORE_WARPS) {
-    const mkv_segment_header hd = hdr[sg];
-    const uint8_t* base = p.pool + (size_t)hd.off16 * 16u;
-    float* out = scores + (int64_t)sg * p.S;
-    if (hd.strategy == MKV_STRATEGY_SM) {
-      for (int j = lane; j < p.c; j += 32) qm[warp][j] = qb[base[j] & 127];
-      __syncwarp();
-      score_segment<MKV_STRATEGY_SM>(base, hd.rows, p.c, lane, qb, qrep, qm[warp], out, hist);
-      __syncwarp();
-    } else if (hd.strategy == MKV_STRATEGY_PV) {
-      score_segment<MKV_STRATEGY_PV>(base, hd.rows, p.c, lane, qb, qrep, qm[warp], out, hist);
-    } else {
-      score_segment<MKV_STRATEGY_DENSE>(base, hd.rows, p.c, lane, qb, qrep, qm[warp], out, hist);
-    }
-  }
-  __syncthreads();
-  uint32_t* gh = p.hist + (size_t)s * HIST_WORDS;
-  for (int x = threadIdx.x; x < HIST1; x += blockDim.x)
-    if (hist[x]) atomicAdd(&gh[x], hist[x]);
-}
-
-// ---------------------------------------------------------------------------
-// Top-k selection: exact radix select on the ordered keys of the fp32 scores,
-// 11 + 11 + 10 bits, ties to the lower token index, output in ascending
-// token order.  Each launch re-derives the digits chosen so far from the
-// (complete) histograms of the earlier levels.
-// ---------------------------------------------------------------------------
-constexpr int TK_THREADS = 256;
-
-// Block-wide: the bin holding the krem-th largest key of histogram h[nbins]
-// (counting from the top), and how many keys of that bin are still needed.
-__device__ void find_bin(const uint32_t* h, int nbins, uint32_t krem, uint32_t* out_bin,
-                         uint32_t* out_krem, uint32_t* sh_warp) {
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const int per = nbins / TK_THREADS;
-  const int lo = t * per;
-  uint32_t mine = 0;
-  for (int i = 0; i < per; ++i) mine += h[lo + i];
-  // suffix sum over threads (higher thread = higher bins): inclusive within warp
-  uint32_t suf = mine;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const uint32_t o = __shfl_down_sync(0xffffffffu, suf, off);
-    if (lane + off < 32) suf += o;
-  }
-  if (lane == 0) sh_warp[warp] = suf;     // warp total
-  __syncthreads();
-  uint32_t above_warps = 0;
-  for (int w = warp + 1; w < TK_THREADS / 32; ++w) above_warps += sh_warp[w];
-  uint32_t running = above_warps + (suf - mine);   // keys in bins above this thread's
-  for (int i = per - 1; i >= 0; --i) {
-    const uint32_t c = h[lo + i];
-    if (running < krem && krem <= running + c) {
-      *out_bin = (uint32_t)(lo + i);
-      *out_krem = krem - running;
-    }
-    running += c;
-  }
-  __syncthreads();
-}
-
-// Digits chosen by the levels before `level` (1-based); fills pre[] and krem.
-struct Sel {
-  uint32_t b1, b2, b3, k1, k2, k3;
+struct StageMeta {
+  int32_t seg0, seg1;
+  uint64_t byte0;
 };
 
-__device__ void resolve(const uint32_t* gh, int levels, uint32_t kk, Sel* sel) {
-  __shared__ uint32_t sh_warp[TK_THREADS / 32];
-  __shared__ uint32_t hs[HIST1];
-  __shared__ Sel r;
-  if (threadIdx.x == 0) r = Sel{0u, 0u, 0u, 1u, 1u, 1u};
-  for (int x = threadIdx.x; x < HIST1; x += TK_THREADS) hs[x] = gh[x];
-  __syncthreads();
-  find_bin(hs, HIST1, kk, &r.b1, &r.k1, sh_warp);
-  if (levels >= 2) {
-    for (int x = threadIdx.x; x < HIST2; x += TK_THREADS) hs[x] = gh[HIST1 + x];
-    __syncthreads();
-    find_bin(hs, HIST2, r.k1, &r.b2, &r.k2, sh_warp);
-  }
-  if (levels >= 3) {
-    for (int x = threadIdx.x; x < HIST3; x += TK_THREADS) hs[x] = gh[HIST1 + HIST2 + x];
-    __syncthreads();
-    find_bin(hs, HIST3, r.k2, &r.b3, &r.k3, sh_warp);
-  }
-  *sel = r;
-  __syncthreads();
-}
-
-// level 2 or 3 histogram of the keys that match the digits chosen so far
-template <int LEVEL>
-__global__ void __launch_bounds__(TK_THREADS) topk_hist_kernel(DecodeParams p) {
-  const int s = blockIdx.y;
-  __shared__ uint32_t hl[HIST2];
-  uint32_t* gh = p.hist + (size_t)s * HIST_WORDS;
-  Sel r;
-  resolve(gh, LEVEL - 1, (uint32_t)p.kk, &r);
-  const int nb = LEVEL == 2 ? HIST2 : HIST3;
-  for (int x = threadIdx.x; x < nb; x += TK_THREADS) hl[x] = 0u;
-  __syncthreads();
-  const int64_t t0 = (int64_t)blockIdx.x * TOPK_CHUNK;
-  const int64_t t1 = imin64(p.T, t0 + TOPK_CHUNK);
-  const float* sc = p.scores + (size_t)s * p.T;
-  for (int64_t t = t0 + threadIdx.x; t < t1; t += TK_THREADS) {
-    const uint32_t key = f2key(sc[t]);
-    if (LEVEL == 2) {
-      if ((key >> 21) == r.b1) atomicAdd(&hl[(key >> 10) & 2047u], 1u);
+// Dot product of one packed row with q_bar, from shared memory; one row per
+// thread.  The 16-byte chunks of the row are visited in an order rotated by
+// the lane, so that lanes reading rows a multiple of 128 B apart hit different
+// banks; q_bar values come from the segment's gathered mask (SM), a
+// bank-replicated table indexed by channel (PV) or q_bar itself (dense).
+template <int STRAT>
+__device__ __forceinline__ float row_dot(const uint8_t* base, int rows, int row, int c, int lane,
+                                         const float* qsrc, const float* qm, const float* qrep) {
+  const int cpr = (STRAT == MKV_STRATEGY_DENSE) ? 16 : (c >> 3);
+  const uint32_t uc = (uint32_t)c;
+  const uint8_t* rowp =
+      (STRAT == MKV_STRATEGY_SM) ? base + pad16(uc) + 2u * uc * row
+      : (STRAT == MKV_STRATEGY_PV) ? base + 2u * uc * row : base + 256u * row;
+  const uint8_t* idxp = base + 2u * uc * (uint32_t)rows + uc * (uint32_t)row;
+  float acc = 0.f;
+  int k = lane % cpr;
+  for (int j = 0; j < cpr; ++j) {
+    float v[8];
+    h8_to_f(*reinterpret_cast<const uint4*>(rowp + 16 * k), v);
+    if (STRAT == MKV_STRATEGY_PV) {
+      const uint2 ix = *reinterpret_cast<const uint2*>(idxp + 8 * k);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t ch = ((e < 4 ? ix.x : ix.y) >> (8 * (e & 3))) & 0x7fu;
+        acc = fmaf(v[e], qrep ? qrep[ch * 32 + lane] : qsrc[ch], acc);
+      }
     } else {
-      if ((key >> 10) == ((r.b1 << 11) | r.b2)) atomicAdd(&hl[key & 1023u], 1u);
+      const float* qq = (STRAT == MKV_STRATEGY_SM ? qm : qsrc) + 8 * k;
+      const float4 a = *reinterpret_cast<const float4*>(qq);
+      const float4 b = *reinterpret_cast<const float4*>(qq + 4);
+      acc = fmaf(v[0], a.x, acc);
+      acc = fmaf(v[1], a.y, acc);
+      acc = fmaf(v[2], a.z, acc);
+      acc = fmaf(v[3], a.w, acc);
+      acc = fmaf(v[4], b.x, acc);
+      acc = fmaf(v[5], b.y, acc);
+      acc = fmaf(v[6], b.z, acc);
+      acc = fmaf(v[7], b.w, acc);
     }
+    k = (k + 1 == cpr) ? 0 : k + 1;
   }
-  __syncthreads();
-  uint32_t* dst = gh + (LEVEL == 2 ? HIST1 : HIST1 + HIST2);
-  for (int x = threadIdx.x; x < nb; x += TK_THREADS)
-    if (hl[x]) atomicAdd(&dst[x], hl[x]);
+  return acc;
 }
 
-// per chunk: keys above the threshold and keys equal to it
-__global__ void __launch_bounds__(TK_THREADS) topk_count_kernel(DecodeParams p) {
-  const int s = blockIdx.y;
-  Sel r;
-  resolve(p.hist + (size_t)s * HIST_WORDS, 3, (uint32_t)p.kk, &r);
-  const uint32_t thr = (r.b1 << 21) | (r.b2 << 10) | r.b3;
-  const int64_t t0 = (int64_t)blockIdx.x * TOPK_CHUNK;
-  const int64_t t1 = imin64(p.T, t0 + TOPK_CHUNK);
-  const float* sc = p.scores + (size_t)s * p.T;
-  int gt = 0, eq = 0;
-  for (int64_t t = t0 + threadIdx.x; t < t1; t += TK_THREADS) {
-    const uint32_t key = f2key(sc[t]);
-    gt += key > thr;
-    eq += key == thr;
-  }
-  __shared__ int sg[TK_THREADS / 32], se[TK_THREADS / 32];
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    gt += __shfl_xor_sync(0xffffffffu, gt, off);
-    eq += __shfl_xor_sync(0xffffffffu, eq, off);
-  }
-  if ((threadIdx.x & 31) == 0) {
-    sg[threadIdx.x >> 5] = gt;
-    se[threadIdx.x >> 5] = eq;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int G = 0, E = 0;
-    for (int w = 0; w < TK_THREADS / 32; ++w) {
-      G += sg[w];
-      E += se[w];
-    }
-    p.cnt[(size_t)s * p.topk_chunks + blockIdx.x] = make_int2(G, E);
-    if (blockIdx.x == 0) p.res[s] = make_int2((int)thr, (int)r.k3);
-  }
-}
+__global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
+  extern __shared__ __align__(128) uint8_t stage_mem[];
+  __shared__ uint64_t full_bar[SC_MAX_STAGES], empty_bar[SC_MAX_STAGES];
+  __shared__ StageMeta meta[SC_MAX_STAGES];
+  __shared__ uint2 shdr[SC_MAX_STAGES][SC_MAX_SEGS];   // headers of each stage's segments
+  __shared__ __align__(16) float qb[SC_NSLOT][D];
+  __shared__ float qrep[SC_NSLOT][D * 32];   // qrep[.][ch * 32 + lane] = q_bar[ch]
+  __shared__ uint32_t hist[SC_NSLOT][HIST1];
+  __shared__ __align__(16) float qm[SC_CONS][D];
+  __shared__ uint32_t sh_warp[8], sh_res[2];
+  __shared__ int sh_flag, sh_issued, sh_consumed;
 
-// writes the selected token ids in ascending order
-__global__ void __launch_bounds__(TK_THREADS) topk_write_kernel(DecodeParams p) {
-  const int s = blockIdx.y;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int2 rs = p.res[s];
-  const uint32_t thr = (uint32_t)rs.x;
-  const int need_eq = rs.y;
-  __shared__ int sh[2][TK_THREADS / 32];
-  __shared__ int before[2];
-  // keys above / equal to the threshold in all earlier chunks of the stream
-  int gb = 0, eb = 0;
-  for (int c = tid; c < (int)blockIdx.x; c += TK_THREADS) {
-    const int2 v = p.cnt[(size_t)s * p.topk_chunks + c];
-    gb += v.x;
-    eb += v.y;
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    gb += __shfl_xor_sync(0xffffffffu, gb, off);
-    eb += __shfl_xor_sync(0xffffffffu, eb, off);
-  }
-  if (lane == 0) {
-    sh[0][warp] = gb;
-    sh[1][warp] = eb;
+  const int a = p.part[blockIdx.x], b = p.part[blockIdx.x + 1];
+  if (a >= b) return;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int s_first = a / p.n_seg, s_last = (b - 1) / p.n_seg;
+  const int NST = p.n_stages;
+  for (int x = tid; x < SC_NSLOT * HIST1; x += SC_THREADS) (&hist[0][0])[x] = 0u;
+  for (int x = tid; x < SC_NSLOT * D; x += SC_THREADS) {
+    const int s = s_first + x / D;
+    (&qb[0][0])[x] = (s <= s_last) ? p.qbar[(size_t)s * D + (x % D)] : 0.f;
   }
   __syncthreads();
+  for (int x = tid; x < SC_NSLOT * D * 32; x += SC_THREADS) (&qrep[0][0])[x] = (&qb[0][0])[x >> 5];
   if (tid == 0) {
-    int G = 0, E = 0;
-    for (int w = 0; w < TK_THREADS / 32; ++w) {
-      G += sh[0][w];
-      E += sh[1][w];
+    for (int st = 0; st < NST; ++st) {
+      mbar_init(&full_bar[st], 1);
+      mbar_init(&empty_bar[st], SC_CONS);
     }
-    before[0] = G;
-    before[1] = E;
+    mbar_init_fence();
+    sh_issued = 0;
+    sh_consumed = 0;
   }
   __syncthreads();
-  // each thread owns TOPK_CHUNK / TK_THREADS consecutive tokens
-  constexpr int PER = TOPK_CHUNK / TK_THREADS;
-  const int64_t t0 = (int64_t)blockIdx.x * TOPK_CHUNK + (int64_t)tid * PER;
-  const float* sc = p.scores + (size_t)s * p.T;
-  uint32_t keys[PER];
-  int lg = 0, le = 0;
-#pragma unroll
-  for (int i = 0; i < PER; ++i) {
-    const int64_t t = t0 + i;
-    keys[i] = (t < p.T) ? f2key(sc[t]) : 0u;
-    const bool valid = t < p.T;
-    lg += valid && keys[i] > thr;
-    le += valid && keys[i] == thr;
+
+  if (warp == SC_CONS) {
+    // ---- producer warp --------------------------------------------------------
+    // Headers come in batches of 32 (one per lane), the next batch already in
+    // flight, so grouping segments into stages never waits on a dependent load.
+    const uint64_t pol = policy_evict_first();
+    int sg = a, k = 0;
+    bool ok = true;
+    int cur_base = a;
+    uint2 cur = load_hdr(p.hdrK, a + lane, b);
+    uint2 nxt = load_hdr(p.hdrK, a + 32 + lane, b);
+    while (true) {
+      const int slot = k % NST, use = k / NST;
+      if (use > 0) {
+        bool got = true;
+        if (lane == 0) got = mbar_wait(&empty_bar[slot], (use - 1) & 1);
+        if (!__shfl_sync(0xffffffffu, (int)got, 0)) {
+          ok = false;
+          break;
+        }
+      }
+      if (sg >= b) {            // end marker: a phase with no bytes
+        if (lane == 0) {
+          meta[slot].seg0 = -1;
+          mbar_arrive(&full_bar[slot]);
+        }
+        ++k;
+        break;
+      }
+      uint64_t off0 = 0, end = 0;
+      int e = sg, nseg = 0;
+      while (e < b && nseg < SC_MAX_SEGS) {
+        if (e >= cur_base + 32) {
+          cur = nxt;
+          cur_base += 32;
+          nxt = load_hdr(p.hdrK, cur_base + 32 + lane, b);
+        }
+        uint2 w;
+        w.x = __shfl_sync(0xffffffffu, cur.x, e - cur_base);
+        w.y = __shfl_sync(0xffffffffu, cur.y, e - cur_base);
+        const mkv_segment_header hd = *reinterpret_cast<const mkv_segment_header*>(&w);
+        const uint64_t st = (uint64_t)hd.off16 * 16u;
+        const uint64_t se = st + segment_bytes(hd.strategy, hd.rows, p.c);
+        if (nseg == 0) off0 = st;
+        if (nseg > 0 && se - off0 > (uint64_t)p.stage_bytes) break;
+        if (lane == 0) shdr[slot][nseg] = w;
+        end = se;
+        ++e;
+        ++nseg;
+      }
+      if (lane == 0) {
+        meta[slot].seg0 = sg;
+        meta[slot].seg1 = e;
+        meta[slot].byte0 = off0;
+        fence_proxy_async();
+        mbar_arrive_expect_tx(&full_bar[slot], (uint32_t)(end - off0));
+        bulk_g2s(stage_mem + (size_t)slot * p.stage_bytes, p.pool + off0, (uint32_t)(end - off0),
+                 &full_bar[slot], pol);
+      }
+      sg = e;
+      ++k;
+    }
+    if (lane == 0) {
+      if (!ok) atomicExch(p.err, DEV_ERR_TIMEOUT);
+      sh_issued = k;
+    }
+    __syncwarp();
+  } else {
+    // ---- consumers ----------------------------------------------------------
+    const uint64_t pol = policy_evict_last();
+    int k = 0, last_sm = -1;
+    while (true) {
+      const int slot = k % NST, use = k / NST;
+      const bool got = __all_sync(0xffffffffu, mbar_wait(&full_bar[slot], use & 1));
+      if (!got) {
+        if (lane == 0) atomicExch(p.err, DEV_ERR_TIMEOUT);
+        break;
+      }
+      const StageMeta m = meta[slot];
+      if (m.seg0 < 0) {
+        ++k;
+        break;
+      }
+      const uint8_t* sbase = stage_mem + (size_t)slot * p.stage_bytes;
+      int item = 0;
+      for (int sg = m.seg0; sg < m.seg1; ++sg) {
+        const uint2 hw = shdr[slot][sg - m.seg0];
+        const mkv_segment_header hd = *reinterpret_cast<const mkv_segment_header*>(&hw);
+        const int rows = hd.rows, strat = hd.strategy;
+        const int nblk = (rows + 31) >> 5;
+        const int first = ((warp - item) % SC_CONS + SC_CONS) % SC_CONS;
+        if (first < nblk) {
+          const uint8_t* base = sbase + ((uint64_t)hd.off16 * 16u - m.byte0);
+          const int s = sg / p.n_seg;
+          const int sl = s - s_first;
+          const float* qsrc = sl < SC_NSLOT ? qb[sl] : p.qbar + (size_t)s * D;
+          const float* qr = sl < SC_NSLOT ? qrep[sl] : nullptr;
+          uint32_t* hs = sl < SC_NSLOT ? hist[sl] : p.hist + (size_t)s * HIST1;
+          float* out = p.scores + (size_t)s * p.Tp + (int64_t)(sg - s * p.n_seg) * p.S;
+          if (strat == MKV_STRATEGY_SM && last_sm != sg) {
+            __syncwarp();
+            for (int jj = lane; jj < p.c; jj += 32) qm[warp][jj] = qsrc[base[jj] & 127];
+            __syncwarp();
+            last_sm = sg;
+          }
+          for (int blk = first; blk < nblk; blk += SC_CONS) {
+            const int row = blk * 32 + lane;
+            if (row < rows) {
+              float sc;
+              if (strat == MKV_STRATEGY_SM)
+                sc = row_dot<MKV_STRATEGY_SM>(base, rows, row, p.c, lane, qsrc, qm[warp], qr);
+              else if (strat == MKV_STRATEGY_PV)
+                sc = row_dot<MKV_STRATEGY_PV>(base, rows, row, p.c, lane, qsrc, qm[warp], qr);
+              else
+                sc = row_dot<MKV_STRATEGY_DENSE>(base, rows, row, p.c, lane, qsrc, qm[warp], qr);
+              st_f32_hint(out + row, sc, pol);
+              atomicAdd(&hs[f2key(sc) >> 20], 1u);
+            }
+          }
+        }
+        item += nblk;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[slot]);
+      ++k;
+    }
+    if (warp == 0 && lane == 0) sh_consumed = k;
   }
-  // exclusive scan of the packed (gt, eq) counts over the block
-  uint32_t v = (uint32_t)lg | ((uint32_t)le << 16);
+  __syncthreads();
+  // after a timeout, wait (bounded) for copies still landing in shared memory
+  if (tid == 0) {
+    for (int k = sh_consumed; k < sh_issued; ++k) mbar_wait(&full_bar[k % NST], (k / NST) & 1);
+  }
+  __syncthreads();
+  // ---- level-1 histogram: merge into the stream's global histogram ----------
+  for (int sl = 0; sl < SC_NSLOT; ++sl) {
+    const int s = s_first + sl;
+    if (s > s_last) break;
+    uint32_t* gh = p.hist + (size_t)s * HIST1;
+    for (int x = tid; x < HIST1; x += SC_THREADS)
+      if (hist[sl][x]) atomicAdd(&gh[x], hist[sl][x]);
+  }
+  __threadfence();
+  __syncthreads();
+  for (int s = s_first; s <= s_last; ++s) {
+    if (tid == 0) sh_flag = (atomicAdd(&p.tick1[s], 1u) == (uint32_t)p.cta_cnt[s] - 1u);
+    __syncthreads();
+    if (sh_flag) {
+      __threadfence();
+      uint32_t* h = &hist[0][0];
+      for (int x = tid; x < HIST1; x += SC_THREADS) h[x] = __ldcg(&p.hist[(size_t)s * HIST1 + x]);
+      __syncthreads();
+      find_bin<HIST1>(h, (uint32_t)p.kk, sh_res, sh_warp);
+      if (tid == 0) {
+        p.state[s].b1 = sh_res[0];
+        p.state[s].k1 = sh_res[1];
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// topk_pass2: per 4096-token chunk, counts the tokens whose key lies above
+// the level-1 bin (all selected) and appends the tokens of that bin to the
+// stream's candidate list.  The CTA that finishes a stream last selects
+// exactly among the candidates (keys by two more radix digits, then equal
+// keys by lowest token index), then turns the per-chunk counts into output
+// offsets.
+// grid: (topk_chunks, BH), block 256, 16 tokens per thread
+// ---------------------------------------------------------------------------
+constexpr int TK_THREADS = 256;
+constexpr int TK_PER = TOPK_CHUNK / TK_THREADS;   // 16
+
+__device__ __forceinline__ void load16(const float* sc, int64_t t0, int64_t T, float v[TK_PER],
+                                       bool hint_first, uint64_t pol) {
+  if (t0 + TK_PER <= T) {
+#pragma unroll
+    for (int i = 0; i < TK_PER / 4; ++i) {
+      const float4 f = hint_first ? ld_f4_hint(sc + t0 + 4 * i, pol)
+                                  : __ldcg(reinterpret_cast<const float4*>(sc + t0) + i);
+      v[4 * i] = f.x;
+      v[4 * i + 1] = f.y;
+      v[4 * i + 2] = f.z;
+      v[4 * i + 3] = f.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < TK_PER; ++i) v[i] = (t0 + i < T) ? __ldcg(sc + t0 + i) : 0.f;
+  }
+}
+
+// exclusive scan of one value per thread over the block (TK_THREADS threads)
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* sh, uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t inc = v;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
     const uint32_t o = __shfl_up_sync(0xffffffffu, inc, off);
     if (lane >= off) inc += o;
   }
-  __shared__ uint32_t wsum[TK_THREADS / 32];
-  if (lane == 31) wsum[warp] = inc;
+  if (lane == 31) sh[warp] = inc;
   __syncthreads();
-  uint32_t wbefore = 0;
-  for (int w = 0; w < warp; ++w) wbefore += wsum[w];
-  const uint32_t excl = wbefore + inc - v;
-  int g_prior = before[0] + (int)(excl & 0xffffu);
-  int e_prior = before[1] + (int)(excl >> 16);
+  uint32_t before = 0, all = 0;
+  for (int w = 0; w < TK_THREADS / 32; ++w) {
+    if (w < warp) before += sh[w];
+    all += sh[w];
+  }
+  __syncthreads();
+  if (total) *total = all;
+  return before + inc - v;
+}
+
+__global__ void __launch_bounds__(TK_THREADS) topk_pass2_kernel(DecodeParams p) {
+  const int s = blockIdx.y, ch = blockIdx.x, tid = threadIdx.x;
+  __shared__ uint32_t sh_scan[TK_THREADS / 32], sh_warp[8], sh_res[2];
+  __shared__ uint32_t hbuf[2048];
+  __shared__ int sh_last;
+  __shared__ uint32_t sh_base;
+  const uint32_t b1 = p.state[s].b1;
+  const int64_t t0 = (int64_t)ch * TOPK_CHUNK + (int64_t)tid * TK_PER;
+  const float* sc = p.scores + (size_t)s * p.Tp;
+  float v[TK_PER];
+  load16(sc, t0, p.T, v, false, 0);
+  uint32_t sure = 0, ncand = 0, keys[TK_PER];
+#pragma unroll
+  for (int i = 0; i < TK_PER; ++i) {
+    keys[i] = f2key(v[i]);
+    const bool valid = t0 + i < p.T;
+    const uint32_t bin = keys[i] >> 20;
+    sure += valid && bin > b1;
+    ncand += valid && bin == b1;
+  }
+  uint32_t sure_all, ncand_all;
+  block_excl_scan(sure, sh_scan, &sure_all);
+  const uint32_t my_off = block_excl_scan(ncand, sh_scan, &ncand_all);
+  if (tid == 0) {
+    p.cnt[(size_t)s * p.topk_chunks + ch] = (int32_t)sure_all;
+    sh_base = ncand_all ? atomicAdd(&p.cand_n[s], ncand_all) : 0u;
+  }
+  __syncthreads();
+  uint2* cand = p.cand + (size_t)s * p.Tp;
+  uint32_t pos = sh_base + my_off;
+#pragma unroll
+  for (int i = 0; i < TK_PER; ++i) {
+    if (t0 + i < p.T && (keys[i] >> 20) == b1) cand[pos++] = make_uint2(keys[i], (uint32_t)(t0 + i));
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) sh_last = (atomicAdd(&p.tick2[s], 1u) == gridDim.x - 1u);
+  __syncthreads();
+  if (!sh_last) return;
+  __threadfence();
+
+  // ---- last CTA of the stream: exact threshold among the candidates --------
+  const uint32_t N = __ldcg(&p.cand_n[s]);
+  const uint32_t need = p.state[s].k1;
+  // key bits 19..10
+  for (int x = tid; x < 1024; x += TK_THREADS) hbuf[x] = 0u;
+  __syncthreads();
+  for (uint32_t i = tid; i < N; i += TK_THREADS) atomicAdd(&hbuf[(__ldcg(&cand[i].x) >> 10) & 1023u], 1u);
+  __syncthreads();
+  find_bin<1024>(hbuf, need, sh_res, sh_warp);
+  const uint32_t bA = sh_res[0], needA = sh_res[1];
+  // key bits 9..0 among keys in bin bA
+  for (int x = tid; x < 1024; x += TK_THREADS) hbuf[x] = 0u;
+  __syncthreads();
+  for (uint32_t i = tid; i < N; i += TK_THREADS) {
+    const uint32_t key = __ldcg(&cand[i].x);
+    if (((key >> 10) & 1023u) == bA) atomicAdd(&hbuf[key & 1023u], 1u);
+  }
+  __syncthreads();
+  find_bin<1024>(hbuf, needA, sh_res, sh_warp);
+  const uint32_t bB = sh_res[0], need_eq = sh_res[1];
+  const uint32_t n_eq = hbuf[bB];
+  const uint32_t thr = (b1 << 20) | (bA << 10) | bB;
+  __syncthreads();
+  int32_t t_cut = 0x7fffffff;
+  if (need_eq < n_eq) {
+    // the need_eq lowest token indices among keys equal to thr: radix select
+    // on u = 0x7fffffff - t (largest u = lowest t), bits 30..20, 19..10, 9..0
+    uint32_t prefix = 0, krem = need_eq;
+    for (int lev = 0; lev < 3; ++lev) {
+      const int nb = lev == 0 ? 2048 : 1024;
+      const int shift = lev == 0 ? 20 : (lev == 1 ? 10 : 0);
+      for (int x = tid; x < nb; x += TK_THREADS) hbuf[x] = 0u;
+      __syncthreads();
+      for (uint32_t i = tid; i < N; i += TK_THREADS) {
+        const uint2 cv = __ldcg(&cand[i]);
+        if (cv.x != thr) continue;
+        const uint32_t u = 0x7fffffffu - cv.y;
+        if (lev > 0 && (u >> (shift + 10)) != prefix) continue;
+        atomicAdd(&hbuf[(u >> shift) & (uint32_t)(nb - 1)], 1u);
+      }
+      __syncthreads();
+      if (lev == 0) find_bin<2048>(hbuf, krem, sh_res, sh_warp);
+      else find_bin<1024>(hbuf, krem, sh_res, sh_warp);
+      prefix = (prefix << (lev == 0 ? 0 : 10)) | sh_res[0];
+      krem = sh_res[1];
+    }
+    t_cut = (int32_t)(0x7fffffffu - prefix);
+  }
+  if (tid == 0) {
+    p.state[s].thr = thr;
+    p.state[s].t_cut = t_cut;
+  }
+  // per-chunk counts of the selected candidates, then exclusive offsets
+  int32_t* cnt = p.cnt + (size_t)s * p.topk_chunks;
+  for (uint32_t i = tid; i < N; i += TK_THREADS) {
+    const uint2 cv = __ldcg(&cand[i]);
+    if (cv.x > thr || (cv.x == thr && (int32_t)cv.y <= t_cut)) atomicAdd(&cnt[cv.y / TOPK_CHUNK], 1);
+  }
+  __threadfence();
+  __syncthreads();
+  const int nch = p.topk_chunks;
+  const int per = (nch + TK_THREADS - 1) / TK_THREADS;
+  const int lo = min(nch, tid * per), hi = min(nch, lo + per);
+  uint32_t mine = 0;
+  for (int x = lo; x < hi; ++x) mine += (uint32_t)__ldcg(&cnt[x]);
+  uint32_t off = block_excl_scan(mine, sh_scan, nullptr);
+  for (int x = lo; x < hi; ++x) {
+    const uint32_t c = (uint32_t)__ldcg(&cnt[x]);
+    cnt[x] = (int32_t)off;
+    off += c;
+  }
+}
+
+// writes the selected token ids of one chunk in ascending order
+__global__ void __launch_bounds__(TK_THREADS) topk_write_kernel(DecodeParams p) {
+  const int s = blockIdx.y, ch = blockIdx.x, tid = threadIdx.x;
+  __shared__ uint32_t sh_scan[TK_THREADS / 32];
+  const uint32_t thr = p.state[s].thr;
+  const int32_t t_cut = p.state[s].t_cut;
+  const int base = p.cnt[(size_t)s * p.topk_chunks + ch];
+  const int64_t t0 = (int64_t)ch * TOPK_CHUNK + (int64_t)tid * TK_PER;
+  float v[TK_PER];
+  load16(p.scores + (size_t)s * p.Tp, t0, p.T, v, true, policy_evict_first());
+  uint32_t n = 0;
+  bool selv[TK_PER];
+#pragma unroll
+  for (int i = 0; i < TK_PER; ++i) {
+    const uint32_t key = f2key(v[i]);
+    const int64_t t = t0 + i;
+    selv[i] = t < p.T && (key > thr || (key == thr && t <= t_cut));
+    n += selv[i];
+  }
+  int pos = base + (int)block_excl_scan(n, sh_scan, nullptr);
   int32_t* out = p.sel + (size_t)s * p.kk;
   int32_t* out2 = p.sel_user ? p.sel_user + (size_t)s * p.kk : nullptr;
 #pragma unroll
-  for (int i = 0; i < PER; ++i) {
-    const int64_t t = t0 + i;
-    if (t >= p.T) break;
-    const bool isg = keys[i] > thr, ise = keys[i] == thr;
-    if (isg || (ise && e_prior < need_eq)) {
-      const int pos = g_prior + min(e_prior, need_eq);
-      if (pos >= p.kk) break;   // cannot happen with consistent histograms
-      out[pos] = (int32_t)t;
-      if (out2) out2[pos] = (int32_t)t;
+  for (int i = 0; i < TK_PER; ++i) {
+    if (selv[i] && pos >= 0 && pos < p.kk) {
+      out[pos] = (int32_t)(t0 + i);
+      if (out2) out2[pos] = (int32_t)(t0 + i);
     }
-    g_prior += isg;
-    e_prior += ise;
+    pos += selv[i];
   }
 }
 
 // ---------------------------------------------------------------------------
-// attn: split-K attention of the g query heads over a chunk of selected tokens,
-// reading the packed K/V rows in place (values + channel indices).
-// Partials per (stream, chunk, head): max logit m, sum of exp l, and the
-// unnormalised output in the rotated V basis.
-// grid: (attn_chunks, BH), block: 128 (4 warps)
+// attn: split-K attention of the g query heads over a chunk of <= 128
+// selected tokens, reading the packed K/V rows in place (fp16 values + uint8
+// channel indices), one token per thread with all of its row loads in flight.
+// Each thread writes its V row into a zeroed fp16 tile (rows padded to 65
+// words, so lanes writing one channel of 32 rows hit 32 banks); after the
+// softmax statistics, thread j sums p_t,i * V[t][j] over the tile's tokens in
+// order.  Partials per (stream, chunk, head): max logit m, sum of exp l and
+// the unnormalised output in the rotated V basis.
+// grid: (attn_chunks, BH), block 128, dynamic smem
 // ---------------------------------------------------------------------------
-constexpr int ATTN_WARPS = 4;
+constexpr int ATTN_THREADS = 128;
+constexpr int VD_LD = 130;          // halves per V tile row
+constexpr uint64_t NO_IDX = ~0ull;
 
-__device__ __forceinline__ int64_t clamp_t(int32_t t, int64_t T) {
-  return t < 0 ? 0 : (t >= T ? T - 1 : (int64_t)t);
-}
-
-struct RowRef {
-  const __half* vals;
-  const uint8_t* idx;   // nullptr for dense rows
-  int nnz;
-};
-
-__device__ __forceinline__ RowRef row_ref(const uint8_t* pool, const mkv_segment_header* hdr,
-                                          int64_t t, int S, int c) {
-  const int64_t sg = t / S;   // t is clamped to [0, T) by the caller
-  const int r = (int)(t - sg * S);
+__device__ __forceinline__ void row_addr(const mkv_segment_header* hdr, int64_t t, int S, int c,
+                                         uint64_t* vals, uint64_t* idx, int* nnz) {
+  const int64_t sg = t / S;
+  const uint32_t r = (uint32_t)(t - sg * S);
   const mkv_segment_header hd = hdr[sg];
-  const uint8_t* base = pool + (size_t)hd.off16 * 16u;
-  RowRef rr;
+  const uint64_t base = (uint64_t)hd.off16 * 16u;
   if (hd.strategy == MKV_STRATEGY_SM) {
-    rr.idx = base;
-    rr.vals = reinterpret_cast<const __half*>(base + pad16((uint32_t)c) + 2u * (uint32_t)c * r);
-    rr.nnz = c;
+    *vals = base + pad16((uint32_t)c) + 2u * (uint32_t)c * r;
+    *idx = base;
+    *nnz = c;
   } else if (hd.strategy == MKV_STRATEGY_PV) {
-    rr.vals = reinterpret_cast<const __half*>(base + 2u * (uint32_t)c * r);
-    rr.idx = base + 2u * (uint32_t)c * hd.rows + (uint32_t)c * r;
-    rr.nnz = c;
+    *vals = base + 2u * (uint32_t)c * r;
+    *idx = base + 2u * (uint32_t)c * hd.rows + (uint32_t)c * r;
+    *nnz = c;
   } else {
-    rr.vals = reinterpret_cast<const __half*>(base + 256u * r);
-    rr.idx = nullptr;
-    rr.nnz = D;
+    *vals = base + 256u * r;
+    *idx = NO_IDX;
+    *nnz = D;
   }
-  return rr;
 }
 
-__global__ void __launch_bounds__(128) attn_kernel(DecodeParams p) {
-  extern __shared__ __align__(16) float sm[];
-  const int s = blockIdx.y, ch = blockIdx.x;
-  const int b = s / p.H, h = s % p.H;
-  const int g = p.g;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float* qs = sm;                                  // [g][128]
-  float* acc = qs + g * D;                         // [4][g][128]
-  float* lg = acc + ATTN_WARPS * g * D;            // [chunk][g]
-  float* ml = lg + p.attn_chunk * g;               // [g][2]
-  const float* qt = p.qt + ((size_t)b * p.Hq + (size_t)h * g) * D;
-  for (int x = threadIdx.x; x < g * D; x += blockDim.x) qs[x] = qt[x];
-  for (int x = threadIdx.x; x < ATTN_WARPS * g * D; x += blockDim.x) acc[x] = 0.f;
-  __syncthreads();
-  const int j0 = ch * p.attn_chunk;
-  const int n = min(p.attn_chunk, p.kk - j0);
-  const int32_t* sel = p.sel + (size_t)s * p.kk + j0;
-  const mkv_segment_header* hK = p.hdrK + (size_t)s * p.n_seg;
-  const mkv_segment_header* hV = p.hdrV + (size_t)s * p.n_seg;
-  const float scale = 0.08838834764831845f;   // 1 / sqrt(128)
+size_t attn_smem_bytes(int g, int chunk) {
+  const int gp = (g + 3) & ~3;
+  return (size_t)chunk * VD_LD * 2 + sizeof(float) * ((size_t)D * gp + (size_t)chunk * g + 2 * g);
+}
 
-  // logits
-  for (int i = warp; i < n; i += ATTN_WARPS) {
-    const RowRef rr = row_ref(p.pool, hK, clamp_t(sel[i], p.T), p.S, p.c);
+__global__ void __launch_bounds__(ATTN_THREADS) attn_kernel(DecodeParams p) {
+  extern __shared__ __align__(16) uint8_t asm_[];
+  const int s = blockIdx.y, chk = blockIdx.x;
+  const int b = s / p.H, h = s % p.H;
+  const int g = p.g, gp = (g + 3) & ~3;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int CH = p.attn_chunk;
+  __half* Vd = reinterpret_cast<__half*>(asm_);                     // [CH][VD_LD]
+  float* qs = reinterpret_cast<float*>(asm_ + (size_t)CH * VD_LD * 2);  // [128][gp]
+  float* lg = qs + D * gp;                                          // [CH][g]
+  float* ml = lg + CH * g;                                          // [g][2]
+  const float* qt = p.qt + ((size_t)b * p.Hq + (size_t)h * g) * D;
+  for (int x = tid; x < g * D; x += ATTN_THREADS) qs[(x % D) * gp + x / D] = qt[x];
+  {
+    uint32_t* z = reinterpret_cast<uint32_t*>(Vd);
+    for (int x = tid; x < CH * VD_LD / 2; x += ATTN_THREADS) z[x] = 0u;
+  }
+  const int j0 = chk * CH;
+  const int n = min(CH, p.kk - j0);
+  __syncthreads();
+  const float scale = 0.08838834764831845f;   // 1 / sqrt(128)
+  if (tid < n) {
+    const int64_t t = clamp_t(p.sel[(size_t)s * p.kk + j0 + tid], p.T);
+    uint64_t kvo, kio, vvo, vio;
+    int kn, vn;
+    row_addr(p.hdrK + (size_t)s * p.n_seg, t, p.S, p.c, &kvo, &kio, &kn);
+    row_addr(p.hdrV + (size_t)s * p.n_seg, t, p.S, p.c, &vvo, &vio, &vn);
+    // ---- V row -> tile (values are stored fp16; copied exactly) -------------
+    {
+      const uint8_t* vals = p.pool + vvo;
+      const bool dense = vio == NO_IDX;
+      const uint8_t* idx = dense ? nullptr : p.pool + vio;
+      __half* row = Vd + (size_t)tid * VD_LD;
+      for (int k8 = 0; k8 < vn; k8 += 8) {
+        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(vals + 2 * k8));
+        const __half* hv = reinterpret_cast<const __half*>(&raw);
+        if (dense) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) row[k8 + e] = hv[e];
+        } else {
+          const uint2 ix = __ldg(reinterpret_cast<const uint2*>(idx + k8));
+#pragma unroll
+          for (int e = 0; e < 8; ++e) row[((e < 4 ? ix.x : ix.y) >> (8 * (e & 3))) & 0x7fu] = hv[e];
+        }
+      }
+    }
+    // ---- logits --------------------------------------------------------------
     float part[MAX_G];
 #pragma unroll
     for (int hh = 0; hh < MAX_G; ++hh) part[hh] = 0.f;
-    for (int j = lane; j < rr.nnz; j += 32) {
-      const float v = __half2float(rr.vals[j]);
-      const int chn = rr.idx ? (rr.idx[j] & 127) : j;
+    const uint8_t* vals = p.pool + kvo;
+    const bool dense = kio == NO_IDX;
+    const uint8_t* idx = dense ? nullptr : p.pool + kio;
+    for (int k8 = 0; k8 < kn; k8 += 8) {
+      float v[8];
+      h8_to_f(__ldg(reinterpret_cast<const uint4*>(vals + 2 * k8)), v);
+      uint2 ix = make_uint2(0u, 0u);
+      if (!dense) ix = __ldg(reinterpret_cast<const uint2*>(idx + k8));
 #pragma unroll
-      for (int hh = 0; hh < MAX_G; ++hh)
-        if (hh < g) part[hh] = fmaf(qs[hh * D + chn], v, part[hh]);
-    }
+      for (int e = 0; e < 8; ++e) {
+        const int chn = dense ? (k8 + e) : (int)(((e < 4 ? ix.x : ix.y) >> (8 * (e & 3))) & 0x7fu);
+        const float* qq = qs + chn * gp;
 #pragma unroll
-    for (int hh = 0; hh < MAX_G; ++hh) {
-      if (hh < g) {
-        float x = part[hh];
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
-        if (lane == 0) lg[i * g + hh] = x * scale;
+        for (int hh = 0; hh < MAX_G; ++hh)
+          if (hh < g) part[hh] = fmaf(qq[hh], v[e], part[hh]);
       }
     }
+#pragma unroll
+    for (int hh = 0; hh < MAX_G; ++hh)
+      if (hh < g) lg[tid * g + hh] = part[hh] * scale;
   }
   __syncthreads();
-  // softmax statistics of the chunk (one thread per head, token order)
-  if ((int)threadIdx.x < g) {
-    const int hh = threadIdx.x;
+  // ---- softmax statistics per head (warp per head, fixed-order reductions) --
+  for (int hh = warp; hh < g; hh += ATTN_THREADS / 32) {
     float m = -INFINITY;
-    for (int i = 0; i < n; ++i) m = fmaxf(m, lg[i * g + hh]);
+    for (int i = lane; i < n; i += 32) m = fmaxf(m, lg[i * g + hh]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
     float l = 0.f;
-    for (int i = 0; i < n; ++i) {
+    for (int i = lane; i < n; i += 32) {
       const float e = expf(lg[i * g + hh] - m);
       lg[i * g + hh] = e;
       l += e;
     }
-    ml[hh * 2] = m;
-    ml[hh * 2 + 1] = l;
-  }
-  __syncthreads();
-  // sum_t p_t v^_t into per-warp accumulators (channels of one row are distinct)
-  float* myacc = acc + warp * g * D;
-  for (int i = warp; i < n; i += ATTN_WARPS) {
-    const RowRef rr = row_ref(p.pool, hV, clamp_t(sel[i], p.T), p.S, p.c);
-    for (int j = lane; j < rr.nnz; j += 32) {
-      const float v = __half2float(rr.vals[j]);
-      const int chn = rr.idx ? (rr.idx[j] & 127) : j;
-      for (int hh = 0; hh < g; ++hh) myacc[hh * D + chn] = fmaf(lg[i * g + hh], v, myacc[hh * D + chn]);
-    }
-    __syncwarp();
-  }
-  __syncthreads();
-  const size_t pbase = ((size_t)s * p.attn_chunks + ch) * g;
-  for (int x = threadIdx.x; x < g * D; x += blockDim.x) {
-    float o = 0.f;
 #pragma unroll
-    for (int w = 0; w < ATTN_WARPS; ++w) o += acc[w * g * D + x];
-    p.part_o[pbase * D + x] = o;
+    for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+    if (lane == 0) {
+      ml[hh * 2] = m;
+      ml[hh * 2 + 1] = l;
+    }
   }
-  if ((int)threadIdx.x < 2 * g) p.part_ml[pbase * 2 + threadIdx.x] = ml[threadIdx.x];
+  __syncthreads();
+  // ---- o~_i[j] = sum_t p_t,i V[t][j]: thread j, tokens in order ------------
+  const int jc = tid;   // channel
+  float o[MAX_G];
+#pragma unroll
+  for (int hh = 0; hh < MAX_G; ++hh) o[hh] = 0.f;
+  for (int i = 0; i < n; ++i) {
+    const float v = __half2float(Vd[(size_t)i * VD_LD + jc]);
+#pragma unroll
+    for (int hh = 0; hh < MAX_G; ++hh)
+      if (hh < g) o[hh] = fmaf(lg[i * g + hh], v, o[hh]);
+  }
+  const size_t pbase = ((size_t)s * p.attn_chunks + chk) * g;
+#pragma unroll
+  for (int hh = 0; hh < MAX_G; ++hh)
+    if (hh < g) p.part_o[(pbase + hh) * D + jc] = o[hh];
+  if (tid < 2 * g) p.part_ml[pbase * 2 + tid] = ml[tid];
 }
 
 // ---------------------------------------------------------------------------
-// merge: log-sum-exp merge of the chunk partials, then o = o~ R_V^T.
-// grid: BH, block: 128
+// merge: log-sum-exp merge of the chunk partials, then o = o~ R_V^T with R_V
+// staged in shared memory.
+// grid: BH, block 256, dynamic smem 64 KB + chunk weights
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(128) merge_kernel(DecodeParams p) {
+constexpr int MG_THREADS = 256;
+
+__global__ void __launch_bounds__(MG_THREADS) merge_kernel(DecodeParams p) {
+  extern __shared__ __align__(16) float msm[];
+  float* Rs = msm;                 // [128][128]
+  float* wsm = msm + D * D;        // [attn_chunks][g] weights
+  __shared__ __align__(16) float ot[MAX_G][D];
+  __shared__ float Linv[MAX_G];
   const int s = blockIdx.x;
   const int b = s / p.H, h = s % p.H;
-  const int g = p.g;
-  const int x = threadIdx.x, warp = x >> 5, lane = x & 31;
-  __shared__ __align__(16) float ot[MAX_G][D];
-  for (int hh = 0; hh < g; ++hh) {
+  const int g = p.g, nc = p.attn_chunks;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  {
+    const float4* R4 = reinterpret_cast<const float4*>(p.RV + (size_t)s * D * D);
+    float4* Rs4 = reinterpret_cast<float4*>(Rs);
+#pragma unroll
+    for (int x = 0; x < D * D / 4 / MG_THREADS; ++x)
+      Rs4[tid + x * MG_THREADS] = __ldg(R4 + tid + x * MG_THREADS);
+  }
+  const float* ml = p.part_ml + (size_t)s * nc * g * 2;
+  for (int x = tid; x < nc * g; x += MG_THREADS) wsm[x] = ml[2 * x];   // m of (chunk, head)
+  __syncthreads();
+  if (tid < g) {
     float M = -INFINITY;
-    for (int c = 0; c < p.attn_chunks; ++c)
-      M = fmaxf(M, p.part_ml[(((size_t)s * p.attn_chunks + c) * g + hh) * 2]);
-    float L = 0.f, o = 0.f;
-    for (int c = 0; c < p.attn_chunks; ++c) {
-      const size_t pi = ((size_t)s * p.attn_chunks + c) * g + hh;
-      const float w = expf(p.part_ml[pi * 2] - M);
-      L = fmaf(p.part_ml[pi * 2 + 1], w, L);
-      o = fmaf(p.part_o[pi * D + x], w, o);
+    for (int c = 0; c < nc; ++c) M = fmaxf(M, wsm[c * g + tid]);
+    float L = 0.f;
+    for (int c = 0; c < nc; ++c) {
+      const float w = expf(wsm[c * g + tid] - M);
+      wsm[c * g + tid] = w;
+      L = fmaf(ml[2 * (c * g + tid) + 1], w, L);
     }
-    ot[hh][x] = o / L;
+    Linv[tid] = 1.f / L;
   }
   __syncthreads();
-  const float* RV = p.RV + (size_t)s * D * D;
+  const float* po = p.part_o + (size_t)s * nc * g * D;
+  for (int x = tid; x < g * D; x += MG_THREADS) {
+    const int hh = x / D;
+    float o = 0.f;
+#pragma unroll 8
+    for (int c = 0; c < nc; ++c) o = fmaf(__ldg(po + (size_t)c * g * D + x), wsm[c * g + hh], o);
+    ot[hh][x % D] = o * Linv[hh];
+  }
+  __syncthreads();
   float* out = p.out + ((size_t)b * p.Hq + (size_t)h * g) * D;
-  for (int r = warp; r < D; r += 4) {
-    float rv[4];
-#pragma unroll
-    for (int m = 0; m < 4; ++m) rv[m] = RV[r * D + lane + 32 * m];
+  for (int r = warp; r < D; r += MG_THREADS / 32) {
+    const float4 rv = *reinterpret_cast<const float4*>(Rs + r * D + 4 * lane);
     for (int hh = 0; hh < g; ++hh) {
-      float d = 0.f;
-#pragma unroll
-      for (int m = 0; m < 4; ++m) d = fmaf(rv[m], ot[hh][lane + 32 * m], d);
+      const float4 o4 = *reinterpret_cast<const float4*>(&ot[hh][4 * lane]);
+      float d = rv.x * o4.x;
+      d = fmaf(rv.y, o4.y, d);
+      d = fmaf(rv.z, o4.z, d);
+      d = fmaf(rv.w, o4.w, d);
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
       if (lane == 0) out[hh * D + r] = d;
@@ -566,44 +801,98 @@ __global__ void __launch_bounds__(128) merge_kernel(DecodeParams p) {
 }
 
 // ---------------------------------------------------------------------------
+// partition of the K segments over the score kernel's CTAs (compression time):
+// CTA i starts at the first segment whose payload starts at or after
+// i * total / G bytes of the K payload.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) partition_kernel(const mkv_segment_header* hdrK,
+                                                         int n_streams, int n_seg, int c, int G,
+                                                         int32_t* part, int32_t* cta_cnt) {
+  const int64_t n = (int64_t)n_streams * n_seg;
+  const mkv_segment_header last = hdrK[n - 1];
+  const uint64_t first = (uint64_t)hdrK[0].off16 * 16u;
+  const uint64_t total =
+      (uint64_t)last.off16 * 16u + segment_bytes(last.strategy, last.rows, c) - first;
+  for (int s = threadIdx.x; s < n_streams; s += blockDim.x) cta_cnt[s] = 0;
+  for (int i = threadIdx.x; i <= G; i += blockDim.x) {
+    const uint64_t target = (uint64_t)(((double)i / (double)G) * (double)total);
+    int64_t lo = 0, hi = n;   // first segment whose start >= target
+    while (lo < hi) {
+      const int64_t mid = (lo + hi) >> 1;
+      if ((uint64_t)hdrK[mid].off16 * 16u - first >= target) hi = mid; else lo = mid + 1;
+    }
+    part[i] = (int32_t)(i == 0 ? 0 : (i == G ? n : lo));
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < G; i += blockDim.x) {
+    const int a = part[i], b = part[i + 1];
+    if (a >= b) continue;
+    for (int s = a / n_seg; s <= (b - 1) / n_seg; ++s) atomicAdd(&cta_cnt[s], 1);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
+void score_stage_plan(int S, int c, int* stage_bytes, int* n_stages) {
+  uint32_t mx = 0;
+  for (int st = 0; st < 3; ++st) {
+    const uint32_t b = segment_bytes(st, S, c);
+    mx = mx > b ? mx : b;
+  }
+  const int sb = (int)(mx > 32768u ? mx : 32768u);
+  const int budget = 227 * 1024 - SC_STATIC_SMEM;
+  int ns = budget / sb;
+  ns = ns > SC_MAX_STAGES ? SC_MAX_STAGES : ns;
+  *stage_bytes = sb;
+  *n_stages = ns;
+}
+
+cudaError_t prepare_decode_kernels() {
+  cudaError_t e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)attn_smem_bytes(MAX_G, ATTN_MAX_CHUNK));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)(sizeof(float) * D * D) + 48 * 1024);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(qrot_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, D * D * 4);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              227 * 1024 - SC_STATIC_SMEM);
+}
+
+cudaError_t launch_partition(const mkv_segment_header* hdrK, int n_streams, int n_seg, int c,
+                             int G, int32_t* part, int32_t* cta_cnt, cudaStream_t st) {
+  partition_kernel<<<1, 1024, 0, st>>>(hdrK, n_streams, n_seg, c, G, part, cta_cnt);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_qrot(const DecodeParams& p, cudaStream_t st) {
-  qrot_kernel<<<p.B * p.H, 128, 0, st>>>(p);
+  qrot_kernel<<<p.B * p.H, QR_THREADS, D * D * 4, st>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_score(const DecodeParams& p, cudaStream_t st) {
-  dim3 grid(p.score_ctas_per_stream, p.B * p.H);
-  score_kernel<<<grid, 256, 0, st>>>(p);
+  score_kernel<<<p.G, SC_THREADS, (size_t)p.stage_bytes * p.n_stages, st>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_topk(const DecodeParams& p, cudaStream_t st) {
   dim3 grid(p.topk_chunks, p.B * p.H);
-  topk_hist_kernel<2><<<grid, TK_THREADS, 0, st>>>(p);
-  topk_hist_kernel<3><<<grid, TK_THREADS, 0, st>>>(p);
-  topk_count_kernel<<<grid, TK_THREADS, 0, st>>>(p);
+  topk_pass2_kernel<<<grid, TK_THREADS, 0, st>>>(p);
   topk_write_kernel<<<grid, TK_THREADS, 0, st>>>(p);
   return cudaGetLastError();
 }
 
-size_t attn_smem_bytes(int g, int chunk) {
-  return sizeof(float) * ((size_t)g * D + (size_t)ATTN_WARPS * g * D + (size_t)chunk * g + 2 * g);
-}
-
 cudaError_t launch_attn(const DecodeParams& p, cudaStream_t st) {
-  const size_t smem = attn_smem_bytes(p.g, p.attn_chunk);
-  cudaError_t e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
-  if (e != cudaSuccess) return e;
   dim3 grid(p.attn_chunks, p.B * p.H);
-  attn_kernel<<<grid, 128, smem, st>>>(p);
+  attn_kernel<<<grid, ATTN_THREADS, attn_smem_bytes(p.g, p.attn_chunk), st>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_merge(const DecodeParams& p, cudaStream_t st) {
-  merge_kernel<<<p.B * p.H, 128, 0, st>>>(p);
+  merge_kernel<<<p.B * p.H, MG_THREADS, sizeof(float) * ((size_t)D * D + (size_t)p.attn_chunks * p.g),
+                 st>>>(p);
   return cudaGetLastError();
 }
 

@@ -15,6 +15,7 @@ using namespace mkv;
 namespace {
 
 constexpr int kSMs = 152;          // GB300
+constexpr int64_t kMergeMaxWeights = 12288;   // 48 KB of fp32 (chunk, head) weights
 thread_local std::string g_last_error = "no error";
 
 mkv_status cuda_fail(cudaError_t e, const char* what) {
@@ -47,9 +48,12 @@ struct mkv_ctx {
   int64_t max_seg = 0;
   int kk_max = 0;
   int gram_chunks_max = 0;
-  int attn_chunk = 64;
+  int attn_chunk = 128;
   int attn_chunks_max = 0;
   int topk_chunks_max = 0;
+  int64_t Tp_max = 0;              // padded row stride of scores / candidates
+  int G = 0;                       // score-kernel CTAs (one per SM)
+  int stage_bytes = 0, n_stages = 0;
 
   // current cache
   int64_t T = 0;
@@ -59,6 +63,8 @@ struct mkv_ctx {
   float* R[2] = {nullptr, nullptr};
   float* lam[2] = {nullptr, nullptr};
   mkv_segment_header* hdr[2] = {nullptr, nullptr};
+  int32_t* part[2] = {nullptr, nullptr};      // score-kernel partition of the K segments
+  int32_t* cta_cnt[2] = {nullptr, nullptr};   // score CTAs per stream
   uint8_t* pool = nullptr;
   uint64_t pool_cap = 0;
 
@@ -73,9 +79,12 @@ struct mkv_ctx {
   float* qbar = nullptr;
   float* scores = nullptr;
   uint32_t* hist = nullptr;
-  int2* cnt = nullptr;
-  int2* res = nullptr;
+  uint32_t* tick = nullptr;        // [3][BH]: tick1, tick2, cand_n
+  uint2* cand = nullptr;
+  TopkState* state = nullptr;
+  int32_t* cnt = nullptr;
   int32_t* sel = nullptr;
+  int* err = nullptr;
   float* part_o = nullptr;
   float* part_ml = nullptr;
 
@@ -112,6 +121,16 @@ mkv_status timer_event(KernelTimer& t, cudaEvent_t* ev) {
   return MKV_OK;
 }
 
+// Records `ev` on `st`.  Inside a stream capture the record must be an
+// external event-record node so that every replay of the graph records it.
+cudaError_t record(cudaEvent_t ev, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(st, &cs);
+  if (e != cudaSuccess) return e;
+  if (cs == cudaStreamCaptureStatusActive) return cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal);
+  return cudaEventRecord(ev, st);
+}
+
 // Runs `launch` on `st`, bracketed by events when timing is on.
 template <typename F>
 mkv_status timed(mkv_ctx* c, int id, cudaStream_t st, int n_kernels, F launch) {
@@ -125,12 +144,12 @@ mkv_status timed(mkv_ctx* c, int id, cudaStream_t st, int n_kernels, F launch) {
     if (s != MKV_OK) return s;
     s = timer_event(c->timers[id], &b);
     if (s != MKV_OK) return s;
-    CK(cudaEventRecord(a, st));
+    CK(record(a, st));
   }
   CK(launch());
   c->launches += n_kernels;
   if (timing_on(c)) {
-    CK(cudaEventRecord(b, st));
+    CK(record(b, st));
     c->timers[id].pending.emplace_back(a, b);
     c->timers[id].launches += 1;
   }
@@ -152,6 +171,8 @@ void release(mkv_ctx* c) {
     cudaFree(c->R[i]);
     cudaFree(c->lam[i]);
     cudaFree(c->hdr[i]);
+    cudaFree(c->part[i]);
+    cudaFree(c->cta_cnt[i]);
   }
   cudaFree(c->pool);
   cudaFree(c->seg);
@@ -162,9 +183,12 @@ void release(mkv_ctx* c) {
   cudaFree(c->qbar);
   cudaFree(c->scores);
   cudaFree(c->hist);
+  cudaFree(c->tick);
+  cudaFree(c->cand);
+  cudaFree(c->state);
   cudaFree(c->cnt);
-  cudaFree(c->res);
   cudaFree(c->sel);
+  cudaFree(c->err);
   cudaFree(c->part_o);
   cudaFree(c->part_ml);
   for (auto& t : c->timers) {
@@ -221,7 +245,7 @@ mkv_status mkv_validate_config(const mkv_config* cfg) {
   if (c.c < 8 || c.c > MKV_HEAD_DIM || c.c % 8 != 0) return MKV_ERR_INVALID_ARG;
   if (!(c.tau > 0.f && c.tau <= 1.f)) return MKV_ERR_INVALID_ARG;
   if (c.top_k < 1) return MKV_ERR_INVALID_ARG;
-  if (c.attn_chunk != 0 && (c.attn_chunk < 8 || c.attn_chunk > 1024 || c.attn_chunk % 8 != 0))
+  if (c.attn_chunk != 0 && (c.attn_chunk < 8 || c.attn_chunk > ATTN_MAX_CHUNK || c.attn_chunk % 8 != 0))
     return MKV_ERR_INVALID_ARG;
   if (c.flags & ~MKV_FLAG_KERNEL_TIMING) return MKV_ERR_INVALID_ARG;
   if (c.device < 0) return MKV_ERR_INVALID_ARG;
@@ -239,6 +263,7 @@ mkv_status mkv_create(const mkv_config* cfg, mkv_ctx** out) {
   CK(cudaGetDeviceCount(&ndev));
   if (cfg->device >= ndev) return MKV_ERR_INVALID_ARG;
   CK(cudaSetDevice(cfg->device));
+  CK(prepare_decode_kernels());
   mkv_ctx* c = new (std::nothrow) mkv_ctx();
   if (!c) return MKV_ERR_OOM;
   c->cfg = *cfg;
@@ -250,9 +275,29 @@ mkv_status mkv_create(const mkv_config* cfg, mkv_ctx** out) {
   c->max_seg = ceil_div(cfg->max_ctx, cfg->segment);
   c->kk_max = (int)std::min<int64_t>(cfg->top_k, cfg->max_ctx);
   c->gram_chunks_max = gram_chunks_for(c->BH, cfg->max_ctx);
-  c->attn_chunk = cfg->attn_chunk ? cfg->attn_chunk : 64;
+  c->attn_chunk = cfg->attn_chunk ? cfg->attn_chunk : 128;
+  // the merge kernel keeps one weight per (chunk, head) in shared memory
+  while (ceil_div(c->kk_max, c->attn_chunk) * c->g > kMergeMaxWeights &&
+         c->attn_chunk < ATTN_MAX_CHUNK)
+    c->attn_chunk = std::min(ATTN_MAX_CHUNK, c->attn_chunk * 2);
+  if (ceil_div(c->kk_max, c->attn_chunk) * c->g > kMergeMaxWeights) {
+    delete c;
+    g_last_error = "top_k too large for the split-K merge";
+    return MKV_ERR_INVALID_ARG;
+  }
   c->attn_chunks_max = (int)ceil_div(c->kk_max, c->attn_chunk);
   c->topk_chunks_max = (int)ceil_div(cfg->max_ctx, TOPK_CHUNK);
+  c->Tp_max = ceil_div(cfg->max_ctx, 16) * 16;
+  {
+    int sms = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, cfg->device);
+    if (e != cudaSuccess) {
+      delete c;
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    }
+    c->G = sms;
+  }
+  score_stage_plan(cfg->segment, cfg->c, &c->stage_bytes, &c->n_stages);
   const size_t BH = c->BH;
   mkv_status s = MKV_OK;
 #define AL(ptr, n)                         \
@@ -265,24 +310,33 @@ mkv_status mkv_create(const mkv_config* cfg, mkv_ctx** out) {
     AL(c->R[i], 2 * BH * D * D);
     AL(c->lam[i], 2 * BH * D);
     AL(c->hdr[i], 2 * BH * (size_t)c->max_seg);
+    AL(c->part[i], (size_t)c->G + 1);
+    AL(c->cta_cnt[i], BH);
   }
   AL(c->seg, 2 * BH * (size_t)c->max_seg);
   AL(c->gram_part, 2 * BH * (size_t)c->gram_chunks_max * D * D);
   AL(c->total_dev, 1);
   AL(c->qt, (size_t)c->B * c->Hq * D);
   AL(c->qbar, BH * D);
-  AL(c->scores, BH * (size_t)cfg->max_ctx);
-  AL(c->hist, BH * HIST_WORDS);
+  AL(c->scores, BH * (size_t)c->Tp_max);
+  AL(c->hist, BH * HIST1);
+  AL(c->tick, 3 * BH);
+  AL(c->cand, BH * (size_t)c->Tp_max);
+  AL(c->state, BH);
   AL(c->cnt, BH * (size_t)c->topk_chunks_max);
-  AL(c->res, BH);
   AL(c->sel, BH * (size_t)c->kk_max);
+  AL(c->err, 1);
   AL(c->part_o, BH * (size_t)c->attn_chunks_max * c->g * D);
   AL(c->part_ml, BH * (size_t)c->attn_chunks_max * c->g * 2);
 #undef AL
   cudaError_t e = cudaMallocHost(reinterpret_cast<void**>(&c->total_host), sizeof(unsigned long long));
+  if (e == cudaSuccess) e = cudaMemset(c->tick, 0, 3 * BH * sizeof(uint32_t));
+  if (e == cudaSuccess) e = cudaMemset(c->err, 0, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(c->sel, 0, BH * (size_t)c->kk_max * sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     release(c);
-    return cuda_fail(e, "cudaMallocHost");
+    return cuda_fail(e, "ctx initialisation");
   }
   *out = c;
   return MKV_OK;
@@ -333,7 +387,8 @@ mkv_status mkv_compress(mkv_ctx* c, const void* k, const void* v, int64_t ctx_le
   CK(launch_eig(p, st));
   CK(launch_analyze(p, st));
   CK(launch_scan(p, st));
-  c->launches += 4;
+  CK(launch_partition(p.hdr, c->BH, p.n_seg, p.c, c->G, c->part[stage], c->cta_cnt[stage], st));
+  c->launches += 5;
   CK(cudaMemcpyAsync(c->total_host, c->total_dev, sizeof(unsigned long long),
                      cudaMemcpyDeviceToHost, st));
   CK(cudaStreamSynchronize(st));
@@ -380,6 +435,7 @@ mkv_status mkv_decode(mkv_ctx* c, const void* q, float* out, int32_t* sel, mkv_s
   p.Hq = c->Hq;
   p.g = c->g;
   p.T = c->T;
+  p.Tp = ceil_div(c->T, 16) * 16;
   p.S = c->cfg.segment;
   p.c = c->cfg.c;
   p.n_seg = c->n_seg;
@@ -394,14 +450,21 @@ mkv_status mkv_decode(mkv_ctx* c, const void* q, float* out, int32_t* sel, mkv_s
   p.qbar = c->qbar;
   p.scores = c->scores;
   p.hist = c->hist;
+  p.part = c->part[c->live];
+  p.cta_cnt = c->cta_cnt[c->live];
+  p.G = c->G;
+  p.stage_bytes = c->stage_bytes;
+  p.n_stages = c->n_stages;
+  p.tick1 = c->tick;
+  p.tick2 = c->tick + c->BH;
+  p.cand_n = c->tick + 2 * c->BH;
+  p.cand = c->cand;
+  p.state = c->state;
   p.cnt = c->cnt;
-  p.res = c->res;
   p.topk_chunks = (int)ceil_div(c->T, TOPK_CHUNK);
   p.sel = c->sel;
   p.sel_user = sel;
-  // score: whole segments per CTA, ~8 segments per warp
-  p.score_segs_per_cta = 64;
-  p.score_ctas_per_stream = (int)ceil_div(c->n_seg, p.score_segs_per_cta);
+  p.err = c->err;
   p.attn_chunk = c->attn_chunk;
   p.attn_chunks = (int)ceil_div(p.kk, p.attn_chunk);
   p.part_o = c->part_o;
@@ -410,7 +473,7 @@ mkv_status mkv_decode(mkv_ctx* c, const void* q, float* out, int32_t* sel, mkv_s
   mkv_status s;
   if ((s = timed(c, MKV_KERNEL_QROT, st, 1, [&] { return launch_qrot(p, st); })) != MKV_OK) return s;
   if ((s = timed(c, MKV_KERNEL_SCORE, st, 1, [&] { return launch_score(p, st); })) != MKV_OK) return s;
-  if ((s = timed(c, MKV_KERNEL_TOPK, st, 4, [&] { return launch_topk(p, st); })) != MKV_OK) return s;
+  if ((s = timed(c, MKV_KERNEL_TOPK, st, 2, [&] { return launch_topk(p, st); })) != MKV_OK) return s;
   if ((s = timed(c, MKV_KERNEL_ATTN, st, 1, [&] { return launch_attn(p, st); })) != MKV_OK) return s;
   if ((s = timed(c, MKV_KERNEL_MERGE, st, 1, [&] { return launch_merge(p, st); })) != MKV_OK) return s;
   c->decode_calls += 1;
@@ -475,6 +538,18 @@ mkv_status mkv_export(const mkv_ctx* c, int b, int h, int which, float* basis, f
     }
   }
   return MKV_OK;
+}
+
+mkv_status mkv_check_device(mkv_ctx* c) {
+  if (!c) return MKV_ERR_INVALID_ARG;
+  CK(cudaSetDevice(c->cfg.device));
+  CK(cudaDeviceSynchronize());
+  int v = 0;
+  CK(cudaMemcpy(&v, c->err, sizeof(int), cudaMemcpyDeviceToHost));
+  if (v == 0) return MKV_OK;
+  CK(cudaMemset(c->err, 0, sizeof(int)));
+  g_last_error = "a bounded device-side wait gave up";
+  return MKV_ERR_TIMEOUT;
 }
 
 mkv_status mkv_kernel_time(mkv_ctx* c, int kernel_id, double* total_ms, int64_t* launches,

@@ -11,12 +11,12 @@ namespace mkv {
 
 constexpr int D = 128;                 // head dim
 constexpr int MAX_G = 16;              // query heads per KV head
-constexpr int HIST1 = 2048;            // radix digit bins: bits 31..21
-constexpr int HIST2 = 2048;            //                    bits 20..10
-constexpr int HIST3 = 1024;            //                    bits  9..0
-constexpr int HIST_WORDS = HIST1 + HIST2 + HIST3;
+constexpr int HIST1 = 4096;            // level-1 radix digit of the score key: bits 31..20
+constexpr int HISTA = 1024;            // candidates, bits 19..10
+constexpr int HISTB = 1024;            // candidates, bits  9..0
 constexpr int TOPK_CHUNK = 4096;       // tokens per CTA in the selection passes
 constexpr int TILE_T = 64;             // tokens per rotation tile
+constexpr int ATTN_MAX_CHUNK = 128;    // selected tokens per attention CTA (one per thread)
 
 __host__ __device__ inline int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
 __host__ __device__ inline uint32_t pad16(uint32_t n) { return (n + 15u) & ~15u; }
@@ -77,38 +77,68 @@ cudaError_t launch_pack(const CompressParams& p, cudaStream_t st);
 // ---------------------------------------------------------------------------
 // Decode
 // ---------------------------------------------------------------------------
+// Per-stream state of the top-k selection within one decode step.
+struct TopkState {
+  uint32_t b1;      // level-1 bin holding the k-th largest key
+  uint32_t k1;      // keys still needed from that bin
+  uint32_t thr;     // the k-th largest key
+  int32_t t_cut;    // keys equal to thr are taken up to this token index
+};
+
 struct DecodeParams {
   int B, H, Hq, g;
   int64_t T;
+  int64_t Tp;                      // row stride of scores / candidates: T rounded up to 16
   int S, c, n_seg;
   int kk;                          // min(top_k, T)
   const __half* q;                 // [B][Hq][128]
   const float* RK;                 // [BH][128][128]
   const float* RV;                 // [BH][128][128]
   const uint8_t* pool;
-  const mkv_segment_header* hdrK;  // [BH][n_seg]
+  const mkv_segment_header* hdrK;  // [BH][n_seg] (all K streams, contiguous)
   const mkv_segment_header* hdrV;  // [BH][n_seg]
   float* qt;                       // [B][Hq][128]
   float* qbar;                     // [BH][128]
-  float* scores;                   // [BH][T]
-  uint32_t* hist;                  // [BH][HIST_WORDS]
-  int2* cnt;                       // [BH][topk_chunks]
-  int2* res;                       // [BH]: (threshold key, how many equal keys to take)
+  float* scores;                   // [BH][Tp]
+  uint32_t* hist;                  // [BH][HIST1]
+  // score-kernel partition, fixed at compression: CTA i covers the flattened
+  // K segments [part[i], part[i+1]) (balanced by bytes); cta_cnt[s] = CTAs
+  // that touch stream s
+  const int32_t* part;
+  const int32_t* cta_cnt;
+  int G;
+  int stage_bytes;                 // bytes per shared-memory stage of the score kernel
+  int n_stages;
+  uint32_t* tick1;                 // [BH] tickets: score CTAs done with a stream
+  uint32_t* tick2;                 // [BH] tickets: selection-pass CTAs done
+  uint2* cand;                     // [BH][Tp] (key, token) of threshold-bin candidates
+  uint32_t* cand_n;                // [BH]
+  TopkState* state;                // [BH]
+  int32_t* cnt;                    // [BH][topk_chunks]: counts, then chunk offsets
   int topk_chunks;                 // ceil(T / TOPK_CHUNK)
   int32_t* sel;                    // [BH][kk] (internal)
   int32_t* sel_user;               // optional copy for the caller
-  int score_segs_per_cta;
-  int score_ctas_per_stream;
-  int attn_chunk;                  // selected tokens per attention CTA
+  int attn_chunk;                  // selected tokens per attention CTA (<= ATTN_MAX_CHUNK)
   int attn_chunks;                 // ceil(kk / attn_chunk)
   float* part_o;                   // [BH][attn_chunks][g][128]
   float* part_ml;                  // [BH][attn_chunks][g][2]
   float* out;                      // [B][Hq][128]
+  int* err;                        // device status word (0 = ok)
 };
 
+// error codes written to the device status word
+constexpr int DEV_ERR_TIMEOUT = 1;
+
+// one-time per device: function attributes (not stream-ordered, so not in decode)
+cudaError_t prepare_decode_kernels();
+// score-kernel shared-memory plan: stage size and number of stages
+void score_stage_plan(int S, int c, int* stage_bytes, int* n_stages);
+// partition of the K segments over G score CTAs (run once per compression)
+cudaError_t launch_partition(const mkv_segment_header* hdrK, int n_streams, int n_seg, int c,
+                             int G, int32_t* part, int32_t* cta_cnt, cudaStream_t st);
 cudaError_t launch_qrot(const DecodeParams& p, cudaStream_t st);
 cudaError_t launch_score(const DecodeParams& p, cudaStream_t st);
-// the four selection launches; returns after enqueueing all of them
+// the two selection launches; returns after enqueueing both
 cudaError_t launch_topk(const DecodeParams& p, cudaStream_t st);
 cudaError_t launch_attn(const DecodeParams& p, cudaStream_t st);
 cudaError_t launch_merge(const DecodeParams& p, cudaStream_t st);

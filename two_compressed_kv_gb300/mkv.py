@@ -80,6 +80,7 @@ def _load():
         "mkv_stats": (c_int, [P, POINTER(mkv_stats_t)]),
         "mkv_export": (c_int, [P, c_int, c_int, c_int, P, P, P, P, POINTER(c_uint64)]),
         "mkv_kernel_time": (c_int, [P, c_int, POINTER(c_double), POINTER(c_int64), c_int]),
+        "mkv_check_device": (c_int, [P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -211,6 +212,11 @@ def mkv_export_headers(ctx, b: int, h: int, which: int, n_segments: int) -> np.n
     _check(_lib.mkv_export(ctx, b, h, which, None, None, hdr.ctypes.data, None,
                            ctypes.byref(nbytes)), "mkv_export(headers)")
     return hdr
+
+
+def mkv_check_device(ctx) -> int:
+    """MKV_OK, or MKV_ERR_TIMEOUT when a bounded device wait gave up (synchronous)."""
+    return _lib.mkv_check_device(ctx)
 
 
 def mkv_kernel_time(ctx, kernel_id: int, reset: bool = False):

@@ -91,14 +91,15 @@ def _gen(seed: int, layer: int, tag: int, device) -> torch.Generator:
     return g
 
 
-def haar_orthogonal(n_mats: int, gen: torch.Generator, device) -> torch.Tensor:
-    """[n_mats, 128, 128] fp32 Haar-random orthogonal matrices."""
-    a = torch.randn(n_mats, HEAD_DIM, HEAD_DIM, generator=gen, device=device,
-                    dtype=torch.float64)
+def haar_orthogonal(n_mats: int, gen: torch.Generator, device=None) -> torch.Tensor:
+    """[n_mats, 128, 128] fp32 Haar-random orthogonal matrices, drawn and
+    factored on the CPU (`gen` is a CPU generator), returned on `device`."""
+    a = torch.randn(n_mats, HEAD_DIM, HEAD_DIM, generator=gen, dtype=torch.float64)
     q, r = torch.linalg.qr(a)
     s = torch.sign(torch.diagonal(r, dim1=-2, dim2=-1))
     s[s == 0] = 1.0
-    return (q * s.unsqueeze(-2)).to(torch.float32)
+    out = (q * s.unsqueeze(-2)).to(torch.float32)
+    return out if device is None else out.to(device)
 
 
 def layer_decays(w: Workload, layer: int):
@@ -119,12 +120,12 @@ def _sigma(decay: float, device) -> torch.Tensor:
 def _draw(w: Workload, layer: int, which: int, decay: float, device,
           ctx: Optional[int] = None, streams: Optional[int] = None) -> torch.Tensor:
     """One of K (which=0) or V (which=1): fp16 [B, H, T, 128] on `device`.
-    streams=1 draws only stream (b=0, h=0) (same values as in the full draw on
-    the same device) and returns [1, 1, T, 128]."""
+    streams=1 draws a single stream [1, 1, T, 128] with the same recipe (its
+    own random values)."""
     T = w.ctx if ctx is None else ctx
     B, H = w.batch, w.n_kv_heads
     gen = _gen(w.seed, layer, 1 + which, device)
-    Q = haar_orthogonal(H, gen, device)                       # [H, 128, 128]
+    Q = haar_orthogonal(H, _gen(w.seed, layer, 11 + which, "cpu"), device)   # [H, 128, 128]
     if streams == 1:
         B, H = 1, 1
     out = torch.empty(B, H, T, HEAD_DIM, dtype=torch.float16, device=device)
@@ -140,13 +141,13 @@ def _draw(w: Workload, layer: int, which: int, decay: float, device,
         sig = _sigma(decay, device).view(1, HEAD_DIM)
         p_out = torch.full((1, 1), w.p_out, device=device)
         mult = torch.full((1, 1), w.mult, device=device)
-    # draw per (b, h) so peak scratch memory stays at one [T, 128] fp32 slab
+    # one batch entry (all H heads) per draw keeps the scratch at [H, T, 128]
     for b in range(B):
-        for h in range(H):
-            z = torch.randn(T, HEAD_DIM, generator=gen, device=device)
-            u = torch.rand(T, HEAD_DIM, generator=gen, device=device)
-            m = torch.where(u < p_out, mult, 1.0)
-            out[b, h] = ((z * m * sig) @ Q[h]).to(torch.float16)
+        z = torch.randn(H, T, HEAD_DIM, generator=gen, device=device)
+        u = torch.rand(H, T, HEAD_DIM, generator=gen, device=device)
+        m = torch.where(u < p_out, mult, 1.0)
+        out[b] = torch.bmm(z * m * sig, Q[:H]).to(torch.float16)
+        del z, u, m
     return out
 
 
