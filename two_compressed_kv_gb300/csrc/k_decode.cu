@@ -40,10 +40,16 @@ __device__ __forceinline__ int64_t clamp_t(int32_t t, int64_t T) {
 // bin of histogram h[NB] (shared memory) holding the krem-th largest key,
 // counting from the top bin, and how many keys of that bin are still needed.
 // Results land in res[0] (bin) and res[1] (remaining count).
+// If no bin holds the krem-th key (an inconsistent histogram), the result is
+// bin 0 with krem: wrong but safe, since every caller masks bins to [0, NB).
 template <int NB>
 __device__ void find_bin(const uint32_t* h, uint32_t krem, uint32_t* res, uint32_t* sh_warp) {
   constexpr int PER = NB / 256;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  if (t == 0) {
+    res[0] = 0u;
+    res[1] = krem;
+  }
   uint32_t mine = 0, suf = 0;
   if (t < 256) {
 #pragma unroll
@@ -121,22 +127,29 @@ __global__ void __launch_bounds__(QR_THREADS) qrot_kernel(DecodeParams p) {
 // score: s_t = q_bar . k^_t for every cached token, straight from the packed
 // segments.  Persistent: CTA i streams the flattened K segments
 // [part[i], part[i+1]) (balanced by bytes at compression time).  One producer
-// warp moves runs of whole, contiguous segments into a ring of shared-memory
-// stages with bulk copies (L2 evict-first); 12 consumer warps score rows from
-// shared memory, one 16-byte chunk (8 channels) per lane, a row's chunks
-// summed in channel order by its first lane.  Scores go to global memory with
-// an L2 evict-last hint for the selection passes; the level-1 radix histogram
-// (key bits 31..20) is built on the way, and the CTA that finishes a stream
-// last turns it into the level-1 bin of the k-th largest score.
-// grid: G, block: 13 warps, dynamic smem n_stages * stage_bytes
+// warp groups runs of whole, contiguous segments into stages of about 52 KB
+// and moves each with one bulk copy (whole 128-byte lines, L2 evict-first)
+// into a ring of shared-memory slots; it also lists the stage's 32-row blocks.
+// 20 consumer warps take those blocks round-robin and score one row per
+// lane from shared memory.  Scores go to global memory with an L2 evict-last
+// hint for the selection passes; the level-1 radix histogram (key bits
+// 31..20) is built on the way, and the CTA that finishes a stream last turns
+// it into the level-1 bin of the k-th largest score.
+// grid: G, block: 21 warps, dynamic smem n_stages * (stage_bytes + 256)
 // ---------------------------------------------------------------------------
-constexpr int SC_CONS = 12;
+constexpr int SC_CONS = 20;
 constexpr int SC_THREADS = (SC_CONS + 1) * 32;
 constexpr int SC_NSLOT = 2;
-constexpr int SC_MAX_STAGES = 8;
-constexpr int SC_MAX_SEGS = 64;   // segments per stage
-constexpr int SC_STATIC_SMEM = SC_NSLOT * HIST1 * 4 + SC_NSLOT * D * 4 + SC_NSLOT * D * 32 * 4 +
-                               SC_CONS * D * 4 + SC_MAX_STAGES * SC_MAX_SEGS * 8 + 1024;
+constexpr int SC_MAX_STAGES = 6;
+constexpr int SC_MAX_SEGS = 64;                  // segments per stage
+constexpr int SC_MAX_ITEMS = SC_MAX_SEGS * 8;    // 32-row blocks per stage (S <= 256)
+constexpr int SC_STAGE_TARGET = 52 * 1024;
+constexpr int SC_STATIC_SMEM = SC_NSLOT * HIST1 * 4 + SC_NSLOT * D * 4 + SC_CONS * D * 4 +
+                               SC_MAX_STAGES * SC_MAX_SEGS * 8 + SC_MAX_STAGES * SC_MAX_ITEMS * 2 +
+                               2048;
+
+// shared-memory bytes of one stage slot: the stage plus slack for line alignment
+__host__ __device__ constexpr size_t sc_slot(int stage_bytes) { return (size_t)stage_bytes + 256; }
 
 // header i of the flattened K segments as two words, or zeros past the end
 __device__ __forceinline__ uint2 load_hdr(const mkv_segment_header* h, int i, int end) {
@@ -145,26 +158,35 @@ __device__ __forceinline__ uint2 load_hdr(const mkv_segment_header* h, int i, in
 
 struct StageMeta {
   int32_t seg0, seg1;
-  uint64_t byte0;
+  uint64_t byte0;      // pool offset of the slot's first byte (128-byte aligned)
+  int32_t n_items;
+  int32_t pad;
 };
 
 // Dot product of one packed row with q_bar, from shared memory; one row per
-// thread.  The 16-byte chunks of the row are visited in an order rotated by
-// the lane, so that lanes reading rows a multiple of 128 B apart hit different
-// banks; q_bar values come from the segment's gathered mask (SM), a
-// bank-replicated table indexed by channel (PV) or q_bar itself (dense).
-template <int STRAT>
-__device__ __forceinline__ float row_dot(const uint8_t* base, int rows, int row, int c, int lane,
-                                         const float* qsrc, const float* qm, const float* qrep) {
-  const int cpr = (STRAT == MKV_STRATEGY_DENSE) ? 16 : (c >> 3);
-  const uint32_t uc = (uint32_t)c;
-  const uint8_t* rowp =
-      (STRAT == MKV_STRATEGY_SM) ? base + pad16(uc) + 2u * uc * row
-      : (STRAT == MKV_STRATEGY_PV) ? base + 2u * uc * row : base + 256u * row;
-  const uint8_t* idxp = base + 2u * uc * (uint32_t)rows + uc * (uint32_t)row;
-  float acc = 0.f;
-  int k = lane % cpr;
-  for (int j = 0; j < cpr; ++j) {
+// thread, CPR = 16-byte chunks per row (c / 8, or 16 for dense rows).  Lane i
+// starts at chunk (i % 8) / P with P = 8 / gcd(CPR, 8): the 8 lanes of a
+// quarter-warp then read 8 different 16-byte bank groups whatever the row
+// stride (16 * CPR bytes), and for odd CPR every lane reads the same chunk of
+// q_bar (a broadcast).  q_bar values come from the segment's gathered mask
+// (SM), q_bar indexed by the stored channel (PV) or q_bar itself (dense).
+// Four independent accumulators, summed in a fixed order.
+template <int STRAT, int CPR>
+__device__ __forceinline__ float row_dot(const uint8_t* base, int rows, int row, int lane,
+                                         const float* qsrc, const float* qm) {
+  constexpr uint32_t C = 8u * CPR;
+  constexpr int G8 = (CPR % 8 == 0) ? 8 : ((CPR % 4 == 0) ? 4 : ((CPR % 2 == 0) ? 2 : 1));
+  constexpr int P = 8 / G8;
+  const uint8_t* rowp = (STRAT == MKV_STRATEGY_SM)   ? base + pad16(C) + 2u * C * row
+                        : (STRAT == MKV_STRATEGY_PV) ? base + 2u * C * row
+                                                     : base + 256u * row;
+  const uint8_t* idxp = base + 2u * C * (uint32_t)rows + C * (uint32_t)row;
+  const int rot = (lane & 7) / P;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < CPR; ++j) {
+    int k = j + rot;
+    k = k >= CPR ? k - CPR : k;
     float v[8];
     h8_to_f(*reinterpret_cast<const uint4*>(rowp + 16 * k), v);
     if (STRAT == MKV_STRATEGY_PV) {
@@ -172,33 +194,60 @@ __device__ __forceinline__ float row_dot(const uint8_t* base, int rows, int row,
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const uint32_t ch = ((e < 4 ? ix.x : ix.y) >> (8 * (e & 3))) & 0x7fu;
-        acc = fmaf(v[e], qrep ? qrep[ch * 32 + lane] : qsrc[ch], acc);
+        acc[e & 3] = fmaf(v[e], qsrc[ch], acc[e & 3]);
       }
     } else {
       const float* qq = (STRAT == MKV_STRATEGY_SM ? qm : qsrc) + 8 * k;
       const float4 a = *reinterpret_cast<const float4*>(qq);
       const float4 b = *reinterpret_cast<const float4*>(qq + 4);
-      acc = fmaf(v[0], a.x, acc);
-      acc = fmaf(v[1], a.y, acc);
-      acc = fmaf(v[2], a.z, acc);
-      acc = fmaf(v[3], a.w, acc);
-      acc = fmaf(v[4], b.x, acc);
-      acc = fmaf(v[5], b.y, acc);
-      acc = fmaf(v[6], b.z, acc);
-      acc = fmaf(v[7], b.w, acc);
+      acc[0] = fmaf(v[0], a.x, acc[0]);
+      acc[1] = fmaf(v[1], a.y, acc[1]);
+      acc[2] = fmaf(v[2], a.z, acc[2]);
+      acc[3] = fmaf(v[3], a.w, acc[3]);
+      acc[0] = fmaf(v[4], b.x, acc[0]);
+      acc[1] = fmaf(v[5], b.y, acc[1]);
+      acc[2] = fmaf(v[6], b.z, acc[2]);
+      acc[3] = fmaf(v[7], b.w, acc[3]);
     }
-    k = (k + 1 == cpr) ? 0 : k + 1;
   }
-  return acc;
+  return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+}
+
+// scores of rows [r0, r0 + 32) of one segment: one row per lane
+template <int STRAT, int CPR>
+__device__ __forceinline__ void score_block(const uint8_t* base, int rows, int r0, int lane,
+                                            const float* qsrc, const float* qm, float* out,
+                                            uint32_t* hs, uint64_t pol) {
+  const int row = r0 + lane;
+  if (row < rows) {
+    const float sc = row_dot<STRAT, CPR>(base, rows, row, lane, qsrc, qm);
+    st_f32_hint(out + row, sc, pol);
+    atomicAdd(&hs[f2key(sc) >> 20], 1u);
+  }
+}
+
+template <int STRAT>
+__device__ __forceinline__ void score_block_c(int cpr, const uint8_t* base, int rows, int r0,
+                                              int lane, const float* qsrc, const float* qm,
+                                              float* out, uint32_t* hs, uint64_t pol) {
+#define MKV_CASE(N) \
+  case N: score_block<STRAT, N>(base, rows, r0, lane, qsrc, qm, out, hs, pol); break;
+  switch (cpr) {
+    MKV_CASE(1) MKV_CASE(2) MKV_CASE(3) MKV_CASE(4) MKV_CASE(5) MKV_CASE(6) MKV_CASE(7)
+    MKV_CASE(8) MKV_CASE(9) MKV_CASE(10) MKV_CASE(11) MKV_CASE(12) MKV_CASE(13) MKV_CASE(14)
+    MKV_CASE(15) MKV_CASE(16)
+    default: break;
+  }
+#undef MKV_CASE
 }
 
 __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
   extern __shared__ __align__(128) uint8_t stage_mem[];
   __shared__ uint64_t full_bar[SC_MAX_STAGES], empty_bar[SC_MAX_STAGES];
   __shared__ StageMeta meta[SC_MAX_STAGES];
-  __shared__ uint2 shdr[SC_MAX_STAGES][SC_MAX_SEGS];   // headers of each stage's segments
+  __shared__ uint2 shdr[SC_MAX_STAGES][SC_MAX_SEGS];         // headers of each stage's segments
+  __shared__ uint16_t sitem[SC_MAX_STAGES][SC_MAX_ITEMS];    // (segment << 8) | 32-row block
   __shared__ __align__(16) float qb[SC_NSLOT][D];
-  __shared__ float qrep[SC_NSLOT][D * 32];   // qrep[.][ch * 32 + lane] = q_bar[ch]
   __shared__ uint32_t hist[SC_NSLOT][HIST1];
   __shared__ __align__(16) float qm[SC_CONS][D];
   __shared__ uint32_t sh_warp[8], sh_res[2];
@@ -209,13 +258,12 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int s_first = a / p.n_seg, s_last = (b - 1) / p.n_seg;
   const int NST = p.n_stages;
+  const size_t slot_bytes = sc_slot(p.stage_bytes);
   for (int x = tid; x < SC_NSLOT * HIST1; x += SC_THREADS) (&hist[0][0])[x] = 0u;
   for (int x = tid; x < SC_NSLOT * D; x += SC_THREADS) {
     const int s = s_first + x / D;
     (&qb[0][0])[x] = (s <= s_last) ? p.qbar[(size_t)s * D + (x % D)] : 0.f;
   }
-  __syncthreads();
-  for (int x = tid; x < SC_NSLOT * D * 32; x += SC_THREADS) (&qrep[0][0])[x] = (&qb[0][0])[x >> 5];
   if (tid == 0) {
     for (int st = 0; st < NST; ++st) {
       mbar_init(&full_bar[st], 1);
@@ -256,7 +304,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
         break;
       }
       uint64_t off0 = 0, end = 0;
-      int e = sg, nseg = 0;
+      int e = sg, nseg = 0, nitem = 0;
       while (e < b && nseg < SC_MAX_SEGS) {
         if (e >= cur_base + 32) {
           cur = nxt;
@@ -272,17 +320,24 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
         if (nseg == 0) off0 = st;
         if (nseg > 0 && se - off0 > (uint64_t)p.stage_bytes) break;
         if (lane == 0) shdr[slot][nseg] = w;
+        const int nblk = (hd.rows + 31) >> 5;   // <= 8
+        if (lane < nblk) sitem[slot][nitem + lane] = (uint16_t)((nseg << 8) | lane);
+        nitem += nblk;
         end = se;
         ++e;
         ++nseg;
       }
       if (lane == 0) {
+        // whole 128-byte lines: start rounded down, end rounded up (the pool
+        // has a 256-byte tail pad and each slot 256 bytes of slack)
+        const uint64_t a0 = off0 & ~127ull, a1 = (end + 127u) & ~127ull;
         meta[slot].seg0 = sg;
         meta[slot].seg1 = e;
-        meta[slot].byte0 = off0;
+        meta[slot].byte0 = a0;
+        meta[slot].n_items = nitem;
         fence_proxy_async();
-        mbar_arrive_expect_tx(&full_bar[slot], (uint32_t)(end - off0));
-        bulk_g2s(stage_mem + (size_t)slot * p.stage_bytes, p.pool + off0, (uint32_t)(end - off0),
+        mbar_arrive_expect_tx(&full_bar[slot], (uint32_t)(a1 - a0));
+        bulk_g2s(stage_mem + (size_t)slot * slot_bytes, p.pool + a0, (uint32_t)(a1 - a0),
                  &full_bar[slot], pol);
       }
       sg = e;
@@ -292,7 +347,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
       if (!ok) atomicExch(p.err, DEV_ERR_TIMEOUT);
       sh_issued = k;
     }
-    __syncwarp();
+    __syncwarp();   // the whole producer warp reaches the block barrier together
   } else {
     // ---- consumers ----------------------------------------------------------
     const uint64_t pol = policy_evict_last();
@@ -309,44 +364,36 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
         ++k;
         break;
       }
-      const uint8_t* sbase = stage_mem + (size_t)slot * p.stage_bytes;
-      int item = 0;
-      for (int sg = m.seg0; sg < m.seg1; ++sg) {
-        const uint2 hw = shdr[slot][sg - m.seg0];
+      const uint8_t* sbase = stage_mem + (size_t)slot * slot_bytes;
+      for (int it = warp; it < m.n_items; it += SC_CONS) {
+        const uint32_t item = sitem[slot][it];
+        const int ls = (int)(item >> 8), blk = (int)(item & 255u);
+        const uint2 hw = shdr[slot][ls];
         const mkv_segment_header hd = *reinterpret_cast<const mkv_segment_header*>(&hw);
+        const int sg = m.seg0 + ls;
         const int rows = hd.rows, strat = hd.strategy;
-        const int nblk = (rows + 31) >> 5;
-        const int first = ((warp - item) % SC_CONS + SC_CONS) % SC_CONS;
-        if (first < nblk) {
-          const uint8_t* base = sbase + ((uint64_t)hd.off16 * 16u - m.byte0);
-          const int s = sg / p.n_seg;
-          const int sl = s - s_first;
-          const float* qsrc = sl < SC_NSLOT ? qb[sl] : p.qbar + (size_t)s * D;
-          const float* qr = sl < SC_NSLOT ? qrep[sl] : nullptr;
-          uint32_t* hs = sl < SC_NSLOT ? hist[sl] : p.hist + (size_t)s * HIST1;
-          float* out = p.scores + (size_t)s * p.Tp + (int64_t)(sg - s * p.n_seg) * p.S;
-          if (strat == MKV_STRATEGY_SM && last_sm != sg) {
+        const uint8_t* base = sbase + ((uint64_t)hd.off16 * 16u - m.byte0);
+        const int s = sg / p.n_seg;
+        const int sl = s - s_first;
+        const float* qsrc = sl < SC_NSLOT ? qb[sl] : p.qbar + (size_t)s * D;
+        uint32_t* hs = sl < SC_NSLOT ? hist[sl] : p.hist + (size_t)s * HIST1;
+        float* out = p.scores + (size_t)s * p.Tp + (int64_t)(sg - s * p.n_seg) * p.S;
+        if (strat == MKV_STRATEGY_SM) {
+          if (last_sm != sg) {
             __syncwarp();
             for (int jj = lane; jj < p.c; jj += 32) qm[warp][jj] = qsrc[base[jj] & 127];
             __syncwarp();
             last_sm = sg;
           }
-          for (int blk = first; blk < nblk; blk += SC_CONS) {
-            const int row = blk * 32 + lane;
-            if (row < rows) {
-              float sc;
-              if (strat == MKV_STRATEGY_SM)
-                sc = row_dot<MKV_STRATEGY_SM>(base, rows, row, p.c, lane, qsrc, qm[warp], qr);
-              else if (strat == MKV_STRATEGY_PV)
-                sc = row_dot<MKV_STRATEGY_PV>(base, rows, row, p.c, lane, qsrc, qm[warp], qr);
-              else
-                sc = row_dot<MKV_STRATEGY_DENSE>(base, rows, row, p.c, lane, qsrc, qm[warp], qr);
-              st_f32_hint(out + row, sc, pol);
-              atomicAdd(&hs[f2key(sc) >> 20], 1u);
-            }
-          }
+          score_block_c<MKV_STRATEGY_SM>(p.c >> 3, base, rows, blk * 32, lane, qsrc, qm[warp],
+                                         out, hs, pol);
+        } else if (strat == MKV_STRATEGY_PV) {
+          score_block_c<MKV_STRATEGY_PV>(p.c >> 3, base, rows, blk * 32, lane, qsrc, qm[warp],
+                                         out, hs, pol);
+        } else {
+          score_block<MKV_STRATEGY_DENSE, 16>(base, rows, blk * 32, lane, qsrc, qm[warp], out, hs,
+                                              pol);
         }
-        item += nblk;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[slot]);
@@ -380,7 +427,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
       __syncthreads();
       find_bin<HIST1>(h, (uint32_t)p.kk, sh_res, sh_warp);
       if (tid == 0) {
-        p.state[s].b1 = sh_res[0];
+        p.state[s].b1 = sh_res[0] & (HIST1 - 1);
         p.state[s].k1 = sh_res[1];
       }
     }
@@ -489,7 +536,7 @@ __global__ void __launch_bounds__(TK_THREADS) topk_pass2_kernel(DecodeParams p) 
   for (uint32_t i = tid; i < N; i += TK_THREADS) atomicAdd(&hbuf[(__ldcg(&cand[i].x) >> 10) & 1023u], 1u);
   __syncthreads();
   find_bin<1024>(hbuf, need, sh_res, sh_warp);
-  const uint32_t bA = sh_res[0], needA = sh_res[1];
+  const uint32_t bA = sh_res[0] & 1023u, needA = sh_res[1];
   // key bits 9..0 among keys in bin bA
   for (int x = tid; x < 1024; x += TK_THREADS) hbuf[x] = 0u;
   __syncthreads();
@@ -499,7 +546,7 @@ __global__ void __launch_bounds__(TK_THREADS) topk_pass2_kernel(DecodeParams p) 
   }
   __syncthreads();
   find_bin<1024>(hbuf, needA, sh_res, sh_warp);
-  const uint32_t bB = sh_res[0], need_eq = sh_res[1];
+  const uint32_t bB = sh_res[0] & 1023u, need_eq = sh_res[1];
   const uint32_t n_eq = hbuf[bB];
   const uint32_t thr = (b1 << 20) | (bA << 10) | bB;
   __syncthreads();
@@ -523,7 +570,7 @@ __global__ void __launch_bounds__(TK_THREADS) topk_pass2_kernel(DecodeParams p) 
       __syncthreads();
       if (lev == 0) find_bin<2048>(hbuf, krem, sh_res, sh_warp);
       else find_bin<1024>(hbuf, krem, sh_res, sh_warp);
-      prefix = (prefix << (lev == 0 ? 0 : 10)) | sh_res[0];
+      prefix = (prefix << (lev == 0 ? 0 : 10)) | (sh_res[0] & (uint32_t)(nb - 1));
       krem = sh_res[1];
     }
     t_cut = (int32_t)(0x7fffffffu - prefix);
@@ -588,12 +635,14 @@ __global__ void __launch_bounds__(TK_THREADS) topk_write_kernel(DecodeParams p) 
 // ---------------------------------------------------------------------------
 // attn: split-K attention of the g query heads over a chunk of <= 128
 // selected tokens, reading the packed K/V rows in place (fp16 values + uint8
-// channel indices), one token per thread with all of its row loads in flight.
-// Each thread writes its V row into a zeroed fp16 tile (rows padded to 65
-// words, so lanes writing one channel of 32 rows hit 32 banks); after the
-// softmax statistics, thread j sums p_t,i * V[t][j] over the tile's tokens in
-// order.  Partials per (stream, chunk, head): max logit m, sum of exp l and
-// the unnormalised output in the rotated V basis.
+// channel indices).  Row addresses of the chunk are resolved first.  Then a
+// group of 8 lanes serves a token, one 16-byte chunk (8 stored values) per
+// lane, and every thread fetches the chunks of its tokens together: K chunks
+// give partial logits (summed over the 8 lanes by a fixed butterfly), V
+// chunks are copied into a zeroed fp16 tile V[token][channel] (rows padded to
+// 65 words).  After the softmax statistics, thread j sums p_t,i * V[t][j] over
+// the tokens in order.  Partials per (stream, chunk, head): max logit m, sum
+// of exp l and the unnormalised output in the rotated V basis.
 // grid: (attn_chunks, BH), block 128, dynamic smem
 // ---------------------------------------------------------------------------
 constexpr int ATTN_THREADS = 128;
@@ -623,91 +672,122 @@ __device__ __forceinline__ void row_addr(const mkv_segment_header* hdr, int64_t 
 
 size_t attn_smem_bytes(int g, int chunk) {
   const int gp = (g + 3) & ~3;
-  return (size_t)chunk * VD_LD * 2 + sizeof(float) * ((size_t)D * gp + (size_t)chunk * g + 2 * g);
+  return (size_t)chunk * VD_LD * 2 + (size_t)chunk * (4 * 8 + 2 * 4) +
+         sizeof(float) * ((size_t)D * gp + (size_t)chunk * gp + 2 * g);
 }
 
-__global__ void __launch_bounds__(ATTN_THREADS) attn_kernel(DecodeParams p) {
-  extern __shared__ __align__(16) uint8_t asm_[];
-  const int s = blockIdx.y, chk = blockIdx.x;
-  const int b = s / p.H, h = s % p.H;
+__device__ __forceinline__ int chan_of(const uint2& x, int e) {
+  return (int)(((e < 4 ? x.x : x.y) >> (8 * (e & 3))) & 0x7fu);
+}
+
+// everything after the row addresses; GM = heads per instantiation (4 or 16)
+template <int GM>
+__device__ __forceinline__ void attn_body(const DecodeParams& p, int s, int chk, int n,
+                                          const uint64_t* kv_, const uint64_t* ki_,
+                                          const int* kn_, const uint64_t* vv_,
+                                          const uint64_t* vi_, const int* vn_, __half* Vd,
+                                          const float* qs, float* lg, float* ml) {
   const int g = p.g, gp = (g + 3) & ~3;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int CH = p.attn_chunk;
-  __half* Vd = reinterpret_cast<__half*>(asm_);                     // [CH][VD_LD]
-  float* qs = reinterpret_cast<float*>(asm_ + (size_t)CH * VD_LD * 2);  // [128][gp]
-  float* lg = qs + D * gp;                                          // [CH][g]
-  float* ml = lg + CH * g;                                          // [g][2]
-  const float* qt = p.qt + ((size_t)b * p.Hq + (size_t)h * g) * D;
-  for (int x = tid; x < g * D; x += ATTN_THREADS) qs[(x % D) * gp + x / D] = qt[x];
-  {
-    uint32_t* z = reinterpret_cast<uint32_t*>(Vd);
-    for (int x = tid; x < CH * VD_LD / 2; x += ATTN_THREADS) z[x] = 0u;
-  }
-  const int j0 = chk * CH;
-  const int n = min(CH, p.kk - j0);
-  __syncthreads();
-  const float scale = 0.08838834764831845f;   // 1 / sqrt(128)
-  if (tid < n) {
-    const int64_t t = clamp_t(p.sel[(size_t)s * p.kk + j0 + tid], p.T);
-    uint64_t kvo, kio, vvo, vio;
-    int kn, vn;
-    row_addr(p.hdrK + (size_t)s * p.n_seg, t, p.S, p.c, &kvo, &kio, &kn);
-    row_addr(p.hdrV + (size_t)s * p.n_seg, t, p.S, p.c, &vvo, &vio, &vn);
-    // ---- V row -> tile (values are stored fp16; copied exactly) -------------
-    {
-      const uint8_t* vals = p.pool + vvo;
-      const bool dense = vio == NO_IDX;
-      const uint8_t* idx = dense ? nullptr : p.pool + vio;
-      __half* row = Vd + (size_t)tid * VD_LD;
-      for (int k8 = 0; k8 < vn; k8 += 8) {
-        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(vals + 2 * k8));
-        const __half* hv = reinterpret_cast<const __half*>(&raw);
-        if (dense) {
+  const int cl = tid & 7, tg = tid >> 3;
+  constexpr int U = 4;                          // tokens per thread per batch
+  const float scale = 0.08838834764831845f;     // 1 / sqrt(128)
+  // ---- logits and V tile: 8 lanes per token, 8 tokens per thread ---------
+  for (int base = 0; base < ATTN_THREADS / 16; base += U) {
+    uint4 kvv[U], vvv[U];
+    uint2 kix[U], vix[U];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) row[k8 + e] = hv[e];
-        } else {
-          const uint2 ix = __ldg(reinterpret_cast<const uint2*>(idx + k8));
-#pragma unroll
-          for (int e = 0; e < 8; ++e) row[((e < 4 ? ix.x : ix.y) >> (8 * (e & 3))) & 0x7fu] = hv[e];
+    for (int u = 0; u < U; ++u) {
+      const int i = tg + 16 * (base + u);
+      kvv[u] = vvv[u] = make_uint4(0u, 0u, 0u, 0u);
+      kix[u] = vix[u] = make_uint2(0u, 0u);
+      if (i < n) {
+        if (8 * cl < kn_[i]) {
+          kvv[u] = __ldg(reinterpret_cast<const uint4*>(p.pool + kv_[i]) + cl);
+          if (ki_[i] != NO_IDX) kix[u] = __ldg(reinterpret_cast<const uint2*>(p.pool + ki_[i]) + cl);
+        }
+        if (8 * cl < vn_[i]) {
+          vvv[u] = __ldg(reinterpret_cast<const uint4*>(p.pool + vv_[i]) + cl);
+          if (vi_[i] != NO_IDX) vix[u] = __ldg(reinterpret_cast<const uint2*>(p.pool + vi_[i]) + cl);
         }
       }
     }
-    // ---- logits --------------------------------------------------------------
-    float part[MAX_G];
 #pragma unroll
-    for (int hh = 0; hh < MAX_G; ++hh) part[hh] = 0.f;
-    const uint8_t* vals = p.pool + kvo;
-    const bool dense = kio == NO_IDX;
-    const uint8_t* idx = dense ? nullptr : p.pool + kio;
-    for (int k8 = 0; k8 < kn; k8 += 8) {
-      float v[8];
-      h8_to_f(__ldg(reinterpret_cast<const uint4*>(vals + 2 * k8)), v);
-      uint2 ix = make_uint2(0u, 0u);
-      if (!dense) ix = __ldg(reinterpret_cast<const uint2*>(idx + k8));
+    for (int u = 0; u < U; ++u) {
+      const int i = tg + 16 * (base + u);
+      float part[GM];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int chn = dense ? (k8 + e) : (int)(((e < 4 ? ix.x : ix.y) >> (8 * (e & 3))) & 0x7fu);
-        const float* qq = qs + chn * gp;
+      for (int hh = 0; hh < GM; ++hh) part[hh] = 0.f;
+      if (i < n) {
+        // rows with more than 64 stored values (dense, or c > 64) have chunks 8..15
+        for (int ck = cl; ck < 16; ck += 8) {
+          uint4 kr = kvv[u], vr = vvv[u];
+          uint2 kx = kix[u], vx = vix[u];
+          if (ck >= 8) {
+            if (8 * ck >= kn_[i] && 8 * ck >= vn_[i]) break;
+            kr = vr = make_uint4(0u, 0u, 0u, 0u);
+            kx = vx = make_uint2(0u, 0u);
+            if (8 * ck < kn_[i]) {
+              kr = __ldg(reinterpret_cast<const uint4*>(p.pool + kv_[i]) + ck);
+              if (ki_[i] != NO_IDX) kx = __ldg(reinterpret_cast<const uint2*>(p.pool + ki_[i]) + ck);
+            }
+            if (8 * ck < vn_[i]) {
+              vr = __ldg(reinterpret_cast<const uint4*>(p.pool + vv_[i]) + ck);
+              if (vi_[i] != NO_IDX) vx = __ldg(reinterpret_cast<const uint2*>(p.pool + vi_[i]) + ck);
+            }
+          }
+          if (8 * ck < vn_[i]) {
+            const __half* hv = reinterpret_cast<const __half*>(&vr);
+            __half* vrow = Vd + (size_t)i * VD_LD;
+            const bool dense = vi_[i] == NO_IDX;
 #pragma unroll
-        for (int hh = 0; hh < MAX_G; ++hh)
-          if (hh < g) part[hh] = fmaf(qq[hh], v[e], part[hh]);
+            for (int e = 0; e < 8; ++e) vrow[dense ? 8 * ck + e : chan_of(vx, e)] = hv[e];
+          }
+          if (8 * ck < kn_[i]) {
+            float v[8];
+            h8_to_f(kr, v);
+            const bool dense = ki_[i] == NO_IDX;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float* qq = qs + (dense ? 8 * ck + e : chan_of(kx, e)) * gp;
+#pragma unroll
+              for (int h4 = 0; h4 < GM; h4 += 4) {
+                if (h4 < g) {
+                  const float4 q4 = *reinterpret_cast<const float4*>(qq + h4);
+                  part[h4] = fmaf(q4.x, v[e], part[h4]);
+                  part[h4 + 1] = fmaf(q4.y, v[e], part[h4 + 1]);
+                  part[h4 + 2] = fmaf(q4.z, v[e], part[h4 + 2]);
+                  part[h4 + 3] = fmaf(q4.w, v[e], part[h4 + 3]);
+                }
+              }
+            }
+          }
+        }
+      }
+      // sum over the token's 8 lanes (fixed butterfly order)
+#pragma unroll
+      for (int hh = 0; hh < GM; ++hh) {
+        if (hh < gp) {
+          float x = part[hh];
+          x += __shfl_xor_sync(0xffffffffu, x, 1);
+          x += __shfl_xor_sync(0xffffffffu, x, 2);
+          x += __shfl_xor_sync(0xffffffffu, x, 4);
+          if (cl == 0 && i < n) lg[i * gp + hh] = x * scale;
+        }
       }
     }
-#pragma unroll
-    for (int hh = 0; hh < MAX_G; ++hh)
-      if (hh < g) lg[tid * g + hh] = part[hh] * scale;
   }
   __syncthreads();
   // ---- softmax statistics per head (warp per head, fixed-order reductions) --
   for (int hh = warp; hh < g; hh += ATTN_THREADS / 32) {
     float m = -INFINITY;
-    for (int i = lane; i < n; i += 32) m = fmaxf(m, lg[i * g + hh]);
+    for (int i = lane; i < n; i += 32) m = fmaxf(m, lg[i * gp + hh]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
     float l = 0.f;
     for (int i = lane; i < n; i += 32) {
-      const float e = expf(lg[i * g + hh] - m);
-      lg[i * g + hh] = e;
+      const float e = expf(lg[i * gp + hh] - m);
+      lg[i * gp + hh] = e;
       l += e;
     }
 #pragma unroll
@@ -720,20 +800,65 @@ __global__ void __launch_bounds__(ATTN_THREADS) attn_kernel(DecodeParams p) {
   __syncthreads();
   // ---- o~_i[j] = sum_t p_t,i V[t][j]: thread j, tokens in order ------------
   const int jc = tid;   // channel
-  float o[MAX_G];
+  float o[GM];
 #pragma unroll
-  for (int hh = 0; hh < MAX_G; ++hh) o[hh] = 0.f;
+  for (int hh = 0; hh < GM; ++hh) o[hh] = 0.f;
   for (int i = 0; i < n; ++i) {
     const float v = __half2float(Vd[(size_t)i * VD_LD + jc]);
 #pragma unroll
-    for (int hh = 0; hh < MAX_G; ++hh)
-      if (hh < g) o[hh] = fmaf(lg[i * g + hh], v, o[hh]);
+    for (int h4 = 0; h4 < GM; h4 += 4) {
+      if (h4 < g) {
+        const float4 p4 = *reinterpret_cast<const float4*>(lg + i * gp + h4);
+        o[h4] = fmaf(p4.x, v, o[h4]);
+        o[h4 + 1] = fmaf(p4.y, v, o[h4 + 1]);
+        o[h4 + 2] = fmaf(p4.z, v, o[h4 + 2]);
+        o[h4 + 3] = fmaf(p4.w, v, o[h4 + 3]);
+      }
+    }
   }
   const size_t pbase = ((size_t)s * p.attn_chunks + chk) * g;
 #pragma unroll
-  for (int hh = 0; hh < MAX_G; ++hh)
+  for (int hh = 0; hh < GM; ++hh)
     if (hh < g) p.part_o[(pbase + hh) * D + jc] = o[hh];
   if (tid < 2 * g) p.part_ml[pbase * 2 + tid] = ml[tid];
+}
+
+__global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(DecodeParams p) {
+  extern __shared__ __align__(16) uint8_t asm_[];
+  const int s = blockIdx.y, chk = blockIdx.x;
+  const int b = s / p.H, h = s % p.H;
+  const int g = p.g, gp = (g + 3) & ~3;
+  const int tid = threadIdx.x;
+  const int CH = p.attn_chunk;
+  __half* Vd = reinterpret_cast<__half*>(asm_);                                // [CH][VD_LD]
+  uint64_t* kv_ = reinterpret_cast<uint64_t*>(asm_ + (size_t)CH * VD_LD * 2);  // [CH]
+  uint64_t* ki_ = kv_ + CH;
+  uint64_t* vv_ = ki_ + CH;
+  uint64_t* vi_ = vv_ + CH;
+  int* kn_ = reinterpret_cast<int*>(vi_ + CH);
+  int* vn_ = kn_ + CH;
+  float* qs = reinterpret_cast<float*>(vn_ + CH);                              // [128][gp]
+  float* lg = qs + D * gp;                                                     // [CH][gp]
+  float* ml = lg + CH * gp;                                                    // [g][2]
+  const float* qt = p.qt + ((size_t)b * p.Hq + (size_t)h * g) * D;
+  for (int x = tid; x < D * gp; x += ATTN_THREADS) {
+    const int chn = x / gp, hh = x % gp;
+    qs[x] = hh < g ? qt[hh * D + chn] : 0.f;
+  }
+  {
+    uint32_t* z = reinterpret_cast<uint32_t*>(Vd);
+    for (int x = tid; x < CH * VD_LD / 2; x += ATTN_THREADS) z[x] = 0u;
+  }
+  const int j0 = chk * CH;
+  const int n = min(CH, p.kk - j0);
+  if (tid < n) {
+    const int64_t t = clamp_t(p.sel[(size_t)s * p.kk + j0 + tid], p.T);
+    row_addr(p.hdrK + (size_t)s * p.n_seg, t, p.S, p.c, &kv_[tid], &ki_[tid], &kn_[tid]);
+    row_addr(p.hdrV + (size_t)s * p.n_seg, t, p.S, p.c, &vv_[tid], &vi_[tid], &vn_[tid]);
+  }
+  __syncthreads();
+  if (g <= 4) attn_body<4>(p, s, chk, n, kv_, ki_, kn_, vv_, vi_, vn_, Vd, qs, lg, ml);
+  else attn_body<MAX_G>(p, s, chk, n, kv_, ki_, kn_, vv_, vi_, vn_, Vd, qs, lg, ml);
 }
 
 // ---------------------------------------------------------------------------
@@ -761,7 +886,12 @@ __global__ void __launch_bounds__(MG_THREADS) merge_kernel(DecodeParams p) {
       Rs4[tid + x * MG_THREADS] = __ldg(R4 + tid + x * MG_THREADS);
   }
   const float* ml = p.part_ml + (size_t)s * nc * g * 2;
-  for (int x = tid; x < nc * g; x += MG_THREADS) wsm[x] = ml[2 * x];   // m of (chunk, head)
+  float* lsm = wsm + nc * g;       // [attn_chunks][g] sums of exp
+  for (int x = tid; x < nc * g; x += MG_THREADS) {
+    const float2 v = __ldg(reinterpret_cast<const float2*>(ml) + x);   // (m, l) of (chunk, head)
+    wsm[x] = v.x;
+    lsm[x] = v.y;
+  }
   __syncthreads();
   if (tid < g) {
     float M = -INFINITY;
@@ -770,7 +900,7 @@ __global__ void __launch_bounds__(MG_THREADS) merge_kernel(DecodeParams p) {
     for (int c = 0; c < nc; ++c) {
       const float w = expf(wsm[c * g + tid] - M);
       wsm[c * g + tid] = w;
-      L = fmaf(ml[2 * (c * g + tid) + 1], w, L);
+      L = fmaf(lsm[c * g + tid], w, L);
     }
     Linv[tid] = 1.f / L;
   }
@@ -840,9 +970,9 @@ void score_stage_plan(int S, int c, int* stage_bytes, int* n_stages) {
     const uint32_t b = segment_bytes(st, S, c);
     mx = mx > b ? mx : b;
   }
-  const int sb = (int)(mx > 32768u ? mx : 32768u);
+  const int sb = (int)(mx > (uint32_t)SC_STAGE_TARGET ? mx : (uint32_t)SC_STAGE_TARGET);
   const int budget = 227 * 1024 - SC_STATIC_SMEM;
-  int ns = budget / sb;
+  int ns = budget / (int)sc_slot(sb);
   ns = ns > SC_MAX_STAGES ? SC_MAX_STAGES : ns;
   *stage_bytes = sb;
   *n_stages = ns;
@@ -853,7 +983,7 @@ cudaError_t prepare_decode_kernels() {
                                        (int)attn_smem_bytes(MAX_G, ATTN_MAX_CHUNK));
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)(sizeof(float) * D * D) + 48 * 1024);
+                           (int)(sizeof(float) * D * D) + 2 * 48 * 1024);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(qrot_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, D * D * 4);
   if (e != cudaSuccess) return e;
@@ -873,7 +1003,7 @@ cudaError_t launch_qrot(const DecodeParams& p, cudaStream_t st) {
 }
 
 cudaError_t launch_score(const DecodeParams& p, cudaStream_t st) {
-  score_kernel<<<p.G, SC_THREADS, (size_t)p.stage_bytes * p.n_stages, st>>>(p);
+  score_kernel<<<p.G, SC_THREADS, sc_slot(p.stage_bytes) * p.n_stages, st>>>(p);
   return cudaGetLastError();
 }
 
@@ -891,8 +1021,8 @@ cudaError_t launch_attn(const DecodeParams& p, cudaStream_t st) {
 }
 
 cudaError_t launch_merge(const DecodeParams& p, cudaStream_t st) {
-  merge_kernel<<<p.B * p.H, MG_THREADS, sizeof(float) * ((size_t)D * D + (size_t)p.attn_chunks * p.g),
-                 st>>>(p);
+  merge_kernel<<<p.B * p.H, MG_THREADS,
+                 sizeof(float) * ((size_t)D * D + 2 * (size_t)p.attn_chunks * p.g), st>>>(p);
   return cudaGetLastError();
 }
 

@@ -401,16 +401,18 @@ mkv_status mkv_compress(mkv_ctx* c, const void* k, const void* v, int64_t ctx_le
     g_last_error = "packed cache exceeds max_pool_bytes";
     return MKV_ERR_OOM;
   }
-  if (total > c->pool_cap) {
+  // the score kernel copies whole 128-byte lines: 256 bytes of tail padding
+  const uint64_t need = total + 256;
+  if (need > c->pool_cap) {
     uint8_t* np = nullptr;
-    cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&np), total);
+    cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&np), need);
     if (e != cudaSuccess) {
       cudaGetLastError();
       return cuda_fail(e, "cudaMalloc(pool)");
     }
     CK(cudaFree(c->pool));   // synchronises: no decode still reads the old pool
     c->pool = np;
-    c->pool_cap = total;
+    c->pool_cap = need;
   }
   p.pool = c->pool;
   c->ready = false;   // the live headers may no longer match the pool

@@ -5,7 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/mkv.h"
+#include "mkv.h"
 
 namespace mkv {
 
