@@ -65,6 +65,9 @@ enum {
 #define MKV_HEAD_DIM 128
 /* Record CUDA events around every decode kernel; read with mkv_kernel_time. */
 #define MKV_FLAG_KERNEL_TIMING 1u
+/* Record CUDA events around the score kernel only (fewer event records in a
+ * captured step); read with mkv_kernel_time(ctx, MKV_KERNEL_SCORE, ...). */
+#define MKV_FLAG_SCORE_TIMING 2u
 
 typedef struct {
   int32_t batch;          /* B >= 1 */

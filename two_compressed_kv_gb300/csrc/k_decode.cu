@@ -354,7 +354,10 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
     int k = 0, last_sm = -1;
     while (true) {
       const int slot = k % NST, use = k / NST;
-      const bool got = __all_sync(0xffffffffu, mbar_wait(&full_bar[slot], use & 1));
+      // one lane polls the barrier for the warp
+      int got = 1;
+      if (lane == 0) got = mbar_wait(&full_bar[slot], use & 1);
+      got = __shfl_sync(0xffffffffu, got, 0);
       if (!got) {
         if (lane == 0) atomicExch(p.err, DEV_ERR_TIMEOUT);
         break;
@@ -885,31 +888,30 @@ __global__ void __launch_bounds__(MG_THREADS) merge_kernel(DecodeParams p) {
     for (int x = 0; x < D * D / 4 / MG_THREADS; ++x)
       Rs4[tid + x * MG_THREADS] = __ldg(R4 + tid + x * MG_THREADS);
   }
-  const float* ml = p.part_ml + (size_t)s * nc * g * 2;
-  float* lsm = wsm + nc * g;       // [attn_chunks][g] sums of exp
-  for (int x = tid; x < nc * g; x += MG_THREADS) {
-    const float2 v = __ldg(reinterpret_cast<const float2*>(ml) + x);   // (m, l) of (chunk, head)
-    wsm[x] = v.x;
-    lsm[x] = v.y;
-  }
-  __syncthreads();
-  if (tid < g) {
+  // weights exp(m_c - M) and 1 / L per head: warp per head, lanes over chunks
+  const float2* ml = reinterpret_cast<const float2*>(p.part_ml + (size_t)s * nc * g * 2);
+  for (int hh = warp; hh < g; hh += MG_THREADS / 32) {
     float M = -INFINITY;
-    for (int c = 0; c < nc; ++c) M = fmaxf(M, wsm[c * g + tid]);
+    for (int c = lane; c < nc; c += 32) M = fmaxf(M, __ldg(ml + c * g + hh).x);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     float L = 0.f;
-    for (int c = 0; c < nc; ++c) {
-      const float w = expf(wsm[c * g + tid] - M);
-      wsm[c * g + tid] = w;
-      L = fmaf(lsm[c * g + tid], w, L);
+    for (int c = lane; c < nc; c += 32) {
+      const float2 v = __ldg(ml + c * g + hh);
+      const float w = expf(v.x - M);
+      wsm[c * g + hh] = w;
+      L = fmaf(v.y, w, L);
     }
-    Linv[tid] = 1.f / L;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    if (lane == 0) Linv[hh] = 1.f / L;
   }
   __syncthreads();
   const float* po = p.part_o + (size_t)s * nc * g * D;
   for (int x = tid; x < g * D; x += MG_THREADS) {
     const int hh = x / D;
     float o = 0.f;
-#pragma unroll 8
+#pragma unroll 32
     for (int c = 0; c < nc; ++c) o = fmaf(__ldg(po + (size_t)c * g * D + x), wsm[c * g + hh], o);
     ot[hh][x % D] = o * Linv[hh];
   }
@@ -1022,7 +1024,7 @@ cudaError_t launch_attn(const DecodeParams& p, cudaStream_t st) {
 
 cudaError_t launch_merge(const DecodeParams& p, cudaStream_t st) {
   merge_kernel<<<p.B * p.H, MG_THREADS,
-                 sizeof(float) * ((size_t)D * D + 2 * (size_t)p.attn_chunks * p.g), st>>>(p);
+                 sizeof(float) * ((size_t)D * D + (size_t)p.attn_chunks * p.g), st>>>(p);
   return cudaGetLastError();
 }
 

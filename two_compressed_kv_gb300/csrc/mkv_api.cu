@@ -95,7 +95,10 @@ struct mkv_ctx {
 
 namespace {
 
-bool timing_on(const mkv_ctx* c) { return (c->cfg.flags & MKV_FLAG_KERNEL_TIMING) != 0u; }
+bool timing_on(const mkv_ctx* c, int id) {
+  return (c->cfg.flags & MKV_FLAG_KERNEL_TIMING) != 0u ||
+         (id == MKV_KERNEL_SCORE && (c->cfg.flags & MKV_FLAG_SCORE_TIMING) != 0u);
+}
 
 mkv_status resolve_timer(KernelTimer& t, size_t keep) {
   while (t.pending.size() > keep) {
@@ -135,7 +138,7 @@ cudaError_t record(cudaEvent_t ev, cudaStream_t st) {
 template <typename F>
 mkv_status timed(mkv_ctx* c, int id, cudaStream_t st, int n_kernels, F launch) {
   cudaEvent_t a = nullptr, b = nullptr;
-  if (timing_on(c)) {
+  if (timing_on(c, id)) {
     if (c->timers[id].pending.size() >= 4096) {
       mkv_status s = resolve_timer(c->timers[id], 2048);
       if (s != MKV_OK) return s;
@@ -148,7 +151,7 @@ mkv_status timed(mkv_ctx* c, int id, cudaStream_t st, int n_kernels, F launch) {
   }
   CK(launch());
   c->launches += n_kernels;
-  if (timing_on(c)) {
+  if (timing_on(c, id)) {
     CK(record(b, st));
     c->timers[id].pending.emplace_back(a, b);
     c->timers[id].launches += 1;
@@ -247,7 +250,7 @@ mkv_status mkv_validate_config(const mkv_config* cfg) {
   if (c.top_k < 1) return MKV_ERR_INVALID_ARG;
   if (c.attn_chunk != 0 && (c.attn_chunk < 8 || c.attn_chunk > ATTN_MAX_CHUNK || c.attn_chunk % 8 != 0))
     return MKV_ERR_INVALID_ARG;
-  if (c.flags & ~MKV_FLAG_KERNEL_TIMING) return MKV_ERR_INVALID_ARG;
+  if (c.flags & ~(MKV_FLAG_KERNEL_TIMING | MKV_FLAG_SCORE_TIMING)) return MKV_ERR_INVALID_ARG;
   if (c.device < 0) return MKV_ERR_INVALID_ARG;
   const int64_t streams = (int64_t)c.batch * c.n_kv_heads;
   if (streams > (1 << 20)) return MKV_ERR_INVALID_ARG;

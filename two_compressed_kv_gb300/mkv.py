@@ -27,6 +27,7 @@ MKV_ERR_TIMEOUT = 6
 
 MKV_STRATEGY_SM, MKV_STRATEGY_PV, MKV_STRATEGY_DENSE = 0, 1, 2
 MKV_FLAG_KERNEL_TIMING = 1
+MKV_FLAG_SCORE_TIMING = 2
 MKV_KERNEL_QROT, MKV_KERNEL_SCORE, MKV_KERNEL_TOPK, MKV_KERNEL_ATTN, MKV_KERNEL_MERGE = range(5)
 KERNEL_NAMES = ["qrot", "score", "topk", "attn", "merge"]
 
