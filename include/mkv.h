@@ -208,6 +208,54 @@ mkv_status mkv_check_device(mkv_ctx* ctx);
 mkv_status mkv_kernel_time(mkv_ctx* ctx, int kernel_id, double* total_ms,
                            int64_t* launches, int reset);
 
+/* Size of the library's static device buffer used by mkv_basis_static. */
+#define MKV_BASIS_STATIC_MAX_BYTES (16u << 20)
+
+/* The basis step of mkv_compress alone, without a ctx and without allocating
+ * any memory.  The paper has no counterpart of this call: it is an interface
+ * addition of this library.
+ *
+ * Who it is for: callers that must not allocate device memory at the point of
+ * the call, or that hold no ctx (mkv_create allocates a whole layer's buffers)
+ * -- e.g. code whose device memory is all reserved by its framework's caching
+ * allocator, where a cudaMalloc could fail or stall the device, and that wants
+ * the per-stream bases of a prefill chunk (to inspect, calibrate or reuse).
+ * The call itself performs no cudaMalloc, cudaFree or other allocating
+ * routine: its scratch (the per-chunk partial Gram matrices, 64 KiB each) is a
+ * file-scope static device array of MKV_BASIS_STATIC_MAX_BYTES (16 MiB) inside
+ * the library.
+ *
+ * Result: the same as the bases and eigenvalues mkv_compress computes for the
+ * same k, v (see mkv_compress and mkv_export for the definition and layout).
+ * When 2 * batch * n_kv_heads * chunks * 64 KiB fits the buffer with the
+ * number of Gram chunks mkv_compress would use, the summation order is the
+ * same and so are the bits; otherwise fewer chunks are used and the results
+ * agree to fp32 rounding.
+ *   k, v:    device fp16 [batch][n_kv_heads][ctx_len][128], contiguous,
+ *            16-byte aligned; only read.
+ *   basis:   device float [2][batch * n_kv_heads][128][128] (K streams, then
+ *            V streams); R[r*128 + j] = entry r of basis vector j.  Written.
+ *   eigvals: device float [2][batch * n_kv_heads][128], descending.  Written.
+ *   All four buffers belong to the caller; nothing is kept after the call.
+ * Limits: 2 * batch * n_kv_heads <= 256 (one 64 KiB partial per stream must
+ * fit the buffer); larger requests return MKV_ERR_INVALID_ARG before any CUDA
+ * call, with the reason in mkv_last_error_string.  So do NULL pointers,
+ * unaligned k or v, batch, n_kv_heads or ctx_len < 1.
+ * Device: the calling thread's current CUDA device.  The first call on each
+ * device looks the buffer's address up (cudaGetSymbolAddress), which may load
+ * the library's device code on that device and reserve the buffer there; make
+ * that first call before any stream capture begins.  Later calls on the same
+ * device only launch two kernels on `stream` (asynchronous, no host
+ * synchronisation).
+ * Nothing in the buffer needs to start at zero: every partial Gram matrix is
+ * written in full before it is read.
+ * The buffer is shared by every call on a device: calls that may overlap in
+ * time (different streams, different host threads) race on it and give
+ * undefined results.  Issue them on one stream, or order them with events. */
+mkv_status mkv_basis_static(const void* k, const void* v, int batch, int n_kv_heads,
+                            int64_t ctx_len, float* basis, float* eigvals,
+                            mkv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

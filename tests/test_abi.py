@@ -108,3 +108,16 @@ def test_status_strings_and_null_safety(M):
     assert M.lib.mkv_decode(None, None, None, None, None) == M.MKV_ERR_INVALID_ARG
     assert M.lib.mkv_compress(None, None, None, 1, None) == M.MKV_ERR_INVALID_ARG
     assert M.lib.mkv_stats(None, None) == M.MKV_ERR_INVALID_ARG
+
+
+def test_basis_static_rejects_before_any_cuda_call(M):
+    """Oversized, NULL and unaligned requests fail on the host; the pointers
+    below are never dereferenced."""
+    p = ctypes.c_void_p(1 << 20)
+    assert M.lib.mkv_basis_static(p, p, 16, 9, 64, p, p, None) == M.MKV_ERR_INVALID_ARG
+    msg = M.mkv_last_error_string()
+    assert "288 streams" in msg and str(M.MKV_BASIS_STATIC_MAX_BYTES) in msg
+    assert M.lib.mkv_basis_static(None, p, 1, 1, 64, p, p, None) == M.MKV_ERR_INVALID_ARG
+    assert M.lib.mkv_basis_static(p, p, 1, 1, 0, p, p, None) == M.MKV_ERR_INVALID_ARG
+    q = ctypes.c_void_p((1 << 20) + 8)
+    assert M.lib.mkv_basis_static(q, p, 1, 1, 64, p, p, None) == M.MKV_ERR_INVALID_ARG

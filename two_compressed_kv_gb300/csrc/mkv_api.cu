@@ -3,6 +3,7 @@
 #include <algorithm>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <string>
 #include <utility>
@@ -209,6 +210,33 @@ int gram_chunks_for(int BH, int64_t T) {
   int64_t ch = ceil_div(target, 2 * (int64_t)BH);
   ch = std::min<int64_t>(ch, std::max<int64_t>(1, ceil_div(T, 256)));
   return (int)std::max<int64_t>(1, ch);
+}
+
+}  // namespace
+
+// Scratch of mkv_basis_static: the partial Gram matrices of every (stream,
+// chunk), each 128 x 128 fp32.  A file-scope static device array, so that the
+// call allocates nothing; its address is looked up once per device.
+static __device__ __align__(256) unsigned char g_basis_scratch[MKV_BASIS_STATIC_MAX_BYTES];
+
+namespace {
+
+constexpr int64_t kGramPartBytes = (int64_t)D * D * sizeof(float);
+constexpr int64_t kBasisStaticParts = MKV_BASIS_STATIC_MAX_BYTES / kGramPartBytes;
+constexpr int kMaxDevices = 256;
+std::mutex g_basis_scratch_mu;
+float* g_basis_scratch_addr[kMaxDevices] = {};
+
+// The buffer's address on the current device (looked up on first use).
+mkv_status basis_scratch_on(int dev, float** out) {
+  std::lock_guard<std::mutex> lock(g_basis_scratch_mu);
+  if (!g_basis_scratch_addr[dev]) {
+    void* a = nullptr;
+    CK(cudaGetSymbolAddress(&a, g_basis_scratch));
+    g_basis_scratch_addr[dev] = static_cast<float*>(a);
+  }
+  *out = g_basis_scratch_addr[dev];
+  return MKV_OK;
 }
 
 }  // namespace
@@ -570,6 +598,61 @@ mkv_status mkv_kernel_time(mkv_ctx* c, int kernel_id, double* total_ms, int64_t*
     t.total_ms = 0.0;
     t.launches = 0;
   }
+  return MKV_OK;
+}
+
+mkv_status mkv_basis_static(const void* k, const void* v, int batch, int n_kv_heads,
+                            int64_t ctx_len, float* basis, float* eigvals,
+                            mkv_stream_t stream) {
+  if (!k || !v || !basis || !eigvals) {
+    g_last_error = "mkv_basis_static: NULL buffer";
+    return MKV_ERR_INVALID_ARG;
+  }
+  if (batch < 1 || n_kv_heads < 1 || ctx_len < 1) {
+    g_last_error = "mkv_basis_static: batch, n_kv_heads and ctx_len must be >= 1";
+    return MKV_ERR_INVALID_ARG;
+  }
+  if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15u) {
+    g_last_error = "mkv_basis_static: k and v must be 16-byte aligned";
+    return MKV_ERR_INVALID_ARG;
+  }
+  const int64_t streams = 2 * (int64_t)batch * n_kv_heads;
+  if (streams > kBasisStaticParts) {
+    char buf[256];
+    snprintf(buf, sizeof(buf),
+             "mkv_basis_static: 2*batch*n_kv_heads = %lld streams need at least %lld bytes of "
+             "scratch; the static buffer holds %lld bytes (at most %lld streams)",
+             (long long)streams, (long long)(streams * kGramPartBytes),
+             (long long)MKV_BASIS_STATIC_MAX_BYTES, (long long)kBasisStaticParts);
+    g_last_error = buf;
+    return MKV_ERR_INVALID_ARG;
+  }
+  int dev = 0;
+  CK(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) {
+    g_last_error = "mkv_basis_static: device ordinal out of range";
+    return MKV_ERR_INVALID_ARG;
+  }
+  float* scratch = nullptr;
+  mkv_status s = basis_scratch_on(dev, &scratch);
+  if (s != MKV_OK) return s;
+  CompressParams p;
+  memset(&p, 0, sizeof(p));
+  p.X[0] = static_cast<const __half*>(k);
+  p.X[1] = static_cast<const __half*>(v);
+  p.BH = (int)(streams / 2);
+  p.T = ctx_len;
+  // mkv_compress's chunk count, reduced only when the partials would not fit
+  p.gram_chunks = (int)std::min<int64_t>(gram_chunks_for(p.BH, ctx_len),
+                                         kBasisStaticParts / streams);
+  p.gram_chunk_tokens = ceil_div(ceil_div(ctx_len, p.gram_chunks), TILE_T) * TILE_T;
+  p.gram_chunks = (int)ceil_div(ctx_len, p.gram_chunk_tokens);
+  p.gram_part = scratch;
+  p.R = basis;
+  p.lam = eigvals;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  CK(launch_gram(p, st));
+  CK(launch_eig(p, st));
   return MKV_OK;
 }
 

@@ -28,6 +28,7 @@ MKV_ERR_TIMEOUT = 6
 MKV_STRATEGY_SM, MKV_STRATEGY_PV, MKV_STRATEGY_DENSE = 0, 1, 2
 MKV_FLAG_KERNEL_TIMING = 1
 MKV_FLAG_SCORE_TIMING = 2
+MKV_BASIS_STATIC_MAX_BYTES = 16 << 20
 MKV_KERNEL_QROT, MKV_KERNEL_SCORE, MKV_KERNEL_TOPK, MKV_KERNEL_ATTN, MKV_KERNEL_MERGE = range(5)
 KERNEL_NAMES = ["qrot", "score", "topk", "attn", "merge"]
 
@@ -82,6 +83,7 @@ def _load():
         "mkv_export": (c_int, [P, c_int, c_int, c_int, P, P, P, P, POINTER(c_uint64)]),
         "mkv_kernel_time": (c_int, [P, c_int, POINTER(c_double), POINTER(c_int64), c_int]),
         "mkv_check_device": (c_int, [P]),
+        "mkv_basis_static": (c_int, [P, P, c_int, c_int, c_int64, P, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -226,6 +228,21 @@ def mkv_kernel_time(ctx, kernel_id: int, reset: bool = False):
     _check(_lib.mkv_kernel_time(ctx, kernel_id, ctypes.byref(ms), ctypes.byref(n), int(reset)),
            "mkv_kernel_time")
     return ms.value, n.value
+
+
+def mkv_basis_static(k, v, basis, eigvals, stream=None) -> None:
+    """Bases and eigenvalues of every K and V stream, with no ctx and no
+    allocation inside the library (its scratch is a static device buffer).
+    k, v: fp16 [B][H][T][128]; basis: fp32 [2][B*H][128][128]; eigvals: fp32
+    [2][B*H][128], all on the current CUDA device."""
+    import torch
+    B, H, T, _ = k.shape
+    pk = _dptr(k, torch.float16, "k", (B, H, T, 128))
+    pv = _dptr(v, torch.float16, "v", (B, H, T, 128))
+    pb = _dptr(basis, torch.float32, "basis", (2, B * H, 128, 128))
+    pe = _dptr(eigvals, torch.float32, "eigvals", (2, B * H, 128))
+    _check(_lib.mkv_basis_static(pk, pv, B, H, T, pb, pe, _stream_ptr(stream, k.device)),
+           "mkv_basis_static")
 
 
 class Mkv:
