@@ -142,11 +142,10 @@ constexpr int SC_THREADS = (SC_CONS + 1) * 32;
 constexpr int SC_NSLOT = 2;
 constexpr int SC_MAX_STAGES = 6;
 constexpr int SC_MAX_SEGS = 64;                  // segments per stage
-constexpr int SC_MAX_ITEMS = SC_MAX_SEGS * 8;    // 32-row blocks per stage (S <= 256)
+constexpr int SC_HDR_SLOT = SC_MAX_SEGS + 2;     // header entries per stage (even start)
 constexpr int SC_STAGE_TARGET = 52 * 1024;
 constexpr int SC_STATIC_SMEM = SC_NSLOT * HIST1 * 4 + SC_NSLOT * D * 4 + SC_CONS * D * 4 +
-                               SC_MAX_STAGES * SC_MAX_SEGS * 8 + SC_MAX_STAGES * SC_MAX_ITEMS * 2 +
-                               2048;
+                               SC_MAX_STAGES * SC_HDR_SLOT * 8 + 2048;
 
 // shared-memory bytes of one stage slot: the stage plus slack for line alignment
 __host__ __device__ constexpr size_t sc_slot(int stage_bytes) { return (size_t)stage_bytes + 256; }
@@ -157,10 +156,9 @@ __device__ __forceinline__ uint2 load_hdr(const mkv_segment_header* h, int i, in
 }
 
 struct StageMeta {
-  int32_t seg0, seg1;
+  int32_t seg0;        // first segment, or -1 for the end marker
+  int32_t nseg;
   uint64_t byte0;      // pool offset of the slot's first byte (128-byte aligned)
-  int32_t n_items;
-  int32_t pad;
 };
 
 // Dot product of one packed row with q_bar, from shared memory; one row per
@@ -177,6 +175,7 @@ __device__ __forceinline__ float row_dot(const uint8_t* base, int rows, int row,
   constexpr uint32_t C = 8u * CPR;
   constexpr int G8 = (CPR % 8 == 0) ? 8 : ((CPR % 4 == 0) ? 4 : ((CPR % 2 == 0) ? 2 : 1));
   constexpr int P = 8 / G8;
+  constexpr int NB = CPR > 5 ? 4 : CPR;      // chunks loaded ahead of the arithmetic
   const uint8_t* rowp = (STRAT == MKV_STRATEGY_SM)   ? base + pad16(C) + 2u * C * row
                         : (STRAT == MKV_STRATEGY_PV) ? base + 2u * C * row
                                                      : base + 256u * row;
@@ -184,30 +183,46 @@ __device__ __forceinline__ float row_dot(const uint8_t* base, int rows, int row,
   const int rot = (lane & 7) / P;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int j = 0; j < CPR; ++j) {
-    int k = j + rot;
-    k = k >= CPR ? k - CPR : k;
-    float v[8];
-    h8_to_f(*reinterpret_cast<const uint4*>(rowp + 16 * k), v);
-    if (STRAT == MKV_STRATEGY_PV) {
-      const uint2 ix = *reinterpret_cast<const uint2*>(idxp + 8 * k);
+  for (int j0 = 0; j0 < CPR; j0 += NB) {
+    uint4 raw[NB];
+    uint2 ixs[NB];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const uint32_t ch = ((e < 4 ? ix.x : ix.y) >> (8 * (e & 3))) & 0x7fu;
-        acc[e & 3] = fmaf(v[e], qsrc[ch], acc[e & 3]);
+    for (int jj = 0; jj < NB; ++jj) {
+      if (j0 + jj < CPR) {
+        int k = j0 + jj + rot;
+        k = k >= CPR ? k - CPR : k;
+        raw[jj] = *reinterpret_cast<const uint4*>(rowp + 16 * k);
+        if (STRAT == MKV_STRATEGY_PV) ixs[jj] = *reinterpret_cast<const uint2*>(idxp + 8 * k);
       }
-    } else {
-      const float* qq = (STRAT == MKV_STRATEGY_SM ? qm : qsrc) + 8 * k;
-      const float4 a = *reinterpret_cast<const float4*>(qq);
-      const float4 b = *reinterpret_cast<const float4*>(qq + 4);
-      acc[0] = fmaf(v[0], a.x, acc[0]);
-      acc[1] = fmaf(v[1], a.y, acc[1]);
-      acc[2] = fmaf(v[2], a.z, acc[2]);
-      acc[3] = fmaf(v[3], a.w, acc[3]);
-      acc[0] = fmaf(v[4], b.x, acc[0]);
-      acc[1] = fmaf(v[5], b.y, acc[1]);
-      acc[2] = fmaf(v[6], b.z, acc[2]);
-      acc[3] = fmaf(v[7], b.w, acc[3]);
+    }
+#pragma unroll
+    for (int jj = 0; jj < NB; ++jj) {
+      if (j0 + jj < CPR) {
+        int k = j0 + jj + rot;
+        k = k >= CPR ? k - CPR : k;
+        float v[8];
+        h8_to_f(raw[jj], v);
+        if (STRAT == MKV_STRATEGY_PV) {
+          const uint2 ix = ixs[jj];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const uint32_t ch = ((e < 4 ? ix.x : ix.y) >> (8 * (e & 3))) & 0x7fu;
+            acc[e & 3] = fmaf(v[e], qsrc[ch], acc[e & 3]);
+          }
+        } else {
+          const float* qq = (STRAT == MKV_STRATEGY_SM ? qm : qsrc) + 8 * k;
+          const float4 a = *reinterpret_cast<const float4*>(qq);
+          const float4 b = *reinterpret_cast<const float4*>(qq + 4);
+          acc[0] = fmaf(v[0], a.x, acc[0]);
+          acc[1] = fmaf(v[1], a.y, acc[1]);
+          acc[2] = fmaf(v[2], a.z, acc[2]);
+          acc[3] = fmaf(v[3], a.w, acc[3]);
+          acc[0] = fmaf(v[4], b.x, acc[0]);
+          acc[1] = fmaf(v[5], b.y, acc[1]);
+          acc[2] = fmaf(v[6], b.z, acc[2]);
+          acc[3] = fmaf(v[7], b.w, acc[3]);
+        }
+      }
     }
   }
   return (acc[0] + acc[1]) + (acc[2] + acc[3]);
@@ -245,8 +260,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
   extern __shared__ __align__(128) uint8_t stage_mem[];
   __shared__ uint64_t full_bar[SC_MAX_STAGES], empty_bar[SC_MAX_STAGES];
   __shared__ StageMeta meta[SC_MAX_STAGES];
-  __shared__ uint2 shdr[SC_MAX_STAGES][SC_MAX_SEGS];         // headers of each stage's segments
-  __shared__ uint16_t sitem[SC_MAX_STAGES][SC_MAX_ITEMS];    // (segment << 8) | 32-row block
+  __shared__ __align__(16) uint2 shdr[SC_MAX_STAGES][SC_HDR_SLOT];   // each stage's headers
   __shared__ __align__(16) float qb[SC_NSLOT][D];
   __shared__ uint32_t hist[SC_NSLOT][HIST1];
   __shared__ __align__(16) float qm[SC_CONS][D];
@@ -277,15 +291,17 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
 
   if (warp == SC_CONS) {
     // ---- producer warp --------------------------------------------------------
-    // Headers come in batches of 32 (one per lane), the next batch already in
-    // flight, so grouping segments into stages never waits on a dependent load.
+    // The stages were planned at compression; plan entries come 32 at a time
+    // (one per lane), the next batch already in flight.  Per stage: one bulk
+    // copy of the segments' lines and one of their headers.
     const uint64_t pol = policy_evict_first();
-    int sg = a, k = 0;
+    const int n_st = p.plan_n[blockIdx.x];
+    const uint4* pl = reinterpret_cast<const uint4*>(p.plan + a);
+    uint4 cur = lane < n_st ? __ldg(pl + lane) : make_uint4(0u, 0u, 0u, 0u);
+    uint4 nxt = 32 + lane < n_st ? __ldg(pl + 32 + lane) : make_uint4(0u, 0u, 0u, 0u);
     bool ok = true;
-    int cur_base = a;
-    uint2 cur = load_hdr(p.hdrK, a + lane, b);
-    uint2 nxt = load_hdr(p.hdrK, a + 32 + lane, b);
-    while (true) {
+    int k = 0;
+    for (; k <= n_st; ++k) {
       const int slot = k % NST, use = k / NST;
       if (use > 0) {
         bool got = true;
@@ -295,7 +311,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
           break;
         }
       }
-      if (sg >= b) {            // end marker: a phase with no bytes
+      if (k == n_st) {          // end marker: a phase with no bytes
         if (lane == 0) {
           meta[slot].seg0 = -1;
           mbar_arrive(&full_bar[slot]);
@@ -303,45 +319,27 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
         ++k;
         break;
       }
-      uint64_t off0 = 0, end = 0;
-      int e = sg, nseg = 0, nitem = 0;
-      while (e < b && nseg < SC_MAX_SEGS) {
-        if (e >= cur_base + 32) {
-          cur = nxt;
-          cur_base += 32;
-          nxt = load_hdr(p.hdrK, cur_base + 32 + lane, b);
-        }
-        uint2 w;
-        w.x = __shfl_sync(0xffffffffu, cur.x, e - cur_base);
-        w.y = __shfl_sync(0xffffffffu, cur.y, e - cur_base);
-        const mkv_segment_header hd = *reinterpret_cast<const mkv_segment_header*>(&w);
-        const uint64_t st = (uint64_t)hd.off16 * 16u;
-        const uint64_t se = st + segment_bytes(hd.strategy, hd.rows, p.c);
-        if (nseg == 0) off0 = st;
-        if (nseg > 0 && se - off0 > (uint64_t)p.stage_bytes) break;
-        if (lane == 0) shdr[slot][nseg] = w;
-        const int nblk = (hd.rows + 31) >> 5;   // <= 8
-        if (lane < nblk) sitem[slot][nitem + lane] = (uint16_t)((nseg << 8) | lane);
-        nitem += nblk;
-        end = se;
-        ++e;
-        ++nseg;
+      if (k > 0 && (k & 31) == 0) {
+        cur = nxt;
+        nxt = k + 32 + lane < n_st ? __ldg(pl + k + 32 + lane) : make_uint4(0u, 0u, 0u, 0u);
       }
+      uint4 e;
+      e.x = __shfl_sync(0xffffffffu, cur.x, k & 31);
+      e.y = __shfl_sync(0xffffffffu, cur.y, k & 31);
+      e.z = __shfl_sync(0xffffffffu, cur.z, k & 31);
+      e.w = __shfl_sync(0xffffffffu, cur.w, k & 31);
+      const StagePlan sp = *reinterpret_cast<const StagePlan*>(&e);
       if (lane == 0) {
-        // whole 128-byte lines: start rounded down, end rounded up (the pool
-        // has a 256-byte tail pad and each slot 256 bytes of slack)
-        const uint64_t a0 = off0 & ~127ull, a1 = (end + 127u) & ~127ull;
-        meta[slot].seg0 = sg;
-        meta[slot].seg1 = e;
-        meta[slot].byte0 = a0;
-        meta[slot].n_items = nitem;
+        const uint32_t nb = sp.nlines * 128u, hb = (uint32_t)sp.nhdr2 * 16u;
+        meta[slot].seg0 = (int32_t)sp.seg0;
+        meta[slot].nseg = sp.nseg;
+        meta[slot].byte0 = (uint64_t)sp.line0 * 128u;
         fence_proxy_async();
-        mbar_arrive_expect_tx(&full_bar[slot], (uint32_t)(a1 - a0));
-        bulk_g2s(stage_mem + (size_t)slot * slot_bytes, p.pool + a0, (uint32_t)(a1 - a0),
+        mbar_arrive_expect_tx(&full_bar[slot], nb + hb);
+        bulk_g2s(stage_mem + (size_t)slot * slot_bytes, p.pool + (uint64_t)sp.line0 * 128u, nb,
                  &full_bar[slot], pol);
+        bulk_g2s(&shdr[slot][0], p.hdrK + (sp.seg0 & ~1u), hb, &full_bar[slot], pol);
       }
-      sg = e;
-      ++k;
     }
     if (lane == 0) {
       if (!ok) atomicExch(p.err, DEV_ERR_TIMEOUT);
@@ -351,6 +349,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
   } else {
     // ---- consumers ----------------------------------------------------------
     const uint64_t pol = policy_evict_last();
+    const int bps = (p.S + 31) >> 5;      // 32-row blocks per segment
     int k = 0, last_sm = -1;
     while (true) {
       const int slot = k % NST, use = k / NST;
@@ -368,13 +367,14 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
         break;
       }
       const uint8_t* sbase = stage_mem + (size_t)slot * slot_bytes;
-      for (int it = warp; it < m.n_items; it += SC_CONS) {
-        const uint32_t item = sitem[slot][it];
-        const int ls = (int)(item >> 8), blk = (int)(item & 255u);
-        const uint2 hw = shdr[slot][ls];
+      const int n_items = m.nseg * bps, hofs = m.seg0 & 1;
+      for (int it = warp; it < n_items; it += SC_CONS) {
+        const int ls = it / bps, blk = it - ls * bps;
+        const uint2 hw = shdr[slot][ls + hofs];
         const mkv_segment_header hd = *reinterpret_cast<const mkv_segment_header*>(&hw);
         const int sg = m.seg0 + ls;
         const int rows = hd.rows, strat = hd.strategy;
+        if (blk * 32 >= rows) continue;
         const uint8_t* base = sbase + ((uint64_t)hd.off16 * 16u - m.byte0);
         const int s = sg / p.n_seg;
         const int sl = s - s_first;
@@ -865,28 +865,37 @@ __global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(DecodeParams p) {
 }
 
 // ---------------------------------------------------------------------------
-// merge: log-sum-exp merge of the chunk partials, then o = o~ R_V^T with R_V
-// staged in shared memory.
-// grid: BH, block 256, dynamic smem 64 KB + chunk weights
+// merge: log-sum-exp merge of the chunk partials, then o = o~ R_V^T.  CTA
+// (s, q) writes output rows [32q, 32q + 32) of every head of stream s; the
+// weights and the merged o~ are recomputed by each of the four CTAs (from
+// L2), and the 32 rows of R_V are staged transposed in shared memory.
+// grid: (BH, 4), block 128, dynamic smem: chunk weights
 // ---------------------------------------------------------------------------
-constexpr int MG_THREADS = 256;
+constexpr int MG_THREADS = 128;
+constexpr int MG_ROWS = 32;
+constexpr int MG_LD = MG_ROWS + 1;
 
 __global__ void __launch_bounds__(MG_THREADS) merge_kernel(DecodeParams p) {
-  extern __shared__ __align__(16) float msm[];
-  float* Rs = msm;                 // [128][128]
-  float* wsm = msm + D * D;        // [attn_chunks][g] weights
+  extern __shared__ __align__(16) float wsm[];     // [attn_chunks][g] weights
+  __shared__ float Rt[D * MG_LD];                  // Rt[j][rr] = R_V[32q + rr][j]
   __shared__ __align__(16) float ot[MAX_G][D];
   __shared__ float Linv[MAX_G];
-  const int s = blockIdx.x;
+  const int s = blockIdx.x, r0 = blockIdx.y * MG_ROWS;
   const int b = s / p.H, h = s % p.H;
   const int g = p.g, nc = p.attn_chunks;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   {
-    const float4* R4 = reinterpret_cast<const float4*>(p.RV + (size_t)s * D * D);
-    float4* Rs4 = reinterpret_cast<float4*>(Rs);
+    const float4* R4 = reinterpret_cast<const float4*>(p.RV + ((size_t)s * D + r0) * D);
 #pragma unroll
-    for (int x = 0; x < D * D / 4 / MG_THREADS; ++x)
-      Rs4[tid + x * MG_THREADS] = __ldg(R4 + tid + x * MG_THREADS);
+    for (int x = 0; x < MG_ROWS * D / 4 / MG_THREADS; ++x) {
+      const int f = tid + x * MG_THREADS;           // float4 index within the 32 rows
+      const int rr = f >> 5, j = (f & 31) * 4;
+      const float4 v = __ldg(R4 + f);
+      Rt[(j + 0) * MG_LD + rr] = v.x;
+      Rt[(j + 1) * MG_LD + rr] = v.y;
+      Rt[(j + 2) * MG_LD + rr] = v.z;
+      Rt[(j + 3) * MG_LD + rr] = v.w;
+    }
   }
   // weights exp(m_c - M) and 1 / L per head: warp per head, lanes over chunks
   const float2* ml = reinterpret_cast<const float2*>(p.part_ml + (size_t)s * nc * g * 2);
@@ -916,19 +925,17 @@ __global__ void __launch_bounds__(MG_THREADS) merge_kernel(DecodeParams p) {
     ot[hh][x % D] = o * Linv[hh];
   }
   __syncthreads();
+  // thread (rr, hq): out[hh][r0 + rr] for hh = hq, hq + 4, ...
   float* out = p.out + ((size_t)b * p.Hq + (size_t)h * g) * D;
-  for (int r = warp; r < D; r += MG_THREADS / 32) {
-    const float4 rv = *reinterpret_cast<const float4*>(Rs + r * D + 4 * lane);
-    for (int hh = 0; hh < g; ++hh) {
-      const float4 o4 = *reinterpret_cast<const float4*>(&ot[hh][4 * lane]);
-      float d = rv.x * o4.x;
-      d = fmaf(rv.y, o4.y, d);
-      d = fmaf(rv.z, o4.z, d);
-      d = fmaf(rv.w, o4.w, d);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-      if (lane == 0) out[hh * D + r] = d;
+  const int rr = tid & 31, hq = tid >> 5;
+  for (int hh = hq; hh < g; hh += MG_THREADS / 32) {
+    float d0 = 0.f, d1 = 0.f;
+#pragma unroll 8
+    for (int j = 0; j < D; j += 2) {
+      d0 = fmaf(Rt[j * MG_LD + rr], ot[hh][j], d0);
+      d1 = fmaf(Rt[(j + 1) * MG_LD + rr], ot[hh][j + 1], d1);
     }
+    out[hh * D + r0 + rr] = d0 + d1;
   }
 }
 
@@ -964,6 +971,58 @@ __global__ void __launch_bounds__(1024) partition_kernel(const mkv_segment_heade
 }
 
 // ---------------------------------------------------------------------------
+// plan: the score kernel's stages for CTA i (one warp per CTA, compression
+// time).  Whole segments are grouped in order while the stage's line-aligned
+// span stays within stage_bytes (at least one segment per stage) and it holds
+// at most SC_MAX_SEGS segments.  A stage never has more entries than its CTA
+// has segments, so CTA i's plan fits in plan[part[i] .. part[i + 1]).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ StagePlan make_stage(int seg0, int nseg, uint64_t off0, uint64_t end) {
+  StagePlan sp;
+  sp.seg0 = (uint32_t)seg0;
+  sp.nseg = (uint16_t)nseg;
+  sp.nhdr2 = (uint16_t)(((uint32_t)(seg0 + nseg) + 1u) / 2u - (uint32_t)seg0 / 2u);
+  sp.line0 = (uint32_t)(off0 >> 7);
+  sp.nlines = (uint32_t)(((end + 127u) >> 7) - (off0 >> 7));
+  return sp;
+}
+
+__global__ void __launch_bounds__(32) plan_kernel(const mkv_segment_header* hdrK, int c,
+                                                  int stage_bytes, const int32_t* part,
+                                                  StagePlan* plan, int32_t* plan_n) {
+  const int i = blockIdx.x, lane = threadIdx.x;
+  const int a = part[i], b = part[i + 1];
+  int k = 0, seg0 = a, nseg = 0;
+  uint64_t off0 = 0, end = 0;
+  for (int base = a; base < b; base += 32) {
+    const uint2 w = load_hdr(hdrK, base + lane, b);
+    const mkv_segment_header hd = *reinterpret_cast<const mkv_segment_header*>(&w);
+    const uint64_t st = (uint64_t)hd.off16 * 16u;
+    const uint64_t se = st + segment_bytes(hd.strategy, hd.rows, c);
+    const int nb = min(32, b - base);
+    for (int j = 0; j < nb; ++j) {
+      const uint64_t sj = __shfl_sync(0xffffffffu, st, j);
+      const uint64_t ej = __shfl_sync(0xffffffffu, se, j);
+      if (nseg > 0 && (nseg == SC_MAX_SEGS || ((ej + 127u) & ~127ull) - (off0 & ~127ull) >
+                                                  (uint64_t)stage_bytes + 128u)) {
+        if (lane == 0) plan[a + k] = make_stage(seg0, nseg, off0, end);
+        ++k;
+        seg0 = base + j;
+        nseg = 0;
+      }
+      if (nseg == 0) off0 = sj;
+      end = ej;
+      ++nseg;
+    }
+  }
+  if (nseg > 0) {
+    if (lane == 0) plan[a + k] = make_stage(seg0, nseg, off0, end);
+    ++k;
+  }
+  if (lane == 0) plan_n[i] = k;
+}
+
+// ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
 void score_stage_plan(int S, int c, int* stage_bytes, int* n_stages) {
@@ -985,7 +1044,7 @@ cudaError_t prepare_decode_kernels() {
                                        (int)attn_smem_bytes(MAX_G, ATTN_MAX_CHUNK));
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)(sizeof(float) * D * D) + 2 * 48 * 1024);
+                           48 * 1024 + 4 * 1024);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(qrot_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, D * D * 4);
   if (e != cudaSuccess) return e;
@@ -994,8 +1053,10 @@ cudaError_t prepare_decode_kernels() {
 }
 
 cudaError_t launch_partition(const mkv_segment_header* hdrK, int n_streams, int n_seg, int c,
-                             int G, int32_t* part, int32_t* cta_cnt, cudaStream_t st) {
+                             int G, int stage_bytes, int32_t* part, int32_t* cta_cnt,
+                             StagePlan* plan, int32_t* plan_n, cudaStream_t st) {
   partition_kernel<<<1, 1024, 0, st>>>(hdrK, n_streams, n_seg, c, G, part, cta_cnt);
+  plan_kernel<<<G, 32, 0, st>>>(hdrK, c, stage_bytes, part, plan, plan_n);
   return cudaGetLastError();
 }
 
@@ -1023,8 +1084,8 @@ cudaError_t launch_attn(const DecodeParams& p, cudaStream_t st) {
 }
 
 cudaError_t launch_merge(const DecodeParams& p, cudaStream_t st) {
-  merge_kernel<<<p.B * p.H, MG_THREADS,
-                 sizeof(float) * ((size_t)D * D + (size_t)p.attn_chunks * p.g), st>>>(p);
+  dim3 grid(p.B * p.H, D / MG_ROWS);
+  merge_kernel<<<grid, MG_THREADS, sizeof(float) * (size_t)p.attn_chunks * p.g, st>>>(p);
   return cudaGetLastError();
 }
 

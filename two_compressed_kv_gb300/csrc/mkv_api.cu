@@ -66,6 +66,8 @@ struct mkv_ctx {
   mkv_segment_header* hdr[2] = {nullptr, nullptr};
   int32_t* part[2] = {nullptr, nullptr};      // score-kernel partition of the K segments
   int32_t* cta_cnt[2] = {nullptr, nullptr};   // score CTAs per stream
+  StagePlan* plan[2] = {nullptr, nullptr};    // score-kernel stages
+  int32_t* plan_n[2] = {nullptr, nullptr};    // stages per score CTA
   uint8_t* pool = nullptr;
   uint64_t pool_cap = 0;
 
@@ -177,6 +179,8 @@ void release(mkv_ctx* c) {
     cudaFree(c->hdr[i]);
     cudaFree(c->part[i]);
     cudaFree(c->cta_cnt[i]);
+    cudaFree(c->plan[i]);
+    cudaFree(c->plan_n[i]);
   }
   cudaFree(c->pool);
   cudaFree(c->seg);
@@ -343,6 +347,8 @@ mkv_status mkv_create(const mkv_config* cfg, mkv_ctx** out) {
     AL(c->hdr[i], 2 * BH * (size_t)c->max_seg);
     AL(c->part[i], (size_t)c->G + 1);
     AL(c->cta_cnt[i], BH);
+    AL(c->plan[i], BH * (size_t)c->max_seg);
+    AL(c->plan_n[i], (size_t)c->G);
   }
   AL(c->seg, 2 * BH * (size_t)c->max_seg);
   AL(c->gram_part, 2 * BH * (size_t)c->gram_chunks_max * D * D);
@@ -418,8 +424,9 @@ mkv_status mkv_compress(mkv_ctx* c, const void* k, const void* v, int64_t ctx_le
   CK(launch_eig(p, st));
   CK(launch_analyze(p, st));
   CK(launch_scan(p, st));
-  CK(launch_partition(p.hdr, c->BH, p.n_seg, p.c, c->G, c->part[stage], c->cta_cnt[stage], st));
-  c->launches += 5;
+  CK(launch_partition(p.hdr, c->BH, p.n_seg, p.c, c->G, c->stage_bytes, c->part[stage],
+                      c->cta_cnt[stage], c->plan[stage], c->plan_n[stage], st));
+  c->launches += 6;
   CK(cudaMemcpyAsync(c->total_host, c->total_dev, sizeof(unsigned long long),
                      cudaMemcpyDeviceToHost, st));
   CK(cudaStreamSynchronize(st));
@@ -485,6 +492,8 @@ mkv_status mkv_decode(mkv_ctx* c, const void* q, float* out, int32_t* sel, mkv_s
   p.hist = c->hist;
   p.part = c->part[c->live];
   p.cta_cnt = c->cta_cnt[c->live];
+  p.plan = c->plan[c->live];
+  p.plan_n = c->plan_n[c->live];
   p.G = c->G;
   p.stage_bytes = c->stage_bytes;
   p.n_stages = c->n_stages;

@@ -85,6 +85,18 @@ struct TopkState {
   int32_t t_cut;    // keys equal to thr are taken up to this token index
 };
 
+// One shared-memory stage of the score kernel, planned at compression: the
+// whole segments [seg0, seg0 + nseg) of the flattened K segments, copied as
+// the 128-byte lines [line0, line0 + nlines) of the pool plus nhdr2 16-byte
+// pairs of their headers (from header index seg0 rounded down to even).
+struct StagePlan {
+  uint32_t seg0;
+  uint16_t nseg;
+  uint16_t nhdr2;
+  uint32_t line0;
+  uint32_t nlines;
+};
+
 struct DecodeParams {
   int B, H, Hq, g;
   int64_t T;
@@ -106,6 +118,9 @@ struct DecodeParams {
   // that touch stream s
   const int32_t* part;
   const int32_t* cta_cnt;
+  // CTA i's stages are plan[part[i] .. part[i] + plan_n[i])
+  const StagePlan* plan;
+  const int32_t* plan_n;
   int G;
   int stage_bytes;                 // bytes per shared-memory stage of the score kernel
   int n_stages;
@@ -133,9 +148,11 @@ constexpr int DEV_ERR_TIMEOUT = 1;
 cudaError_t prepare_decode_kernels();
 // score-kernel shared-memory plan: stage size and number of stages
 void score_stage_plan(int S, int c, int* stage_bytes, int* n_stages);
-// partition of the K segments over G score CTAs (run once per compression)
+// partition of the K segments over G score CTAs and their stage plans (run
+// once per compression); plan holds n_streams * n_seg entries
 cudaError_t launch_partition(const mkv_segment_header* hdrK, int n_streams, int n_seg, int c,
-                             int G, int32_t* part, int32_t* cta_cnt, cudaStream_t st);
+                             int G, int stage_bytes, int32_t* part, int32_t* cta_cnt,
+                             StagePlan* plan, int32_t* plan_n, cudaStream_t st);
 cudaError_t launch_qrot(const DecodeParams& p, cudaStream_t st);
 cudaError_t launch_score(const DecodeParams& p, cudaStream_t st);
 // the two selection launches; returns after enqueueing both
