@@ -116,7 +116,7 @@ typedef struct {
 enum {
   MKV_KERNEL_QROT = 0,
   MKV_KERNEL_SCORE = 1,
-  MKV_KERNEL_TOPK = 2,   /* the two selection launches together */
+  MKV_KERNEL_TOPK = 2,   /* the exact top-k selection */
   MKV_KERNEL_ATTN = 3,
   MKV_KERNEL_MERGE = 4,
   MKV_KERNEL_COUNT = 5

@@ -4,11 +4,13 @@
 // (prior-work paragraph) and attention computed on the packed dense format
 // with CUDA cores, without unpacking ("Observation & Method 2").
 //
-// Launch order per step: qrot -> score -> topk_pass2 -> topk_write -> attn -> merge.
+// Launch order per step: qrot -> score -> select -> attn -> merge.
 // No kernel waits on another CTA.  Cross-CTA results are combined with
 // integer atomics (order-independent), "last CTA finishes" tickets, or a
 // later launch; every floating-point sum runs in a fixed order, so a decode is
 // bit-for-bit repeatable.
+#include <cooperative_groups.h>
+
 #include "mkv_internal.cuh"
 #include "ptx.cuh"
 
@@ -103,11 +105,7 @@ __global__ void __launch_bounds__(QR_THREADS) qrot_kernel(DecodeParams p) {
   for (int x = tid; x < p.g * D; x += QR_THREADS) qs[x / D][x % D] = __half2float(q[x]);
   uint4* hz = reinterpret_cast<uint4*>(p.hist + (size_t)s * HIST1);
   for (int x = tid; x < HIST1 / 4; x += QR_THREADS) hz[x] = make_uint4(0u, 0u, 0u, 0u);
-  if (tid == 0) {
-    p.tick1[s] = 0u;
-    p.tick2[s] = 0u;
-    p.cand_n[s] = 0u;
-  }
+  if (tid == 0) p.tick1[s] = 0u;
   __syncthreads();
   float* qt = p.qt + ((size_t)b * p.Hq + (size_t)h * p.g) * D;
   float mine = 0.f;
@@ -241,21 +239,9 @@ __device__ __forceinline__ void score_block(const uint8_t* base, int rows, int r
   }
 }
 
-template <int STRAT>
-__device__ __forceinline__ void score_block_c(int cpr, const uint8_t* base, int rows, int r0,
-                                              int lane, const float* qsrc, const float* qm,
-                                              float* out, uint32_t* hs, uint64_t pol) {
-#define MKV_CASE(N) \
-  case N: score_block<STRAT, N>(base, rows, r0, lane, qsrc, qm, out, hs, pol); break;
-  switch (cpr) {
-    MKV_CASE(1) MKV_CASE(2) MKV_CASE(3) MKV_CASE(4) MKV_CASE(5) MKV_CASE(6) MKV_CASE(7)
-    MKV_CASE(8) MKV_CASE(9) MKV_CASE(10) MKV_CASE(11) MKV_CASE(12) MKV_CASE(13) MKV_CASE(14)
-    MKV_CASE(15) MKV_CASE(16)
-    default: break;
-  }
-#undef MKV_CASE
-}
-
+// CPR = c / 8 is a template parameter of the whole kernel (one instantiation
+// per c), so the per-item dispatch is only on the segment's strategy.
+template <int CPR>
 __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
   extern __shared__ __align__(128) uint8_t stage_mem[];
   __shared__ uint64_t full_bar[SC_MAX_STAGES], empty_bar[SC_MAX_STAGES];
@@ -349,7 +335,9 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
   } else {
     // ---- consumers ----------------------------------------------------------
     const uint64_t pol = policy_evict_last();
-    const int bps = (p.S + 31) >> 5;      // 32-row blocks per segment
+    const int bps = (p.S + 31) >> 5;      // 32-row blocks per segment (1..8)
+    // it / bps = (it * bps_inv) >> 16, exact for it < 512
+    const uint32_t bps_inv = (65536u + (uint32_t)bps - 1u) / (uint32_t)bps;
     int k = 0, last_sm = -1;
     while (true) {
       const int slot = k % NST, use = k / NST;
@@ -368,15 +356,22 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
       }
       const uint8_t* sbase = stage_mem + (size_t)slot * slot_bytes;
       const int n_items = m.nseg * bps, hofs = m.seg0 & 1;
+      // stream of the stage's first segment; later segments step over stream
+      // boundaries (at most a few per stage)
+      int s_cur = m.seg0 / p.n_seg, s_end = (s_cur + 1) * p.n_seg;
       for (int it = warp; it < n_items; it += SC_CONS) {
-        const int ls = it / bps, blk = it - ls * bps;
+        const int ls = (int)(((uint32_t)it * bps_inv) >> 16), blk = it - ls * bps;
         const uint2 hw = shdr[slot][ls + hofs];
         const mkv_segment_header hd = *reinterpret_cast<const mkv_segment_header*>(&hw);
         const int sg = m.seg0 + ls;
         const int rows = hd.rows, strat = hd.strategy;
         if (blk * 32 >= rows) continue;
         const uint8_t* base = sbase + ((uint64_t)hd.off16 * 16u - m.byte0);
-        const int s = sg / p.n_seg;
+        while (sg >= s_end) {
+          ++s_cur;
+          s_end += p.n_seg;
+        }
+        const int s = s_cur;
         const int sl = s - s_first;
         const float* qsrc = sl < SC_NSLOT ? qb[sl] : p.qbar + (size_t)s * D;
         uint32_t* hs = sl < SC_NSLOT ? hist[sl] : p.hist + (size_t)s * HIST1;
@@ -388,11 +383,11 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
             __syncwarp();
             last_sm = sg;
           }
-          score_block_c<MKV_STRATEGY_SM>(p.c >> 3, base, rows, blk * 32, lane, qsrc, qm[warp],
-                                         out, hs, pol);
+          score_block<MKV_STRATEGY_SM, CPR>(base, rows, blk * 32, lane, qsrc, qm[warp], out, hs,
+                                            pol);
         } else if (strat == MKV_STRATEGY_PV) {
-          score_block_c<MKV_STRATEGY_PV>(p.c >> 3, base, rows, blk * 32, lane, qsrc, qm[warp],
-                                         out, hs, pol);
+          score_block<MKV_STRATEGY_PV, CPR>(base, rows, blk * 32, lane, qsrc, qm[warp], out, hs,
+                                            pol);
         } else {
           score_block<MKV_STRATEGY_DENSE, 16>(base, rows, blk * 32, lane, qsrc, qm[warp], out, hs,
                                               pol);
@@ -439,37 +434,35 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
 }
 
 // ---------------------------------------------------------------------------
-// topk_pass2: per 4096-token chunk, counts the tokens whose key lies above
-// the level-1 bin (all selected) and appends the tokens of that bin to the
-// stream's candidate list.  The CTA that finishes a stream last selects
-// exactly among the candidates (keys by two more radix digits, then equal
-// keys by lowest token index), then turns the per-chunk counts into output
-// offsets.
-// grid: (topk_chunks, BH), block 256, 16 tokens per thread
+// select: exact top-k of one stream by a cluster of R CTAs (R = 1..8).  CTA r
+// owns the token range [r * per, (r + 1) * per) and its warp w a contiguous
+// sub-range (a "block" (r, w)); blocks in (r, w) order cover the tokens in
+// order.  The score kernel left the level-1 bin b1 of the k-th largest key and
+// the number k1 of keys still needed from that bin.
+//   1. one pass over the scores: each warp lists, in token order, its "sure"
+//      tokens (key bin above b1: all selected) and its candidates (key bin
+//      b1, with the key), in its own part of the stream's scratch area;
+//   2. cluster barrier; every CTA reads the per-block counts of all ranks
+//      (distributed shared memory) and the candidates of the whole stream
+//      (in token order), and selects the same threshold: the key thr of the
+//      k1-th largest candidate (two more 10-bit radix digits), then among
+//      keys equal to thr the lowest tokens (radix on 0x7fffffff - t): t_cut;
+//   3. the selected candidates B (token order) and the sure tokens are merged
+//      by position: sure token j of the stream lands at j + |{b in B : b < t}|,
+//      B[i] at i + |{sure tokens < B[i]}|; each warp places its own block.
+// With more than SEL_CAP candidates the threshold is found the same way from
+// the scratch area and step 3 re-reads the scores instead.  Deterministic:
+// candidates are only counted, never summed.
+// grid: (R, BH), cluster (R, 1, 1), block 1024, dynamic smem SEL_CAP * 12
 // ---------------------------------------------------------------------------
-constexpr int TK_THREADS = 256;
-constexpr int TK_PER = TOPK_CHUNK / TK_THREADS;   // 16
+constexpr int SEL_THREADS = 1024;
+constexpr int SEL_WARPS = SEL_THREADS / 32;
+constexpr int SEL_CAP = 8192;                 // candidates kept in shared memory
+constexpr int SEL_UNROLL = 8;                 // 128-token steps per warp loaded together
+constexpr size_t SEL_SMEM = (size_t)SEL_CAP * (sizeof(uint2) + sizeof(int32_t));
 
-__device__ __forceinline__ void load16(const float* sc, int64_t t0, int64_t T, float v[TK_PER],
-                                       bool hint_first, uint64_t pol) {
-  if (t0 + TK_PER <= T) {
-#pragma unroll
-    for (int i = 0; i < TK_PER / 4; ++i) {
-      const float4 f = hint_first ? ld_f4_hint(sc + t0 + 4 * i, pol)
-                                  : __ldcg(reinterpret_cast<const float4*>(sc + t0) + i);
-      v[4 * i] = f.x;
-      v[4 * i + 1] = f.y;
-      v[4 * i + 2] = f.z;
-      v[4 * i + 3] = f.w;
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < TK_PER; ++i) v[i] = (t0 + i < T) ? __ldcg(sc + t0 + i) : 0.f;
-  }
-}
-
-// exclusive scan of one value per thread over the block (TK_THREADS threads)
-__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* sh, uint32_t* total) {
+// exclusive scan of one value per thread over SEL_THREADS threads
+__device__ __forceinline__ uint32_t sel_excl_scan(uint32_t v, uint32_t* sh, uint32_t* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t inc = v;
 #pragma unroll
@@ -479,159 +472,319 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* sh, ui
   }
   if (lane == 31) sh[warp] = inc;
   __syncthreads();
-  uint32_t before = 0, all = 0;
-  for (int w = 0; w < TK_THREADS / 32; ++w) {
-    if (w < warp) before += sh[w];
-    all += sh[w];
+  if (warp == 0) {
+    const uint32_t w = sh[lane];
+    uint32_t x = w;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t o = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += o;
+    }
+    sh[32 + lane] = x - w;                    // exclusive warp offsets
+    if (lane == 31) sh[64] = x;
   }
   __syncthreads();
-  if (total) *total = all;
+  const uint32_t before = sh[32 + warp];
+  if (total) *total = sh[64];
+  __syncthreads();
   return before + inc - v;
 }
 
-__global__ void __launch_bounds__(TK_THREADS) topk_pass2_kernel(DecodeParams p) {
-  const int s = blockIdx.y, ch = blockIdx.x, tid = threadIdx.x;
-  __shared__ uint32_t sh_scan[TK_THREADS / 32], sh_warp[8], sh_res[2];
-  __shared__ uint32_t hbuf[2048];
-  __shared__ int sh_last;
-  __shared__ uint32_t sh_base;
-  const uint32_t b1 = p.state[s].b1;
-  const int64_t t0 = (int64_t)ch * TOPK_CHUNK + (int64_t)tid * TK_PER;
-  const float* sc = p.scores + (size_t)s * p.Tp;
-  float v[TK_PER];
-  load16(sc, t0, p.T, v, false, 0);
-  uint32_t sure = 0, ncand = 0, keys[TK_PER];
-#pragma unroll
-  for (int i = 0; i < TK_PER; ++i) {
-    keys[i] = f2key(v[i]);
-    const bool valid = t0 + i < p.T;
-    const uint32_t bin = keys[i] >> 20;
-    sure += valid && bin > b1;
-    ncand += valid && bin == b1;
+// first index i in [0, n) with a[i] >= x (n if none); a ascending
+__device__ __forceinline__ uint32_t lower_bound_i32(const int32_t* a, uint32_t n, int64_t x) {
+  uint32_t lo = 0, hi = n;
+  while (lo < hi) {
+    const uint32_t mid = (lo + hi) >> 1;
+    if ((int64_t)a[mid] < x) lo = mid + 1; else hi = mid;
   }
-  uint32_t sure_all, ncand_all;
-  block_excl_scan(sure, sh_scan, &sure_all);
-  const uint32_t my_off = block_excl_scan(ncand, sh_scan, &ncand_all);
-  if (tid == 0) {
-    p.cnt[(size_t)s * p.topk_chunks + ch] = (int32_t)sure_all;
-    sh_base = ncand_all ? atomicAdd(&p.cand_n[s], ncand_all) : 0u;
-  }
-  __syncthreads();
-  uint2* cand = p.cand + (size_t)s * p.Tp;
-  uint32_t pos = sh_base + my_off;
-#pragma unroll
-  for (int i = 0; i < TK_PER; ++i) {
-    if (t0 + i < p.T && (keys[i] >> 20) == b1) cand[pos++] = make_uint2(keys[i], (uint32_t)(t0 + i));
-  }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) sh_last = (atomicAdd(&p.tick2[s], 1u) == gridDim.x - 1u);
-  __syncthreads();
-  if (!sh_last) return;
-  __threadfence();
+  return lo;
+}
 
-  // ---- last CTA of the stream: exact threshold among the candidates --------
-  const uint32_t N = __ldcg(&p.cand_n[s]);
+struct SelShared {
+  uint32_t ws[SEL_WARPS], wc[SEL_WARPS];     // this CTA: sure / candidate count per warp
+  uint32_t Sp[8 * SEL_WARPS + 1];            // exclusive prefix over blocks (q, w): sure
+  uint32_t Cp[8 * SEL_WARPS + 1];            // same for candidates
+  uint32_t scan[72];
+  uint32_t hist[2048];
+  uint32_t warp8[8], res[2];
+};
+
+struct SelGeom {
+  int64_t per, T;
+  __device__ int64_t rank_lo(int q) const { return (int64_t)q * per; }
+  __device__ int64_t rank_hi(int q) const {
+    const int64_t h = (int64_t)(q + 1) * per;
+    return h < T ? h : T;
+  }
+  __device__ int64_t wlen(int q) const {
+    const int64_t len = rank_hi(q) - rank_lo(q);
+    return len > 0 ? (len + SEL_WARPS * 128 - 1) / (SEL_WARPS * 128) * 128 : 0;
+  }
+  __device__ int64_t block_lo(int q, int w) const {
+    const int64_t x = rank_lo(q) + (int64_t)w * wlen(q);
+    return x < rank_hi(q) ? x : rank_hi(q);
+  }
+  __device__ int64_t block_hi(int q, int w) const {
+    const int64_t x = rank_lo(q) + (int64_t)(w + 1) * wlen(q);
+    return x < rank_hi(q) ? x : rank_hi(q);
+  }
+};
+
+__global__ void __launch_bounds__(SEL_THREADS, 1) select_kernel(DecodeParams p) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cl = cg::this_cluster();
+  extern __shared__ __align__(16) uint8_t sel_dyn[];
+  uint2* cbuf = reinterpret_cast<uint2*>(sel_dyn);                        // [SEL_CAP]
+  int32_t* bbuf = reinterpret_cast<int32_t*>(sel_dyn + SEL_CAP * sizeof(uint2));  // [SEL_CAP]
+  __shared__ SelShared sh;
+  const int R = (int)cl.num_blocks(), r = (int)cl.block_rank();
+  const int s = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  SelGeom geo;
+  geo.per = (((p.Tp + R - 1) / R) + 15) / 16 * 16;
+  geo.T = p.T;
+  const float* sc = p.scores + (size_t)s * p.Tp;
+  uint2* cs = p.cand + (size_t)s * p.Tp;             // the stream's scratch area
+  const uint32_t b1 = p.state[s].b1;
+  const int64_t w_lo = geo.block_lo(r, warp), w_hi = geo.block_hi(r, warp);
+  // block (q, w): candidates at cs[lo + i]; sure tokens at int32 slot
+  // 2 * (hi - lo) - 1 - j of the same area (2 nc + ns <= 2 (hi - lo))
+  uint2* cand_w = cs + w_lo;
+  int32_t* sure_w = reinterpret_cast<int32_t*>(cand_w);
+  const int64_t L_w = w_hi - w_lo;
+
+  // ---- 1. sure tokens and candidates of this warp's block, in token order --
+  uint32_t ns_w = 0, nc_w = 0;
+  for (int64_t b0 = w_lo; b0 < w_hi; b0 += 128 * SEL_UNROLL) {
+    float4 f[SEL_UNROLL];
+#pragma unroll
+    for (int j = 0; j < SEL_UNROLL; ++j) {
+      const int64_t t0 = b0 + 128 * j + 4 * lane;
+      f[j] = t0 < w_hi ? __ldcg(reinterpret_cast<const float4*>(sc + t0))
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < SEL_UNROLL; ++j) {
+      const int64_t t0 = b0 + 128 * j + 4 * lane;
+      const float v4[4] = {f[j].x, f[j].y, f[j].z, f[j].w};
+      uint32_t keys[4], sb = 0, cb = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        keys[e] = f2key(v4[e]);
+        const bool ok = t0 + e < w_hi;
+        const uint32_t bin = keys[e] >> 20;
+        sb |= (uint32_t)(ok && bin > b1) << e;
+        cb |= (uint32_t)(ok && bin == b1) << e;
+      }
+      const uint32_t packed = (uint32_t)__popc(sb) | ((uint32_t)__popc(cb) << 16);
+      uint32_t inc = packed;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t o = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += o;
+      }
+      const uint32_t excl = inc - packed, tot = __shfl_sync(0xffffffffu, inc, 31);
+      uint32_t ps = ns_w + (excl & 0xffffu), pc = nc_w + (excl >> 16);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if ((sb >> e) & 1u) sure_w[2 * L_w - 1 - (int64_t)(ps++)] = (int32_t)(t0 + e);
+        if ((cb >> e) & 1u) cand_w[pc++] = make_uint2(keys[e], (uint32_t)(t0 + e));
+      }
+      ns_w += tot & 0xffffu;
+      nc_w += tot >> 16;
+    }
+  }
+  if (lane == 0) {
+    sh.ws[warp] = ns_w;
+    sh.wc[warp] = nc_w;
+  }
+  cl.sync();
+
+  // ---- 2. counts of every block of the stream, then the threshold ----------
+  {
+    uint32_t sv = 0, cv = 0;
+    if (tid < R * SEL_WARPS) {
+      const SelShared* rs = cl.map_shared_rank(&sh, tid / SEL_WARPS);
+      sv = rs->ws[tid % SEL_WARPS];
+      cv = rs->wc[tid % SEL_WARPS];
+    }
+    uint32_t st, ct;
+    const uint32_t se = sel_excl_scan(sv, sh.scan, &st);
+    const uint32_t ce = sel_excl_scan(cv, sh.scan, &ct);
+    if (tid < R * SEL_WARPS) {
+      sh.Sp[tid] = se;
+      sh.Cp[tid] = ce;
+    }
+    if (tid == 0) {
+      sh.Sp[R * SEL_WARPS] = st;
+      sh.Cp[R * SEL_WARPS] = ct;
+    }
+  }
+  cl.sync();   // no remote shared-memory reads past this point
+  const int NB = R * SEL_WARPS;
+  const uint32_t N = sh.Cp[NB];
+  const bool fast = N <= (uint32_t)SEL_CAP;
+  if (fast) {
+    for (int b = warp; b < NB; b += SEL_WARPS) {
+      const uint32_t c0 = sh.Cp[b], cnt = sh.Cp[b + 1] - c0;
+      const uint2* src = cs + geo.block_lo(b / SEL_WARPS, b % SEL_WARPS);
+      for (uint32_t i = lane; i < cnt; i += 32) cbuf[c0 + i] = __ldcg(src + i);
+    }
+    __syncthreads();
+  }
+  auto cand_at = [&](uint32_t i) -> uint2 {
+    if (fast) return cbuf[i];
+    int lo = 0, hi = NB - 1;                  // last block b with Cp[b] <= i
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (sh.Cp[mid] <= i) lo = mid; else hi = mid - 1;
+    }
+    return __ldcg(cs + geo.block_lo(lo / SEL_WARPS, lo % SEL_WARPS) + (i - sh.Cp[lo]));
+  };
   const uint32_t need = p.state[s].k1;
-  // key bits 19..10
-  for (int x = tid; x < 1024; x += TK_THREADS) hbuf[x] = 0u;
+  for (int x = tid; x < 1024; x += SEL_THREADS) sh.hist[x] = 0u;
   __syncthreads();
-  for (uint32_t i = tid; i < N; i += TK_THREADS) atomicAdd(&hbuf[(__ldcg(&cand[i].x) >> 10) & 1023u], 1u);
+  for (uint32_t i = tid; i < N; i += SEL_THREADS) atomicAdd(&sh.hist[(cand_at(i).x >> 10) & 1023u], 1u);
   __syncthreads();
-  find_bin<1024>(hbuf, need, sh_res, sh_warp);
-  const uint32_t bA = sh_res[0] & 1023u, needA = sh_res[1];
-  // key bits 9..0 among keys in bin bA
-  for (int x = tid; x < 1024; x += TK_THREADS) hbuf[x] = 0u;
+  find_bin<1024>(sh.hist, need, sh.res, sh.warp8);
+  const uint32_t bA = sh.res[0] & 1023u, needA = sh.res[1];
   __syncthreads();
-  for (uint32_t i = tid; i < N; i += TK_THREADS) {
-    const uint32_t key = __ldcg(&cand[i].x);
-    if (((key >> 10) & 1023u) == bA) atomicAdd(&hbuf[key & 1023u], 1u);
+  for (int x = tid; x < 1024; x += SEL_THREADS) sh.hist[x] = 0u;
+  __syncthreads();
+  for (uint32_t i = tid; i < N; i += SEL_THREADS) {
+    const uint32_t key = cand_at(i).x;
+    if (((key >> 10) & 1023u) == bA) atomicAdd(&sh.hist[key & 1023u], 1u);
   }
   __syncthreads();
-  find_bin<1024>(hbuf, needA, sh_res, sh_warp);
-  const uint32_t bB = sh_res[0] & 1023u, need_eq = sh_res[1];
-  const uint32_t n_eq = hbuf[bB];
+  find_bin<1024>(sh.hist, needA, sh.res, sh.warp8);
+  const uint32_t bB = sh.res[0] & 1023u, need_eq = sh.res[1];
+  const uint32_t n_eq = sh.hist[bB];
   const uint32_t thr = (b1 << 20) | (bA << 10) | bB;
   __syncthreads();
   int32_t t_cut = 0x7fffffff;
   if (need_eq < n_eq) {
-    // the need_eq lowest token indices among keys equal to thr: radix select
-    // on u = 0x7fffffff - t (largest u = lowest t), bits 30..20, 19..10, 9..0
+    // the need_eq lowest token ids among keys equal to thr
     uint32_t prefix = 0, krem = need_eq;
     for (int lev = 0; lev < 3; ++lev) {
       const int nb = lev == 0 ? 2048 : 1024;
       const int shift = lev == 0 ? 20 : (lev == 1 ? 10 : 0);
-      for (int x = tid; x < nb; x += TK_THREADS) hbuf[x] = 0u;
+      for (int x = tid; x < nb; x += SEL_THREADS) sh.hist[x] = 0u;
       __syncthreads();
-      for (uint32_t i = tid; i < N; i += TK_THREADS) {
-        const uint2 cv = __ldcg(&cand[i]);
+      for (uint32_t i = tid; i < N; i += SEL_THREADS) {
+        const uint2 cv = cand_at(i);
         if (cv.x != thr) continue;
         const uint32_t u = 0x7fffffffu - cv.y;
         if (lev > 0 && (u >> (shift + 10)) != prefix) continue;
-        atomicAdd(&hbuf[(u >> shift) & (uint32_t)(nb - 1)], 1u);
+        atomicAdd(&sh.hist[(u >> shift) & (uint32_t)(nb - 1)], 1u);
       }
       __syncthreads();
-      if (lev == 0) find_bin<2048>(hbuf, krem, sh_res, sh_warp);
-      else find_bin<1024>(hbuf, krem, sh_res, sh_warp);
-      prefix = (prefix << (lev == 0 ? 0 : 10)) | (sh_res[0] & (uint32_t)(nb - 1));
-      krem = sh_res[1];
+      if (lev == 0) find_bin<2048>(sh.hist, krem, sh.res, sh.warp8);
+      else find_bin<1024>(sh.hist, krem, sh.res, sh.warp8);
+      prefix = (prefix << (lev == 0 ? 0 : 10)) | (sh.res[0] & (uint32_t)(nb - 1));
+      krem = sh.res[1];
+      __syncthreads();
     }
     t_cut = (int32_t)(0x7fffffffu - prefix);
   }
-  if (tid == 0) {
+  if (r == 0 && tid == 0) {
     p.state[s].thr = thr;
     p.state[s].t_cut = t_cut;
   }
-  // per-chunk counts of the selected candidates, then exclusive offsets
-  int32_t* cnt = p.cnt + (size_t)s * p.topk_chunks;
-  for (uint32_t i = tid; i < N; i += TK_THREADS) {
-    const uint2 cv = __ldcg(&cand[i]);
-    if (cv.x > thr || (cv.x == thr && (int32_t)cv.y <= t_cut)) atomicAdd(&cnt[cv.y / TOPK_CHUNK], 1);
-  }
-  __threadfence();
-  __syncthreads();
-  const int nch = p.topk_chunks;
-  const int per = (nch + TK_THREADS - 1) / TK_THREADS;
-  const int lo = min(nch, tid * per), hi = min(nch, lo + per);
-  uint32_t mine = 0;
-  for (int x = lo; x < hi; ++x) mine += (uint32_t)__ldcg(&cnt[x]);
-  uint32_t off = block_excl_scan(mine, sh_scan, nullptr);
-  for (int x = lo; x < hi; ++x) {
-    const uint32_t c = (uint32_t)__ldcg(&cnt[x]);
-    cnt[x] = (int32_t)off;
-    off += c;
-  }
-}
-
-// writes the selected token ids of one chunk in ascending order
-__global__ void __launch_bounds__(TK_THREADS) topk_write_kernel(DecodeParams p) {
-  const int s = blockIdx.y, ch = blockIdx.x, tid = threadIdx.x;
-  __shared__ uint32_t sh_scan[TK_THREADS / 32];
-  const uint32_t thr = p.state[s].thr;
-  const int32_t t_cut = p.state[s].t_cut;
-  const int base = p.cnt[(size_t)s * p.topk_chunks + ch];
-  const int64_t t0 = (int64_t)ch * TOPK_CHUNK + (int64_t)tid * TK_PER;
-  float v[TK_PER];
-  load16(p.scores + (size_t)s * p.Tp, t0, p.T, v, true, policy_evict_first());
-  uint32_t n = 0;
-  bool selv[TK_PER];
-#pragma unroll
-  for (int i = 0; i < TK_PER; ++i) {
-    const uint32_t key = f2key(v[i]);
-    const int64_t t = t0 + i;
-    selv[i] = t < p.T && (key > thr || (key == thr && t <= t_cut));
-    n += selv[i];
-  }
-  int pos = base + (int)block_excl_scan(n, sh_scan, nullptr);
+  auto chosen = [&](uint32_t key, int64_t t) -> bool {
+    return key > thr || (key == thr && t <= (int64_t)t_cut);
+  };
   int32_t* out = p.sel + (size_t)s * p.kk;
   int32_t* out2 = p.sel_user ? p.sel_user + (size_t)s * p.kk : nullptr;
-#pragma unroll
-  for (int i = 0; i < TK_PER; ++i) {
-    if (selv[i] && pos >= 0 && pos < p.kk) {
-      out[pos] = (int32_t)(t0 + i);
-      if (out2) out2[pos] = (int32_t)(t0 + i);
+  auto put = [&](uint32_t pos, int32_t t) {
+    if (pos < (uint32_t)p.kk) {
+      out[pos] = t;
+      if (out2) out2[pos] = t;
     }
-    pos += selv[i];
+  };
+
+  if (fast) {
+    // ---- 3. B = selected candidates in token order; merge with sure tokens -
+    uint32_t cnt = 0;
+    const uint32_t i0 = (uint32_t)tid * (SEL_CAP / SEL_THREADS);
+#pragma unroll
+    for (int e = 0; e < SEL_CAP / SEL_THREADS; ++e) {
+      const uint32_t i = i0 + e;
+      if (i < N && chosen(cbuf[i].x, cbuf[i].y)) ++cnt;
+    }
+    uint32_t nB;
+    uint32_t pos = sel_excl_scan(cnt, sh.scan, &nB);
+#pragma unroll
+    for (int e = 0; e < SEL_CAP / SEL_THREADS; ++e) {
+      const uint32_t i = i0 + e;
+      if (i < N && chosen(cbuf[i].x, cbuf[i].y)) bbuf[pos++] = (int32_t)cbuf[i].y;
+    }
+    __syncthreads();
+    const uint32_t gS = sh.Sp[r * SEL_WARPS + warp];
+    const uint32_t bl = lower_bound_i32(bbuf, nB, w_lo), bh = lower_bound_i32(bbuf, nB, w_hi);
+    for (uint32_t bg = bl;; bg += 32) {
+      const uint32_t b = bg + lane;
+      const int64_t tb = b < bh ? (int64_t)bbuf[b] : -1;
+      uint32_t below = 0;
+      for (uint32_t j0 = 0; j0 < ns_w; j0 += 32) {
+        const uint32_t j = j0 + lane;
+        const int64_t t = j < ns_w ? (int64_t)sure_w[2 * L_w - 1 - (int64_t)j] : INT64_MAX;
+        if (bg == bl && j < ns_w) put(gS + j + lower_bound_i32(bbuf, nB, t), (int32_t)t);
+        const int nk = ns_w - j0 < 32u ? (int)(ns_w - j0) : 32;
+        for (int k = 0; k < nk; ++k) {
+          const int64_t tk = __shfl_sync(0xffffffffu, t, k);
+          below += tk < tb;
+        }
+      }
+      if (b < bh) put(b + gS + below, (int32_t)tb);
+      if (bg + 32 >= bh) break;
+    }
+  } else {
+    // ---- 3'. many candidates: count, then write, re-reading the scores -----
+    auto is_sel = [&](float x, int64_t t) -> uint32_t {
+      return (t < w_hi && chosen(f2key(x), t)) ? 1u : 0u;
+    };
+    uint32_t offset = 0;
+    {
+      // selected tokens of every earlier block: sure ones plus chosen candidates
+      uint32_t c = 0;
+      const uint32_t lim = sh.Cp[r * SEL_WARPS];
+      for (uint32_t i = tid; i < lim; i += SEL_THREADS) {
+        const uint2 cv = cand_at(i);
+        c += chosen(cv.x, cv.y);
+      }
+      uint32_t tot;
+      sel_excl_scan(c, sh.scan, &tot);
+      offset = sh.Sp[r * SEL_WARPS] + tot;
+    }
+    uint32_t wcount = 0;
+    for (int64_t b0 = w_lo; b0 < w_hi; b0 += 128) {
+      const int64_t t0 = b0 + 4 * lane;
+      const float4 f = t0 < w_hi ? __ldcg(reinterpret_cast<const float4*>(sc + t0))
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+      wcount += is_sel(f.x, t0) + is_sel(f.y, t0 + 1) + is_sel(f.z, t0 + 2) + is_sel(f.w, t0 + 3);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) wcount += __shfl_xor_sync(0xffffffffu, wcount, off);
+    uint32_t wbase = offset + sel_excl_scan(lane == 0 ? wcount : 0u, sh.scan, nullptr);
+    wbase = __shfl_sync(0xffffffffu, wbase, 0);
+    for (int64_t b0 = w_lo; b0 < w_hi; b0 += 128) {
+      const int64_t t0 = b0 + 4 * lane;
+      const float4 f = t0 < w_hi ? __ldcg(reinterpret_cast<const float4*>(sc + t0))
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+      const uint32_t m = is_sel(f.x, t0) | (is_sel(f.y, t0 + 1) << 1) |
+                         (is_sel(f.z, t0 + 2) << 2) | (is_sel(f.w, t0 + 3) << 3);
+      const uint32_t n = __popc(m);
+      uint32_t inc = n;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t o = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += o;
+      }
+      uint32_t q = wbase + inc - n;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if ((m >> e) & 1u) put(q++, (int32_t)(t0 + e));
+      wbase += __shfl_sync(0xffffffffu, inc, 31);
+    }
   }
 }
 
@@ -642,14 +795,17 @@ __global__ void __launch_bounds__(TK_THREADS) topk_write_kernel(DecodeParams p) 
 // group of 8 lanes serves a token, one 16-byte chunk (8 stored values) per
 // lane, and every thread fetches the chunks of its tokens together: K chunks
 // give partial logits (summed over the 8 lanes by a fixed butterfly), V
-// chunks are copied into a zeroed fp16 tile V[token][channel] (rows padded to
-// 65 words).  After the softmax statistics, thread j sums p_t,i * V[t][j] over
-// the tokens in order.  Partials per (stream, chunk, head): max logit m, sum
-// of exp l and the unnormalised output in the rotated V basis.
+// chunks are copied into a zeroed fp16 tile V[token][channel].  The softmax
+// weights p (fp32) are split into fp16 hi + 2^11 * lo parts, stored
+// transposed P[head][token], and o~ = P V runs on tensor cores (mma.sync,
+// fp32 accumulation, one accumulator per part): warp w owns channels
+// [32w, 32w + 32).  Partials per (stream, chunk, head): max logit m, sum of
+// exp l and the unnormalised output in the rotated V basis.
 // grid: (attn_chunks, BH), block 128, dynamic smem
 // ---------------------------------------------------------------------------
 constexpr int ATTN_THREADS = 128;
-constexpr int VD_LD = 130;          // halves per V tile row
+constexpr int VLD = 136;            // halves per V tile row (272 B: ldmatrix without conflicts)
+constexpr int PLD = 136;            // halves per P row
 constexpr uint64_t NO_IDX = ~0ull;
 
 __device__ __forceinline__ void row_addr(const mkv_segment_header* hdr, int64_t t, int S, int c,
@@ -673,9 +829,13 @@ __device__ __forceinline__ void row_addr(const mkv_segment_header* hdr, int64_t 
   }
 }
 
+// tokens of a chunk rounded up to the mma K step
+__host__ __device__ constexpr int attn_rows16(int chunk) { return (chunk + 15) & ~15; }
+
 size_t attn_smem_bytes(int g, int chunk) {
   const int gp = (g + 3) & ~3;
-  return (size_t)chunk * VD_LD * 2 + (size_t)chunk * (4 * 8 + 2 * 4) +
+  return (size_t)attn_rows16(chunk) * VLD * 2 + 2 * MAX_G * PLD * 2 +
+         (size_t)chunk * (4 * 8 + 2 * 4) +
          sizeof(float) * ((size_t)D * gp + (size_t)chunk * gp + 2 * g);
 }
 
@@ -689,7 +849,7 @@ __device__ __forceinline__ void attn_body(const DecodeParams& p, int s, int chk,
                                           const uint64_t* kv_, const uint64_t* ki_,
                                           const int* kn_, const uint64_t* vv_,
                                           const uint64_t* vi_, const int* vn_, __half* Vd,
-                                          const float* qs, float* lg, float* ml) {
+                                          __half* Pt, const float* qs, float* lg, float* ml) {
   const int g = p.g, gp = (g + 3) & ~3;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cl = tid & 7, tg = tid >> 3;
@@ -706,12 +866,12 @@ __device__ __forceinline__ void attn_body(const DecodeParams& p, int s, int chk,
       kix[u] = vix[u] = make_uint2(0u, 0u);
       if (i < n) {
         if (8 * cl < kn_[i]) {
-          kvv[u] = __ldg(reinterpret_cast<const uint4*>(p.pool + kv_[i]) + cl);
-          if (ki_[i] != NO_IDX) kix[u] = __ldg(reinterpret_cast<const uint2*>(p.pool + ki_[i]) + cl);
+          kvv[u] = ld_cg_u4(reinterpret_cast<const uint4*>(p.pool + kv_[i]) + cl);
+          if (ki_[i] != NO_IDX) kix[u] = ld_cg_u2(reinterpret_cast<const uint2*>(p.pool + ki_[i]) + cl);
         }
         if (8 * cl < vn_[i]) {
-          vvv[u] = __ldg(reinterpret_cast<const uint4*>(p.pool + vv_[i]) + cl);
-          if (vi_[i] != NO_IDX) vix[u] = __ldg(reinterpret_cast<const uint2*>(p.pool + vi_[i]) + cl);
+          vvv[u] = ld_cg_u4(reinterpret_cast<const uint4*>(p.pool + vv_[i]) + cl);
+          if (vi_[i] != NO_IDX) vix[u] = ld_cg_u2(reinterpret_cast<const uint2*>(p.pool + vi_[i]) + cl);
         }
       }
     }
@@ -731,17 +891,17 @@ __device__ __forceinline__ void attn_body(const DecodeParams& p, int s, int chk,
             kr = vr = make_uint4(0u, 0u, 0u, 0u);
             kx = vx = make_uint2(0u, 0u);
             if (8 * ck < kn_[i]) {
-              kr = __ldg(reinterpret_cast<const uint4*>(p.pool + kv_[i]) + ck);
-              if (ki_[i] != NO_IDX) kx = __ldg(reinterpret_cast<const uint2*>(p.pool + ki_[i]) + ck);
+              kr = ld_cg_u4(reinterpret_cast<const uint4*>(p.pool + kv_[i]) + ck);
+              if (ki_[i] != NO_IDX) kx = ld_cg_u2(reinterpret_cast<const uint2*>(p.pool + ki_[i]) + ck);
             }
             if (8 * ck < vn_[i]) {
-              vr = __ldg(reinterpret_cast<const uint4*>(p.pool + vv_[i]) + ck);
-              if (vi_[i] != NO_IDX) vx = __ldg(reinterpret_cast<const uint2*>(p.pool + vi_[i]) + ck);
+              vr = ld_cg_u4(reinterpret_cast<const uint4*>(p.pool + vv_[i]) + ck);
+              if (vi_[i] != NO_IDX) vx = ld_cg_u2(reinterpret_cast<const uint2*>(p.pool + vi_[i]) + ck);
             }
           }
           if (8 * ck < vn_[i]) {
             const __half* hv = reinterpret_cast<const __half*>(&vr);
-            __half* vrow = Vd + (size_t)i * VD_LD;
+            __half* vrow = Vd + (size_t)i * VLD;
             const bool dense = vi_[i] == NO_IDX;
 #pragma unroll
             for (int e = 0; e < 8; ++e) vrow[dense ? 8 * ck + e : chan_of(vx, e)] = hv[e];
@@ -781,7 +941,10 @@ __device__ __forceinline__ void attn_body(const DecodeParams& p, int s, int chk,
     }
   }
   __syncthreads();
-  // ---- softmax statistics per head (warp per head, fixed-order reductions) --
+  // ---- softmax per head (warp per head, fixed-order reductions); weights go
+  // to P[head][token] as fp16 hi and 2^11 * (p - hi) ----------------------
+  __half* Ph = Pt;
+  __half* Pl = Pt + MAX_G * PLD;
   for (int hh = warp; hh < g; hh += ATTN_THREADS / 32) {
     float m = -INFINITY;
     for (int i = lane; i < n; i += 32) m = fmaxf(m, lg[i * gp + hh]);
@@ -790,7 +953,9 @@ __device__ __forceinline__ void attn_body(const DecodeParams& p, int s, int chk,
     float l = 0.f;
     for (int i = lane; i < n; i += 32) {
       const float e = expf(lg[i * gp + hh] - m);
-      lg[i * gp + hh] = e;
+      const __half hi = __float2half_rn(e);
+      Ph[hh * PLD + i] = hi;
+      Pl[hh * PLD + i] = __float2half_rn((e - __half2float(hi)) * 2048.f);
       l += e;
     }
 #pragma unroll
@@ -801,28 +966,47 @@ __device__ __forceinline__ void attn_body(const DecodeParams& p, int s, int chk,
     }
   }
   __syncthreads();
-  // ---- o~_i[j] = sum_t p_t,i V[t][j]: thread j, tokens in order ------------
-  const int jc = tid;   // channel
-  float o[GM];
+  // ---- o~ = P V on tensor cores: warp w, channels [32w, 32w + 32) ----------
+  float ch_[4][4], cl_[4][4];
 #pragma unroll
-  for (int hh = 0; hh < GM; ++hh) o[hh] = 0.f;
-  for (int i = 0; i < n; ++i) {
-    const float v = __half2float(Vd[(size_t)i * VD_LD + jc]);
+  for (int a = 0; a < 4; ++a)
 #pragma unroll
-    for (int h4 = 0; h4 < GM; h4 += 4) {
-      if (h4 < g) {
-        const float4 p4 = *reinterpret_cast<const float4*>(lg + i * gp + h4);
-        o[h4] = fmaf(p4.x, v, o[h4]);
-        o[h4 + 1] = fmaf(p4.y, v, o[h4 + 1]);
-        o[h4 + 2] = fmaf(p4.z, v, o[h4 + 2]);
-        o[h4 + 3] = fmaf(p4.w, v, o[h4 + 3]);
-      }
+    for (int e = 0; e < 4; ++e) ch_[a][e] = cl_[a][e] = 0.f;
+  const int mm = lane >> 3, r8 = lane & 7;
+  const uint32_t ph = smem_u32(Ph), pl = smem_u32(Pl), vd = smem_u32(Vd);
+  const int ksteps = (n + 15) >> 4;
+  for (int ks = 0; ks < ksteps; ++ks) {
+    const int k0 = ks * 16;
+    uint32_t ah[4], al[4];
+    const uint32_t aoff = (uint32_t)(((r8 + (mm & 1) * 8) * PLD + k0 + (mm >> 1) * 8) * 2);
+    ldsm_x4(ph + aoff, ah);
+    ldsm_x4(pl + aoff, al);
+#pragma unroll
+    for (int np = 0; np < 2; ++np) {
+      uint32_t bb[4];
+      const int row = k0 + (mm & 1) * 8 + r8;
+      const int col = warp * 32 + np * 16 + (mm >> 1) * 8;
+      ldsm_x4_t(vd + (uint32_t)((row * VLD + col) * 2), bb);
+      mma16816(ch_[2 * np], ah, bb[0], bb[1]);
+      mma16816(ch_[2 * np + 1], ah, bb[2], bb[3]);
+      mma16816(cl_[2 * np], al, bb[0], bb[1]);
+      mma16816(cl_[2 * np + 1], al, bb[2], bb[3]);
     }
   }
   const size_t pbase = ((size_t)s * p.attn_chunks + chk) * g;
+  const int h0 = lane >> 2, c0 = warp * 32 + 2 * (lane & 3);
 #pragma unroll
-  for (int hh = 0; hh < GM; ++hh)
-    if (hh < g) p.part_o[(pbase + hh) * D + jc] = o[hh];
+  for (int nt = 0; nt < 4; ++nt) {
+    const int chn = c0 + nt * 8;
+    if (h0 < g)
+      *reinterpret_cast<float2*>(p.part_o + (pbase + h0) * D + chn) =
+          make_float2(fmaf(cl_[nt][0], 1.f / 2048.f, ch_[nt][0]),
+                      fmaf(cl_[nt][1], 1.f / 2048.f, ch_[nt][1]));
+    if (h0 + 8 < g)
+      *reinterpret_cast<float2*>(p.part_o + (pbase + h0 + 8) * D + chn) =
+          make_float2(fmaf(cl_[nt][2], 1.f / 2048.f, ch_[nt][2]),
+                      fmaf(cl_[nt][3], 1.f / 2048.f, ch_[nt][3]));
+  }
   if (tid < 2 * g) p.part_ml[pbase * 2 + tid] = ml[tid];
 }
 
@@ -833,8 +1017,10 @@ __global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(DecodeParams p) {
   const int g = p.g, gp = (g + 3) & ~3;
   const int tid = threadIdx.x;
   const int CH = p.attn_chunk;
-  __half* Vd = reinterpret_cast<__half*>(asm_);                                // [CH][VD_LD]
-  uint64_t* kv_ = reinterpret_cast<uint64_t*>(asm_ + (size_t)CH * VD_LD * 2);  // [CH]
+  const int R16 = attn_rows16(CH);
+  __half* Vd = reinterpret_cast<__half*>(asm_);                                // [R16][VLD]
+  __half* Pt = Vd + (size_t)R16 * VLD;                                         // [2][16][PLD]
+  uint64_t* kv_ = reinterpret_cast<uint64_t*>(Pt + 2 * MAX_G * PLD);           // [CH]
   uint64_t* ki_ = kv_ + CH;
   uint64_t* vv_ = ki_ + CH;
   uint64_t* vi_ = vv_ + CH;
@@ -849,8 +1035,10 @@ __global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(DecodeParams p) {
     qs[x] = hh < g ? qt[hh * D + chn] : 0.f;
   }
   {
-    uint32_t* z = reinterpret_cast<uint32_t*>(Vd);
-    for (int x = tid; x < CH * VD_LD / 2; x += ATTN_THREADS) z[x] = 0u;
+    // the V tile and both P parts start at zero (rows past n, heads past g)
+    uint4* z = reinterpret_cast<uint4*>(Vd);
+    const int nz = (R16 * VLD + 2 * MAX_G * PLD) / 8;
+    for (int x = tid; x < nz; x += ATTN_THREADS) z[x] = make_uint4(0u, 0u, 0u, 0u);
   }
   const int j0 = chk * CH;
   const int n = min(CH, p.kk - j0);
@@ -860,8 +1048,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(DecodeParams p) {
     row_addr(p.hdrV + (size_t)s * p.n_seg, t, p.S, p.c, &vv_[tid], &vi_[tid], &vn_[tid]);
   }
   __syncthreads();
-  if (g <= 4) attn_body<4>(p, s, chk, n, kv_, ki_, kn_, vv_, vi_, vn_, Vd, qs, lg, ml);
-  else attn_body<MAX_G>(p, s, chk, n, kv_, ki_, kn_, vv_, vi_, vn_, Vd, qs, lg, ml);
+  if (g <= 4) attn_body<4>(p, s, chk, n, kv_, ki_, kn_, vv_, vi_, vn_, Vd, Pt, qs, lg, ml);
+  else attn_body<MAX_G>(p, s, chk, n, kv_, ki_, kn_, vv_, vi_, vn_, Vd, Pt, qs, lg, ml);
 }
 
 // ---------------------------------------------------------------------------
@@ -1048,8 +1236,19 @@ cudaError_t prepare_decode_kernels() {
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(qrot_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, D * D * 4);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              227 * 1024 - SC_STATIC_SMEM);
+  e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)SEL_SMEM);
+  if (e != cudaSuccess) return e;
+#define MKV_SCORE_ATTR(N)                                                                   \
+  e = cudaFuncSetAttribute(score_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
+                           227 * 1024 - SC_STATIC_SMEM);                                  \
+  if (e != cudaSuccess) return e;
+  MKV_SCORE_ATTR(1) MKV_SCORE_ATTR(2) MKV_SCORE_ATTR(3) MKV_SCORE_ATTR(4) MKV_SCORE_ATTR(5)
+  MKV_SCORE_ATTR(6) MKV_SCORE_ATTR(7) MKV_SCORE_ATTR(8) MKV_SCORE_ATTR(9) MKV_SCORE_ATTR(10)
+  MKV_SCORE_ATTR(11) MKV_SCORE_ATTR(12) MKV_SCORE_ATTR(13) MKV_SCORE_ATTR(14)
+  MKV_SCORE_ATTR(15) MKV_SCORE_ATTR(16)
+#undef MKV_SCORE_ATTR
+  return cudaSuccess;
 }
 
 cudaError_t launch_partition(const mkv_segment_header* hdrK, int n_streams, int n_seg, int c,
@@ -1066,15 +1265,40 @@ cudaError_t launch_qrot(const DecodeParams& p, cudaStream_t st) {
 }
 
 cudaError_t launch_score(const DecodeParams& p, cudaStream_t st) {
-  score_kernel<<<p.G, SC_THREADS, sc_slot(p.stage_bytes) * p.n_stages, st>>>(p);
+  const size_t smem = sc_slot(p.stage_bytes) * p.n_stages;
+  switch (p.c >> 3) {
+#define MKV_SCORE_CASE(N) \
+  case N: score_kernel<N><<<p.G, SC_THREADS, smem, st>>>(p); break;
+    MKV_SCORE_CASE(1) MKV_SCORE_CASE(2) MKV_SCORE_CASE(3) MKV_SCORE_CASE(4) MKV_SCORE_CASE(5)
+    MKV_SCORE_CASE(6) MKV_SCORE_CASE(7) MKV_SCORE_CASE(8) MKV_SCORE_CASE(9) MKV_SCORE_CASE(10)
+    MKV_SCORE_CASE(11) MKV_SCORE_CASE(12) MKV_SCORE_CASE(13) MKV_SCORE_CASE(14)
+    MKV_SCORE_CASE(15) MKV_SCORE_CASE(16)
+#undef MKV_SCORE_CASE
+    default: return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 
+int select_cluster_size(int n_streams, int64_t T, int G) {
+  int R = 1;
+  while (R < 8 && (int64_t)n_streams * R * 2 <= G && T / (2 * R) >= 4096) R *= 2;
+  return R;
+}
+
 cudaError_t launch_topk(const DecodeParams& p, cudaStream_t st) {
-  dim3 grid(p.topk_chunks, p.B * p.H);
-  topk_pass2_kernel<<<grid, TK_THREADS, 0, st>>>(p);
-  topk_write_kernel<<<grid, TK_THREADS, 0, st>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.sel_R, p.B * p.H, 1);
+  cfg.blockDim = dim3(SEL_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SEL_SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = p.sel_R;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, select_kernel, p);
 }
 
 cudaError_t launch_attn(const DecodeParams& p, cudaStream_t st) {

@@ -51,7 +51,6 @@ struct mkv_ctx {
   int gram_chunks_max = 0;
   int attn_chunk = 128;
   int attn_chunks_max = 0;
-  int topk_chunks_max = 0;
   int64_t Tp_max = 0;              // padded row stride of scores / candidates
   int G = 0;                       // score-kernel CTAs (one per SM)
   int stage_bytes = 0, n_stages = 0;
@@ -82,10 +81,9 @@ struct mkv_ctx {
   float* qbar = nullptr;
   float* scores = nullptr;
   uint32_t* hist = nullptr;
-  uint32_t* tick = nullptr;        // [3][BH]: tick1, tick2, cand_n
+  uint32_t* tick = nullptr;        // [BH]: score CTAs done with a stream
   uint2* cand = nullptr;
   TopkState* state = nullptr;
-  int32_t* cnt = nullptr;
   int32_t* sel = nullptr;
   int* err = nullptr;
   float* part_o = nullptr;
@@ -194,7 +192,6 @@ void release(mkv_ctx* c) {
   cudaFree(c->tick);
   cudaFree(c->cand);
   cudaFree(c->state);
-  cudaFree(c->cnt);
   cudaFree(c->sel);
   cudaFree(c->err);
   cudaFree(c->part_o);
@@ -321,7 +318,6 @@ mkv_status mkv_create(const mkv_config* cfg, mkv_ctx** out) {
     return MKV_ERR_INVALID_ARG;
   }
   c->attn_chunks_max = (int)ceil_div(c->kk_max, c->attn_chunk);
-  c->topk_chunks_max = (int)ceil_div(cfg->max_ctx, TOPK_CHUNK);
   c->Tp_max = ceil_div(cfg->max_ctx, 16) * 16;
   {
     int sms = 0;
@@ -357,17 +353,16 @@ mkv_status mkv_create(const mkv_config* cfg, mkv_ctx** out) {
   AL(c->qbar, BH * D);
   AL(c->scores, BH * (size_t)c->Tp_max);
   AL(c->hist, BH * HIST1);
-  AL(c->tick, 3 * BH);
+  AL(c->tick, BH);
   AL(c->cand, BH * (size_t)c->Tp_max);
   AL(c->state, BH);
-  AL(c->cnt, BH * (size_t)c->topk_chunks_max);
   AL(c->sel, BH * (size_t)c->kk_max);
   AL(c->err, 1);
   AL(c->part_o, BH * (size_t)c->attn_chunks_max * c->g * D);
   AL(c->part_ml, BH * (size_t)c->attn_chunks_max * c->g * 2);
 #undef AL
   cudaError_t e = cudaMallocHost(reinterpret_cast<void**>(&c->total_host), sizeof(unsigned long long));
-  if (e == cudaSuccess) e = cudaMemset(c->tick, 0, 3 * BH * sizeof(uint32_t));
+  if (e == cudaSuccess) e = cudaMemset(c->tick, 0, BH * sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(c->err, 0, sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(c->sel, 0, BH * (size_t)c->kk_max * sizeof(int32_t));
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -498,12 +493,9 @@ mkv_status mkv_decode(mkv_ctx* c, const void* q, float* out, int32_t* sel, mkv_s
   p.stage_bytes = c->stage_bytes;
   p.n_stages = c->n_stages;
   p.tick1 = c->tick;
-  p.tick2 = c->tick + c->BH;
-  p.cand_n = c->tick + 2 * c->BH;
   p.cand = c->cand;
   p.state = c->state;
-  p.cnt = c->cnt;
-  p.topk_chunks = (int)ceil_div(c->T, TOPK_CHUNK);
+  p.sel_R = select_cluster_size(c->BH, c->T, c->G);
   p.sel = c->sel;
   p.sel_user = sel;
   p.err = c->err;
@@ -515,7 +507,7 @@ mkv_status mkv_decode(mkv_ctx* c, const void* q, float* out, int32_t* sel, mkv_s
   mkv_status s;
   if ((s = timed(c, MKV_KERNEL_QROT, st, 1, [&] { return launch_qrot(p, st); })) != MKV_OK) return s;
   if ((s = timed(c, MKV_KERNEL_SCORE, st, 1, [&] { return launch_score(p, st); })) != MKV_OK) return s;
-  if ((s = timed(c, MKV_KERNEL_TOPK, st, 2, [&] { return launch_topk(p, st); })) != MKV_OK) return s;
+  if ((s = timed(c, MKV_KERNEL_TOPK, st, 1, [&] { return launch_topk(p, st); })) != MKV_OK) return s;
   if ((s = timed(c, MKV_KERNEL_ATTN, st, 1, [&] { return launch_attn(p, st); })) != MKV_OK) return s;
   if ((s = timed(c, MKV_KERNEL_MERGE, st, 1, [&] { return launch_merge(p, st); })) != MKV_OK) return s;
   c->decode_calls += 1;

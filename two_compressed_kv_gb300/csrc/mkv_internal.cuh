@@ -14,7 +14,6 @@ constexpr int MAX_G = 16;              // query heads per KV head
 constexpr int HIST1 = 4096;            // level-1 radix digit of the score key: bits 31..20
 constexpr int HISTA = 1024;            // candidates, bits 19..10
 constexpr int HISTB = 1024;            // candidates, bits  9..0
-constexpr int TOPK_CHUNK = 4096;       // tokens per CTA in the selection passes
 constexpr int TILE_T = 64;             // tokens per rotation tile
 constexpr int ATTN_MAX_CHUNK = 128;    // selected tokens per attention CTA (one per thread)
 
@@ -125,12 +124,9 @@ struct DecodeParams {
   int stage_bytes;                 // bytes per shared-memory stage of the score kernel
   int n_stages;
   uint32_t* tick1;                 // [BH] tickets: score CTAs done with a stream
-  uint32_t* tick2;                 // [BH] tickets: selection-pass CTAs done
   uint2* cand;                     // [BH][Tp] (key, token) of threshold-bin candidates
-  uint32_t* cand_n;                // [BH]
   TopkState* state;                // [BH]
-  int32_t* cnt;                    // [BH][topk_chunks]: counts, then chunk offsets
-  int topk_chunks;                 // ceil(T / TOPK_CHUNK)
+  int sel_R;                       // CTAs (one cluster) per stream in the selection
   int32_t* sel;                    // [BH][kk] (internal)
   int32_t* sel_user;               // optional copy for the caller
   int attn_chunk;                  // selected tokens per attention CTA (<= ATTN_MAX_CHUNK)
@@ -155,8 +151,10 @@ cudaError_t launch_partition(const mkv_segment_header* hdrK, int n_streams, int 
                              StagePlan* plan, int32_t* plan_n, cudaStream_t st);
 cudaError_t launch_qrot(const DecodeParams& p, cudaStream_t st);
 cudaError_t launch_score(const DecodeParams& p, cudaStream_t st);
-// the two selection launches; returns after enqueueing both
+// the selection launch (one cluster of sel_R CTAs per stream)
 cudaError_t launch_topk(const DecodeParams& p, cudaStream_t st);
+// CTAs per stream for the selection: up to 8 while the grid fits G SMs twice
+int select_cluster_size(int n_streams, int64_t T, int G);
 cudaError_t launch_attn(const DecodeParams& p, cudaStream_t st);
 cudaError_t launch_merge(const DecodeParams& p, cudaStream_t st);
 
