@@ -24,6 +24,11 @@ __device__ __forceinline__ uint32_t f2key(float x) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Inverse of f2key for keys of finite floats (key 0x80000000 gives +0).
+__device__ __forceinline__ float key2f(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 __device__ __forceinline__ void h8_to_f(const uint4& raw, float v[8]) {
   const __half2* h = reinterpret_cast<const __half2*>(&raw);
 #pragma unroll
@@ -458,7 +463,6 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
 constexpr int SEL_THREADS = 1024;
 constexpr int SEL_WARPS = SEL_THREADS / 32;
 constexpr int SEL_CAP = 8192;                 // candidates kept in shared memory
-constexpr int SEL_UNROLL = 8;                 // 128-token steps per warp loaded together
 constexpr size_t SEL_SMEM = (size_t)SEL_CAP * (sizeof(uint2) + sizeof(int32_t));
 
 // exclusive scan of one value per thread over SEL_THREADS threads
@@ -553,45 +557,72 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) select_kernel(DecodeParams p) 
   const int64_t L_w = w_hi - w_lo;
 
   // ---- 1. sure tokens and candidates of this warp's block, in token order --
+  // Lane l takes the 32 consecutive tokens at b0 + 32 l of each 1024-token
+  // step.  bin(key) > b1 and bin(key) == b1 are tested as float compares
+  // against the smallest floats of bins b1 and b1 + 1 (the key map is
+  // monotone; both zeros fall in the same bin and compare equal).
   uint32_t ns_w = 0, nc_w = 0;
-  for (int64_t b0 = w_lo; b0 < w_hi; b0 += 128 * SEL_UNROLL) {
-    float4 f[SEL_UNROLL];
+  // bins 0 and >= 4088 also hold infinities and NaNs: those compare by key
+  const bool by_key = b1 == 0u || b1 >= 4088u;
+  const float f_lo = by_key ? 0.f : key2f(b1 << 20);
+  const float f_hi = by_key ? 0.f : key2f((b1 + 1u) << 20);
+  for (int64_t b0 = w_lo; b0 < w_hi; b0 += 32 * 32) {
+    const int64_t t0 = b0 + 32 * lane;
+    float4 f[8];
 #pragma unroll
-    for (int j = 0; j < SEL_UNROLL; ++j) {
-      const int64_t t0 = b0 + 128 * j + 4 * lane;
-      f[j] = t0 < w_hi ? __ldcg(reinterpret_cast<const float4*>(sc + t0))
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+    for (int j = 0; j < 8; ++j)
+      f[j] = t0 + 4 * j < w_hi ? __ldcg(reinterpret_cast<const float4*>(sc + t0) + j)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+    const int nv = t0 >= w_hi ? 0 : (w_hi - t0 >= 32 ? 32 : (int)(w_hi - t0));
+    uint32_t sm = 0, cm = 0;        // bit i: token t0 + i is sure / a candidate
 #pragma unroll
-    for (int j = 0; j < SEL_UNROLL; ++j) {
-      const int64_t t0 = b0 + 128 * j + 4 * lane;
+    for (int j = 0; j < 8; ++j) {
       const float v4[4] = {f[j].x, f[j].y, f[j].z, f[j].w};
-      uint32_t keys[4], sb = 0, cb = 0;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        keys[e] = f2key(v4[e]);
-        const bool ok = t0 + e < w_hi;
-        const uint32_t bin = keys[e] >> 20;
-        sb |= (uint32_t)(ok && bin > b1) << e;
-        cb |= (uint32_t)(ok && bin == b1) << e;
+        sm |= (uint32_t)(v4[e] >= f_hi) << (4 * j + e);
+        cm |= (uint32_t)(v4[e] >= f_lo && v4[e] < f_hi) << (4 * j + e);
       }
-      const uint32_t packed = (uint32_t)__popc(sb) | ((uint32_t)__popc(cb) << 16);
-      uint32_t inc = packed;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t o = __shfl_up_sync(0xffffffffu, inc, off);
-        if (lane >= off) inc += o;
-      }
-      const uint32_t excl = inc - packed, tot = __shfl_sync(0xffffffffu, inc, 31);
-      uint32_t ps = ns_w + (excl & 0xffffu), pc = nc_w + (excl >> 16);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if ((sb >> e) & 1u) sure_w[2 * L_w - 1 - (int64_t)(ps++)] = (int32_t)(t0 + e);
-        if ((cb >> e) & 1u) cand_w[pc++] = make_uint2(keys[e], (uint32_t)(t0 + e));
-      }
-      ns_w += tot & 0xffffu;
-      nc_w += tot >> 16;
     }
+    if (by_key) {
+      sm = 0;
+      cm = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float v4[4] = {f[j].x, f[j].y, f[j].z, f[j].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t bin = f2key(v4[e]) >> 20;
+          sm |= (uint32_t)(bin > b1) << (4 * j + e);
+          cm |= (uint32_t)(bin == b1) << (4 * j + e);
+        }
+      }
+    }
+    const uint32_t valid = nv >= 32 ? 0xffffffffu : ((1u << nv) - 1u);
+    sm &= valid;
+    cm &= valid;
+    const uint32_t packed = (uint32_t)__popc(sm) | ((uint32_t)__popc(cm) << 16);
+    uint32_t inc = packed;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t o = __shfl_up_sync(0xffffffffu, inc, off);
+      if (lane >= off) inc += o;
+    }
+    const uint32_t excl = inc - packed, tot = __shfl_sync(0xffffffffu, inc, 31);
+    int32_t* sp = sure_w + (2 * L_w - 1 - (int64_t)(ns_w + (excl & 0xffffu)));
+    uint2* cp = cand_w + (nc_w + (excl >> 16));
+    while (sm) {
+      const int i = __ffs(sm) - 1;
+      sm &= sm - 1;
+      *sp-- = (int32_t)(t0 + i);
+    }
+    while (cm) {
+      const int i = __ffs(cm) - 1;
+      cm &= cm - 1;
+      *cp++ = make_uint2(f2key(__ldcg(sc + t0 + i)), (uint32_t)(t0 + i));
+    }
+    ns_w += tot & 0xffffu;
+    nc_w += tot >> 16;
   }
   if (lane == 0) {
     sh.ws[warp] = ns_w;
@@ -722,19 +753,18 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) select_kernel(DecodeParams p) 
     const uint32_t bl = lower_bound_i32(bbuf, nB, w_lo), bh = lower_bound_i32(bbuf, nB, w_hi);
     for (uint32_t bg = bl;; bg += 32) {
       const uint32_t b = bg + lane;
-      const int64_t tb = b < bh ? (int64_t)bbuf[b] : -1;
+      const int32_t tb = b < bh ? bbuf[b] : -1;
       uint32_t below = 0;
       for (uint32_t j0 = 0; j0 < ns_w; j0 += 32) {
         const uint32_t j = j0 + lane;
-        const int64_t t = j < ns_w ? (int64_t)sure_w[2 * L_w - 1 - (int64_t)j] : INT64_MAX;
-        if (bg == bl && j < ns_w) put(gS + j + lower_bound_i32(bbuf, nB, t), (int32_t)t);
-        const int nk = ns_w - j0 < 32u ? (int)(ns_w - j0) : 32;
-        for (int k = 0; k < nk; ++k) {
-          const int64_t tk = __shfl_sync(0xffffffffu, t, k);
-          below += tk < tb;
+        const int32_t t = j < ns_w ? sure_w[2 * L_w - 1 - (int64_t)j] : 0x7fffffff;
+        if (bg == bl && j < ns_w) put(gS + j + lower_bound_i32(bbuf, nB, t), t);
+        if (bh > bl) {
+          const int nk = ns_w - j0 < 32u ? (int)(ns_w - j0) : 32;
+          for (int k = 0; k < nk; ++k) below += __shfl_sync(0xffffffffu, t, k) < tb;
         }
       }
-      if (b < bh) put(b + gS + below, (int32_t)tb);
+      if (b < bh) put(b + gS + below, tb);
       if (bg + 32 >= bh) break;
     }
   } else {
@@ -806,27 +836,26 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) select_kernel(DecodeParams p) 
 constexpr int ATTN_THREADS = 128;
 constexpr int VLD = 136;            // halves per V tile row (272 B: ldmatrix without conflicts)
 constexpr int PLD = 136;            // halves per P row
-constexpr uint64_t NO_IDX = ~0ull;
 
-__device__ __forceinline__ void row_addr(const mkv_segment_header* hdr, int64_t t, int S, int c,
-                                         uint64_t* vals, uint64_t* idx, int* nnz) {
+constexpr int32_t NO_IDX = (int32_t)0x80000000;
+
+// Row of token t in one stream: pool offset of its stored values / 16, and
+// the byte distance / 8 from the values to the row's channel list (the
+// segment mask for SM, the row's own indices for PV; NO_IDX for dense rows).
+__device__ __forceinline__ uint2 row_meta(const mkv_segment_header* hdr, int64_t t, int S, int c) {
   const int64_t sg = t / S;
   const uint32_t r = (uint32_t)(t - sg * S);
   const mkv_segment_header hd = hdr[sg];
-  const uint64_t base = (uint64_t)hd.off16 * 16u;
+  const uint32_t c2 = 2u * (uint32_t)c;
   if (hd.strategy == MKV_STRATEGY_SM) {
-    *vals = base + pad16((uint32_t)c) + 2u * (uint32_t)c * r;
-    *idx = base;
-    *nnz = c;
-  } else if (hd.strategy == MKV_STRATEGY_PV) {
-    *vals = base + 2u * (uint32_t)c * r;
-    *idx = base + 2u * (uint32_t)c * hd.rows + (uint32_t)c * r;
-    *nnz = c;
-  } else {
-    *vals = base + 256u * r;
-    *idx = NO_IDX;
-    *nnz = D;
+    const uint32_t dv = pad16((uint32_t)c) + c2 * r;       // values after the mask
+    return make_uint2(hd.off16 + dv / 16u, (uint32_t)(-(int32_t)(dv / 8u)));
   }
+  if (hd.strategy == MKV_STRATEGY_PV) {
+    const uint32_t dv = c2 * r;
+    return make_uint2(hd.off16 + dv / 16u, (uint32_t)c * (2u * hd.rows - r) / 8u);
+  }
+  return make_uint2(hd.off16 + 16u * r, (uint32_t)NO_IDX);
 }
 
 // tokens of a chunk rounded up to the mma K step
@@ -834,8 +863,7 @@ __host__ __device__ constexpr int attn_rows16(int chunk) { return (chunk + 15) &
 
 size_t attn_smem_bytes(int g, int chunk) {
   const int gp = (g + 3) & ~3;
-  return (size_t)attn_rows16(chunk) * VLD * 2 + 2 * MAX_G * PLD * 2 +
-         (size_t)chunk * (4 * 8 + 2 * 4) +
+  return (size_t)attn_rows16(chunk) * VLD * 2 + 2 * MAX_G * PLD * 2 + (size_t)chunk * 16 +
          sizeof(float) * ((size_t)D * gp + (size_t)chunk * gp + 2 * g);
 }
 
@@ -846,38 +874,45 @@ __device__ __forceinline__ int chan_of(const uint2& x, int e) {
 // everything after the row addresses; GM = heads per instantiation (4 or 16)
 template <int GM>
 __device__ __forceinline__ void attn_body(const DecodeParams& p, int s, int chk, int n,
-                                          const uint64_t* kv_, const uint64_t* ki_,
-                                          const int* kn_, const uint64_t* vv_,
-                                          const uint64_t* vi_, const int* vn_, __half* Vd,
-                                          __half* Pt, const float* qs, float* lg, float* ml) {
+                                          const uint4* __restrict__ meta,
+                                          __half* __restrict__ Vd, __half* __restrict__ Pt,
+                                          const float* __restrict__ qs, float* __restrict__ lg,
+                                          float* __restrict__ ml) {
   const int g = p.g, gp = (g + 3) & ~3;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cl = tid & 7, tg = tid >> 3;
+  const int c = p.c;
   constexpr int U = 4;                          // tokens per thread per batch
   const float scale = 0.08838834764831845f;     // 1 / sqrt(128)
   // ---- logits and V tile: 8 lanes per token, 8 tokens per thread ---------
   for (int base = 0; base < ATTN_THREADS / 16; base += U) {
-    uint4 kvv[U], vvv[U];
+    uint4 mt[U], kvv[U], vvv[U];
     uint2 kix[U], vix[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int i = tg + 16 * (base + u);
+      mt[u] = i < n ? meta[i] : make_uint4(0u, (uint32_t)NO_IDX, 0u, (uint32_t)NO_IDX);
       kvv[u] = vvv[u] = make_uint4(0u, 0u, 0u, 0u);
       kix[u] = vix[u] = make_uint2(0u, 0u);
       if (i < n) {
-        if (8 * cl < kn_[i]) {
-          kvv[u] = ld_cg_u4(reinterpret_cast<const uint4*>(p.pool + kv_[i]) + cl);
-          if (ki_[i] != NO_IDX) kix[u] = ld_cg_u2(reinterpret_cast<const uint2*>(p.pool + ki_[i]) + cl);
+        const bool kd = (int32_t)mt[u].y == NO_IDX, vd = (int32_t)mt[u].w == NO_IDX;
+        const uint8_t* kp = p.pool + (uint64_t)mt[u].x * 16u;
+        const uint8_t* vp = p.pool + (uint64_t)mt[u].z * 16u;
+        if (8 * cl < (kd ? D : c)) {
+          kvv[u] = ld_cg_u4(kp + 16 * cl);
+          if (!kd) kix[u] = ld_cg_u2(kp + 8 * (int64_t)(int32_t)mt[u].y + 8 * cl);
         }
-        if (8 * cl < vn_[i]) {
-          vvv[u] = ld_cg_u4(reinterpret_cast<const uint4*>(p.pool + vv_[i]) + cl);
-          if (vi_[i] != NO_IDX) vix[u] = ld_cg_u2(reinterpret_cast<const uint2*>(p.pool + vi_[i]) + cl);
+        if (8 * cl < (vd ? D : c)) {
+          vvv[u] = ld_cg_u4(vp + 16 * cl);
+          if (!vd) vix[u] = ld_cg_u2(vp + 8 * (int64_t)(int32_t)mt[u].w + 8 * cl);
         }
       }
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int i = tg + 16 * (base + u);
+      const bool kd = (int32_t)mt[u].y == NO_IDX, vd = (int32_t)mt[u].w == NO_IDX;
+      const int kn = kd ? D : c, vn = vd ? D : c;
       float part[GM];
 #pragma unroll
       for (int hh = 0; hh < GM; ++hh) part[hh] = 0.f;
@@ -887,32 +922,32 @@ __device__ __forceinline__ void attn_body(const DecodeParams& p, int s, int chk,
           uint4 kr = kvv[u], vr = vvv[u];
           uint2 kx = kix[u], vx = vix[u];
           if (ck >= 8) {
-            if (8 * ck >= kn_[i] && 8 * ck >= vn_[i]) break;
+            if (8 * ck >= kn && 8 * ck >= vn) break;
+            const uint8_t* kp = p.pool + (uint64_t)mt[u].x * 16u;
+            const uint8_t* vp = p.pool + (uint64_t)mt[u].z * 16u;
             kr = vr = make_uint4(0u, 0u, 0u, 0u);
             kx = vx = make_uint2(0u, 0u);
-            if (8 * ck < kn_[i]) {
-              kr = ld_cg_u4(reinterpret_cast<const uint4*>(p.pool + kv_[i]) + ck);
-              if (ki_[i] != NO_IDX) kx = ld_cg_u2(reinterpret_cast<const uint2*>(p.pool + ki_[i]) + ck);
+            if (8 * ck < kn) {
+              kr = ld_cg_u4(kp + 16 * ck);
+              if (!kd) kx = ld_cg_u2(kp + 8 * (int64_t)(int32_t)mt[u].y + 8 * ck);
             }
-            if (8 * ck < vn_[i]) {
-              vr = ld_cg_u4(reinterpret_cast<const uint4*>(p.pool + vv_[i]) + ck);
-              if (vi_[i] != NO_IDX) vx = ld_cg_u2(reinterpret_cast<const uint2*>(p.pool + vi_[i]) + ck);
+            if (8 * ck < vn) {
+              vr = ld_cg_u4(vp + 16 * ck);
+              if (!vd) vx = ld_cg_u2(vp + 8 * (int64_t)(int32_t)mt[u].w + 8 * ck);
             }
           }
-          if (8 * ck < vn_[i]) {
+          if (8 * ck < vn) {
             const __half* hv = reinterpret_cast<const __half*>(&vr);
             __half* vrow = Vd + (size_t)i * VLD;
-            const bool dense = vi_[i] == NO_IDX;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) vrow[dense ? 8 * ck + e : chan_of(vx, e)] = hv[e];
+            for (int e = 0; e < 8; ++e) vrow[vd ? 8 * ck + e : chan_of(vx, e)] = hv[e];
           }
-          if (8 * ck < kn_[i]) {
+          if (8 * ck < kn) {
             float v[8];
             h8_to_f(kr, v);
-            const bool dense = ki_[i] == NO_IDX;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-              const float* qq = qs + (dense ? 8 * ck + e : chan_of(kx, e)) * gp;
+              const float* qq = qs + (kd ? 8 * ck + e : chan_of(kx, e)) * gp;
 #pragma unroll
               for (int h4 = 0; h4 < GM; h4 += 4) {
                 if (h4 < g) {
@@ -1020,13 +1055,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(DecodeParams p) {
   const int R16 = attn_rows16(CH);
   __half* Vd = reinterpret_cast<__half*>(asm_);                                // [R16][VLD]
   __half* Pt = Vd + (size_t)R16 * VLD;                                         // [2][16][PLD]
-  uint64_t* kv_ = reinterpret_cast<uint64_t*>(Pt + 2 * MAX_G * PLD);           // [CH]
-  uint64_t* ki_ = kv_ + CH;
-  uint64_t* vv_ = ki_ + CH;
-  uint64_t* vi_ = vv_ + CH;
-  int* kn_ = reinterpret_cast<int*>(vi_ + CH);
-  int* vn_ = kn_ + CH;
-  float* qs = reinterpret_cast<float*>(vn_ + CH);                              // [128][gp]
+  uint4* meta = reinterpret_cast<uint4*>(Pt + 2 * MAX_G * PLD);               // [CH]
+  float* qs = reinterpret_cast<float*>(meta + CH);                             // [128][gp]
   float* lg = qs + D * gp;                                                     // [CH][gp]
   float* ml = lg + CH * gp;                                                    // [g][2]
   const float* qt = p.qt + ((size_t)b * p.Hq + (size_t)h * g) * D;
@@ -1044,12 +1074,13 @@ __global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(DecodeParams p) {
   const int n = min(CH, p.kk - j0);
   if (tid < n) {
     const int64_t t = clamp_t(p.sel[(size_t)s * p.kk + j0 + tid], p.T);
-    row_addr(p.hdrK + (size_t)s * p.n_seg, t, p.S, p.c, &kv_[tid], &ki_[tid], &kn_[tid]);
-    row_addr(p.hdrV + (size_t)s * p.n_seg, t, p.S, p.c, &vv_[tid], &vi_[tid], &vn_[tid]);
+    const uint2 km = row_meta(p.hdrK + (size_t)s * p.n_seg, t, p.S, p.c);
+    const uint2 vm = row_meta(p.hdrV + (size_t)s * p.n_seg, t, p.S, p.c);
+    meta[tid] = make_uint4(km.x, km.y, vm.x, vm.y);
   }
   __syncthreads();
-  if (g <= 4) attn_body<4>(p, s, chk, n, kv_, ki_, kn_, vv_, vi_, vn_, Vd, Pt, qs, lg, ml);
-  else attn_body<MAX_G>(p, s, chk, n, kv_, ki_, kn_, vv_, vi_, vn_, Vd, Pt, qs, lg, ml);
+  if (g <= 4) attn_body<4>(p, s, chk, n, meta, Vd, Pt, qs, lg, ml);
+  else attn_body<MAX_G>(p, s, chk, n, meta, Vd, Pt, qs, lg, ml);
 }
 
 // ---------------------------------------------------------------------------
