@@ -387,7 +387,7 @@ def run_gpu(args, w: W.Workload, ws: int, rank: int, local: int):
     roof = {"kernel": "score_kernel", "bound": "hbm",
             "achieved": score_bytes / score_avg_s / 1e9, "peak": peak, "unit": "GB/s",
             "frac": score_bytes / score_avg_s / 1e9 / peak, "peak_kind": peak_kind,
-            "traffic": committed_traffic("k_decode.cu", "score_kernel_headline_128k.txt"),
+            "traffic": committed_traffic("k_score.cu", "score_kernel_headline_128k.txt"),
             "algorithmic_bytes_per_launch": score_bytes,
             "avg_launch_us": score_avg_s * 1e6}
 

@@ -142,6 +142,9 @@ constexpr int DEV_ERR_TIMEOUT = 1;
 
 // one-time per device: function attributes (not stream-ordered, so not in decode)
 cudaError_t prepare_decode_kernels();
+cudaError_t prepare_score_kernels();
+cudaError_t prepare_select_kernels();
+cudaError_t prepare_attn_kernels();
 // score-kernel shared-memory plan: stage size and number of stages
 void score_stage_plan(int S, int c, int* stage_bytes, int* n_stages);
 // partition of the K segments over G score CTAs and their stage plans (run

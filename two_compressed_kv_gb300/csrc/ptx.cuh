@@ -47,7 +47,7 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return r != 0u;
 }
 // Slow path of mbar_wait: polls with a device-time limit of about two seconds.
-__device__ __noinline__ bool mbar_wait_timed(uint64_t* bar, uint32_t parity) {
+static __device__ __noinline__ bool mbar_wait_timed(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_test(bar, parity)) {
     if (globaltimer_ns() - t0 > 2000000000ull) return false;
