@@ -48,7 +48,8 @@ def _dist():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if ws > 1:
         import torch.distributed as dist
-        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        backend = os.environ.get("MKV_DIST_BACKEND") or ("nccl" if torch.cuda.is_available()
+                                                          else "gloo")
         dist.init_process_group(backend=backend)
     return ws, rank, local
 
@@ -66,6 +67,15 @@ def _max_over_ranks(x: float, ws: int, device) -> float:
     t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def _job_value(ms_local: float, steps: int, units_per_rank_step: float, ws: int, device):
+    """Whole-job throughput: every rank runs the same per-rank work (weak
+    scaling); the step time is the slowest rank's.  Returns (ms per step,
+    units per second over all ranks)."""
+    ms = _max_over_ranks(ms_local, ws, device)
+    ms_step = ms / steps
+    return ms_step, ws * units_per_rank_step / (ms_step / 1e3)
 
 
 def measured_peaks():
@@ -233,7 +243,7 @@ def run_reference(args, w: W.Workload, ws: int, rank: int):
         "data": "synthetic", "config": cfg,
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"oracle decode (unpack + score + top-k + attention) of one "
-                                   f"131072-token stream of layer 0, {n} timed repetitions"},
+                                   f"{w.ctx}-token stream of layer 0, {n} timed repetitions"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -352,15 +362,12 @@ def run_gpu(args, w: W.Workload, ws: int, rank: int, local: int):
     for m in ctxs:
         if M.mkv_check_device(m.ctx) != M.MKV_OK:
             raise RuntimeError("a device-side wait gave up during the timed region")
-    ms = ev0.elapsed_time(ev1)
-    ms = _max_over_ranks(ms, ws, dev)
     if use_graph:   # kernels are counted when captured: one step's worth per graph
         launches = per_step_launches * args.steps
     else:
         launches = sum(m.stats()["kernel_launches"] for m in ctxs) - launches0
-    ms_step = ms / args.steps
     units_step = L * w.batch * w.ctx
-    value = ws * units_step / (ms_step / 1e3)
+    ms_step, value = _job_value(ev0.elapsed_time(ev1), args.steps, units_step, ws, dev)
 
     # per-kernel device time inside the timed region
     ktimes = {}
