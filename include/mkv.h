@@ -80,7 +80,9 @@ typedef struct {
   float tau;              /* retained-energy threshold, 0 < tau <= 1 */
   int32_t top_k;          /* tokens attended per KV head per step, >= 1 */
   int32_t attn_chunk;     /* selected tokens per split-K attention block; 0 = auto
-                             (128), else 8..128 and a multiple of 8.  With
+                             (64 when Hq / H <= 4, else 128; doubled while the
+                             merge below would overflow), else 8..128 and a
+                             multiple of 8.  With
                              g = Hq / H, ceil(min(top_k, max_ctx) / 128) * g must
                              not exceed 12288 (mkv_create: MKV_ERR_INVALID_ARG) */
   uint64_t max_pool_bytes;/* cap on the packed cache of one ctx; 0 = no cap */

@@ -74,7 +74,7 @@ __device__ __forceinline__ void attn_body(const DecodeParams& p, int s, int chk,
   constexpr int U = 4;                          // tokens per thread per batch
   const float scale = 0.08838834764831845f;     // 1 / sqrt(128)
   // ---- logits and V tile: 8 lanes per token, 8 tokens per thread ---------
-  for (int base = 0; base < ATTN_THREADS / 16; base += U) {
+  for (int base = 0; base < ATTN_THREADS / 16 && 16 * base < n; base += U) {
     uint4 mt[U], kvv[U], vvv[U];
     uint2 kix[U], vix[U];
 #pragma unroll
@@ -234,7 +234,10 @@ __device__ __forceinline__ void attn_body(const DecodeParams& p, int s, int chk,
   if (tid < 2 * g) p.part_ml[pbase * 2 + tid] = ml[tid];
 }
 
-__global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(DecodeParams p) {
+// GM: heads per instantiation (4 or 16); MINB: resident CTAs per SM asked of
+// the register allocator (6 for chunks of <= 64 tokens and g <= 4).
+template <int GM, int MINB>
+__global__ void __launch_bounds__(ATTN_THREADS, MINB) attn_kernel(DecodeParams p) {
   extern __shared__ __align__(16) uint8_t asm_[];
   const int s = blockIdx.y, chk = blockIdx.x;
   const int b = s / p.H, h = s % p.H;
@@ -268,8 +271,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 4) attn_kernel(DecodeParams p) {
     meta[tid] = make_uint4(km.x, km.y, vm.x, vm.y);
   }
   __syncthreads();
-  if (g <= 4) attn_body<4>(p, s, chk, n, meta, Vd, Pt, qs, lg, ml);
-  else attn_body<MAX_G>(p, s, chk, n, meta, Vd, Pt, qs, lg, ml);
+  attn_body<GM>(p, s, chk, n, meta, Vd, Pt, qs, lg, ml);
 }
 
 // ---------------------------------------------------------------------------
@@ -348,8 +350,12 @@ __global__ void __launch_bounds__(MG_THREADS) merge_kernel(DecodeParams p) {
 }
 
 cudaError_t prepare_attn_kernels() {
-  cudaError_t e = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)attn_smem_bytes(MAX_G, ATTN_MAX_CHUNK));
+  const int mx = (int)attn_smem_bytes(MAX_G, ATTN_MAX_CHUNK);
+  cudaError_t e = cudaFuncSetAttribute(attn_kernel<4, 6>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_kernel<4, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attn_kernel<MAX_G, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               48 * 1024 + 4 * 1024);
@@ -357,7 +363,10 @@ cudaError_t prepare_attn_kernels() {
 
 cudaError_t launch_attn(const DecodeParams& p, cudaStream_t st) {
   dim3 grid(p.attn_chunks, p.B * p.H);
-  attn_kernel<<<grid, ATTN_THREADS, attn_smem_bytes(p.g, p.attn_chunk), st>>>(p);
+  const size_t smem = attn_smem_bytes(p.g, p.attn_chunk);
+  if (p.g <= 4 && p.attn_chunk <= 64) attn_kernel<4, 6><<<grid, ATTN_THREADS, smem, st>>>(p);
+  else if (p.g <= 4) attn_kernel<4, 4><<<grid, ATTN_THREADS, smem, st>>>(p);
+  else attn_kernel<MAX_G, 4><<<grid, ATTN_THREADS, smem, st>>>(p);
   return cudaGetLastError();
 }
 

@@ -306,25 +306,31 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
         }
         const int s = s_cur;
         const int sl = s - s_first;
-        const float* qsrc = sl < SC_NSLOT ? qb[sl] : p.qbar + (size_t)s * D;
-        uint32_t* hs = sl < SC_NSLOT ? hist[sl] : p.hist + (size_t)s * HIST1;
         float* out = p.scores + (size_t)s * p.Tp + (int64_t)(sg - s * p.n_seg) * p.S;
-        if (strat == MKV_STRATEGY_SM) {
-          if (last_sm != sg) {
-            __syncwarp();
-            for (int jj = lane; jj < p.c; jj += 32) qm[warp][jj] = qsrc[base[jj] & 127];
-            __syncwarp();
-            last_sm = sg;
-          }
-          score_block<MKV_STRATEGY_SM, CPR>(base, rows, blk * 32, lane, qsrc, qm[warp], out, hs,
-                                            pol);
-        } else if (strat == MKV_STRATEGY_PV) {
-          score_block<MKV_STRATEGY_PV, CPR>(base, rows, blk * 32, lane, qsrc, qm[warp], out, hs,
-                                            pol);
-        } else {
-          score_block<MKV_STRATEGY_DENSE, 16>(base, rows, blk * 32, lane, qsrc, qm[warp], out, hs,
+        // the common case reads q_bar and counts into this CTA's shared copies;
+        // keeping the two cases apart lets both compile to shared-memory
+        // loads and atomics instead of generic ones
+        auto item = [&](const float* qsrc, uint32_t* hs) {
+          if (strat == MKV_STRATEGY_SM) {
+            if (last_sm != sg) {
+              __syncwarp();
+              for (int jj = lane; jj < p.c; jj += 32) qm[warp][jj] = qsrc[base[jj] & 127];
+              __syncwarp();
+              last_sm = sg;
+            }
+            score_block<MKV_STRATEGY_SM, CPR>(base, rows, blk * 32, lane, qsrc, qm[warp], out, hs,
                                               pol);
-        }
+          } else if (strat == MKV_STRATEGY_PV) {
+            score_block<MKV_STRATEGY_PV, CPR>(base, rows, blk * 32, lane, qsrc, qm[warp], out, hs,
+                                              pol);
+          } else {
+            score_block<MKV_STRATEGY_DENSE, 16>(base, rows, blk * 32, lane, qsrc, qm[warp], out,
+                                                hs, pol);
+          }
+        };
+        if (sl == 0) item(qb[0], hist[0]);
+        else if (sl == 1) item(qb[1], hist[1]);
+        else item(p.qbar + (size_t)s * D, p.hist + (size_t)s * HIST1);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[slot]);

@@ -307,7 +307,7 @@ mkv_status mkv_create(const mkv_config* cfg, mkv_ctx** out) {
   c->max_seg = ceil_div(cfg->max_ctx, cfg->segment);
   c->kk_max = (int)std::min<int64_t>(cfg->top_k, cfg->max_ctx);
   c->gram_chunks_max = gram_chunks_for(c->BH, cfg->max_ctx);
-  c->attn_chunk = cfg->attn_chunk ? cfg->attn_chunk : 128;
+  c->attn_chunk = cfg->attn_chunk ? cfg->attn_chunk : (c->g <= 4 ? 64 : 128);
   // the merge kernel keeps one weight per (chunk, head) in shared memory
   while (ceil_div(c->kk_max, c->attn_chunk) * c->g > kMergeMaxWeights &&
          c->attn_chunk < ATTN_MAX_CHUNK)
