@@ -164,32 +164,38 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # CPU oracle leg (cpu_baseline and --impl reference)
 # ---------------------------------------------------------------------------
-def oracle_decode_sample(w: W.Workload, seconds: float, K=None, V=None, q=None):
-    """Times the oracle's decode (unpack the packed stream + scores + top-k +
-    attention) on stream (b=0, h=0) of layer 0, repeated for about `seconds`.
-    Compression of the sample runs first and is not timed."""
+def oracle_prepare(w: W.Workload, K=None, V=None, q=None):
+    """Compresses stream (b=0, h=0) of layer 0 with the oracle (not timed) and
+    returns what the timed oracle decode needs."""
     from oracle import mosaickv as O
     if K is None:
         K, V = W.draw_kv(w, layer=0, device="cpu", streams=1)
         q = W.draw_queries(w, K)
     Kn = K[0, 0].cpu().numpy()
     Vn = V[0, 0].cpu().numpy()
-    g = w.group
-    qn = q[0, :g].cpu().numpy()
+    qn = q[0, :w.group].cpu().numpy()
     ck = O.compress_stream(Kn, w.segment, w.c, w.tau)
     cv = O.compress_stream(Vn, w.segment, w.c, w.tau)
     hk, pk = O.pack_stream(ck)
     hv, pv = O.pack_stream(cv)
-    T = Kn.shape[0]
+    return {"T": Kn.shape[0], "q": qn, "ck": ck, "cv": cv, "hk": hk, "pk": pk, "hv": hv, "pv": pv}
+
+
+def oracle_decode_sample(w: W.Workload, seconds: float, prep):
+    """Times the oracle's decode (unpack the packed stream + scores + top-k +
+    attention) of the prepared stream, repeated for about `seconds` (at least
+    once).  Returns (ctx-tokens/s, repetitions, median seconds per decode)."""
+    from oracle import mosaickv as O
+    T = prep["T"]
     times = []
     t_end = time.perf_counter() + seconds
     while True:
         t0 = time.perf_counter()
-        Kh = O.unpack_stream(hk, pk, T, w.segment, w.c)
-        Vh = O.unpack_stream(hv, pv, T, w.segment, w.c)
-        O.decode_stream(qn, ck.R, cv.R, Kh, Vh, w.top_k)
+        Kh = O.unpack_stream(prep["hk"], prep["pk"], T, w.segment, w.c)
+        Vh = O.unpack_stream(prep["hv"], prep["pv"], T, w.segment, w.c)
+        O.decode_stream(prep["q"], prep["ck"].R, prep["cv"].R, Kh, Vh, w.top_k)
         times.append(time.perf_counter() - t0)
-        if time.perf_counter() > t_end and len(times) >= 1:
+        if time.perf_counter() > t_end:
             break
     per = statistics.median(times)
     return T / per, len(times), per
@@ -226,11 +232,14 @@ def run_reference(args, w: W.Workload, ws: int, rank: int):
         return
     cfg = workload_config(w, 1)
     cfg["sample"] = "stream (b=0, h=0) of layer 0"
-    per_step = max(0.5, args.ref_seconds)
+    # each step is a bounded sample of the oracle's decode; the whole run stays
+    # within about 90 s of oracle time whatever --steps is
+    per_step = max(0.25, min(args.ref_seconds, 90.0 / (args.warmup + args.steps)))
     vals = []
     n = 0
+    prep = oracle_prepare(w)
     for i in range(args.warmup + args.steps):
-        v, reps, per = oracle_decode_sample(w, per_step)
+        v, reps, per = oracle_decode_sample(w, per_step, prep)
         if i >= args.warmup:
             vals.append(v)
             n += reps
@@ -425,7 +434,7 @@ def run_gpu(args, w: W.Workload, ws: int, rank: int, local: int):
 
     cpu = None
     if cpu_args is not None:
-        cv, reps, per = oracle_decode_sample(w, args.cpu_seconds, *cpu_args)
+        cv, reps, per = oracle_decode_sample(w, args.cpu_seconds, oracle_prepare(w, *cpu_args))
         cpu = {"value": cv, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
                "sample": f"oracle decode (unpack + score + top-k + attention) of one "
                          f"{w.ctx}-token stream (b=0, h=0) of layer 0, {reps} repetitions, "

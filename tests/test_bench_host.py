@@ -52,3 +52,12 @@ def test_job_value_single_rank():
     ms_step, value = bench._job_value(80.0, 10, 4.0e6, 1, "cpu")
     assert ms_step == pytest.approx(8.0)
     assert value == pytest.approx(4.0e6 / 8e-3)
+
+
+def test_oracle_sample_prepares_once_and_times_decodes():
+    from two_compressed_kv_gb300 import workloads as W
+    w = W.small_workload("bench-sample", ctx=256, top_k=16)
+    prep = bench.oracle_prepare(w)
+    assert prep["T"] == 256 and prep["q"].shape == (w.group, 128)
+    value, reps, per = bench.oracle_decode_sample(w, 0.05, prep)
+    assert reps >= 1 and per > 0 and value == pytest.approx(256 / per)
