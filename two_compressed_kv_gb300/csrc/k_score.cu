@@ -17,7 +17,7 @@ namespace mkv {
 // ---------------------------------------------------------------------------
 // qrot: q~_i = q_i R_K for the g query heads of a KV head, q_bar = sum_i q~_i.
 // R_K is staged in shared memory with 16-byte loads.  Also clears the stream's
-// histogram, tickets and candidate counter for this step.
+// histogram and ticket for this step.
 // grid: BH, block: 512 (column j = tid % 128, heads tid / 128 + 4n), dynamic
 // smem 64 KB
 // ---------------------------------------------------------------------------
