@@ -215,6 +215,28 @@ def blas_threads() -> int:
     return os.cpu_count() or 1
 
 
+def host_cpu() -> dict:
+    """Host CPU description for the CPU-baseline record: logical CPU count and
+    model name (the "model name" line on x86, "CPU implementer/part" codes on
+    Arm, else the platform string)."""
+    import platform
+    model = ""
+    try:
+        fields = {}
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields.setdefault(k.strip(), v.strip())
+        model = fields.get("model name") or fields.get("Model name") or ""
+        if not model and "CPU implementer" in fields:
+            model = f"implementer {fields['CPU implementer']} part {fields.get('CPU part', '?')}"
+    except OSError:
+        pass
+    return {"cpu_count": os.cpu_count() or 1,
+            "cpu_model": model or platform.processor() or platform.machine()}
+
+
 def workload_config(w: W.Workload, layers: int) -> dict:
     return {
         "workload": f"{w.name}: batch {w.batch}, {w.n_kv_heads} KV / {w.n_q_heads} query heads, "
@@ -251,6 +273,7 @@ def run_reference(args, w: W.Workload, ws: int, rank: int):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": cfg,
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         **host_cpu(),
                          "sample": f"oracle decode (unpack + score + top-k + attention) of one "
                                    f"{w.ctx}-token stream of layer 0, {n} timed repetitions"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -435,7 +458,7 @@ def run_gpu(args, w: W.Workload, ws: int, rank: int, local: int):
     cpu = None
     if cpu_args is not None:
         cv, reps, per = oracle_decode_sample(w, args.cpu_seconds, oracle_prepare(w, *cpu_args))
-        cpu = {"value": cv, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+        cpu = {"value": cv, "unit": UNIT, "cores": blas_threads(), "kind": "oracle", **host_cpu(),
                "sample": f"oracle decode (unpack + score + top-k + attention) of one "
                          f"{w.ctx}-token stream (b=0, h=0) of layer 0, {reps} repetitions, "
                          f"median {per * 1e3:.0f} ms"}

@@ -61,3 +61,8 @@ def test_oracle_sample_prepares_once_and_times_decodes():
     assert prep["T"] == 256 and prep["q"].shape == (w.group, 128)
     value, reps, per = bench.oracle_decode_sample(w, 0.05, prep)
     assert reps >= 1 and per > 0 and value == pytest.approx(256 / per)
+
+
+def test_host_cpu_description():
+    info = bench.host_cpu()
+    assert info["cpu_count"] >= 1 and isinstance(info["cpu_model"], str)
