@@ -249,6 +249,27 @@ def workload_config(w: W.Workload, layers: int) -> dict:
     }
 
 
+def one_thread_oracle(workload: str, seconds: float) -> dict:
+    """The same oracle decode sample in a child process whose BLAS and OpenMP
+    pools have one thread (the pool size is fixed when numpy loads)."""
+    import subprocess
+    code = ("import json, sys; sys.path.insert(0, %r); import bench; "
+            "from two_compressed_kv_gb300 import workloads as W; "
+            "w = W.WORKLOADS[%r]; v, reps, per = bench.oracle_decode_sample(w, %r, "
+            "bench.oracle_prepare(w)); print(json.dumps({'value': v, 'reps': reps}))"
+            % (ROOT, workload, float(seconds)))
+    env = dict(os.environ)
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[var] = "1"
+    try:
+        r = subprocess.run([sys.executable, "-c", code], env=env, cwd=ROOT, timeout=900,
+                           stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True)
+        d = json.loads(r.stdout.strip().splitlines()[-1])
+        return {"value": d["value"], "unit": UNIT, "cores": 1, "repetitions": d["reps"]}
+    except Exception as e:   # the all-core figure stands on its own
+        return {"unavailable": f"{type(e).__name__}: {e}"[:200]}
+
+
 def run_reference(args, w: W.Workload, ws: int, rank: int):
     if rank != 0:
         return
@@ -278,6 +299,8 @@ def run_reference(args, w: W.Workload, ws: int, rank: int):
                                    f"{w.ctx}-token stream of layer 0, {n} timed repetitions"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+    if not args.no_one_thread:
+        line["cpu_baseline"]["one_thread"] = one_thread_oracle(args.workload, 5.0)
     print(json.dumps(line), flush=True)
 
 
@@ -512,6 +535,8 @@ def main(argv=None):
     ap.add_argument("--ref-seconds", type=float, default=2.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-one-thread", action="store_true",
+                    help="reference arm: skip the extra one-thread oracle timing")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (profiling runs)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
