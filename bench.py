@@ -184,7 +184,9 @@ def oracle_prepare(w: W.Workload, K=None, V=None, q=None):
 def oracle_decode_sample(w: W.Workload, seconds: float, prep):
     """Times the oracle's decode (unpack the packed stream + scores + top-k +
     attention) of the prepared stream, repeated for about `seconds` (at least
-    once).  Returns (ctx-tokens/s, repetitions, median seconds per decode)."""
+    once).  Returns (ctx-tokens/s, repetitions, median seconds per decode).
+    A context token has one stream per KV head, so the rate is T over the time
+    of n_kv_heads such decodes (one stream timed, scaled)."""
     from oracle import mosaickv as O
     T = prep["T"]
     times = []
@@ -198,7 +200,7 @@ def oracle_decode_sample(w: W.Workload, seconds: float, prep):
         if time.perf_counter() > t_end:
             break
     per = statistics.median(times)
-    return T / per, len(times), per
+    return T / (per * w.n_kv_heads), len(times), per
 
 
 def blas_threads() -> int:
@@ -296,7 +298,8 @@ def run_reference(args, w: W.Workload, ws: int, rank: int):
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          **host_cpu(),
                          "sample": f"oracle decode (unpack + score + top-k + attention) of one "
-                                   f"{w.ctx}-token stream of layer 0, {n} timed repetitions"},
+                                   f"{w.ctx}-token stream of layer 0, {n} timed repetitions, "
+                                   f"scaled to the {w.n_kv_heads} KV heads of a token"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     if not args.no_one_thread:
@@ -484,7 +487,8 @@ def run_gpu(args, w: W.Workload, ws: int, rank: int, local: int):
         cpu = {"value": cv, "unit": UNIT, "cores": blas_threads(), "kind": "oracle", **host_cpu(),
                "sample": f"oracle decode (unpack + score + top-k + attention) of one "
                          f"{w.ctx}-token stream (b=0, h=0) of layer 0, {reps} repetitions, "
-                         f"median {per * 1e3:.0f} ms"}
+                         f"median {per * 1e3:.0f} ms, scaled to the {w.n_kv_heads} KV heads "
+                         f"of a token"}
 
     if rank == 0:
         cfgd = workload_config(w, L)

@@ -60,7 +60,7 @@ def test_oracle_sample_prepares_once_and_times_decodes():
     prep = bench.oracle_prepare(w)
     assert prep["T"] == 256 and prep["q"].shape == (w.group, 128)
     value, reps, per = bench.oracle_decode_sample(w, 0.05, prep)
-    assert reps >= 1 and per > 0 and value == pytest.approx(256 / per)
+    assert reps >= 1 and per > 0 and value == pytest.approx(256 / (per * w.n_kv_heads))
 
 
 def test_host_cpu_description():
