@@ -292,6 +292,40 @@ def test_gqa_head_mapping():
     assert np.allclose(scores[0, 1], ck.dense_hat() @ qt.sum(0), rtol=1e-12, atol=1e-9)
 
 
+def check_zero_energy():
+    """A stream with no energy (all zeros): every retained fraction is 1 by the
+    rule for an empty segment, every per-token and shared channel choice is a
+    tie resolved to the lowest channels, SM and PV cost the same here and the
+    tie goes to SM; all scores are 0, so the first k tokens are selected and
+    the softmax is uniform (all logits 0), giving a zero output."""
+    d, T, S, c, k = 16, 10, 4, 4, 3
+    X = np.zeros((T, d), dtype=np.float16)
+    I = np.eye(d)
+    cs = O.compress_stream(X, S, c, 0.9, R=I)
+    assert np.array_equal(cs.P, np.tile(np.arange(c), (T, 1)))
+    for seg in cs.segs:
+        assert seg.e_tot == 0.0 and seg.f_pv == 1.0 and seg.f_sm == 1.0
+        assert list(seg.mask) == list(range(c))
+        assert O.segment_cost(O.SM, seg.rows, c, d) == O.segment_cost(O.PV, seg.rows, c, d)
+        assert seg.strategy == O.SM
+    hdr, payload = O.pack_stream(cs)
+    want = b""
+    for rows in (4, 4, 2):
+        want += bytes(range(c)) + bytes(16 - c) + bytes(2 * c * rows)
+    assert payload == want
+    assert [int(h["off16"]) for h in hdr] == [0, 3, 6]
+    q = np.ones((2, d), dtype=np.float16)
+    khat = O.unpack_stream(hdr, payload, T, S, c, d)
+    r = O.decode_stream(q, I, I, khat, khat, k)
+    assert list(r.sel) == [0, 1, 2]
+    assert np.all(r.scores == 0.0) and np.all(r.logits == 0.0)
+    assert np.all(r.out == 0.0)
+
+
+def test_zero_energy_stream_closed_form():
+    check_zero_energy()
+
+
 def test_kv_size_arithmetic_from_paper():
     """§1 and §2.1 of the paper: eight Llama-3.1-8B requests at 128K tokens need
     128 GB of KV cache, and 1 TB at 1M tokens (fp16, 32 layers, 8 KV heads)."""
@@ -368,8 +402,20 @@ def _mut_stats_drop_pad(mp):
     mp.setattr(O, "segment_cost", f)
 
 
+def _mut_empty_segment_unkept(mp):
+    orig = O.segment_stats
+
+    def f(Xt_seg, P_seg, c):
+        st = orig(Xt_seg, P_seg, c)
+        if st.e_tot == 0.0:
+            st.f_pv = st.f_sm = 0.0
+        return st
+    mp.setattr(O, "segment_stats", f)
+
+
 MUTATIONS = [_mut_rotate_transposed, _mut_ties_high, _mut_most_retained, _mut_topk_ties_high,
-             _mut_no_scale, _mut_sign_flipped, _mut_ascending, _mut_stats_drop_pad]
+             _mut_no_scale, _mut_sign_flipped, _mut_ascending, _mut_stats_drop_pad,
+             _mut_empty_segment_unkept]
 
 
 @pytest.mark.parametrize("mutation", MUTATIONS, ids=[m.__name__ for m in MUTATIONS])
@@ -378,7 +424,7 @@ def test_pins_catch_planted_mistake(mutation, monkeypatch):
     rng = np.random.default_rng(5)
     Xr = (rng.standard_normal((300, 16)) * np.exp(-np.arange(16) / 4)).astype(np.float16)
     checks = [check_hand_case, check_basis_closed_forms, check_costs_and_choice,
-              lambda: check_basis_invariants(Xr)]
+              lambda: check_basis_invariants(Xr), check_zero_energy]
     caught = 0
     for chk in checks:
         try:
