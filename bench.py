@@ -239,7 +239,12 @@ def host_cpu() -> dict:
             "cpu_model": model or platform.processor() or platform.machine()}
 
 
-def workload_config(w: W.Workload, layers: int) -> dict:
+def workload_config(w: W.Workload, layers: int, k_bytes: float = None) -> dict:
+    if k_bytes is None:
+        l2 = "inputs larger than L2 (129 MB), layers cycled"
+    else:
+        l2 = (f"inputs larger than L2 (129 MB): each layer streams {k_bytes / 1e6:.0f} MB of "
+              f"packed keys, {layers} layers cycled")
     return {
         "workload": f"{w.name}: batch {w.batch}, {w.n_kv_heads} KV / {w.n_q_heads} query heads, "
                     f"head dim 128, context {w.ctx}, {layers} layers, segment {w.segment}, "
@@ -247,7 +252,7 @@ def workload_config(w: W.Workload, layers: int) -> dict:
         "batch": w.batch, "ctx": w.ctx, "layers": layers, "n_kv_heads": w.n_kv_heads,
         "n_q_heads": w.n_q_heads, "head_dim": 128, "segment": w.segment, "c": w.c,
         "tau": w.tau, "top_k": w.top_k, "storage": "fp16 values, uint8 channel indices",
-        "l2": "inputs larger than L2: each layer streams ~674 MB of packed keys, layers cycled",
+        "l2": l2,
     }
 
 
@@ -490,8 +495,18 @@ def run_gpu(args, w: W.Workload, ws: int, rank: int, local: int):
                          f"median {per * 1e3:.0f} ms, scaled to the {w.n_kv_heads} KV heads "
                          f"of a token"}
 
+    side = {}
+    if rank == 0 and not args.no_side:
+        for c in ctxs:
+            c.close()
+        ctxs = []
+        torch.cuda.empty_cache()
+        for name, layers in ((W.MILLION_1M.name, 1), (W.MIXED_256K.name, 1)):
+            side[name] = side_workload(W.WORKLOADS[name], layers, max(5, args.steps), dev, stream)
+            torch.cuda.empty_cache()
+
     if rank == 0:
-        cfgd = workload_config(w, L)
+        cfgd = workload_config(w, L, score_bytes)
         cfgd["parallelism"] = f"replicas x{ws}" if ws > 1 else "single GPU"
         tok = L * w.batch * w.ctx
         line = {
@@ -522,9 +537,117 @@ def run_gpu(args, w: W.Workload, ws: int, rank: int, local: int):
                             "strategies_V": st0["strategy_count"][1]},
             "ctx_tokens_per_step": tok,
         }
+        line["prefill"].update(prefill_roofline(w, statistics.median(comp_ms), st0, peak))
+        if side:
+            line["other_workloads"] = side
         print(json.dumps(line), flush=True)
     for m in ctxs:
         m.close()
+
+
+def prefill_roofline(w: W.Workload, ms: float, st: dict, peak_gbs: float) -> dict:
+    """mkv_compress against its bounds.  Algorithmic bytes: K and V read twice
+    (the Gram pass, then the rotation pass, which needs the finished basis)
+    plus the packed cache written.  Tensor work: the Gram (2 T d^2 per stream)
+    and the rotation (2 T d^2 per stream and pass, two fp16 parts of R, two
+    passes), all fp16 with fp32 accumulation; peak = the measured bf16 GEMM
+    rate (the fp16 dense rate is the same)."""
+    streams = 2 * w.batch * w.n_kv_heads
+    x_bytes = streams * w.ctx * 128 * 2
+    alg = 2 * x_bytes + st["payload_bytes"][0] + st["payload_bytes"][1] + st["header_bytes"]
+    flops = streams * w.ctx * 128 * 128 * 2 * (1 + 2 * 2)
+    tf_peak = None
+    pth = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pth):
+        with open(pth) as f:
+            tf_peak = float(json.load(f).get("bf16_tflops", 0.0)) or None
+    gbs = alg / (ms / 1e3) / 1e9
+    tfs = flops / (ms / 1e3) / 1e12
+    return {"algorithmic_bytes_per_layer": alg, "hbm_gbs": gbs, "hbm_frac_of_measured": gbs / peak_gbs,
+            "tensor_flops_per_layer": flops, "tensor_tflops": tfs,
+            "tensor_frac_of_measured_bf16": (tfs / tf_peak) if tf_peak else None}
+
+
+def side_workload(w: W.Workload, layers: int, steps: int, dev, stream) -> dict:
+    """One more workload, timed like the headline (CUDA-graph replays of a
+    decode of every layer, 3 warm-up steps, CUDA events on the launching
+    stream) plus its mkv_compress time per layer."""
+    from two_compressed_kv_gb300 import mkv as M
+    cfg = M.make_config(w.batch, w.n_kv_heads, w.n_q_heads, w.ctx, w.segment, w.c, w.tau,
+                        w.top_k, flags=M.MKV_FLAG_SCORE_TIMING, device=dev.index or 0)
+    ctxs, qs, outs, comp = [], [], [], []
+    for layer in range(layers):
+        K, V = W.draw_kv(w, layer=layer, device=dev)
+        q = W.draw_queries(w, K, layer=layer)
+        m = M.Mkv(cfg)
+        m.compress(K, V)          # first compression of a shape: not timed
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        m.compress(K, V)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        comp.append(e0.elapsed_time(e1))
+        ctxs.append(m)
+        qs.append(q)
+        outs.append(torch.empty(q.shape, dtype=torch.float32, device=dev))
+        del K, V
+    st0 = ctxs[0].stats()
+
+    def step():
+        for m, q, o in zip(ctxs, qs, outs):
+            M.mkv_decode(m.ctx, q, o, None, None)
+
+    step()
+    torch.cuda.synchronize(dev)
+    graphs = []
+    for _ in range(steps + 3):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        graphs.append(g)
+    for g in graphs[:3]:
+        g.replay()
+    torch.cuda.synchronize(dev)
+    for m in ctxs:
+        M.mkv_kernel_time(m.ctx, M.MKV_KERNEL_SCORE, reset=True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for g in graphs[3:]:
+        g.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms_step = ev0.elapsed_time(ev1) / steps
+    s_ms, s_n = 0.0, 0
+    for m in ctxs:
+        a, b = M.mkv_kernel_time(m.ctx, M.MKV_KERNEL_SCORE)
+        s_ms, s_n = s_ms + a, s_n + b
+        if M.mkv_check_device(m.ctx) != M.MKV_OK:
+            raise RuntimeError("a device-side check fired during the timed region")
+    kk = min(w.top_k, w.ctx)
+    sel0 = torch.empty(w.batch, w.n_kv_heads, kk, dtype=torch.int32, device=dev)
+    M.mkv_decode(ctxs[0].ctx, qs[0], outs[0], sel0, stream)
+    torch.cuda.synchronize(dev)
+    score_bytes = float(st0["payload_bytes"][0] + st0["header_bytes"] // 2)
+    small = (w.batch * w.n_q_heads * 128 * (2 + 4) + 2 * w.streams * 128 * 128 * 4)
+    alg = score_bytes + gathered_bytes(ctxs[0], M, sel0.cpu().numpy(), w) + small
+    peak, kind = measured_peaks()
+    score_us = s_ms / max(1, s_n) * 1e3
+    res = {"config": workload_config(w, layers, score_bytes), "ms_per_step": ms_step,
+           "value": layers * w.batch * w.ctx / (ms_step / 1e3), "unit": UNIT,
+           "algorithmic_bytes_per_layer_step": alg,
+           "hbm_gbs": alg * layers / (ms_step / 1e3) / 1e9,
+           "hbm_frac_of_measured": alg * layers / (ms_step / 1e3) / 1e9 / peak,
+           "score_kernel_us": score_us,
+           "score_kernel_frac_of_measured": score_bytes / (score_us / 1e6) / 1e9 / peak,
+           "prefill": {"value": w.batch * w.ctx / (statistics.median(comp) / 1e3),
+                       "unit": "prefill-tokens/s per layer (K and V)",
+                       "ms_per_layer_median": statistics.median(comp)},
+           "strategies_K": st0["strategy_count"][0], "strategies_V": st0["strategy_count"][1]}
+    res["prefill"].update(prefill_roofline(w, statistics.median(comp), st0, peak))
+    for m in ctxs:
+        m.close()
+    return res
 
 
 def main(argv=None):
@@ -542,6 +665,8 @@ def main(argv=None):
     ap.add_argument("--no-one-thread", action="store_true",
                     help="reference arm: skip the extra one-thread oracle timing")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (profiling runs)")
+    ap.add_argument("--no-side", action="store_true",
+                    help="skip the 1M-context and mixed-256K lines added to the headline line")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

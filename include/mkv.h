@@ -50,7 +50,7 @@ typedef enum {
   MKV_ERR_STATE = 2,        /* e.g. mkv_decode before any mkv_compress */
   MKV_ERR_OOM = 3,          /* device allocation failed or max_pool_bytes exceeded */
   MKV_ERR_CUDA = 4,         /* a CUDA runtime call failed */
-  MKV_ERR_DEVICE_CHECK = 5, /* a kernel's own bounds check fired */
+  MKV_ERR_DEVICE_CHECK = 5, /* a kernel's bounds check fired (see mkv_check_device) */
   MKV_ERR_TIMEOUT = 6       /* a bounded device-side wait gave up */
 } mkv_status;
 
@@ -196,13 +196,40 @@ mkv_status mkv_export(const mkv_ctx* ctx, int b, int h, int which, float* basis,
                       float* eigvals, mkv_segment_header* headers, void* payload,
                       uint64_t* payload_bytes);
 
-/* Waits for all work on the ctx's device, then reports whether a kernel of
- * this ctx gave up a bounded device-side wait since the last check
- * (MKV_ERR_TIMEOUT; the word is then cleared) or MKV_OK.  Kernels never spin
- * without a bound: a wait that exceeds about two seconds sets the word,
- * abandons the rest of its work (the outputs of that call are undefined) and
- * returns. */
+/* Waits for all work on the ctx's device, then reports the ctx's device
+ * status word since the last check (the word is then cleared):
+ *   MKV_ERR_DEVICE_CHECK  a kernel found a packed-cache access that would end
+ *                         past the checked pool extent (the live cache's
+ *                         pool, or the smaller extent set with
+ *                         mkv_debug_set_check_extent); it skipped that access
+ *                         (decode reads a stand-in row, the score pass stops,
+ *                         packing skips the row), so that call's outputs are
+ *                         undefined;
+ *   MKV_ERR_TIMEOUT       a kernel gave up a bounded device-side wait (about
+ *                         two seconds of device time), abandoned the rest of
+ *                         its work (outputs undefined) and returned;
+ *   MKV_OK                neither.
+ * Kernels never spin without a bound and never trap: the ctx stays usable. */
 mkv_status mkv_check_device(mkv_ctx* ctx);
+
+/* Test hooks for the failure detection above (interface additions with no
+ * counterpart in the paper).  Neither can fault or hang the GPU.
+ *
+ * mkv_debug_wait_test: launches, on `stream`, one CTA that runs the library's
+ * bounded mbarrier wait on a barrier no thread ever arrives on, with a limit
+ * of limit_ns of device time (1000 <= limit_ns <= 2e9, else
+ * MKV_ERR_INVALID_ARG).  When the limit runs out the kernel records a timeout
+ * in the ctx's status word and returns; mkv_check_device then returns
+ * MKV_ERR_TIMEOUT.  No other ctx state is touched.
+ *
+ * mkv_debug_set_check_extent: makes the kernels of later mkv_compress and
+ * mkv_decode calls check packed-cache accesses against `bytes` instead of the
+ * live pool's size when `bytes` is smaller (0 restores the pool's size).
+ * Accesses are never allowed past the real pool: with a small `bytes`,
+ * in-bounds accesses are reported as MKV_ERR_DEVICE_CHECK, which is how the
+ * checks are tested without any out-of-bounds access. */
+mkv_status mkv_debug_wait_test(mkv_ctx* ctx, uint64_t limit_ns, mkv_stream_t stream);
+mkv_status mkv_debug_set_check_extent(mkv_ctx* ctx, uint64_t bytes);
 
 /* With MKV_FLAG_KERNEL_TIMING: total device time (ms) and launch count of one
  * decode kernel id since creation or the last reset (synchronous).  reset != 0
@@ -243,12 +270,13 @@ mkv_status mkv_kernel_time(mkv_ctx* ctx, int kernel_id, double* total_ms,
  * fit the buffer); larger requests return MKV_ERR_INVALID_ARG before any CUDA
  * call, with the reason in mkv_last_error_string.  So do NULL pointers,
  * unaligned k or v, batch, n_kv_heads or ctx_len < 1.
- * Device: the calling thread's current CUDA device.  The first call on each
- * device looks the buffer's address up (cudaGetSymbolAddress), which may load
- * the library's device code on that device and reserve the buffer there; make
- * that first call before any stream capture begins.  Later calls on the same
- * device only launch two kernels on `stream` (asynchronous, no host
- * synchronisation).
+ * Device: the calling thread's current CUDA device; k, v, basis, eigvals and
+ * `stream` must all belong to it.  Every call looks the buffer's address up in
+ * the current context (cudaGetSymbolAddress), so a device reset or a new
+ * primary context is picked up.  The first call on each device may load the
+ * library's device code there and reserve the buffer; make that first call
+ * before any stream capture begins.  Each call then launches two kernels on
+ * `stream` (asynchronous, no host synchronisation).
  * Nothing in the buffer needs to start at zero: every partial Gram matrix is
  * written in full before it is read.
  * The buffer is shared by every call on a device: calls that may overlap in

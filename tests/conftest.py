@@ -16,3 +16,13 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def repo_root():
     return ROOT
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Near-tie counts and errors of every GPU parity check of the session."""
+    mod = sys.modules.get("parity_util")
+    if mod is None or not getattr(mod, "REPORTS", None):
+        return
+    terminalreporter.write_sep("-", "parity near-tie counts (count / denominator)")
+    for line in mod.summary_lines():
+        terminalreporter.write_line(line)

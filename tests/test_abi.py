@@ -121,3 +121,27 @@ def test_basis_static_rejects_before_any_cuda_call(M):
     assert M.lib.mkv_basis_static(p, p, 1, 1, 0, p, p, None) == M.MKV_ERR_INVALID_ARG
     q = ctypes.c_void_p((1 << 20) + 8)
     assert M.lib.mkv_basis_static(q, p, 1, 1, 64, p, p, None) == M.MKV_ERR_INVALID_ARG
+
+
+def test_basis_static_binding_rejects_mixed_devices(M, monkeypatch):
+    """The binding refuses tensors on different devices before it calls the
+    library (the library works on the current device only)."""
+    import torch
+    calls = []
+    monkeypatch.setattr(M._lib, "mkv_basis_static", lambda *a: calls.append(a) or 0,
+                        raising=False)
+    k = torch.empty((1, 1, 16, 128), dtype=torch.float16, device="meta")
+    v = torch.empty((1, 1, 16, 128), dtype=torch.float16, device="cpu")
+    R = torch.empty((2, 1, 128, 128), dtype=torch.float32, device="meta")
+    lam = torch.empty((2, 1, 128), dtype=torch.float32, device="meta")
+    with pytest.raises(ValueError, match="one device"):
+        M.mkv_basis_static(k, v, R, lam)
+    assert not calls
+
+
+def test_debug_hooks_reject_bad_arguments_without_gpu(M):
+    assert M.lib.mkv_debug_wait_test(None, 1_000_000, None) == M.MKV_ERR_INVALID_ARG
+    fake = ctypes.c_void_p(1 << 20)     # never dereferenced: the limit is checked first
+    assert M.lib.mkv_debug_wait_test(fake, 10, None) == M.MKV_ERR_INVALID_ARG
+    assert M.lib.mkv_debug_wait_test(fake, 3_000_000_000, None) == M.MKV_ERR_INVALID_ARG
+    assert M.lib.mkv_debug_set_check_extent(None, 0) == M.MKV_ERR_INVALID_ARG

@@ -47,6 +47,15 @@ __device__ __forceinline__ uint2 row_meta(const mkv_segment_header* hdr, int64_t
   return make_uint2(hd.off16 + 16u * r, (uint32_t)NO_IDX);
 }
 
+// One past the last pool byte that the row (values and channel list) spans.
+__device__ __forceinline__ uint64_t row_end(const uint2& m, int c) {
+  const uint64_t v0 = (uint64_t)m.x * 16u;
+  if ((int32_t)m.y == NO_IDX) return v0 + 256u;
+  const uint64_t vend = v0 + 2u * (uint32_t)c;
+  const uint64_t iend = (uint64_t)((int64_t)v0 + 8 * (int64_t)(int32_t)m.y) + (uint32_t)c;
+  return vend > iend ? vend : iend;
+}
+
 // tokens of a chunk rounded up to the mma K step
 __host__ __device__ constexpr int attn_rows16(int chunk) { return (chunk + 15) & ~15; }
 
@@ -266,8 +275,14 @@ __global__ void __launch_bounds__(ATTN_THREADS, MINB) attn_kernel(DecodeParams p
   const int n = min(CH, p.kk - j0);
   if (tid < n) {
     const int64_t t = clamp_t(p.sel[(size_t)s * p.kk + j0 + tid], p.T);
-    const uint2 km = row_meta(p.hdrK + (size_t)s * p.n_seg, t, p.S, p.c);
-    const uint2 vm = row_meta(p.hdrV + (size_t)s * p.n_seg, t, p.S, p.c);
+    uint2 km = row_meta(p.hdrK + (size_t)s * p.n_seg, t, p.S, p.c);
+    uint2 vm = row_meta(p.hdrV + (size_t)s * p.n_seg, t, p.S, p.c);
+    if (row_end(km, p.c) > p.pool_check || row_end(vm, p.c) > p.pool_check) {
+      // outside the checked pool extent: report it and read a dense row at
+      // offset 0 instead (inside every pool)
+      atomicOr(p.err, DEV_ERR_CHECK);
+      km = vm = make_uint2(0u, (uint32_t)NO_IDX);
+    }
     meta[tid] = make_uint4(km.x, km.y, vm.x, vm.y);
   }
   __syncthreads();

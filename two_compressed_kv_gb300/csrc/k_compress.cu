@@ -149,27 +149,142 @@ __global__ void __launch_bounds__(256) gram_kernel(CompressParams p) {
 // ---------------------------------------------------------------------------
 // eig: symmetric eigendecomposition of one stream's G (fp32 cyclic Jacobi with
 // the round-robin parallel ordering: 64 disjoint rotations per round, 127
-// rounds per sweep).  Then one Newton-Schulz step re-orthonormalises the
-// accumulated rotations, eigenvalues are sorted descending (ties to the lower
-// index), and each column's largest-magnitude entry is made positive (ties to
-// the lower row).
-// grid: 2 * BH, block 512, dynamic smem 2 x 128 x 129 floats
+// rounds per sweep).  Refinement: after the first solve the accumulated
+// rotations V are re-orthonormalised (one Newton-Schulz step) and A = V^T G V
+// is formed afresh from the original G, then swept again; this removes the
+// rounding drift that in-place updates leave in A, so the eigen-residual is
+// set by the fp32 rounding of the products (about sqrt(n) eps_32 of ||G||).
+// Eigenvalues are sorted descending (ties to the lower index), and each
+// column's largest-magnitude entry is made positive (ties to the lower row).
+// grid: 2 * BH, block 512, dynamic smem 3 x 128 x 129 floats
 // ---------------------------------------------------------------------------
 constexpr int EIG_THREADS = 512;
 constexpr int LDA = D + 1;
 constexpr int EIG_MAX_SWEEPS = 16;
+constexpr int EIG_REFINE_SWEEPS = 6;
 
 __device__ __forceinline__ int rr_player(int pos, int round) {
   return pos == 0 ? 0 : 1 + (pos - 1 + round) % (D - 1);
+}
+
+struct EigShared {
+  float cs[64], sn[64], tt[64];
+  int top[64], bot[64];
+  int rotated;
+};
+
+// Jacobi sweeps on A (in place), accumulating the rotations into V, until a
+// sweep rotates nothing or max_sweeps have run.  Block-wide.
+__device__ void jacobi_sweeps(float* A, float* V, int max_sweeps, EigShared& sh) {
+  const int tid = threadIdx.x;
+  for (int sweep = 0; sweep < max_sweeps; ++sweep) {
+    if (tid == 0) sh.rotated = 0;
+    __syncthreads();
+    for (int round = 0; round < D - 1; ++round) {
+      if (tid < 64) {
+        int a = rr_player(tid, round), b = rr_player(D - 1 - tid, round);
+        const int pp = min(a, b), qq = max(a, b);
+        const float app = A[pp * LDA + pp], aqq = A[qq * LDA + qq], apq = A[pp * LDA + qq];
+        float c = 1.f, s = 0.f, t = 0.f;
+        if (apq != 0.f && fabsf(apq) > 1e-7f * sqrtf(fabsf(app * aqq))) {
+          const float th = (aqq - app) / (2.f * apq);
+          t = (th >= 0.f ? 1.f : -1.f) / (fabsf(th) + sqrtf(1.f + th * th));
+          c = 1.f / sqrtf(1.f + t * t);
+          s = t * c;
+          sh.rotated = 1;
+        }
+        sh.cs[tid] = c;
+        sh.sn[tid] = s;
+        sh.tt[tid] = t;
+        sh.top[tid] = pp;
+        sh.bot[tid] = qq;
+      }
+      __syncthreads();
+      for (int blk = tid; blk < 64 * 64; blk += EIG_THREADS) {
+        const int P = blk >> 6, Q = blk & 63;
+        const int p1 = sh.top[P], p2 = sh.bot[P];
+        if (P == Q) {
+          const float apq = A[p1 * LDA + p2], t = sh.tt[P];
+          A[p1 * LDA + p1] -= t * apq;
+          A[p2 * LDA + p2] += t * apq;
+          A[p1 * LDA + p2] = 0.f;
+          A[p2 * LDA + p1] = 0.f;
+        } else {
+          const int q1 = sh.top[Q], q2 = sh.bot[Q];
+          const float cP = sh.cs[P], sP = sh.sn[P], cQ = sh.cs[Q], sQ = sh.sn[Q];
+          const float b11 = A[p1 * LDA + q1], b12 = A[p1 * LDA + q2];
+          const float b21 = A[p2 * LDA + q1], b22 = A[p2 * LDA + q2];
+          const float u11 = cP * b11 - sP * b21, u12 = cP * b12 - sP * b22;
+          const float u21 = sP * b11 + cP * b21, u22 = sP * b12 + cP * b22;
+          A[p1 * LDA + q1] = cQ * u11 - sQ * u12;
+          A[p1 * LDA + q2] = sQ * u11 + cQ * u12;
+          A[p2 * LDA + q1] = cQ * u21 - sQ * u22;
+          A[p2 * LDA + q2] = sQ * u21 + cQ * u22;
+        }
+      }
+      for (int e = tid; e < D * 64; e += EIG_THREADS) {
+        const int r = e >> 6, k = e & 63;
+        const int pp = sh.top[k], qq = sh.bot[k];
+        const float c = sh.cs[k], s = sh.sn[k];
+        const float vp = V[r * LDA + pp], vq = V[r * LDA + qq];
+        V[r * LDA + pp] = c * vp - s * vq;
+        V[r * LDA + qq] = s * vp + c * vq;
+      }
+      __syncthreads();
+    }
+    const int any = sh.rotated;
+    __syncthreads();
+    if (!any) break;
+  }
+}
+
+// C = op(X) Y for 128 x 128 matrices in shared memory (row stride LDA), with
+// op(X) = X^T when TRANS_X.  Each thread owns D * D / EIG_THREADS entries of
+// C; C must not alias X or Y.  Block-wide.
+template <bool TRANS_X>
+__device__ void smem_matmul(const float* X, const float* Y, float* C) {
+  const int tid = threadIdx.x;
+#pragma unroll 1
+  for (int k = 0; k < D * D / EIG_THREADS; ++k) {
+    const int e = tid + k * EIG_THREADS;
+    const int r = e >> 7, cc = e & 127;
+    float acc = 0.f;
+#pragma unroll 8
+    for (int i = 0; i < D; ++i)
+      acc = fmaf(TRANS_X ? X[i * LDA + r] : X[r * LDA + i], Y[i * LDA + cc], acc);
+    C[r * LDA + cc] = acc;
+  }
+  __syncthreads();
+}
+
+// One Newton-Schulz step V <- V (1.5 I - 0.5 V^T V); W is scratch.
+__device__ void newton_schulz(float* V, float* W) {
+  const int tid = threadIdx.x;
+  smem_matmul<true>(V, V, W);
+  float nv[D * D / EIG_THREADS];
+#pragma unroll
+  for (int k = 0; k < D * D / EIG_THREADS; ++k) {
+    const int e = tid + k * EIG_THREADS;
+    const int r = e >> 7, a = e & 127;
+    float acc = 0.f;
+    for (int b = 0; b < D; ++b) acc = fmaf(V[r * LDA + b], W[b * LDA + a], acc);
+    nv[k] = 1.5f * V[r * LDA + a] - 0.5f * acc;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < D * D / EIG_THREADS; ++k) {
+    const int e = tid + k * EIG_THREADS;
+    V[(e >> 7) * LDA + (e & 127)] = nv[k];
+  }
+  __syncthreads();
 }
 
 __global__ void __launch_bounds__(EIG_THREADS) eig_kernel(CompressParams p) {
   extern __shared__ __align__(16) float esm[];
   float* A = esm;
   float* V = esm + D * LDA;
-  __shared__ float cs[64], sn[64], tt[64];
-  __shared__ int top[64], bot[64];
-  __shared__ int rotated;
+  float* Gs = esm + 2 * D * LDA;
+  __shared__ EigShared sh;
   __shared__ float lam[D];
   __shared__ int rank[D];
   __shared__ float sgn[D];
@@ -184,103 +299,41 @@ __global__ void __launch_bounds__(EIG_THREADS) eig_kernel(CompressParams p) {
     V[i * LDA + j] = (i == j) ? 1.f : 0.f;
   }
   __syncthreads();
-  // symmetrise: each (i, j), i < j, pair is owned by one thread
+  // symmetrise: each (i, j), i < j, pair is owned by one thread; keep G
   for (int e = tid; e < D * D; e += EIG_THREADS) {
     const int i = e >> 7, j = e & 127;
     if (i < j) {
       const float v = 0.5f * (A[i * LDA + j] + A[j * LDA + i]);
       A[i * LDA + j] = v;
       A[j * LDA + i] = v;
+      Gs[i * LDA + j] = v;
+      Gs[j * LDA + i] = v;
+    } else if (i == j) {
+      Gs[i * LDA + i] = A[i * LDA + i];
     }
   }
   __syncthreads();
 
-  for (int sweep = 0; sweep < EIG_MAX_SWEEPS; ++sweep) {
-    if (tid == 0) rotated = 0;
-    __syncthreads();
-    for (int round = 0; round < D - 1; ++round) {
-      if (tid < 64) {
-        int a = rr_player(tid, round), b = rr_player(D - 1 - tid, round);
-        const int pp = min(a, b), qq = max(a, b);
-        const float app = A[pp * LDA + pp], aqq = A[qq * LDA + qq], apq = A[pp * LDA + qq];
-        float c = 1.f, s = 0.f, t = 0.f;
-        if (apq != 0.f && fabsf(apq) > 1e-7f * sqrtf(fabsf(app * aqq))) {
-          const float th = (aqq - app) / (2.f * apq);
-          t = (th >= 0.f ? 1.f : -1.f) / (fabsf(th) + sqrtf(1.f + th * th));
-          c = 1.f / sqrtf(1.f + t * t);
-          s = t * c;
-          rotated = 1;
-        }
-        cs[tid] = c;
-        sn[tid] = s;
-        tt[tid] = t;
-        top[tid] = pp;
-        bot[tid] = qq;
-      }
-      __syncthreads();
-      for (int blk = tid; blk < 64 * 64; blk += EIG_THREADS) {
-        const int P = blk >> 6, Q = blk & 63;
-        const int p1 = top[P], p2 = bot[P];
-        if (P == Q) {
-          const float apq = A[p1 * LDA + p2], t = tt[P];
-          A[p1 * LDA + p1] -= t * apq;
-          A[p2 * LDA + p2] += t * apq;
-          A[p1 * LDA + p2] = 0.f;
-          A[p2 * LDA + p1] = 0.f;
-        } else {
-          const int q1 = top[Q], q2 = bot[Q];
-          const float cP = cs[P], sP = sn[P], cQ = cs[Q], sQ = sn[Q];
-          const float b11 = A[p1 * LDA + q1], b12 = A[p1 * LDA + q2];
-          const float b21 = A[p2 * LDA + q1], b22 = A[p2 * LDA + q2];
-          const float u11 = cP * b11 - sP * b21, u12 = cP * b12 - sP * b22;
-          const float u21 = sP * b11 + cP * b21, u22 = sP * b12 + cP * b22;
-          A[p1 * LDA + q1] = cQ * u11 - sQ * u12;
-          A[p1 * LDA + q2] = sQ * u11 + cQ * u12;
-          A[p2 * LDA + q1] = cQ * u21 - sQ * u22;
-          A[p2 * LDA + q2] = sQ * u21 + cQ * u22;
-        }
-      }
-      for (int e = tid; e < D * 64; e += EIG_THREADS) {
-        const int r = e >> 6, k = e & 63;
-        const int pp = top[k], qq = bot[k];
-        const float c = cs[k], s = sn[k];
-        const float vp = V[r * LDA + pp], vq = V[r * LDA + qq];
-        V[r * LDA + pp] = c * vp - s * vq;
-        V[r * LDA + qq] = s * vp + c * vq;
-      }
-      __syncthreads();
-    }
-    const int any = rotated;
-    __syncthreads();
-    if (!any) break;
-  }
-
-  if (tid < D) lam[tid] = A[tid * LDA + tid];
-  __syncthreads();
-  // Newton-Schulz: V <- V (1.5 I - 0.5 V^T V); A holds W = V^T V
+  jacobi_sweeps(A, V, EIG_MAX_SWEEPS, sh);
+  // refinement: orthonormal V, then A = V^T G V from the original G
+  newton_schulz(V, A);
+  smem_matmul<false>(Gs, V, A);     // A = G V
+  smem_matmul<true>(V, A, Gs);      // Gs = V^T G V
+  float* Ar = Gs;
+  float* W = A;
   for (int e = tid; e < D * D; e += EIG_THREADS) {
-    const int a = e >> 7, b = e & 127;
-    float w = 0.f;
-    for (int r = 0; r < D; ++r) w = fmaf(V[r * LDA + a], V[r * LDA + b], w);
-    A[a * LDA + b] = w;
+    const int i = e >> 7, j = e & 127;
+    if (i < j) {
+      const float v = 0.5f * (Ar[i * LDA + j] + Ar[j * LDA + i]);
+      Ar[i * LDA + j] = v;
+      Ar[j * LDA + i] = v;
+    }
   }
   __syncthreads();
-  float nv[D * D / EIG_THREADS];
-#pragma unroll
-  for (int k = 0; k < D * D / EIG_THREADS; ++k) {
-    const int e = tid + k * EIG_THREADS;
-    const int r = e >> 7, a = e & 127;
-    float acc = 0.f;
-    for (int b = 0; b < D; ++b) acc = fmaf(V[r * LDA + b], A[b * LDA + a], acc);
-    nv[k] = 1.5f * V[r * LDA + a] - 0.5f * acc;
-  }
+  jacobi_sweeps(Ar, V, EIG_REFINE_SWEEPS, sh);
+  if (tid < D) lam[tid] = Ar[tid * LDA + tid];
   __syncthreads();
-#pragma unroll
-  for (int k = 0; k < D * D / EIG_THREADS; ++k) {
-    const int e = tid + k * EIG_THREADS;
-    V[(e >> 7) * LDA + (e & 127)] = nv[k];
-  }
-  __syncthreads();
+  newton_schulz(V, W);
   if (tid < D) {
     const int j = tid;
     const float lj = lam[j];
@@ -486,6 +539,11 @@ __global__ void __launch_bounds__(256, 1) analyze_kernel(CompressParams p) {
         const int sg = (int)(t / p.S);
         const int rl = (int)(t - (int64_t)sg * p.S);
         const SegInfo si = seginfo[sg];
+        if ((uint64_t)hdr[sg].off16 * 16u + si.size > p.pool_check) {
+          // the segment would end past the checked pool extent: report, skip
+          if (lane == 0) atomicOr(p.err, DEV_ERR_CHECK);
+          continue;
+        }
         uint8_t* seg = p.pool + (size_t)hdr[sg].off16 * 16u;
         const uint32_t c = (uint32_t)p.c;
         if (si.strategy == MKV_STRATEGY_DENSE) {
@@ -662,7 +720,7 @@ cudaError_t launch_gram(const CompressParams& p, cudaStream_t st) {
 }
 
 cudaError_t launch_eig(const CompressParams& p, cudaStream_t st) {
-  const int smem = 2 * D * LDA * (int)sizeof(float);
+  const int smem = 3 * D * LDA * (int)sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(eig_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   eig_kernel<<<2 * p.BH, EIG_THREADS, smem, st>>>(p);

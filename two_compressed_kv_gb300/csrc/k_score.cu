@@ -248,6 +248,17 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
       e.z = __shfl_sync(0xffffffffu, cur.z, k & 31);
       e.w = __shfl_sync(0xffffffffu, cur.w, k & 31);
       const StagePlan sp = *reinterpret_cast<const StagePlan*>(&e);
+      if ((uint64_t)(sp.line0 + sp.nlines) * 128u > p.pool_check) {
+        // the stage would read past the checked pool extent: report it and
+        // end the pass here (consumers see the end marker)
+        if (lane == 0) {
+          atomicOr(p.err, DEV_ERR_CHECK);
+          meta[slot].seg0 = -1;
+          mbar_arrive(&full_bar[slot]);
+        }
+        ++k;
+        break;
+      }
       if (lane == 0) {
         const uint32_t nb = sp.nlines * 128u, hb = (uint32_t)sp.nhdr2 * 16u;
         meta[slot].seg0 = (int32_t)sp.seg0;
@@ -261,7 +272,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
       }
     }
     if (lane == 0) {
-      if (!ok) atomicExch(p.err, DEV_ERR_TIMEOUT);
+      if (!ok) atomicOr(p.err, DEV_ERR_TIMEOUT);
       sh_issued = k;
     }
     __syncwarp();   // the whole producer warp reaches the block barrier together
@@ -279,7 +290,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
       if (lane == 0) got = mbar_wait(&full_bar[slot], use & 1);
       got = __shfl_sync(0xffffffffu, got, 0);
       if (!got) {
-        if (lane == 0) atomicExch(p.err, DEV_ERR_TIMEOUT);
+        if (lane == 0) atomicOr(p.err, DEV_ERR_TIMEOUT);
         break;
       }
       const StageMeta m = meta[slot];

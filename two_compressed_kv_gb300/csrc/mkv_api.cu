@@ -3,13 +3,13 @@
 #include <algorithm>
 #include <cstdio>
 #include <cstring>
-#include <mutex>
 #include <new>
 #include <string>
 #include <utility>
 #include <vector>
 
 #include "mkv_internal.cuh"
+#include "ptx.cuh"
 
 using namespace mkv;
 
@@ -69,6 +69,8 @@ struct mkv_ctx {
   int32_t* plan_n[2] = {nullptr, nullptr};    // stages per score CTA
   uint8_t* pool = nullptr;
   uint64_t pool_cap = 0;
+  uint64_t pool_need = 0;          // bytes of the live cache's pool (packed size + tail pad)
+  uint64_t check_override = 0;     // test hook: a smaller checked pool extent (0 = none)
 
   // compression scratch
   SegInfo* seg = nullptr;
@@ -217,26 +219,21 @@ int gram_chunks_for(int BH, int64_t T) {
 
 // Scratch of mkv_basis_static: the partial Gram matrices of every (stream,
 // chunk), each 128 x 128 fp32.  A file-scope static device array, so that the
-// call allocates nothing; its address is looked up once per device.
+// call allocates nothing; its address is looked up at every call.
 static __device__ __align__(256) unsigned char g_basis_scratch[MKV_BASIS_STATIC_MAX_BYTES];
 
 namespace {
 
 constexpr int64_t kGramPartBytes = (int64_t)D * D * sizeof(float);
 constexpr int64_t kBasisStaticParts = MKV_BASIS_STATIC_MAX_BYTES / kGramPartBytes;
-constexpr int kMaxDevices = 256;
-std::mutex g_basis_scratch_mu;
-float* g_basis_scratch_addr[kMaxDevices] = {};
 
-// The buffer's address on the current device (looked up on first use).
-mkv_status basis_scratch_on(int dev, float** out) {
-  std::lock_guard<std::mutex> lock(g_basis_scratch_mu);
-  if (!g_basis_scratch_addr[dev]) {
-    void* a = nullptr;
-    CK(cudaGetSymbolAddress(&a, g_basis_scratch));
-    g_basis_scratch_addr[dev] = static_cast<float*>(a);
-  }
-  *out = g_basis_scratch_addr[dev];
+// The buffer's address in the current device's context.  Looked up on every
+// call (cheap once the module is loaded): a cached address would go stale
+// after a device reset or a new primary context.
+mkv_status basis_scratch_here(float** out) {
+  void* a = nullptr;
+  CK(cudaGetSymbolAddress(&a, g_basis_scratch));
+  *out = static_cast<float*>(a);
   return MKV_OK;
 }
 
@@ -448,10 +445,13 @@ mkv_status mkv_compress(mkv_ctx* c, const void* k, const void* v, int64_t ctx_le
     c->pool_cap = need;
   }
   p.pool = c->pool;
+  p.pool_check = c->check_override ? std::min(c->check_override, need) : need;
+  p.err = c->err;
   c->ready = false;   // the live headers may no longer match the pool
   CK(launch_pack(p, st));
   c->launches += 1;
   c->live = stage;
+  c->pool_need = need;
   c->T = ctx_len;
   c->n_seg = p.n_seg;
   c->ready = true;
@@ -479,6 +479,7 @@ mkv_status mkv_decode(mkv_ctx* c, const void* q, float* out, int32_t* sel, mkv_s
   p.RK = c->R[c->live];
   p.RV = c->R[c->live] + (size_t)c->BH * D * D;
   p.pool = c->pool;
+  p.pool_check = c->check_override ? std::min(c->check_override, c->pool_need) : c->pool_need;
   p.hdrK = c->hdr[c->live];
   p.hdrV = c->hdr[c->live] + (size_t)c->BH * c->n_seg;
   p.qt = c->qt;
@@ -582,8 +583,28 @@ mkv_status mkv_check_device(mkv_ctx* c) {
   CK(cudaMemcpy(&v, c->err, sizeof(int), cudaMemcpyDeviceToHost));
   if (v == 0) return MKV_OK;
   CK(cudaMemset(c->err, 0, sizeof(int)));
+  if (v & DEV_ERR_CHECK) {
+    g_last_error = (v & DEV_ERR_TIMEOUT)
+                       ? "a pool access fell outside the checked extent; a bounded wait gave up"
+                       : "a pool access fell outside the checked extent";
+    return MKV_ERR_DEVICE_CHECK;
+  }
   g_last_error = "a bounded device-side wait gave up";
   return MKV_ERR_TIMEOUT;
+}
+
+mkv_status mkv_debug_wait_test(mkv_ctx* c, uint64_t limit_ns, mkv_stream_t stream) {
+  if (!c || limit_ns < 1000u || limit_ns > WAIT_LIMIT_NS) return MKV_ERR_INVALID_ARG;
+  CK(cudaSetDevice(c->cfg.device));
+  CK(launch_wait_test(c->err, limit_ns, reinterpret_cast<cudaStream_t>(stream)));
+  c->launches += 1;
+  return MKV_OK;
+}
+
+mkv_status mkv_debug_set_check_extent(mkv_ctx* c, uint64_t bytes) {
+  if (!c) return MKV_ERR_INVALID_ARG;
+  c->check_override = bytes;
+  return MKV_OK;
 }
 
 mkv_status mkv_kernel_time(mkv_ctx* c, int kernel_id, double* total_ms, int64_t* launches,
@@ -628,14 +649,8 @@ mkv_status mkv_basis_static(const void* k, const void* v, int batch, int n_kv_he
     g_last_error = buf;
     return MKV_ERR_INVALID_ARG;
   }
-  int dev = 0;
-  CK(cudaGetDevice(&dev));
-  if (dev < 0 || dev >= kMaxDevices) {
-    g_last_error = "mkv_basis_static: device ordinal out of range";
-    return MKV_ERR_INVALID_ARG;
-  }
   float* scratch = nullptr;
-  mkv_status s = basis_scratch_on(dev, &scratch);
+  mkv_status s = basis_scratch_here(&scratch);
   if (s != MKV_OK) return s;
   CompressParams p;
   memset(&p, 0, sizeof(p));

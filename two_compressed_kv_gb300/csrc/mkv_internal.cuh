@@ -65,6 +65,8 @@ struct CompressParams {
   mkv_segment_header* hdr;   // [2][BH][n_seg]
   unsigned long long* total; // device: total packed bytes
   uint8_t* pool;
+  uint64_t pool_check;       // pack writes must end within this many pool bytes
+  int* err;                  // device status word
 };
 
 cudaError_t launch_gram(const CompressParams& p, cudaStream_t st);
@@ -106,6 +108,7 @@ struct DecodeParams {
   const float* RK;                 // [BH][128][128]
   const float* RV;                 // [BH][128][128]
   const uint8_t* pool;
+  uint64_t pool_check;             // pool reads must end within this many bytes
   const mkv_segment_header* hdrK;  // [BH][n_seg] (all K streams, contiguous)
   const mkv_segment_header* hdrV;  // [BH][n_seg]
   float* qt;                       // [B][Hq][128]
@@ -137,8 +140,13 @@ struct DecodeParams {
   int* err;                        // device status word (0 = ok)
 };
 
-// error codes written to the device status word
-constexpr int DEV_ERR_TIMEOUT = 1;
+// bits of the device status word (0 = ok), set with atomicOr
+constexpr int DEV_ERR_TIMEOUT = 1;   // a bounded wait gave up
+constexpr int DEV_ERR_CHECK = 2;     // an access fell outside the checked pool extent
+
+// test hook: one CTA runs the library's bounded mbarrier wait on a barrier no
+// thread arrives on, with the given limit
+cudaError_t launch_wait_test(int* err, uint64_t limit_ns, cudaStream_t st);
 
 // one-time per device: function attributes (not stream-ordered, so not in decode)
 cudaError_t prepare_decode_kernels();

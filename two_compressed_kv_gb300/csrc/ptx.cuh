@@ -46,22 +46,28 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
       : "memory");
   return r != 0u;
 }
-// Slow path of mbar_wait: polls with a device-time limit of about two seconds.
-static __device__ __noinline__ bool mbar_wait_timed(uint64_t* bar, uint32_t parity) {
+// Default limit of every bounded wait: about two seconds of device time.
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+
+// Slow path of mbar_wait: polls until the phase completes or limit_ns of
+// device time have passed.
+static __device__ __noinline__ bool mbar_wait_timed(uint64_t* bar, uint32_t parity,
+                                                    uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_test(bar, parity)) {
-    if (globaltimer_ns() - t0 > 2000000000ull) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
   return true;
 }
 // Waits for the phase with the given parity to complete; gives up (returns
-// false) after about two seconds of device time so that no bug can hang the GPU.
+// false) after limit_ns of device time so that no bug can hang the GPU.
 // The first 4096 polls do not read the timer: reading %globaltimer on every
 // poll made waiting warps slow down the working warps of the same SM.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          uint64_t limit_ns = WAIT_LIMIT_NS) {
   for (int i = 0; i < 4096; ++i)
     if (mbar_test(bar, parity)) return true;
-  return mbar_wait_timed(bar, parity);
+  return mbar_wait_timed(bar, parity, limit_ns);
 }
 
 // ---- bulk copies and cache policies --------------------------------------

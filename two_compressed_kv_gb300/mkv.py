@@ -84,6 +84,8 @@ def _load():
         "mkv_kernel_time": (c_int, [P, c_int, POINTER(c_double), POINTER(c_int64), c_int]),
         "mkv_check_device": (c_int, [P]),
         "mkv_basis_static": (c_int, [P, P, c_int, c_int, c_int64, P, P, P]),
+        "mkv_debug_wait_test": (c_int, [P, c_uint64, P]),
+        "mkv_debug_set_check_extent": (c_int, [P, c_uint64]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -222,6 +224,17 @@ def mkv_check_device(ctx) -> int:
     return _lib.mkv_check_device(ctx)
 
 
+def mkv_debug_wait_test(ctx, limit_ns: int, stream=None) -> None:
+    """Test hook: one CTA waits on an mbarrier nobody arrives on, for limit_ns."""
+    _check(_lib.mkv_debug_wait_test(ctx, int(limit_ns), _stream_ptr(stream)),
+           "mkv_debug_wait_test")
+
+
+def mkv_debug_set_check_extent(ctx, nbytes: int) -> None:
+    """Test hook: check pool accesses against min(nbytes, pool size); 0 resets."""
+    _check(_lib.mkv_debug_set_check_extent(ctx, int(nbytes)), "mkv_debug_set_check_extent")
+
+
 def mkv_kernel_time(ctx, kernel_id: int, reset: bool = False):
     ms = c_double(0.0)
     n = c_int64(0)
@@ -236,13 +249,19 @@ def mkv_basis_static(k, v, basis, eigvals, stream=None) -> None:
     k, v: fp16 [B][H][T][128]; basis: fp32 [2][B*H][128][128]; eigvals: fp32
     [2][B*H][128], all on the current CUDA device."""
     import torch
+    devs = {t.device for t in (k, v, basis, eigvals)}
+    if len(devs) != 1:
+        raise ValueError("k, v, basis and eigvals must be on one device, got "
+                         f"{sorted(map(str, devs))}")
     B, H, T, _ = k.shape
     pk = _dptr(k, torch.float16, "k", (B, H, T, 128))
     pv = _dptr(v, torch.float16, "v", (B, H, T, 128))
     pb = _dptr(basis, torch.float32, "basis", (2, B * H, 128, 128))
     pe = _dptr(eigvals, torch.float32, "eigvals", (2, B * H, 128))
-    _check(_lib.mkv_basis_static(pk, pv, B, H, T, pb, pe, _stream_ptr(stream, k.device)),
-           "mkv_basis_static")
+    # the library works on the current device: make it the tensors' own
+    with torch.cuda.device(k.device):
+        _check(_lib.mkv_basis_static(pk, pv, B, H, T, pb, pe, _stream_ptr(stream, k.device)),
+               "mkv_basis_static")
 
 
 class Mkv:
