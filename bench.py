@@ -315,6 +315,50 @@ def run_reference(args, w: W.Workload, ws: int, rank: int):
 # ---------------------------------------------------------------------------
 # GPU leg
 # ---------------------------------------------------------------------------
+def capture_steps(step, n: int, dev):
+    """n CUDA graphs, each holding one call of step()."""
+    out = []
+    for _ in range(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        out.append(g)
+    torch.cuda.synchronize(dev)
+    return out
+
+
+def kernel_times(ctxs, step, flags: int, n: int, dev, base_flags: int = 0) -> dict:
+    """Per-kernel device time of n decode steps run with the given timing
+    flags (events are recorded when a graph is captured, so the timers are
+    reset after a warm-up graph has run and each timed graph runs exactly
+    once before they are read).  Returns {kernel name: (total ms, launches)}."""
+    from two_compressed_kv_gb300 import mkv as M
+    for m in ctxs:
+        M.mkv_set_flags(m.ctx, flags)
+    try:
+        for g in capture_steps(step, 1, dev):
+            g.replay()
+        torch.cuda.synchronize(dev)
+        for m in ctxs:
+            for kid in range(len(M.KERNEL_NAMES)):
+                M.mkv_kernel_time(m.ctx, kid, reset=True)
+        for g in capture_steps(step, n, dev):
+            g.replay()
+        torch.cuda.synchronize(dev)
+        out = {}
+        for kid, name in enumerate(M.KERNEL_NAMES):
+            tot, cnt = 0.0, 0
+            for m in ctxs:
+                a, b = M.mkv_kernel_time(m.ctx, kid, reset=True)
+                tot, cnt = tot + a, cnt + b
+            if cnt:
+                out[name] = (tot, cnt)
+        return out
+    finally:
+        for m in ctxs:
+            M.mkv_set_flags(m.ctx, base_flags)
+
+
 def gathered_bytes(m, M, sel: np.ndarray, w: W.Workload) -> float:
     """Bytes of the K and V rows (plus shared masks) that the selected tokens
     read, counted from the packed layout of every stream."""
@@ -339,8 +383,9 @@ def run_gpu(args, w: W.Workload, ws: int, rank: int, local: int):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
     L = args.layers
+    base_flags = M.MKV_FLAG_NO_PDL if args.no_pdl else 0
     cfg = M.make_config(w.batch, w.n_kv_heads, w.n_q_heads, w.ctx, w.segment, w.c, w.tau,
-                        w.top_k, flags=M.MKV_FLAG_SCORE_TIMING, device=local)
+                        w.top_k, flags=base_flags, device=local)
     ctxs, qs, outs = [], [], []
     comp_ms = []
     cpu_args = None
@@ -373,18 +418,10 @@ def run_gpu(args, w: W.Workload, ws: int, rank: int, local: int):
             M.mkv_decode(m.ctx, q, o, None, None)
 
     # One CUDA graph per step (all layers): replays have no host launch gaps.
-    # Each graph owns its own timing events; the timed graphs are captured
-    # after the warm-up timers were reset, so every event pair is read only
-    # after the graph holding it has run.
+    # The timed graphs hold no events: each decode kernel may start while the
+    # one before it finishes (programmatic dependent launch).
     def capture(n):
-        out = []
-        for _ in range(n):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                step()
-            out.append(g)
-        torch.cuda.synchronize(dev)
-        return out
+        return capture_steps(step, n, dev)
 
     l0 = sum(m.stats()["kernel_launches"] for m in ctxs)
     step()
@@ -395,9 +432,6 @@ def run_gpu(args, w: W.Workload, ws: int, rank: int, local: int):
     for i in range(args.warmup):
         warm[i].replay() if use_graph else step()
     torch.cuda.synchronize(dev)
-    for m in ctxs:
-        for kid in range(5):
-            M.mkv_kernel_time(m.ctx, kid, reset=True)
     timed = capture(args.steps) if use_graph else []
     if use_graph:              # re-warm after the capture pause
         timed[0].replay()
@@ -432,15 +466,13 @@ def run_gpu(args, w: W.Workload, ws: int, rank: int, local: int):
     units_step = L * w.batch * w.ctx
     ms_step, value = _job_value(ev0.elapsed_time(ev1), args.steps, units_step, ws, dev)
 
-    # per-kernel device time inside the timed region
-    ktimes = {}
-    for kid, name in enumerate(M.KERNEL_NAMES):
-        tot, n = 0.0, 0
-        for m in ctxs:
-            a, b = M.mkv_kernel_time(m.ctx, kid)
-            tot += a
-            n += b
-        ktimes[name] = (tot, n)
+    # per-kernel device time: the same steps again, with events around every
+    # kernel (which launches them one after another), then around the score
+    # kernel alone
+    ktimes = kernel_times(ctxs, step, M.MKV_FLAG_KERNEL_TIMING, min(args.steps, 10), dev,
+                          base_flags)
+    ktimes["score"] = kernel_times(ctxs, step, M.MKV_FLAG_SCORE_TIMING, min(args.steps, 10),
+                                   dev, base_flags)["score"]
 
     # algorithmic bytes of one layer-step (layer 0), counted from its layout
     M.mkv_decode(ctxs[0].ctx, qs[0], outs[0], sel0, stream)
@@ -519,6 +551,9 @@ def run_gpu(args, w: W.Workload, ws: int, rank: int, local: int):
             "algorithmic_bytes_per_layer_step": alg_layer,
             "roofline": roof,
             "score_kernel_us_per_layer": ktimes["score"][0] / max(1, ktimes["score"][1]) * 1e3,
+            "kernel_us_per_layer_standalone": {k: v[0] / max(1, v[1]) * 1e3
+                                               for k, v in ktimes.items()},
+            "pdl": not args.no_pdl,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
@@ -574,7 +609,7 @@ def side_workload(w: W.Workload, layers: int, steps: int, dev, stream) -> dict:
     stream) plus its mkv_compress time per layer."""
     from two_compressed_kv_gb300 import mkv as M
     cfg = M.make_config(w.batch, w.n_kv_heads, w.n_q_heads, w.ctx, w.segment, w.c, w.tau,
-                        w.top_k, flags=M.MKV_FLAG_SCORE_TIMING, device=dev.index or 0)
+                        w.top_k, flags=0, device=dev.index or 0)
     ctxs, qs, outs, comp = [], [], [], []
     for layer in range(layers):
         K, V = W.draw_kv(w, layer=layer, device=dev)
@@ -600,17 +635,10 @@ def side_workload(w: W.Workload, layers: int, steps: int, dev, stream) -> dict:
 
     step()
     torch.cuda.synchronize(dev)
-    graphs = []
-    for _ in range(steps + 3):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            step()
-        graphs.append(g)
+    graphs = capture_steps(step, steps + 3, dev)
     for g in graphs[:3]:
         g.replay()
     torch.cuda.synchronize(dev)
-    for m in ctxs:
-        M.mkv_kernel_time(m.ctx, M.MKV_KERNEL_SCORE, reset=True)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
     for g in graphs[3:]:
@@ -618,12 +646,11 @@ def side_workload(w: W.Workload, layers: int, steps: int, dev, stream) -> dict:
     ev1.record(stream)
     torch.cuda.synchronize(dev)
     ms_step = ev0.elapsed_time(ev1) / steps
-    s_ms, s_n = 0.0, 0
     for m in ctxs:
-        a, b = M.mkv_kernel_time(m.ctx, M.MKV_KERNEL_SCORE)
-        s_ms, s_n = s_ms + a, s_n + b
         if M.mkv_check_device(m.ctx) != M.MKV_OK:
             raise RuntimeError("a device-side check fired during the timed region")
+    kt = kernel_times(ctxs, step, M.MKV_FLAG_KERNEL_TIMING, 5, dev)
+    s_ms, s_n = kernel_times(ctxs, step, M.MKV_FLAG_SCORE_TIMING, 5, dev)["score"]
     kk = min(w.top_k, w.ctx)
     sel0 = torch.empty(w.batch, w.n_kv_heads, kk, dtype=torch.int32, device=dev)
     M.mkv_decode(ctxs[0].ctx, qs[0], outs[0], sel0, stream)
@@ -643,6 +670,7 @@ def side_workload(w: W.Workload, layers: int, steps: int, dev, stream) -> dict:
            "prefill": {"value": w.batch * w.ctx / (statistics.median(comp) / 1e3),
                        "unit": "prefill-tokens/s per layer (K and V)",
                        "ms_per_layer_median": statistics.median(comp)},
+           "kernel_us_per_layer_standalone": {k: v[0] / max(1, v[1]) * 1e3 for k, v in kt.items()},
            "strategies_K": st0["strategy_count"][0], "strategies_V": st0["strategy_count"][1]}
     res["prefill"].update(prefill_roofline(w, statistics.median(comp), st0, peak))
     for m in ctxs:
@@ -665,6 +693,8 @@ def main(argv=None):
     ap.add_argument("--no-one-thread", action="store_true",
                     help="reference arm: skip the extra one-thread oracle timing")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (profiling runs)")
+    ap.add_argument("--no-pdl", action="store_true",
+                    help="launch the decode kernels without programmatic dependent launch")
     ap.add_argument("--no-side", action="store_true",
                     help="skip the 1M-context and mixed-256K lines added to the headline line")
     args = ap.parse_args(argv)

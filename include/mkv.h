@@ -68,6 +68,14 @@ enum {
 /* Record CUDA events around the score kernel only (fewer event records in a
  * captured step); read with mkv_kernel_time(ctx, MKV_KERNEL_SCORE, ...). */
 #define MKV_FLAG_SCORE_TIMING 2u
+/* Launch the decode kernels one after another without programmatic dependent
+ * launch.  By default (and whenever no timing flag is set) each decode kernel
+ * may start while the one before it is finishing: its prologue (staging of
+ * ctx data, barrier set-up, the first copies of packed keys) overlaps that
+ * kernel's tail.  Timing flags imply this flag, since an event between two
+ * kernels separates them. */
+#define MKV_FLAG_NO_PDL 4u
+#define MKV_FLAGS_ALL (MKV_FLAG_KERNEL_TIMING | MKV_FLAG_SCORE_TIMING | MKV_FLAG_NO_PDL)
 
 typedef struct {
   int32_t batch;          /* B >= 1 */
@@ -168,6 +176,11 @@ mkv_status mkv_compress(mkv_ctx* ctx, const void* k, const void* v, int64_t ctx_
  * Fully asynchronous on `stream`; no host synchronisation, no allocation. */
 mkv_status mkv_decode(mkv_ctx* ctx, const void* q, float* out, int32_t* sel,
                       mkv_stream_t stream);
+
+/* Replaces the ctx's MKV_FLAG_* bits (e.g. to time the kernels of a few
+ * decode steps).  Host only; applies to later calls.  MKV_ERR_INVALID_ARG for
+ * unknown bits. */
+mkv_status mkv_set_flags(mkv_ctx* ctx, uint32_t flags);
 
 /* Frees everything the ctx owns.  NULL is allowed.  Synchronises the device. */
 void mkv_free(mkv_ctx* ctx);

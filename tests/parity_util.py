@@ -31,7 +31,7 @@ from oracle import mosaickv as O
 NEAR_REL = 1e-4       # selected tokens: relative to the k-th score
 TOK_WIN = 2e-5        # channel magnitudes: relative to the token norm
 COL_WIN = 4e-5        # column energies: times sqrt(col * segment energy)
-TAU_WIN = 1e-4
+TAU_WIN = 1e-5
 MID_WIN = 1e-5        # rounding midpoints: relative to the token norm
 OUT_TOL = 2e-3
 # fp32 Jacobi on a dense 128 x 128 G: the eigen-residual and eigenvalue errors
@@ -55,10 +55,21 @@ def _near_tie_tok(mags_desc: np.ndarray, c: int, norm: float) -> bool:
     return mags_desc[c - 1] - mags_desc[c] <= TOK_WIN * norm
 
 
+def _floor_tok(mags_desc: np.ndarray, c: int, norm: float) -> bool:
+    """The c-th largest magnitude is itself within the rotation error of zero
+    (a stream of rank < c): every choice among those channels is a tie."""
+    return c < len(mags_desc) and mags_desc[c - 1] <= TOK_WIN * norm
+
+
 def _near_tie_col(col_desc: np.ndarray, c: int, e_tot: float) -> bool:
     if c >= len(col_desc):
         return False
     return col_desc[c - 1] - col_desc[c] <= COL_WIN * np.sqrt(col_desc[c - 1] * e_tot) + 1e-300
+
+
+def _floor_col(col_desc: np.ndarray, c: int, e_tot: float) -> bool:
+    """Same for column energies: col_(c) <= COL_WIN * sqrt(col_(c) * e_tot)."""
+    return c < len(col_desc) and col_desc[c - 1] <= COL_WIN ** 2 * e_tot + 1e-300
 
 
 def check_basis(X: np.ndarray, R: np.ndarray, lam: np.ndarray, report: dict):
@@ -105,7 +116,7 @@ def compare_compressed(X: np.ndarray, R: np.ndarray, hdr: np.ndarray, payload: b
     q16 = O.to_fp16(cs.Xt)
     tau32 = float(np.float32(tau))
     cnt = dict(segments=len(cs.segs), rows=cs.T, bytes_equal=0, strat_near=0, idx_near=0,
-               ulp_near=0, values=0)
+               idx_floor=0, ulp_near=0, values=0)
     expect_off = 0
     for si, (a, b) in enumerate(O.segment_bounds(cs.T, S)):
         seg = cs.segs[si]
@@ -142,7 +153,7 @@ def compare_compressed(X: np.ndarray, R: np.ndarray, hdr: np.ndarray, payload: b
             if not np.array_equal(gidx, seg.mask):
                 col = np.sort(sq.sum(axis=0))[::-1]
                 assert _near_tie_col(col, c, seg.e_tot), f"segment {si}: shared mask differs"
-                cnt["idx_near"] += 1
+                cnt["idx_floor" if _floor_col(col, c, seg.e_tot) else "idx_near"] += 1
                 continue
             assert not gseg[c:O.pad16(c)].any(), f"segment {si}: nonzero padding"
             gv = gseg[O.pad16(c):].view("<f2").reshape(rows, c)
@@ -156,9 +167,9 @@ def compare_compressed(X: np.ndarray, R: np.ndarray, hdr: np.ndarray, payload: b
                 P = cs.P[a + r]
                 if not np.array_equal(gidx[r], P):
                     mags = np.sort(np.abs(cs.Xt[a + r]))[::-1]
-                    assert _near_tie_tok(mags, c, np.sqrt(sq[r].sum())), \
-                        f"segment {si} row {r}: channels differ"
-                    cnt["idx_near"] += 1
+                    nrm = np.sqrt(sq[r].sum())
+                    assert _near_tie_tok(mags, c, nrm), f"segment {si} row {r}: channels differ"
+                    cnt["idx_floor" if _floor_tok(mags, c, nrm) else "idx_near"] += 1
                     continue
                 _check_vals(gv[r:r + 1], q16[a + r:a + r + 1][:, P],
                             cs.Xt[a + r:a + r + 1][:, P], norms[r:r + 1], cnt,
@@ -211,12 +222,16 @@ def compare_decode(q: np.ndarray, RK: np.ndarray, RV: np.ndarray, K_hat: np.ndar
 
 
 def compare_oracle_packed(q: np.ndarray, ck, cv, k: int, gsel: np.ndarray, gout: np.ndarray,
-                          report: dict):
+                          K_lib: np.ndarray, report: dict):
     """End to end through the oracle alone: the oracle packs the streams it
     compressed (given the library's bases), unpacks its own bytes and decodes;
     the library's output must match within the output tolerance, and its
-    selection must equal the oracle's outside near-ties of the k-th score.
-    Unlike compare_decode, nothing here reads the library's packed bytes."""
+    selection must equal the oracle's own, except for tokens within the
+    near-tie window of the k-th score widened by the largest score difference
+    between the oracle's cache and the library's (K_lib, already validated
+    value by value): a stored value whose fp16 rounding legitimately differs
+    moves a score by |q_bar_j| ulp(k_j), more than 1e-4 when scores crowd.
+    Unlike compare_decode, the decode here reads none of the library's bytes."""
     hk, pk = O.pack_stream(ck)
     hv, pv = O.pack_stream(cv)
     Kh = O.unpack_stream(hk, pk, ck.T, ck.S, ck.c, ck.d)
@@ -225,15 +240,20 @@ def compare_oracle_packed(q: np.ndarray, ck, cv, k: int, gsel: np.ndarray, gout:
     kk = min(k, ck.T)
     s = r.scores
     sk = np.sort(s)[::-1][kk - 1]
+    qt = O.rotate_queries(q, ck.R)
+    s_lib = (qt @ K_lib.T).sum(axis=0)
+    cache_diff = float(np.abs(s - s_lib).max())
+    win = NEAR_REL * max(abs(sk), 1e-30) + 2.0 * cache_diff
     gsel = np.asarray(gsel, dtype=np.int64)
     diff = np.setxor1d(gsel, r.sel)
     for t in diff:
-        assert abs(s[t] - sk) <= NEAR_REL * max(abs(sk), 1e-30), \
-            f"token {t}: selection differs from the oracle-packed decode"
-    err = float(np.abs(r.out - gout).max()) if not len(diff) else None
-    if err is None:
-        # with a differing (near-tie) set, compare on the library's set
-        qt = O.rotate_queries(q, ck.R)
+        assert abs(s[t] - sk) <= win, \
+            f"token {t}: selection differs from the oracle-packed decode ({s[t]} vs {sk}, {win})"
+    report["e2e_sel_diff"] = report.get("e2e_sel_diff", 0) + len(diff) // 2
+    if not len(diff):
+        err = float(np.abs(r.out - gout).max())
+    else:
+        # with a differing set, compare on the library's set
         out_o, _ = O.attend(qt, cv.R, Kh, Vh, gsel)
         err = float(np.abs(out_o - gout).max())
     report["e2e_out_err"] = max(report.get("e2e_out_err", 0.0), err)
@@ -245,7 +265,9 @@ def compare_oracle_packed(q: np.ndarray, ck, cv, k: int, gsel: np.ndarray, gout:
 # tests/conftest.py prints at the end of a run.
 #   * selected tokens: near-tie swaps <= 0.1% of the selected tokens (+2);
 #   * per-token channel sets and shared masks: near-tie flips <= 0.1% of the
-#     stored rows (+2);
+#     stored rows (+2); flips where the c-th magnitude is itself within the
+#     rotation error of zero (streams of rank < c: every choice is a tie) are
+#     counted apart (idx_floor) and not budgeted;
 #   * strategies: near-tie flips <= 1% of the segments (+2);
 #   * stored fp16 values: values that are not the rounding of the exact
 #     rotated value <= ULP_BUDGET of the stored values.  The library's rotated
@@ -253,7 +275,7 @@ def compare_oracle_packed(q: np.ndarray, ck, cv, k: int, gsel: np.ndarray, gout:
 #     value of magnitude |x| flips its rounding with probability about
 #     1e-3 * norm / |x|: a few tenths of a percent over kept values.
 # ---------------------------------------------------------------------------
-ULP_BUDGET = 0.02
+ULP_BUDGET = 0.01
 REPORTS = []
 
 
@@ -270,8 +292,9 @@ def assert_budgets(name: str, rep: dict):
 def summary_lines():
     """One line per recorded parity check, for the end-of-session summary."""
     out = []
-    keys = ("sel_near", "selected", "idx_near", "rows", "strat_near", "segments", "ulp_near",
-            "values", "out_err", "e2e_out_err", "resid", "orth")
+    keys = ("sel_near", "selected", "idx_near", "idx_floor", "rows", "strat_near", "segments",
+            "ulp_near", "values", "out_err", "e2e_sel_diff", "e2e_out_err", "resid", "orth",
+            "lam_err", "min_cos_sep")
     for name, rep in REPORTS:
         parts = []
         for k in keys:

@@ -85,7 +85,7 @@ def test_validate_config(M):
            dict(segment=72), dict(segment=272), dict(c=4), dict(c=36), dict(c=136),
            dict(tau=0.0), dict(tau=1.5), dict(tau=float("nan")), dict(top_k=0),
            dict(max_ctx=0), dict(batch=0), dict(attn_chunk=4), dict(attn_chunk=12),
-           dict(flags=4), dict(device=-1), dict(attn_chunk=136)]
+           dict(flags=8), dict(device=-1), dict(attn_chunk=136)]
     for b in bad:
         assert M.mkv_validate_config(_cfg(M, **b)) == M.MKV_ERR_INVALID_ARG, b
     for good in [dict(segment=16), dict(segment=256), dict(c=8), dict(c=128), dict(tau=1.0),

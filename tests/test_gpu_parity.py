@@ -56,7 +56,8 @@ def check_streams(w, K, V, q, m, out, sel, streams, basis=True, oracle_packed=Tr
         qn = q[b, h * g:(h + 1) * g].cpu().numpy()
         compare_decode(qn, RK, RV, Kh, Vh, w.top_k, sel[b, h], out[b, h * g:(h + 1) * g], rep)
         if oracle_packed:
-            compare_oracle_packed(qn, ck, cv, w.top_k, sel[b, h], out[b, h * g:(h + 1) * g], rep)
+            compare_oracle_packed(qn, ck, cv, w.top_k, sel[b, h], out[b, h * g:(h + 1) * g], Kh,
+                                  rep)
     return rep
 
 

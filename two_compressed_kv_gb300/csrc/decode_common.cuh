@@ -7,6 +7,37 @@
 
 namespace mkv {
 
+// Launches a decode kernel with cudaLaunchKernelEx: a thread-block cluster of
+// cluster_x CTAs when cluster_x > 0, and programmatic stream serialization
+// (the kernel may start before the previous kernel of the stream ends; see
+// griddep_wait) when pdl is set.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t st, bool pdl, int cluster_x, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (cluster_x > 0) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Order-preserving map of fp32 to uint32 (larger float -> larger key);
 // -0 and +0 map to the same key so that equal scores tie.
 __device__ __forceinline__ uint32_t f2key(float x) {

@@ -273,6 +273,10 @@ __global__ void __launch_bounds__(ATTN_THREADS, MINB) attn_kernel(DecodeParams p
   }
   const int j0 = chk * CH;
   const int n = min(CH, p.kk - j0);
+  // q~ (from the rotation kernel, two launches back) and the ctx's headers
+  // are ready; the selection is not
+  griddep_wait();
+  griddep_launch();
   if (tid < n) {
     const int64_t t = clamp_t(p.sel[(size_t)s * p.kk + j0 + tid], p.T);
     uint2 km = row_meta(p.hdrK + (size_t)s * p.n_seg, t, p.S, p.c);
@@ -322,6 +326,8 @@ __global__ void __launch_bounds__(MG_THREADS) merge_kernel(DecodeParams p) {
       Rt[(j + 3) * MG_LD + rr] = v.w;
     }
   }
+  griddep_wait();     // the partials come from the attention kernel
+  griddep_launch();
   // weights exp(m_c - M) and 1 / L per head: warp per head, lanes over chunks
   const float2* ml = reinterpret_cast<const float2*>(p.part_ml + (size_t)s * nc * g * 2);
   for (int hh = warp; hh < g; hh += MG_THREADS / 32) {
@@ -379,16 +385,16 @@ cudaError_t prepare_attn_kernels() {
 cudaError_t launch_attn(const DecodeParams& p, cudaStream_t st) {
   dim3 grid(p.attn_chunks, p.B * p.H);
   const size_t smem = attn_smem_bytes(p.g, p.attn_chunk);
-  if (p.g <= 4 && p.attn_chunk <= 64) attn_kernel<4, 6><<<grid, ATTN_THREADS, smem, st>>>(p);
-  else if (p.g <= 4) attn_kernel<4, 4><<<grid, ATTN_THREADS, smem, st>>>(p);
-  else attn_kernel<MAX_G, 4><<<grid, ATTN_THREADS, smem, st>>>(p);
-  return cudaGetLastError();
+  const bool pdl = p.pdl != 0;
+  if (p.g <= 4 && p.attn_chunk <= 64)
+    return launch_kernel(attn_kernel<4, 6>, grid, dim3(ATTN_THREADS), smem, st, pdl, 0, p);
+  if (p.g <= 4) return launch_kernel(attn_kernel<4, 4>, grid, dim3(ATTN_THREADS), smem, st, pdl, 0, p);
+  return launch_kernel(attn_kernel<MAX_G, 4>, grid, dim3(ATTN_THREADS), smem, st, pdl, 0, p);
 }
 
 cudaError_t launch_merge(const DecodeParams& p, cudaStream_t st) {
-  dim3 grid(p.B * p.H, D / MG_ROWS);
-  merge_kernel<<<grid, MG_THREADS, sizeof(float) * (size_t)p.attn_chunks * p.g, st>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(merge_kernel, dim3(p.B * p.H, D / MG_ROWS), dim3(MG_THREADS),
+                       sizeof(float) * (size_t)p.attn_chunks * p.g, st, p.pdl != 0, 0, p);
 }
 
 }  // namespace mkv

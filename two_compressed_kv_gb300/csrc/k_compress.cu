@@ -73,10 +73,15 @@ __device__ __forceinline__ void load_tile(uint32_t tile, const __half* X, int64_
 // ---------------------------------------------------------------------------
 // gram: partial G over one chunk of tokens.  8 warps; warp w owns the 32 x 64
 // block G[i0:i0+32, j0:j0+64].  A = X^T and B = X both come from the token-major
-// tile through ldmatrix.trans.
+// tile through ldmatrix.trans.  The tensor-core accumulators take GR_FLUSH
+// tiles at a time and are then added into a separate fp32 sum: tensor-core
+// accumulation does not round to nearest, so its error grows with the number
+// of products summed in one accumulator; flushing keeps G good to a few 1e-6
+// relative at any context length.
 // grid: (gram_chunks, BH, 2), block 256, dynamic smem 3 x 16 KB
 // ---------------------------------------------------------------------------
 constexpr int GR_STAGES = 3;
+constexpr int GR_FLUSH = 2;     // tiles (of 64 tokens) per accumulator flush
 
 __global__ void __launch_bounds__(256) gram_kernel(CompressParams p) {
   extern __shared__ __align__(128) uint8_t gsm[];
@@ -89,13 +94,13 @@ __global__ void __launch_bounds__(256) gram_kernel(CompressParams p) {
   const uint32_t base = smem_u32(gsm);
   const int i0 = (warp & 3) * 32, j0 = (warp >> 2) * 64;
 
-  float acc[2][8][4];
+  float acc[2][8][4], tot[2][8][4];
 #pragma unroll
   for (int a = 0; a < 2; ++a)
 #pragma unroll
     for (int b = 0; b < 8; ++b)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[a][b][e] = 0.f;
+      for (int e = 0; e < 4; ++e) acc[a][b][e] = tot[a][b][e] = 0.f;
 
   for (int st = 0; st < GR_STAGES - 1; ++st) {
     if (st < n_tiles) load_tile(base + st * 16384u, X, tb + (int64_t)st * TILE_T, te);
@@ -132,6 +137,17 @@ __global__ void __launch_bounds__(256) gram_kernel(CompressParams p) {
         }
       }
     }
+    if ((it + 1) % GR_FLUSH == 0 || it + 1 == n_tiles) {
+#pragma unroll
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int b = 0; b < 8; ++b)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            tot[a][b][e] += acc[a][b][e];
+            acc[a][b][e] = 0.f;
+          }
+    }
   }
   cp_async_wait<0>();
   float* out = p.gram_part + (((size_t)x * p.BH + s) * p.gram_chunks + chunk) * (D * D);
@@ -141,8 +157,8 @@ __global__ void __launch_bounds__(256) gram_kernel(CompressParams p) {
 #pragma unroll
     for (int ni = 0; ni < 8; ++ni) {
       const int i = i0 + mi * 16 + g, j = j0 + ni * 8 + 2 * q;
-      *reinterpret_cast<float2*>(out + i * D + j) = make_float2(acc[mi][ni][0], acc[mi][ni][1]);
-      *reinterpret_cast<float2*>(out + (i + 8) * D + j) = make_float2(acc[mi][ni][2], acc[mi][ni][3]);
+      *reinterpret_cast<float2*>(out + i * D + j) = make_float2(tot[mi][ni][0], tot[mi][ni][1]);
+      *reinterpret_cast<float2*>(out + (i + 8) * D + j) = make_float2(tot[mi][ni][2], tot[mi][ni][3]);
     }
 }
 

@@ -34,6 +34,10 @@ __global__ void __launch_bounds__(QR_THREADS) qrot_kernel(DecodeParams p) {
   float4* Rs4 = reinterpret_cast<float4*>(Rs);
 #pragma unroll
   for (int x = 0; x < D * D / 4 / QR_THREADS; ++x) Rs4[tid + x * QR_THREADS] = __ldg(R4 + tid + x * QR_THREADS);
+  // R_K belongs to the ctx; q and the step's buffers may still be in use by
+  // the kernel before this one
+  griddep_wait();
+  griddep_launch();
   const __half* q = p.q + ((size_t)b * p.Hq + (size_t)h * p.g) * D;
   for (int x = tid; x < p.g * D; x += QR_THREADS) qs[x / D][x % D] = __half2float(q[x]);
   uint4* hz = reinterpret_cast<uint4*>(p.hist + (size_t)s * HIST1);
@@ -187,16 +191,16 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
   __shared__ int sh_flag, sh_issued, sh_consumed;
 
   const int a = p.part[blockIdx.x], b = p.part[blockIdx.x + 1];
-  if (a >= b) return;
+  if (a >= b) {
+    griddep_wait();
+    griddep_launch();
+    return;
+  }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int s_first = a / p.n_seg, s_last = (b - 1) / p.n_seg;
   const int NST = p.n_stages;
   const size_t slot_bytes = sc_slot(p.stage_bytes);
   for (int x = tid; x < SC_NSLOT * HIST1; x += SC_THREADS) (&hist[0][0])[x] = 0u;
-  for (int x = tid; x < SC_NSLOT * D; x += SC_THREADS) {
-    const int s = s_first + x / D;
-    (&qb[0][0])[x] = (s <= s_last) ? p.qbar[(size_t)s * D + (x % D)] : 0.f;
-  }
   if (tid == 0) {
     for (int st = 0; st < NST; ++st) {
       mbar_init(&full_bar[st], 1);
@@ -208,6 +212,9 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
   }
   __syncthreads();
 
+  // The producer starts copying packed keys (ctx data) at once; q_bar, the
+  // histograms, tickets and scores are touched only after griddep_wait, which
+  // the consumers pass before their loop and the producer after its own.
   if (warp == SC_CONS) {
     // ---- producer warp --------------------------------------------------------
     // The stages were planned at compression; plan entries come 32 at a time
@@ -271,6 +278,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
         bulk_g2s(&shdr[slot][0], p.hdrK + (sp.seg0 & ~1u), hb, &full_bar[slot], pol);
       }
     }
+    griddep_wait();
     if (lane == 0) {
       if (!ok) atomicOr(p.err, DEV_ERR_TIMEOUT);
       sh_issued = k;
@@ -278,6 +286,13 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
     __syncwarp();   // the whole producer warp reaches the block barrier together
   } else {
     // ---- consumers ----------------------------------------------------------
+    griddep_wait();
+    if (warp == 0) griddep_launch();
+    for (int x = tid; x < SC_NSLOT * D; x += SC_CONS * 32) {
+      const int s = s_first + x / D;
+      (&qb[0][0])[x] = (s <= s_last) ? p.qbar[(size_t)s * D + (x % D)] : 0.f;
+    }
+    named_barrier_sync(1, SC_CONS * 32);
     const uint64_t pol = policy_evict_last();
     const int bps = (p.S + 31) >> 5;      // 32-row blocks per segment (1..8)
     // it / bps = (it * bps_inv) >> 16, exact for it < 512
@@ -514,15 +529,17 @@ cudaError_t launch_partition(const mkv_segment_header* hdrK, int n_streams, int 
 }
 
 cudaError_t launch_qrot(const DecodeParams& p, cudaStream_t st) {
-  qrot_kernel<<<p.B * p.H, QR_THREADS, D * D * 4, st>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(qrot_kernel, dim3(p.B * p.H), dim3(QR_THREADS), (size_t)D * D * 4, st,
+                       p.pdl != 0, 0, p);
 }
 
 cudaError_t launch_score(const DecodeParams& p, cudaStream_t st) {
   const size_t smem = sc_slot(p.stage_bytes) * p.n_stages;
   switch (p.c >> 3) {
-#define MKV_SCORE_CASE(N) \
-  case N: score_kernel<N><<<p.G, SC_THREADS, smem, st>>>(p); break;
+#define MKV_SCORE_CASE(N)                                                                   \
+  case N:                                                                                 \
+    return launch_kernel(score_kernel<N>, dim3(p.G), dim3(SC_THREADS), smem, st, p.pdl != 0, \
+                         0, p);
     MKV_SCORE_CASE(1) MKV_SCORE_CASE(2) MKV_SCORE_CASE(3) MKV_SCORE_CASE(4) MKV_SCORE_CASE(5)
     MKV_SCORE_CASE(6) MKV_SCORE_CASE(7) MKV_SCORE_CASE(8) MKV_SCORE_CASE(9) MKV_SCORE_CASE(10)
     MKV_SCORE_CASE(11) MKV_SCORE_CASE(12) MKV_SCORE_CASE(13) MKV_SCORE_CASE(14)
@@ -530,7 +547,6 @@ cudaError_t launch_score(const DecodeParams& p, cudaStream_t st) {
 #undef MKV_SCORE_CASE
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace mkv

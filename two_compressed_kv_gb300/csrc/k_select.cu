@@ -114,6 +114,8 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) select_kernel(DecodeParams p) 
   __shared__ SelShared sh;
   const int R = (int)cl.num_blocks(), r = (int)cl.block_rank();
   const int s = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  griddep_wait();     // scores and the level-1 state come from the score kernel
+  griddep_launch();
   SelGeom geo;
   geo.per = (((p.Tp + R - 1) / R) + 15) / 16 * 16;
   geo.T = p.T;
@@ -401,19 +403,8 @@ cudaError_t prepare_select_kernels() {
 }
 
 cudaError_t launch_topk(const DecodeParams& p, cudaStream_t st) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.sel_R, p.B * p.H, 1);
-  cfg.blockDim = dim3(SEL_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = SEL_SMEM;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = p.sel_R;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, select_kernel, p);
+  return launch_kernel(select_kernel, dim3(p.sel_R, p.B * p.H, 1), dim3(SEL_THREADS), SEL_SMEM,
+                       st, p.pdl != 0, p.sel_R, p);
 }
 
 }  // namespace mkv

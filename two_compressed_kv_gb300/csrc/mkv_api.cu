@@ -276,7 +276,7 @@ mkv_status mkv_validate_config(const mkv_config* cfg) {
   if (c.top_k < 1) return MKV_ERR_INVALID_ARG;
   if (c.attn_chunk != 0 && (c.attn_chunk < 8 || c.attn_chunk > ATTN_MAX_CHUNK || c.attn_chunk % 8 != 0))
     return MKV_ERR_INVALID_ARG;
-  if (c.flags & ~(MKV_FLAG_KERNEL_TIMING | MKV_FLAG_SCORE_TIMING)) return MKV_ERR_INVALID_ARG;
+  if (c.flags & ~MKV_FLAGS_ALL) return MKV_ERR_INVALID_ARG;
   if (c.device < 0) return MKV_ERR_INVALID_ARG;
   const int64_t streams = (int64_t)c.batch * c.n_kv_heads;
   if (streams > (1 << 20)) return MKV_ERR_INVALID_ARG;
@@ -505,6 +505,8 @@ mkv_status mkv_decode(mkv_ctx* c, const void* q, float* out, int32_t* sel, mkv_s
   p.part_o = c->part_o;
   p.part_ml = c->part_ml;
   p.out = out;
+  // kernel timing records events between kernels: launch those plainly
+  p.pdl = (c->cfg.flags & (MKV_FLAG_KERNEL_TIMING | MKV_FLAG_SCORE_TIMING | MKV_FLAG_NO_PDL)) == 0u;
   mkv_status s;
   if ((s = timed(c, MKV_KERNEL_QROT, st, 1, [&] { return launch_qrot(p, st); })) != MKV_OK) return s;
   if ((s = timed(c, MKV_KERNEL_SCORE, st, 1, [&] { return launch_score(p, st); })) != MKV_OK) return s;
@@ -591,6 +593,12 @@ mkv_status mkv_check_device(mkv_ctx* c) {
   }
   g_last_error = "a bounded device-side wait gave up";
   return MKV_ERR_TIMEOUT;
+}
+
+mkv_status mkv_set_flags(mkv_ctx* c, uint32_t flags) {
+  if (!c || (flags & ~MKV_FLAGS_ALL)) return MKV_ERR_INVALID_ARG;
+  c->cfg.flags = flags;
+  return MKV_OK;
 }
 
 mkv_status mkv_debug_wait_test(mkv_ctx* c, uint64_t limit_ns, mkv_stream_t stream) {

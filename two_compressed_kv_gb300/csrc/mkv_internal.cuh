@@ -138,6 +138,7 @@ struct DecodeParams {
   float* part_ml;                  // [BH][attn_chunks][g][2]
   float* out;                      // [B][Hq][128]
   int* err;                        // device status word (0 = ok)
+  int pdl;                         // launch with programmatic dependent launch
 };
 
 // bits of the device status word (0 = ok), set with atomicOr

@@ -18,6 +18,26 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// ---- programmatic dependent launch ------------------------------------------
+// A kernel launched with programmatic stream serialization may start while the
+// previous kernel of the stream is still running.  griddep_wait blocks the
+// calling thread until that kernel has completed and its writes are visible;
+// nothing the previous kernel writes (or reads) may be touched before it.
+// griddep_launch lets the next kernel start; every kernel of the library calls
+// it only after its own griddep_wait, so a kernel's prologue can overlap only
+// the kernel just before it, never an earlier one.  Both are no-ops for a
+// kernel launched without the attribute.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
+// Barrier `id` (1..15) over the first `nthreads` threads that reach it (a
+// multiple of 32); barrier 0 is __syncthreads.
+__device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // ---- mbarrier -------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count)

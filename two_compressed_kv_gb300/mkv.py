@@ -28,6 +28,7 @@ MKV_ERR_TIMEOUT = 6
 MKV_STRATEGY_SM, MKV_STRATEGY_PV, MKV_STRATEGY_DENSE = 0, 1, 2
 MKV_FLAG_KERNEL_TIMING = 1
 MKV_FLAG_SCORE_TIMING = 2
+MKV_FLAG_NO_PDL = 4
 MKV_BASIS_STATIC_MAX_BYTES = 16 << 20
 MKV_KERNEL_QROT, MKV_KERNEL_SCORE, MKV_KERNEL_TOPK, MKV_KERNEL_ATTN, MKV_KERNEL_MERGE = range(5)
 KERNEL_NAMES = ["qrot", "score", "topk", "attn", "merge"]
@@ -85,6 +86,7 @@ def _load():
         "mkv_check_device": (c_int, [P]),
         "mkv_basis_static": (c_int, [P, P, c_int, c_int, c_int64, P, P, P]),
         "mkv_debug_wait_test": (c_int, [P, c_uint64, P]),
+        "mkv_set_flags": (c_int, [P, c_uint32]),
         "mkv_debug_set_check_extent": (c_int, [P, c_uint64]),
     }
     for name, (res, args) in sig.items():
@@ -222,6 +224,10 @@ def mkv_export_headers(ctx, b: int, h: int, which: int, n_segments: int) -> np.n
 def mkv_check_device(ctx) -> int:
     """MKV_OK, or MKV_ERR_TIMEOUT when a bounded device wait gave up (synchronous)."""
     return _lib.mkv_check_device(ctx)
+
+
+def mkv_set_flags(ctx, flags: int) -> None:
+    _check(_lib.mkv_set_flags(ctx, int(flags)), "mkv_set_flags")
 
 
 def mkv_debug_wait_test(ctx, limit_ns: int, stream=None) -> None:
