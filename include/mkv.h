@@ -87,12 +87,15 @@ typedef struct {
   int32_t c;              /* kept channels per vector: 8..128, multiple of 8 */
   float tau;              /* retained-energy threshold, 0 < tau <= 1 */
   int32_t top_k;          /* tokens attended per KV head per step, >= 1 */
-  int32_t attn_chunk;     /* selected tokens per split-K attention block; 0 = auto
-                             (64 when Hq / H <= 4, else 128; doubled while the
-                             merge below would overflow), else 8..128 and a
-                             multiple of 8.  With
-                             g = Hq / H, ceil(min(top_k, max_ctx) / 128) * g must
-                             not exceed 12288 (mkv_create: MKV_ERR_INVALID_ARG) */
+  int32_t attn_chunk;     /* split-K of the attention: selected tokens per slice.
+                             0 = auto: the B * H * min(top_k, T) selected
+                             positions are spread evenly over the resident
+                             attention CTAs (at least 32 per slice); else
+                             8..128 and a multiple of 8 (doubled while the
+                             merge below would overflow).  A stream then has
+                             at most ceil(min(top_k, max_ctx) / slice) + 1
+                             slices; with g = Hq / H, slices * g must not
+                             exceed 12288 (mkv_create: MKV_ERR_INVALID_ARG) */
   uint64_t max_pool_bytes;/* cap on the packed cache of one ctx; 0 = no cap */
   uint32_t flags;         /* MKV_FLAG_* */
   int32_t device;         /* CUDA device ordinal */
@@ -242,6 +245,14 @@ mkv_status mkv_check_device(mkv_ctx* ctx);
  * in-bounds accesses are reported as MKV_ERR_DEVICE_CHECK, which is how the
  * checks are tested without any out-of-bounds access. */
 mkv_status mkv_debug_wait_test(mkv_ctx* ctx, uint64_t limit_ns, mkv_stream_t stream);
+
+/* Measurement hook (no counterpart in the paper): which decode kernels are
+ * launched with programmatic dependent launch when no flag disables it.  Bit
+ * k (k = MKV_KERNEL_* id) enables it for kernel k; bit 8 keeps the kernels
+ * from signalling early (the next kernel then starts when they end).
+ * Default 0x1f.  Results do not depend on it.  MKV_ERR_INVALID_ARG for other
+ * bits. */
+mkv_status mkv_debug_set_pdl(mkv_ctx* ctx, uint32_t mask);
 mkv_status mkv_debug_set_check_extent(mkv_ctx* ctx, uint64_t bytes);
 
 /* With MKV_FLAG_KERNEL_TIMING: total device time (ms) and launch count of one

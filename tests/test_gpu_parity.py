@@ -65,9 +65,10 @@ def all_streams(w):
     return [(b, h) for b in range(w.batch) for h in range(w.n_kv_heads)]
 
 
-def _near_tie_budget(rep, name=None):
+def _near_tie_budget(rep, name=None, crowded=False):
     import os
-    assert_budgets(name or os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0], rep)
+    assert_budgets(name or os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0], rep,
+                   crowded)
 
 
 # ---------------------------------------------------------------------------
@@ -225,7 +226,8 @@ def test_many_candidates_one_bin_distinct_scores_cluster4(M):
         assert (bins == bins[0]).all(), "scores do not share one level-1 bin"
         assert len(np.unique(sc)) > 8192
     rep = check_streams(w, K, V, q, m, out, sel, all_streams(w), basis=False)
-    _near_tie_budget(rep)
+    # ~400 tokens per stream lie within 1e-4 of the k-th score here
+    _near_tie_budget(rep, crowded=True)
     m.close()
 
 

@@ -8,23 +8,34 @@
 namespace mkv {
 
 // ---------------------------------------------------------------------------
-// attn: split-K attention of the g query heads over a chunk of <= 128
-// selected tokens, reading the packed K/V rows in place (fp16 values + uint8
-// channel indices).  Row addresses of the chunk are resolved first.  Then a
-// group of 8 lanes serves a token, one 16-byte chunk (8 stored values) per
-// lane, and every thread fetches the chunks of its tokens together: K chunks
-// give partial logits (summed over the 8 lanes by a fixed butterfly), V
-// chunks are copied into a zeroed fp16 tile V[token][channel].  The softmax
-// weights p (fp32) are split into fp16 hi + 2^11 * lo parts, stored
-// transposed P[head][token], and o~ = P V runs on tensor cores (mma.sync,
-// fp32 accumulation, one accumulator per part): warp w owns channels
-// [32w, 32w + 32).  Partials per (stream, chunk, head): max logit m, sum of
-// exp l and the unnormalised output in the rotated V basis.
-// grid: (attn_chunks, BH), block 128, dynamic smem
+// attn: persistent split-K attention.  The selected tokens of all streams,
+// flattened in (stream, position) order, are cut into equal slices of
+// attn_per positions, one slice per CTA.  A CTA walks its slice in chunks of
+// up to 64 tokens that never cross a stream boundary (chunk = the 64-position
+// blocks of a stream, clipped to the slice).  Per chunk:
+//   issue   (stages - 1 chunks ahead) every lane of the token's 8-lane group
+//           reads the token id and its K and V segment headers, and copies
+//           its pieces of the two packed rows (16-byte value chunks, 8-byte
+//           channel lists) into the chunk's stage slot with cp.async;
+//   A       8 lanes per token: partial logits q~_i . k^_t over the lane's
+//           stored values (q~ indexed by the stored channel), summed over the
+//           group by a fixed butterfly; V values scattered into a zeroed fp16
+//           tile V[token][channel];
+//   B       per head (one warp each): online softmax over the CTA's tokens of
+//           the stream so far (running max m, sum l, factor alpha for the
+//           earlier output); weights split into fp16 hi + 2^11 * lo parts;
+//   C       per warp (8 output channels): o~ <- alpha o~ + P V on tensor cores
+//           (mma.sync, fp32 accumulation, one accumulator per part), then the
+//           warp clears its columns of the V tile.
+// At the end of its part of a stream the CTA writes one partial (m, l, o~ in
+// the rotated V basis); the merge kernel combines the partials of a stream.
+// Every sum has a fixed order, so the output is bit-for-bit repeatable.
+// grid: ceil(B H k / attn_per), block 512, dynamic smem at_smem_bytes()
 // ---------------------------------------------------------------------------
-constexpr int ATTN_THREADS = 128;
-constexpr int VLD = 136;            // halves per V tile row (272 B: ldmatrix without conflicts)
-constexpr int PLD = 136;            // halves per P row
+constexpr int AT_THREADS = 512;
+constexpr int AT_CHUNK = 64;        // tokens per chunk: 8 lanes each
+constexpr int AT_VLD = 136;         // halves per V tile row (272 B: ldmatrix without conflicts)
+constexpr int AT_PLD = 72;          // halves per P row (144 B)
 
 constexpr int32_t NO_IDX = (int32_t)0x80000000;
 
@@ -56,262 +67,322 @@ __device__ __forceinline__ uint64_t row_end(const uint2& m, int c) {
   return vend > iend ? vend : iend;
 }
 
-// tokens of a chunk rounded up to the mma K step
-__host__ __device__ constexpr int attn_rows16(int chunk) { return (chunk + 15) & ~15; }
-
-size_t attn_smem_bytes(int g, int chunk) {
-  const int gp = (g + 3) & ~3;
-  return (size_t)attn_rows16(chunk) * VLD * 2 + 2 * MAX_G * PLD * 2 + (size_t)chunk * 16 +
-         sizeof(float) * ((size_t)D * gp + (size_t)chunk * gp + 2 * g);
-}
-
 __device__ __forceinline__ int chan_of(const uint2& x, int e) {
   return (int)(((e < 4 ? x.x : x.y) >> (8 * (e & 3))) & 0x7fu);
 }
 
-// everything after the row addresses; GM = heads per instantiation (4 or 16)
-template <int GM>
-__device__ __forceinline__ void attn_body(const DecodeParams& p, int s, int chk, int n,
-                                          const uint4* __restrict__ meta,
-                                          __half* __restrict__ Vd, __half* __restrict__ Pt,
-                                          const float* __restrict__ qs, float* __restrict__ lg,
-                                          float* __restrict__ ml) {
-  const int g = p.g, gp = (g + 3) & ~3;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int cl = tid & 7, tg = tid >> 3;
+// Shared-memory carve-up of the attention kernel (byte offsets).
+struct AtLayout {
+  uint32_t stages, vt, ph, pl, qs, lg, meta, total;
+};
+
+__host__ __device__ inline AtLayout at_layout(int g, int slot, int nst) {
+  const int gp = (g + 3) & ~3;
+  AtLayout L;
+  L.stages = 0;
+  L.vt = L.stages + (uint32_t)nst * AT_CHUNK * slot;
+  L.ph = L.vt + AT_CHUNK * AT_VLD * 2;
+  L.pl = L.ph + MAX_G * AT_PLD * 2;
+  L.qs = L.pl + MAX_G * AT_PLD * 2;
+  L.lg = L.qs + D * gp * 4;
+  L.meta = L.lg + AT_CHUNK * gp * 4;
+  L.total = L.meta + (uint32_t)nst * AT_CHUNK * 16;
+  return L;
+}
+
+size_t at_smem_bytes(int g, int slot, int nst) { return at_layout(g, slot, nst).total; }
+
+// Chunk f (a 64-position block of a stream, in (stream, block) order) clipped
+// to the slice [lo, hi); false once the block starts at or after hi.
+struct AtChunk {
+  int s;        // stream
+  int j0;       // first position within the stream's selection
+  int n;        // tokens
+  bool last;    // the slice's last chunk of this stream
+};
+
+__device__ __forceinline__ bool at_chunk(int kk, int64_t lo, int64_t hi, int64_t f, AtChunk& c) {
+  const int nbs = (kk + AT_CHUNK - 1) / AT_CHUNK;
+  const int64_t s = f / nbs;
+  const int b = (int)(f - s * nbs);
+  const int64_t start = s * kk + (int64_t)AT_CHUNK * b;
+  const int64_t end = s * kk + min(AT_CHUNK * b + AT_CHUNK, kk);
+  const int64_t a = start > lo ? start : lo;
+  const int64_t e = end < hi ? end : hi;
+  if (a >= e) return false;
+  c.s = (int)s;
+  c.j0 = (int)(a - s * kk);
+  c.n = (int)(e - a);
+  c.last = (e == hi) || (b == nbs - 1);
+  return true;
+}
+
+// Issues the copies of chunk f into stage `st`: token tid / 8, lane tid % 8.
+__device__ __forceinline__ void at_issue(const DecodeParams& p, int64_t lo, int64_t hi, int64_t f,
+                                         int st, uint8_t* smem, const AtLayout& L) {
+  AtChunk ch;
+  if (!at_chunk(p.kk, lo, hi, f, ch)) return;
+  const int i = threadIdx.x >> 3, cl = threadIdx.x & 7;
+  if (i >= ch.n) return;
   const int c = p.c;
-  constexpr int U = 4;                          // tokens per thread per batch
-  const float scale = 0.08838834764831845f;     // 1 / sqrt(128)
-  // ---- logits and V tile: 8 lanes per token, 8 tokens per thread ---------
-  for (int base = 0; base < ATTN_THREADS / 16 && 16 * base < n; base += U) {
-    uint4 mt[U], kvv[U], vvv[U];
-    uint2 kix[U], vix[U];
+  const int s = ch.s;
+  const int64_t t = clamp_t(p.sel[(size_t)s * p.kk + ch.j0 + i], p.T);
+  uint2 km = row_meta(p.hdrK + (size_t)s * p.n_seg, t, p.S, c);
+  uint2 vm = row_meta(p.hdrV + (size_t)s * p.n_seg, t, p.S, c);
+  if (row_end(km, c) > p.pool_check || row_end(vm, c) > p.pool_check) {
+    // outside the checked pool extent: report it and read a stand-in row of
+    // c values with its channel list at pool offset 0 (inside every pool,
+    // and the size of a non-dense slot)
+    if (cl == 0) atomicOr(p.err, DEV_ERR_CHECK);
+    km = vm = make_uint2(0u, 0u);
+  }
+  const uint32_t slot = smem_u32(smem + L.stages) + (uint32_t)((st * AT_CHUNK + i) * p.at_slot);
+  const bool kd = (int32_t)km.y == NO_IDX, vd = (int32_t)vm.y == NO_IDX;
+  const int kn = kd ? D : c, vn = vd ? D : c;
+  const uint8_t* kv = p.pool + (uint64_t)km.x * 16u;
+  const uint8_t* vv = p.pool + (uint64_t)vm.x * 16u;
+  const uint32_t vs = slot + p.at_kv + p.at_ki;
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int i = tg + 16 * (base + u);
-      mt[u] = i < n ? meta[i] : make_uint4(0u, (uint32_t)NO_IDX, 0u, (uint32_t)NO_IDX);
-      kvv[u] = vvv[u] = make_uint4(0u, 0u, 0u, 0u);
-      kix[u] = vix[u] = make_uint2(0u, 0u);
-      if (i < n) {
-        const bool kd = (int32_t)mt[u].y == NO_IDX, vd = (int32_t)mt[u].w == NO_IDX;
-        const uint8_t* kp = p.pool + (uint64_t)mt[u].x * 16u;
-        const uint8_t* vp = p.pool + (uint64_t)mt[u].z * 16u;
-        if (8 * cl < (kd ? D : c)) {
-          kvv[u] = ld_cg_u4(kp + 16 * cl);
-          if (!kd) kix[u] = ld_cg_u2(kp + 8 * (int64_t)(int32_t)mt[u].y + 8 * cl);
-        }
-        if (8 * cl < (vd ? D : c)) {
-          vvv[u] = ld_cg_u4(vp + 16 * cl);
-          if (!vd) vix[u] = ld_cg_u2(vp + 8 * (int64_t)(int32_t)mt[u].w + 8 * cl);
-        }
-      }
+  for (int ck = cl; ck < 16; ck += 8) {
+    if (8 * ck < kn) {
+      cpa16(slot + 16 * ck, kv + 16 * ck);
+      if (!kd) cpa8(slot + p.at_kv + 8 * ck, kv + 8 * (int64_t)(int32_t)km.y + 8 * ck);
     }
+    if (8 * ck < vn) {
+      cpa16(vs + 16 * ck, vv + 16 * ck);
+      if (!vd) cpa8(vs + p.at_vv + 8 * ck, vv + 8 * (int64_t)(int32_t)vm.y + 8 * ck);
+    }
+  }
+  if (cl == 0)
+    reinterpret_cast<uint4*>(smem + L.meta)[st * AT_CHUNK + i] = make_uint4(km.x, km.y, vm.x, vm.y);
+}
+
+template <int NST>
+__global__ void __launch_bounds__(AT_THREADS, 2) attn_kernel(DecodeParams p) {
+  extern __shared__ __align__(128) uint8_t at_smem[];
+  __shared__ float s_m[MAX_G], s_l[MAX_G], s_alpha[MAX_G];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tok = tid >> 3, cl = tid & 7;
+  const int g = p.g, gp = (g + 3) & ~3, c = p.c;
+  const AtLayout L = at_layout(g, p.at_slot, NST);
+  __half* Vt = reinterpret_cast<__half*>(at_smem + L.vt);
+  __half* Ph = reinterpret_cast<__half*>(at_smem + L.ph);
+  __half* Pl = reinterpret_cast<__half*>(at_smem + L.pl);
+  float* qs = reinterpret_cast<float*>(at_smem + L.qs);
+  float* lg = reinterpret_cast<float*>(at_smem + L.lg);
+  const uint4* meta = reinterpret_cast<const uint4*>(at_smem + L.meta);
+  const int64_t N = (int64_t)p.B * p.H * p.kk;
+  const int64_t lo = (int64_t)blockIdx.x * p.attn_per;
+  const int64_t hi = lo + p.attn_per < N ? lo + p.attn_per : N;
+
+  // prologue (shared memory only): zero the V tile and both P parts
+  {
+    uint4* z = reinterpret_cast<uint4*>(at_smem + L.vt);
+    const int nz = (int)((L.qs - L.vt) / 16);
+    for (int x = tid; x < nz; x += AT_THREADS) z[x] = make_uint4(0u, 0u, 0u, 0u);
+    if (tid < MAX_G) {
+      s_m[tid] = -INFINITY;
+      s_l[tid] = 0.f;
+    }
+  }
+  griddep_wait();     // the selection comes from the kernel before this one
+  if (p.pdl_trigger) griddep_launch();
+  if (lo >= N) return;
+  const int nbs = (p.kk + AT_CHUNK - 1) / AT_CHUNK;
+  const int64_t f0 = (lo / p.kk) * nbs + (lo % p.kk) / AT_CHUNK;
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int i = tg + 16 * (base + u);
-      const bool kd = (int32_t)mt[u].y == NO_IDX, vd = (int32_t)mt[u].w == NO_IDX;
-      const int kn = kd ? D : c, vn = vd ? D : c;
-      float part[GM];
+  for (int n = 0; n < NST - 1; ++n) {
+    at_issue(p, lo, hi, f0 + n, n, at_smem, L);
+    cpa_commit();
+  }
+  const float scale = 0.08838834764831845f;     // 1 / sqrt(128)
+  const int mm = lane >> 3, r8 = lane & 7;
+  const int n0 = warp * 8;                       // this warp's output channels in phase C
+  float acc_h[4] = {0.f, 0.f, 0.f, 0.f}, acc_l[4] = {0.f, 0.f, 0.f, 0.f};
+  int cur_s = -1;
+  for (int n = 0;; ++n) {
+    AtChunk ch;
+    if (!at_chunk(p.kk, lo, hi, f0 + n, ch)) break;
+    at_issue(p, lo, hi, f0 + n + NST - 1, (n + NST - 1) % NST, at_smem, L);
+    cpa_commit();
+    cpa_wait<NST - 1>();
+    __syncthreads();
+    const int st = n % NST;
+    if (ch.s != cur_s) {
+      cur_s = ch.s;
+      const int b = ch.s / p.H, h = ch.s % p.H;
+      const float* qt = p.qt + ((size_t)b * p.Hq + (size_t)h * g) * D;
+      for (int x = tid; x < D * gp; x += AT_THREADS) {
+        const int chn = x / gp, hh = x % gp;
+        qs[x] = hh < g ? qt[hh * D + chn] : 0.f;
+      }
+      __syncthreads();
+    }
+    // ---- A: logits and the V tile --------------------------------------------
+    {
+      const bool valid = tok < ch.n;
+      const uint4 mt = valid ? meta[st * AT_CHUNK + tok] : make_uint4(0u, 0u, 0u, 0u);
+      const uint8_t* slot = at_smem + L.stages + (size_t)(st * AT_CHUNK + tok) * p.at_slot;
+      const bool kd = (int32_t)mt.y == NO_IDX, vd = (int32_t)mt.w == NO_IDX;
+      const int kn = valid ? (kd ? D : c) : 0, vn = valid ? (vd ? D : c) : 0;
+      for (int h4 = 0; h4 < gp; h4 += 4) {
+        float part[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int hh = 0; hh < GM; ++hh) part[hh] = 0.f;
-      if (i < n) {
-        // rows with more than 64 stored values (dense, or c > 64) have chunks 8..15
         for (int ck = cl; ck < 16; ck += 8) {
-          uint4 kr = kvv[u], vr = vvv[u];
-          uint2 kx = kix[u], vx = vix[u];
-          if (ck >= 8) {
-            if (8 * ck >= kn && 8 * ck >= vn) break;
-            const uint8_t* kp = p.pool + (uint64_t)mt[u].x * 16u;
-            const uint8_t* vp = p.pool + (uint64_t)mt[u].z * 16u;
-            kr = vr = make_uint4(0u, 0u, 0u, 0u);
-            kx = vx = make_uint2(0u, 0u);
-            if (8 * ck < kn) {
-              kr = ld_cg_u4(kp + 16 * ck);
-              if (!kd) kx = ld_cg_u2(kp + 8 * (int64_t)(int32_t)mt[u].y + 8 * ck);
-            }
-            if (8 * ck < vn) {
-              vr = ld_cg_u4(vp + 16 * ck);
-              if (!vd) vx = ld_cg_u2(vp + 8 * (int64_t)(int32_t)mt[u].w + 8 * ck);
-            }
-          }
-          if (8 * ck < vn) {
-            const __half* hv = reinterpret_cast<const __half*>(&vr);
-            __half* vrow = Vd + (size_t)i * VLD;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) vrow[vd ? 8 * ck + e : chan_of(vx, e)] = hv[e];
-          }
           if (8 * ck < kn) {
+            const uint4 kr = *reinterpret_cast<const uint4*>(slot + 16 * ck);
+            const uint2 kx = kd ? make_uint2(0u, 0u)
+                                : *reinterpret_cast<const uint2*>(slot + p.at_kv + 8 * ck);
             float v[8];
             h8_to_f(kr, v);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-              const float* qq = qs + (kd ? 8 * ck + e : chan_of(kx, e)) * gp;
-#pragma unroll
-              for (int h4 = 0; h4 < GM; h4 += 4) {
-                if (h4 < g) {
-                  const float4 q4 = *reinterpret_cast<const float4*>(qq + h4);
-                  part[h4] = fmaf(q4.x, v[e], part[h4]);
-                  part[h4 + 1] = fmaf(q4.y, v[e], part[h4 + 1]);
-                  part[h4 + 2] = fmaf(q4.z, v[e], part[h4 + 2]);
-                  part[h4 + 3] = fmaf(q4.w, v[e], part[h4 + 3]);
-                }
-              }
+              const int chn = kd ? 8 * ck + e : chan_of(kx, e);
+              const float4 q4 = *reinterpret_cast<const float4*>(qs + chn * gp + h4);
+              part[0] = fmaf(q4.x, v[e], part[0]);
+              part[1] = fmaf(q4.y, v[e], part[1]);
+              part[2] = fmaf(q4.z, v[e], part[2]);
+              part[3] = fmaf(q4.w, v[e], part[3]);
             }
           }
         }
-      }
-      // sum over the token's 8 lanes (fixed butterfly order)
 #pragma unroll
-      for (int hh = 0; hh < GM; ++hh) {
-        if (hh < gp) {
-          float x = part[hh];
+        for (int k = 0; k < 4; ++k) {
+          float x = part[k];
           x += __shfl_xor_sync(0xffffffffu, x, 1);
           x += __shfl_xor_sync(0xffffffffu, x, 2);
           x += __shfl_xor_sync(0xffffffffu, x, 4);
-          if (cl == 0 && i < n) lg[i * gp + hh] = x * scale;
+          part[k] = x;
+        }
+        if (valid && cl == 0)
+          *reinterpret_cast<float4*>(lg + tok * gp + h4) =
+              make_float4(part[0] * scale, part[1] * scale, part[2] * scale, part[3] * scale);
+      }
+#pragma unroll
+      for (int ck = cl; ck < 16; ck += 8) {
+        if (8 * ck < vn) {
+          const uint8_t* vs = slot + p.at_kv + p.at_ki;
+          const uint4 vr = *reinterpret_cast<const uint4*>(vs + 16 * ck);
+          const uint2 vx = vd ? make_uint2(0u, 0u)
+                              : *reinterpret_cast<const uint2*>(vs + p.at_vv + 8 * ck);
+          const __half* hv = reinterpret_cast<const __half*>(&vr);
+          __half* vrow = Vt + tok * AT_VLD;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) vrow[vd ? 8 * ck + e : chan_of(vx, e)] = hv[e];
+        }
+      }
+    }
+    __syncthreads();
+    // ---- B: online softmax, one warp per head ----------------------------------
+    if (warp < g) {
+      const int hh = warp;
+      float mloc = -INFINITY;
+      for (int i = lane; i < ch.n; i += 32) mloc = fmaxf(mloc, lg[i * gp + hh]);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1)
+        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, off));
+      const float m_old = s_m[hh];
+      const float m_new = fmaxf(m_old, mloc);
+      const float alpha = expf(m_old - m_new);
+      float lsum = 0.f;
+      for (int i = lane; i < AT_CHUNK; i += 32) {
+        const float e = i < ch.n ? expf(lg[i * gp + hh] - m_new) : 0.f;
+        const __half hi = __float2half_rn(e);
+        Ph[hh * AT_PLD + i] = hi;
+        Pl[hh * AT_PLD + i] = __float2half_rn((e - __half2float(hi)) * 2048.f);
+        lsum += e;
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+      if (lane == 0) {
+        s_alpha[hh] = alpha;
+        s_m[hh] = m_new;
+        s_l[hh] = fmaf(s_l[hh], alpha, lsum);
+      }
+    }
+    __syncthreads();
+    // ---- C: o~ <- alpha o~ + P V, warp w owns channels [8w, 8w + 8) -------------
+    {
+      const int r0 = lane >> 2;
+      const float a0 = r0 < g ? s_alpha[r0] : 1.f;
+      const float a1 = r0 + 8 < g ? s_alpha[r0 + 8] : 1.f;
+      acc_h[0] *= a0;
+      acc_h[1] *= a0;
+      acc_h[2] *= a1;
+      acc_h[3] *= a1;
+      acc_l[0] *= a0;
+      acc_l[1] *= a0;
+      acc_l[2] *= a1;
+      acc_l[3] *= a1;
+      const uint32_t ph = smem_u32(Ph), pl = smem_u32(Pl), vt = smem_u32(Vt);
+      const int ksteps = (ch.n + 15) >> 4;
+      for (int ks = 0; ks < ksteps; ++ks) {
+        const int k0 = ks * 16;
+        uint32_t ah[4], al[4], bb[2];
+        const uint32_t aoff = (uint32_t)(((r8 + (mm & 1) * 8) * AT_PLD + k0 + (mm >> 1) * 8) * 2);
+        ldsm_x4(ph + aoff, ah);
+        ldsm_x4(pl + aoff, al);
+        ldsm_x2_t(vt + (uint32_t)(((k0 + (lane & 15)) * AT_VLD + n0) * 2), bb);
+        mma16816(acc_h, ah, bb[0], bb[1]);
+        mma16816(acc_l, al, bb[0], bb[1]);
+      }
+      // clear this warp's columns of the V tile for the next chunk
+      *reinterpret_cast<uint4*>(Vt + lane * AT_VLD + n0) = make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(Vt + (lane + 32) * AT_VLD + n0) = make_uint4(0u, 0u, 0u, 0u);
+      if (ch.last) {
+        // the slice's part of this stream is done: write its partial
+        const int first = (int)(((int64_t)ch.s * p.kk) / p.attn_per);
+        const size_t pbase = ((size_t)ch.s * p.attn_mp + (blockIdx.x - first)) * g;
+        const int col = n0 + 2 * (lane & 3);
+        if (r0 < g)
+          *reinterpret_cast<float2*>(p.part_o + (pbase + r0) * D + col) =
+              make_float2(fmaf(acc_l[0], 1.f / 2048.f, acc_h[0]),
+                          fmaf(acc_l[1], 1.f / 2048.f, acc_h[1]));
+        if (r0 + 8 < g)
+          *reinterpret_cast<float2*>(p.part_o + (pbase + r0 + 8) * D + col) =
+              make_float2(fmaf(acc_l[2], 1.f / 2048.f, acc_h[2]),
+                          fmaf(acc_l[3], 1.f / 2048.f, acc_h[3]));
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc_h[e] = acc_l[e] = 0.f;
+        if (warp < g && lane == 0) {
+          p.part_ml[(pbase + warp) * 2] = s_m[warp];
+          p.part_ml[(pbase + warp) * 2 + 1] = s_l[warp];
+          s_m[warp] = -INFINITY;
+          s_l[warp] = 0.f;
         }
       }
     }
   }
-  __syncthreads();
-  // ---- softmax per head (warp per head, fixed-order reductions); weights go
-  // to P[head][token] as fp16 hi and 2^11 * (p - hi) ----------------------
-  __half* Ph = Pt;
-  __half* Pl = Pt + MAX_G * PLD;
-  for (int hh = warp; hh < g; hh += ATTN_THREADS / 32) {
-    float m = -INFINITY;
-    for (int i = lane; i < n; i += 32) m = fmaxf(m, lg[i * gp + hh]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    float l = 0.f;
-    for (int i = lane; i < n; i += 32) {
-      const float e = expf(lg[i * gp + hh] - m);
-      const __half hi = __float2half_rn(e);
-      Ph[hh * PLD + i] = hi;
-      Pl[hh * PLD + i] = __float2half_rn((e - __half2float(hi)) * 2048.f);
-      l += e;
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-    if (lane == 0) {
-      ml[hh * 2] = m;
-      ml[hh * 2 + 1] = l;
-    }
-  }
-  __syncthreads();
-  // ---- o~ = P V on tensor cores: warp w, channels [32w, 32w + 32) ----------
-  float ch_[4][4], cl_[4][4];
-#pragma unroll
-  for (int a = 0; a < 4; ++a)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) ch_[a][e] = cl_[a][e] = 0.f;
-  const int mm = lane >> 3, r8 = lane & 7;
-  const uint32_t ph = smem_u32(Ph), pl = smem_u32(Pl), vd = smem_u32(Vd);
-  const int ksteps = (n + 15) >> 4;
-  for (int ks = 0; ks < ksteps; ++ks) {
-    const int k0 = ks * 16;
-    uint32_t ah[4], al[4];
-    const uint32_t aoff = (uint32_t)(((r8 + (mm & 1) * 8) * PLD + k0 + (mm >> 1) * 8) * 2);
-    ldsm_x4(ph + aoff, ah);
-    ldsm_x4(pl + aoff, al);
-#pragma unroll
-    for (int np = 0; np < 2; ++np) {
-      uint32_t bb[4];
-      const int row = k0 + (mm & 1) * 8 + r8;
-      const int col = warp * 32 + np * 16 + (mm >> 1) * 8;
-      ldsm_x4_t(vd + (uint32_t)((row * VLD + col) * 2), bb);
-      mma16816(ch_[2 * np], ah, bb[0], bb[1]);
-      mma16816(ch_[2 * np + 1], ah, bb[2], bb[3]);
-      mma16816(cl_[2 * np], al, bb[0], bb[1]);
-      mma16816(cl_[2 * np + 1], al, bb[2], bb[3]);
-    }
-  }
-  const size_t pbase = ((size_t)s * p.attn_chunks + chk) * g;
-  const int h0 = lane >> 2, c0 = warp * 32 + 2 * (lane & 3);
-#pragma unroll
-  for (int nt = 0; nt < 4; ++nt) {
-    const int chn = c0 + nt * 8;
-    if (h0 < g)
-      *reinterpret_cast<float2*>(p.part_o + (pbase + h0) * D + chn) =
-          make_float2(fmaf(cl_[nt][0], 1.f / 2048.f, ch_[nt][0]),
-                      fmaf(cl_[nt][1], 1.f / 2048.f, ch_[nt][1]));
-    if (h0 + 8 < g)
-      *reinterpret_cast<float2*>(p.part_o + (pbase + h0 + 8) * D + chn) =
-          make_float2(fmaf(cl_[nt][2], 1.f / 2048.f, ch_[nt][2]),
-                      fmaf(cl_[nt][3], 1.f / 2048.f, ch_[nt][3]));
-  }
-  if (tid < 2 * g) p.part_ml[pbase * 2 + tid] = ml[tid];
+  cpa_wait<0>();
 }
 
-// GM: heads per instantiation (4 or 16); MINB: resident CTAs per SM asked of
-// the register allocator (6 for chunks of <= 64 tokens and g <= 4).
-template <int GM, int MINB>
-__global__ void __launch_bounds__(ATTN_THREADS, MINB) attn_kernel(DecodeParams p) {
-  extern __shared__ __align__(16) uint8_t asm_[];
-  const int s = blockIdx.y, chk = blockIdx.x;
-  const int b = s / p.H, h = s % p.H;
-  const int g = p.g, gp = (g + 3) & ~3;
-  const int tid = threadIdx.x;
-  const int CH = p.attn_chunk;
-  const int R16 = attn_rows16(CH);
-  __half* Vd = reinterpret_cast<__half*>(asm_);                                // [R16][VLD]
-  __half* Pt = Vd + (size_t)R16 * VLD;                                         // [2][16][PLD]
-  uint4* meta = reinterpret_cast<uint4*>(Pt + 2 * MAX_G * PLD);               // [CH]
-  float* qs = reinterpret_cast<float*>(meta + CH);                             // [128][gp]
-  float* lg = qs + D * gp;                                                     // [CH][gp]
-  float* ml = lg + CH * gp;                                                    // [g][2]
-  const float* qt = p.qt + ((size_t)b * p.Hq + (size_t)h * g) * D;
-  for (int x = tid; x < D * gp; x += ATTN_THREADS) {
-    const int chn = x / gp, hh = x % gp;
-    qs[x] = hh < g ? qt[hh * D + chn] : 0.f;
-  }
-  {
-    // the V tile and both P parts start at zero (rows past n, heads past g)
-    uint4* z = reinterpret_cast<uint4*>(Vd);
-    const int nz = (R16 * VLD + 2 * MAX_G * PLD) / 8;
-    for (int x = tid; x < nz; x += ATTN_THREADS) z[x] = make_uint4(0u, 0u, 0u, 0u);
-  }
-  const int j0 = chk * CH;
-  const int n = min(CH, p.kk - j0);
-  // q~ (from the rotation kernel, two launches back) and the ctx's headers
-  // are ready; the selection is not
-  griddep_wait();
-  griddep_launch();
-  if (tid < n) {
-    const int64_t t = clamp_t(p.sel[(size_t)s * p.kk + j0 + tid], p.T);
-    uint2 km = row_meta(p.hdrK + (size_t)s * p.n_seg, t, p.S, p.c);
-    uint2 vm = row_meta(p.hdrV + (size_t)s * p.n_seg, t, p.S, p.c);
-    if (row_end(km, p.c) > p.pool_check || row_end(vm, p.c) > p.pool_check) {
-      // outside the checked pool extent: report it and read a dense row at
-      // offset 0 instead (inside every pool)
-      atomicOr(p.err, DEV_ERR_CHECK);
-      km = vm = make_uint2(0u, (uint32_t)NO_IDX);
-    }
-    meta[tid] = make_uint4(km.x, km.y, vm.x, vm.y);
-  }
-  __syncthreads();
-  attn_body<GM>(p, s, chk, n, meta, Vd, Pt, qs, lg, ml);
+// Slices that cover stream s's selection: the first one and how many.
+__device__ __forceinline__ int at_first_part(const DecodeParams& p, int s) {
+  return (int)(((int64_t)s * p.kk) / p.attn_per);
+}
+__device__ __forceinline__ int at_num_parts(const DecodeParams& p, int s) {
+  return (int)((((int64_t)s + 1) * p.kk - 1) / p.attn_per) - at_first_part(p, s) + 1;
 }
 
 // ---------------------------------------------------------------------------
-// merge: log-sum-exp merge of the chunk partials, then o = o~ R_V^T.  CTA
+// merge: log-sum-exp merge of a stream's partials, then o = o~ R_V^T.  CTA
 // (s, q) writes output rows [32q, 32q + 32) of every head of stream s; the
 // weights and the merged o~ are recomputed by each of the four CTAs (from
 // L2), and the 32 rows of R_V are staged transposed in shared memory.
-// grid: (BH, 4), block 128, dynamic smem: chunk weights
+// grid: (BH, 4), block 128, dynamic smem: partial weights
 // ---------------------------------------------------------------------------
 constexpr int MG_THREADS = 128;
 constexpr int MG_ROWS = 32;
 constexpr int MG_LD = MG_ROWS + 1;
 
 __global__ void __launch_bounds__(MG_THREADS) merge_kernel(DecodeParams p) {
-  extern __shared__ __align__(16) float wsm[];     // [attn_chunks][g] weights
+  extern __shared__ __align__(16) float wsm[];     // [parts][g] weights
   __shared__ float Rt[D * MG_LD];                  // Rt[j][rr] = R_V[32q + rr][j]
   __shared__ __align__(16) float ot[MAX_G][D];
   __shared__ float Linv[MAX_G];
   const int s = blockIdx.x, r0 = blockIdx.y * MG_ROWS;
   const int b = s / p.H, h = s % p.H;
-  const int g = p.g, nc = p.attn_chunks;
+  const int g = p.g;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   {
     const float4* R4 = reinterpret_cast<const float4*>(p.RV + ((size_t)s * D + r0) * D);
@@ -327,17 +398,19 @@ __global__ void __launch_bounds__(MG_THREADS) merge_kernel(DecodeParams p) {
     }
   }
   griddep_wait();     // the partials come from the attention kernel
-  griddep_launch();
-  // weights exp(m_c - M) and 1 / L per head: warp per head, lanes over chunks
-  const float2* ml = reinterpret_cast<const float2*>(p.part_ml + (size_t)s * nc * g * 2);
+  if (p.pdl_trigger) griddep_launch();
+  const int nc = at_num_parts(p, s);
+  const size_t base = (size_t)s * p.attn_mp * g;
+  // weights exp(m_c - M) and 1 / L per head: warp per head, lanes over parts
+  const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + base;
   for (int hh = warp; hh < g; hh += MG_THREADS / 32) {
     float M = -INFINITY;
-    for (int c = lane; c < nc; c += 32) M = fmaxf(M, __ldg(ml + c * g + hh).x);
+    for (int c = lane; c < nc; c += 32) M = fmaxf(M, __ldcg(ml + c * g + hh).x);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     float L = 0.f;
     for (int c = lane; c < nc; c += 32) {
-      const float2 v = __ldg(ml + c * g + hh);
+      const float2 v = __ldcg(ml + c * g + hh);
       const float w = expf(v.x - M);
       wsm[c * g + hh] = w;
       L = fmaf(v.y, w, L);
@@ -347,12 +420,11 @@ __global__ void __launch_bounds__(MG_THREADS) merge_kernel(DecodeParams p) {
     if (lane == 0) Linv[hh] = 1.f / L;
   }
   __syncthreads();
-  const float* po = p.part_o + (size_t)s * nc * g * D;
+  const float* po = p.part_o + base * D;
   for (int x = tid; x < g * D; x += MG_THREADS) {
     const int hh = x / D;
     float o = 0.f;
-#pragma unroll 32
-    for (int c = 0; c < nc; ++c) o = fmaf(__ldg(po + (size_t)c * g * D + x), wsm[c * g + hh], o);
+    for (int c = 0; c < nc; ++c) o = fmaf(__ldcg(po + (size_t)c * g * D + x), wsm[c * g + hh], o);
     ot[hh][x % D] = o * Linv[hh];
   }
   __syncthreads();
@@ -370,31 +442,51 @@ __global__ void __launch_bounds__(MG_THREADS) merge_kernel(DecodeParams p) {
   }
 }
 
+cudaError_t attn_shape(int g, int slot, int* stages, int* ctas_per_sm) {
+  // four stages when two CTAs still fit an SM, else fewer
+  int nst = 2;
+  for (int n = 4; n > 2; --n)
+    if (at_smem_bytes(g, slot, n) <= 113 * 1024) {
+      nst = n;
+      break;
+    }
+  const size_t smem = at_smem_bytes(g, slot, nst);
+  int occ = 0;
+  cudaError_t e;
+  if (nst == 4) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, attn_kernel<4>, AT_THREADS, smem);
+  else if (nst == 3) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, attn_kernel<3>, AT_THREADS, smem);
+  else e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, attn_kernel<2>, AT_THREADS, smem);
+  if (e != cudaSuccess) return e;
+  *stages = nst;
+  *ctas_per_sm = occ > 0 ? occ : 1;
+  return cudaSuccess;
+}
+
 cudaError_t prepare_attn_kernels() {
-  const int mx = (int)attn_smem_bytes(MAX_G, ATTN_MAX_CHUNK);
-  cudaError_t e = cudaFuncSetAttribute(attn_kernel<4, 6>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+  const int mx = 227 * 1024;
+  cudaError_t e = cudaFuncSetAttribute(attn_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(attn_kernel<4, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    e = cudaFuncSetAttribute(attn_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(attn_kernel<MAX_G, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    e = cudaFuncSetAttribute(attn_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
   if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               48 * 1024 + 4 * 1024);
 }
 
 cudaError_t launch_attn(const DecodeParams& p, cudaStream_t st) {
-  dim3 grid(p.attn_chunks, p.B * p.H);
-  const size_t smem = attn_smem_bytes(p.g, p.attn_chunk);
-  const bool pdl = p.pdl != 0;
-  if (p.g <= 4 && p.attn_chunk <= 64)
-    return launch_kernel(attn_kernel<4, 6>, grid, dim3(ATTN_THREADS), smem, st, pdl, 0, p);
-  if (p.g <= 4) return launch_kernel(attn_kernel<4, 4>, grid, dim3(ATTN_THREADS), smem, st, pdl, 0, p);
-  return launch_kernel(attn_kernel<MAX_G, 4>, grid, dim3(ATTN_THREADS), smem, st, pdl, 0, p);
+  const size_t smem = at_smem_bytes(p.g, p.at_slot, p.at_stages);
+  const dim3 grid(p.attn_ctas), block(AT_THREADS);
+  const bool pdl = ((p.pdl >> MKV_KERNEL_ATTN) & 1) != 0;
+  if (p.at_stages >= 4) return launch_kernel(attn_kernel<4>, grid, block, smem, st, pdl, 0, p);
+  if (p.at_stages == 3) return launch_kernel(attn_kernel<3>, grid, block, smem, st, pdl, 0, p);
+  return launch_kernel(attn_kernel<2>, grid, block, smem, st, pdl, 0, p);
 }
 
 cudaError_t launch_merge(const DecodeParams& p, cudaStream_t st) {
   return launch_kernel(merge_kernel, dim3(p.B * p.H, D / MG_ROWS), dim3(MG_THREADS),
-                       sizeof(float) * (size_t)p.attn_chunks * p.g, st, p.pdl != 0, 0, p);
+                       sizeof(float) * (size_t)p.attn_mp * p.g, st,
+                       ((p.pdl >> MKV_KERNEL_MERGE) & 1) != 0, 0, p);
 }
 
 }  // namespace mkv

@@ -712,8 +712,13 @@ __global__ void __launch_bounds__(1024) scan_kernel(CompressParams p) {
   unsigned long long wb = 0;
   for (int w = 0; w < warp; ++w) wb += ws[w];
   unsigned long long off = wb + inc - mine;
+  __shared__ unsigned int n_dense[2];
+  if (tid < 2) n_dense[tid] = 0u;
+  __syncthreads();
+  const int64_t per_x = (int64_t)p.BH * p.n_seg;
   for (int64_t e = lo; e < hi; ++e) {
     const SegInfo si = p.seg[e];
+    if (si.strategy == MKV_STRATEGY_DENSE) atomicAdd(&n_dense[e >= per_x ? 1 : 0], 1u);
     mkv_segment_header h;
     h.off16 = (uint32_t)(off >> 4);
     h.strategy = si.strategy;
@@ -722,7 +727,9 @@ __global__ void __launch_bounds__(1024) scan_kernel(CompressParams p) {
     p.hdr[e] = h;
     off += si.size;
   }
-  if (tid == 1023) *p.total = wb + inc;
+  __syncthreads();
+  if (tid == 1023) p.total[0] = wb + inc;
+  if (tid < 2) p.total[1 + tid] = n_dense[tid];
 }
 
 // ---------------------------------------------------------------------------

@@ -37,7 +37,7 @@ __global__ void __launch_bounds__(QR_THREADS) qrot_kernel(DecodeParams p) {
   // R_K belongs to the ctx; q and the step's buffers may still be in use by
   // the kernel before this one
   griddep_wait();
-  griddep_launch();
+  if (p.pdl_trigger) griddep_launch();
   const __half* q = p.q + ((size_t)b * p.Hq + (size_t)h * p.g) * D;
   for (int x = tid; x < p.g * D; x += QR_THREADS) qs[x / D][x % D] = __half2float(q[x]);
   uint4* hz = reinterpret_cast<uint4*>(p.hist + (size_t)s * HIST1);
@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
   const int a = p.part[blockIdx.x], b = p.part[blockIdx.x + 1];
   if (a >= b) {
     griddep_wait();
-    griddep_launch();
+    if (p.pdl_trigger) griddep_launch();
     return;
   }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
   } else {
     // ---- consumers ----------------------------------------------------------
     griddep_wait();
-    if (warp == 0) griddep_launch();
+    if (warp == 0 && p.pdl_trigger) griddep_launch();
     for (int x = tid; x < SC_NSLOT * D; x += SC_CONS * 32) {
       const int s = s_first + x / D;
       (&qb[0][0])[x] = (s <= s_last) ? p.qbar[(size_t)s * D + (x % D)] : 0.f;
@@ -530,16 +530,15 @@ cudaError_t launch_partition(const mkv_segment_header* hdrK, int n_streams, int 
 
 cudaError_t launch_qrot(const DecodeParams& p, cudaStream_t st) {
   return launch_kernel(qrot_kernel, dim3(p.B * p.H), dim3(QR_THREADS), (size_t)D * D * 4, st,
-                       p.pdl != 0, 0, p);
+                       ((p.pdl >> MKV_KERNEL_QROT) & 1) != 0, 0, p);
 }
 
 cudaError_t launch_score(const DecodeParams& p, cudaStream_t st) {
   const size_t smem = sc_slot(p.stage_bytes) * p.n_stages;
+  const bool pdl = ((p.pdl >> MKV_KERNEL_SCORE) & 1) != 0;
   switch (p.c >> 3) {
-#define MKV_SCORE_CASE(N)                                                                   \
-  case N:                                                                                 \
-    return launch_kernel(score_kernel<N>, dim3(p.G), dim3(SC_THREADS), smem, st, p.pdl != 0, \
-                         0, p);
+#define MKV_SCORE_CASE(N) \
+  case N: return launch_kernel(score_kernel<N>, dim3(p.G), dim3(SC_THREADS), smem, st, pdl, 0, p);
     MKV_SCORE_CASE(1) MKV_SCORE_CASE(2) MKV_SCORE_CASE(3) MKV_SCORE_CASE(4) MKV_SCORE_CASE(5)
     MKV_SCORE_CASE(6) MKV_SCORE_CASE(7) MKV_SCORE_CASE(8) MKV_SCORE_CASE(9) MKV_SCORE_CASE(10)
     MKV_SCORE_CASE(11) MKV_SCORE_CASE(12) MKV_SCORE_CASE(13) MKV_SCORE_CASE(14)

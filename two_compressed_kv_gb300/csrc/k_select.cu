@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) select_kernel(DecodeParams p) 
   const int R = (int)cl.num_blocks(), r = (int)cl.block_rank();
   const int s = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   griddep_wait();     // scores and the level-1 state come from the score kernel
-  griddep_launch();
+  if (p.pdl_trigger) griddep_launch();
   SelGeom geo;
   geo.per = (((p.Tp + R - 1) / R) + 15) / 16 * 16;
   geo.T = p.T;
@@ -404,7 +404,7 @@ cudaError_t prepare_select_kernels() {
 
 cudaError_t launch_topk(const DecodeParams& p, cudaStream_t st) {
   return launch_kernel(select_kernel, dim3(p.sel_R, p.B * p.H, 1), dim3(SEL_THREADS), SEL_SMEM,
-                       st, p.pdl != 0, p.sel_R, p);
+                       st, ((p.pdl >> MKV_KERNEL_TOPK) & 1) != 0, p.sel_R, p);
 }
 
 }  // namespace mkv

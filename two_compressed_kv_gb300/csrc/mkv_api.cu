@@ -16,7 +16,8 @@ using namespace mkv;
 namespace {
 
 constexpr int kSMs = 152;          // GB300
-constexpr int64_t kMergeMaxWeights = 12288;   // 48 KB of fp32 (chunk, head) weights
+constexpr int64_t kMergeMaxWeights = 12288;   // 48 KB of fp32 (slice, head) weights
+constexpr int64_t kMinSlice = 32;              // smallest automatic attention slice
 thread_local std::string g_last_error = "no error";
 
 mkv_status cuda_fail(cudaError_t e, const char* what) {
@@ -49,8 +50,10 @@ struct mkv_ctx {
   int64_t max_seg = 0;
   int kk_max = 0;
   int gram_chunks_max = 0;
-  int attn_chunk = 128;
-  int attn_chunks_max = 0;
+  int64_t attn_per_fixed = 0;      // mkv_config.attn_chunk (0 = spread over the SMs)
+  int attn_mp = 0;                 // partial slots per stream
+  int at_stages = 2, at_ctas_per_sm = 1;
+  int at_kv = 0, at_ki = 0, at_vv = 0, at_vi = 0;
   int64_t Tp_max = 0;              // padded row stride of scores / candidates
   int G = 0;                       // score-kernel CTAs (one per SM)
   int stage_bytes = 0, n_stages = 0;
@@ -71,6 +74,7 @@ struct mkv_ctx {
   uint64_t pool_cap = 0;
   uint64_t pool_need = 0;          // bytes of the live cache's pool (packed size + tail pad)
   uint64_t check_override = 0;     // test hook: a smaller checked pool extent (0 = none)
+  uint32_t pdl_mask = 0x1f;        // test hook: decode kernels launched with PDL (bit k)
 
   // compression scratch
   SegInfo* seg = nullptr;
@@ -304,17 +308,6 @@ mkv_status mkv_create(const mkv_config* cfg, mkv_ctx** out) {
   c->max_seg = ceil_div(cfg->max_ctx, cfg->segment);
   c->kk_max = (int)std::min<int64_t>(cfg->top_k, cfg->max_ctx);
   c->gram_chunks_max = gram_chunks_for(c->BH, cfg->max_ctx);
-  c->attn_chunk = cfg->attn_chunk ? cfg->attn_chunk : (c->g <= 4 ? 64 : 128);
-  // the merge kernel keeps one weight per (chunk, head) in shared memory
-  while (ceil_div(c->kk_max, c->attn_chunk) * c->g > kMergeMaxWeights &&
-         c->attn_chunk < ATTN_MAX_CHUNK)
-    c->attn_chunk = std::min(ATTN_MAX_CHUNK, c->attn_chunk * 2);
-  if (ceil_div(c->kk_max, c->attn_chunk) * c->g > kMergeMaxWeights) {
-    delete c;
-    g_last_error = "top_k too large for the split-K merge";
-    return MKV_ERR_INVALID_ARG;
-  }
-  c->attn_chunks_max = (int)ceil_div(c->kk_max, c->attn_chunk);
   c->Tp_max = ceil_div(cfg->max_ctx, 16) * 16;
   {
     int sms = 0;
@@ -324,6 +317,26 @@ mkv_status mkv_create(const mkv_config* cfg, mkv_ctx** out) {
       return cuda_fail(e, "cudaDeviceGetAttribute");
     }
     c->G = sms;
+  }
+  // Split-K slices of the attention: an explicit size, or the selected
+  // positions spread over at most two CTAs per SM with at least
+  // kMinSlice positions each.  A stream's selection then meets at most
+  // ceil(kk / slice) + 1 slices; the merge keeps one weight per (slice,
+  // head) of a stream in shared memory.
+  c->attn_per_fixed = cfg->attn_chunk;
+  if (c->attn_per_fixed) {
+    while (ceil_div(c->kk_max, c->attn_per_fixed) + 1 > kMergeMaxWeights / c->g &&
+           c->attn_per_fixed < ATTN_MAX_CHUNK)
+      c->attn_per_fixed = std::min<int64_t>(ATTN_MAX_CHUNK, 2 * c->attn_per_fixed);
+    c->attn_mp = (int)ceil_div(c->kk_max, c->attn_per_fixed) + 1;
+  } else {
+    c->attn_mp = (int)std::min<int64_t>(ceil_div(2 * (int64_t)c->G, c->BH),
+                                        ceil_div(c->kk_max, kMinSlice)) + 2;
+  }
+  if ((int64_t)c->attn_mp * c->g > kMergeMaxWeights) {
+    delete c;
+    g_last_error = "top_k too large for the split-K merge";
+    return MKV_ERR_INVALID_ARG;
   }
   score_stage_plan(cfg->segment, cfg->c, &c->stage_bytes, &c->n_stages);
   const size_t BH = c->BH;
@@ -345,7 +358,7 @@ mkv_status mkv_create(const mkv_config* cfg, mkv_ctx** out) {
   }
   AL(c->seg, 2 * BH * (size_t)c->max_seg);
   AL(c->gram_part, 2 * BH * (size_t)c->gram_chunks_max * D * D);
-  AL(c->total_dev, 1);
+  AL(c->total_dev, 3);
   AL(c->qt, (size_t)c->B * c->Hq * D);
   AL(c->qbar, BH * D);
   AL(c->scores, BH * (size_t)c->Tp_max);
@@ -355,10 +368,11 @@ mkv_status mkv_create(const mkv_config* cfg, mkv_ctx** out) {
   AL(c->state, BH);
   AL(c->sel, BH * (size_t)c->kk_max);
   AL(c->err, 1);
-  AL(c->part_o, BH * (size_t)c->attn_chunks_max * c->g * D);
-  AL(c->part_ml, BH * (size_t)c->attn_chunks_max * c->g * 2);
+  AL(c->part_o, BH * (size_t)c->attn_mp * c->g * D);
+  AL(c->part_ml, BH * (size_t)c->attn_mp * c->g * 2);
 #undef AL
-  cudaError_t e = cudaMallocHost(reinterpret_cast<void**>(&c->total_host), sizeof(unsigned long long));
+  cudaError_t e = cudaMallocHost(reinterpret_cast<void**>(&c->total_host),
+                                 3 * sizeof(unsigned long long));
   if (e == cudaSuccess) e = cudaMemset(c->tick, 0, BH * sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(c->err, 0, sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(c->sel, 0, BH * (size_t)c->kk_max * sizeof(int32_t));
@@ -419,10 +433,11 @@ mkv_status mkv_compress(mkv_ctx* c, const void* k, const void* v, int64_t ctx_le
   CK(launch_partition(p.hdr, c->BH, p.n_seg, p.c, c->G, c->stage_bytes, c->part[stage],
                       c->cta_cnt[stage], c->plan[stage], c->plan_n[stage], st));
   c->launches += 6;
-  CK(cudaMemcpyAsync(c->total_host, c->total_dev, sizeof(unsigned long long),
+  CK(cudaMemcpyAsync(c->total_host, c->total_dev, 3 * sizeof(unsigned long long),
                      cudaMemcpyDeviceToHost, st));
   CK(cudaStreamSynchronize(st));
-  const uint64_t total = *c->total_host;
+  const uint64_t total = c->total_host[0];
+  const bool dense_k = c->total_host[1] != 0, dense_v = c->total_host[2] != 0;
   if ((total >> 4) > 0xffffffffull) {
     g_last_error = "packed cache exceeds 64 GiB per ctx";
     return MKV_ERR_INVALID_ARG;
@@ -452,6 +467,13 @@ mkv_status mkv_compress(mkv_ctx* c, const void* k, const void* v, int64_t ctx_le
   c->launches += 1;
   c->live = stage;
   c->pool_need = need;
+  // the attention kernel's per-token slot: room for a dense row only when
+  // the cache has dense segments
+  c->at_kv = dense_k ? 256 : 2 * p.c;
+  c->at_vv = dense_v ? 256 : 2 * p.c;
+  c->at_ki = c->at_vi = (int)pad16((uint32_t)p.c);
+  CK(attn_shape(c->g, c->at_kv + c->at_ki + c->at_vv + c->at_vi, &c->at_stages,
+                &c->at_ctas_per_sm));
   c->T = ctx_len;
   c->n_seg = p.n_seg;
   c->ready = true;
@@ -500,13 +522,29 @@ mkv_status mkv_decode(mkv_ctx* c, const void* q, float* out, int32_t* sel, mkv_s
   p.sel = c->sel;
   p.sel_user = sel;
   p.err = c->err;
-  p.attn_chunk = c->attn_chunk;
-  p.attn_chunks = (int)ceil_div(p.kk, p.attn_chunk);
+  {
+    const int64_t N = (int64_t)c->BH * p.kk;
+    const int64_t P = (int64_t)c->G * c->at_ctas_per_sm;
+    p.attn_per = c->attn_per_fixed
+                     ? c->attn_per_fixed
+                     : std::max({ceil_div(N, P), kMinSlice, ceil_div(p.kk, c->attn_mp - 1)});
+    p.attn_ctas = (int)ceil_div(N, p.attn_per);
+    p.attn_mp = c->attn_mp;
+    p.at_kv = c->at_kv;
+    p.at_ki = c->at_ki;
+    p.at_vv = c->at_vv;
+    p.at_vi = c->at_vi;
+    p.at_slot = c->at_kv + c->at_ki + c->at_vv + c->at_vi;
+    p.at_stages = c->at_stages;
+  }
   p.part_o = c->part_o;
   p.part_ml = c->part_ml;
   p.out = out;
   // kernel timing records events between kernels: launch those plainly
-  p.pdl = (c->cfg.flags & (MKV_FLAG_KERNEL_TIMING | MKV_FLAG_SCORE_TIMING | MKV_FLAG_NO_PDL)) == 0u;
+  const bool pdl_on =
+      (c->cfg.flags & (MKV_FLAG_KERNEL_TIMING | MKV_FLAG_SCORE_TIMING | MKV_FLAG_NO_PDL)) == 0u;
+  p.pdl = pdl_on ? (c->pdl_mask & 0x1f) : 0;
+  p.pdl_trigger = (c->pdl_mask & 0x100) ? 0 : 1;
   mkv_status s;
   if ((s = timed(c, MKV_KERNEL_QROT, st, 1, [&] { return launch_qrot(p, st); })) != MKV_OK) return s;
   if ((s = timed(c, MKV_KERNEL_SCORE, st, 1, [&] { return launch_score(p, st); })) != MKV_OK) return s;
@@ -606,6 +644,12 @@ mkv_status mkv_debug_wait_test(mkv_ctx* c, uint64_t limit_ns, mkv_stream_t strea
   CK(cudaSetDevice(c->cfg.device));
   CK(launch_wait_test(c->err, limit_ns, reinterpret_cast<cudaStream_t>(stream)));
   c->launches += 1;
+  return MKV_OK;
+}
+
+mkv_status mkv_debug_set_pdl(mkv_ctx* c, uint32_t mask) {
+  if (!c || (mask & ~0x11fu)) return MKV_ERR_INVALID_ARG;
+  c->pdl_mask = mask;
   return MKV_OK;
 }
 

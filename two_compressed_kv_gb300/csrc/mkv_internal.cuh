@@ -15,7 +15,7 @@ constexpr int HIST1 = 4096;            // level-1 radix digit of the score key: 
 constexpr int HISTA = 1024;            // candidates, bits 19..10
 constexpr int HISTB = 1024;            // candidates, bits  9..0
 constexpr int TILE_T = 64;             // tokens per rotation tile
-constexpr int ATTN_MAX_CHUNK = 128;    // selected tokens per attention CTA (one per thread)
+constexpr int ATTN_MAX_CHUNK = 128;    // largest explicit attention slice (mkv_config.attn_chunk)
 
 __host__ __device__ inline int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
 __host__ __device__ inline uint32_t pad16(uint32_t n) { return (n + 15u) & ~15u; }
@@ -63,7 +63,7 @@ struct CompressParams {
   int ctas_per_stream;
   SegInfo* seg;              // [2][BH][n_seg]
   mkv_segment_header* hdr;   // [2][BH][n_seg]
-  unsigned long long* total; // device: total packed bytes
+  unsigned long long* total; // device: [0] total packed bytes, [1..2] dense segments of K, V
   uint8_t* pool;
   uint64_t pool_check;       // pack writes must end within this many pool bytes
   int* err;                  // device status word
@@ -132,13 +132,21 @@ struct DecodeParams {
   int sel_R;                       // CTAs (one cluster) per stream in the selection
   int32_t* sel;                    // [BH][kk] (internal)
   int32_t* sel_user;               // optional copy for the caller
-  int attn_chunk;                  // selected tokens per attention CTA (<= ATTN_MAX_CHUNK)
-  int attn_chunks;                 // ceil(kk / attn_chunk)
-  float* part_o;                   // [BH][attn_chunks][g][128]
-  float* part_ml;                  // [BH][attn_chunks][g][2]
+  // attention: the B H kk selected positions, flattened, in slices of
+  // attn_per positions (one CTA each); attn_mp partial slots per stream
+  int64_t attn_per;
+  int attn_ctas;
+  int attn_mp;
+  // per-token shared-memory slot of the attention kernel: K values, K channel
+  // list, V values, V channel list (bytes, multiples of 16), and stages
+  int at_kv, at_ki, at_vv, at_vi, at_slot, at_stages;
+  float* part_o;                   // [BH][attn_mp][g][128]
+  float* part_ml;                  // [BH][attn_mp][g][2]
   float* out;                      // [B][Hq][128]
   int* err;                        // device status word (0 = ok)
-  int pdl;                         // launch with programmatic dependent launch
+  int pdl;                         // bit k: launch decode kernel k (MKV_KERNEL_* order)
+                                   // with programmatic dependent launch
+  int pdl_trigger;                 // kernels let their dependents start early
 };
 
 // bits of the device status word (0 = ok), set with atomicOr
@@ -168,6 +176,8 @@ cudaError_t launch_topk(const DecodeParams& p, cudaStream_t st);
 // CTAs per stream for the selection: up to 8 while the grid fits G SMs twice
 int select_cluster_size(int n_streams, int64_t T, int G);
 cudaError_t launch_attn(const DecodeParams& p, cudaStream_t st);
+// attention kernel shape for a slot size: stages and resident CTAs per SM
+cudaError_t attn_shape(int g, int slot, int* stages, int* ctas_per_sm);
 cudaError_t launch_merge(const DecodeParams& p, cudaStream_t st);
 
 }  // namespace mkv

@@ -87,6 +87,7 @@ def _load():
         "mkv_basis_static": (c_int, [P, P, c_int, c_int, c_int64, P, P, P]),
         "mkv_debug_wait_test": (c_int, [P, c_uint64, P]),
         "mkv_set_flags": (c_int, [P, c_uint32]),
+        "mkv_debug_set_pdl": (c_int, [P, c_uint32]),
         "mkv_debug_set_check_extent": (c_int, [P, c_uint64]),
     }
     for name, (res, args) in sig.items():
@@ -228,6 +229,11 @@ def mkv_check_device(ctx) -> int:
 
 def mkv_set_flags(ctx, flags: int) -> None:
     _check(_lib.mkv_set_flags(ctx, int(flags)), "mkv_set_flags")
+
+
+def mkv_debug_set_pdl(ctx, mask: int) -> None:
+    """Measurement hook: decode kernels launched with PDL (bit k), bit 8 = no early signal."""
+    _check(_lib.mkv_debug_set_pdl(ctx, int(mask)), "mkv_debug_set_pdl")
 
 
 def mkv_debug_wait_test(ctx, limit_ns: int, stream=None) -> None:
