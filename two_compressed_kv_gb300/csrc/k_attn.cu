@@ -451,6 +451,7 @@ cudaError_t attn_shape(int g, int slot, int* stages, int* ctas_per_sm) {
       break;
     }
   const size_t smem = at_smem_bytes(g, slot, nst);
+  if (smem > at_smem_bytes(MAX_G, 768, 2)) return cudaErrorInvalidValue;
   int occ = 0;
   cudaError_t e;
   if (nst == 4) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, attn_kernel<4>, AT_THREADS, smem);
@@ -463,7 +464,9 @@ cudaError_t attn_shape(int g, int slot, int* stages, int* ctas_per_sm) {
 }
 
 cudaError_t prepare_attn_kernels() {
-  const int mx = 227 * 1024;
+  // the largest carve-up attn_shape can choose: two stages of dense rows
+  // (256 + 128 bytes of K and of V per token) and 16 heads
+  const int mx = (int)at_smem_bytes(MAX_G, 768, 2);
   cudaError_t e = cudaFuncSetAttribute(attn_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(attn_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
