@@ -69,11 +69,11 @@ enum {
  * captured step); read with mkv_kernel_time(ctx, MKV_KERNEL_SCORE, ...). */
 #define MKV_FLAG_SCORE_TIMING 2u
 /* Launch the decode kernels one after another without programmatic dependent
- * launch.  By default (and whenever no timing flag is set) each decode kernel
- * may start while the one before it is finishing: its prologue (staging of
- * ctx data, barrier set-up, the first copies of packed keys) overlaps that
- * kernel's tail.  Timing flags imply this flag, since an event between two
- * kernels separates them. */
+ * launch.  By default (and whenever no timing flag is set) the rotation,
+ * score and attention kernels may start while the kernel before them is
+ * finishing: their prologues (staging of ctx data, barrier set-up, the first
+ * copies of packed keys) overlap that kernel's tail.  Timing flags imply this
+ * flag, since an event between two kernels separates them. */
 #define MKV_FLAG_NO_PDL 4u
 #define MKV_FLAGS_ALL (MKV_FLAG_KERNEL_TIMING | MKV_FLAG_SCORE_TIMING | MKV_FLAG_NO_PDL)
 
@@ -250,8 +250,8 @@ mkv_status mkv_debug_wait_test(mkv_ctx* ctx, uint64_t limit_ns, mkv_stream_t str
  * launched with programmatic dependent launch when no flag disables it.  Bit
  * k (k = MKV_KERNEL_* id) enables it for kernel k; bit 8 keeps the kernels
  * from signalling early (the next kernel then starts when they end).
- * Default 0x1f.  Results do not depend on it.  MKV_ERR_INVALID_ARG for other
- * bits. */
+ * Default 0x0b (the rotation, score and attention kernels).  Results do not
+ * depend on it.  MKV_ERR_INVALID_ARG for other bits. */
 mkv_status mkv_debug_set_pdl(mkv_ctx* ctx, uint32_t mask);
 mkv_status mkv_debug_set_check_extent(mkv_ctx* ctx, uint64_t bytes);
 

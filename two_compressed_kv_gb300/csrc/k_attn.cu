@@ -76,6 +76,9 @@ struct AtLayout {
   uint32_t stages, vt, ph, pl, qs, lg, meta, total;
 };
 
+// Row addresses resolved per pass (positions of the CTA's slice).
+constexpr int AT_META = 1024;
+
 __host__ __device__ inline AtLayout at_layout(int g, int slot, int nst) {
   const int gp = (g + 3) & ~3;
   AtLayout L;
@@ -86,7 +89,7 @@ __host__ __device__ inline AtLayout at_layout(int g, int slot, int nst) {
   L.qs = L.pl + MAX_G * AT_PLD * 2;
   L.lg = L.qs + D * gp * 4;
   L.meta = L.lg + AT_CHUNK * gp * 4;
-  L.total = L.meta + (uint32_t)nst * AT_CHUNK * 16;
+  L.total = L.meta + AT_META * 16;
   return L;
 }
 
@@ -101,7 +104,9 @@ struct AtChunk {
   bool last;    // the slice's last chunk of this stream
 };
 
-__device__ __forceinline__ bool at_chunk(int kk, int64_t lo, int64_t hi, int64_t f, AtChunk& c) {
+// Chunk f clipped to the pass [lo, hi) of the slice that ends at slice_hi.
+__device__ __forceinline__ bool at_chunk(int kk, int64_t lo, int64_t hi, int64_t slice_hi,
+                                         int64_t f, AtChunk& c) {
   const int nbs = (kk + AT_CHUNK - 1) / AT_CHUNK;
   const int64_t s = f / nbs;
   const int b = (int)(f - s * nbs);
@@ -113,48 +118,78 @@ __device__ __forceinline__ bool at_chunk(int kk, int64_t lo, int64_t hi, int64_t
   c.s = (int)s;
   c.j0 = (int)(a - s * kk);
   c.n = (int)(e - a);
-  c.last = (e == hi) || (b == nbs - 1);
+  c.last = (e == slice_hi) || (e == end && b == nbs - 1);
   return true;
 }
 
-// Issues the copies of chunk f into stage `st`: token tid / 8, lane tid % 8.
-__device__ __forceinline__ void at_issue(const DecodeParams& p, int64_t lo, int64_t hi, int64_t f,
-                                         int st, uint8_t* smem, const AtLayout& L) {
+// Resolves the rows of positions [lo, hi) (at most AT_META) into meta[]:
+// token id -> K and V segment headers -> (value offset, channel-list
+// distance) of each row.  Four positions per thread are loaded together.
+__device__ __forceinline__ void at_meta_pass(const DecodeParams& p, int64_t lo, int64_t hi,
+                                             uint4* meta) {
+  const int n = (int)(hi - lo);
+  for (int x0 = threadIdx.x; x0 < n; x0 += 4 * AT_THREADS) {
+    int64_t t[4];
+    int sidx[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int x = x0 + u * AT_THREADS;
+      sidx[u] = 0;
+      t[u] = 0;
+      if (x < n) {
+        const int64_t pos = lo + x;
+        sidx[u] = (int)(pos / p.kk);
+        t[u] = p.sel[pos];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int x = x0 + u * AT_THREADS;
+      if (x < n) {
+        const int64_t tt = clamp_t((int32_t)t[u], p.T);
+        uint2 km = row_meta(p.hdrK + (size_t)sidx[u] * p.n_seg, tt, p.S, p.c);
+        uint2 vm = row_meta(p.hdrV + (size_t)sidx[u] * p.n_seg, tt, p.S, p.c);
+        if (row_end(km, p.c) > p.pool_check || row_end(vm, p.c) > p.pool_check) {
+          // outside the checked pool extent: report it and read a stand-in
+          // row of c values with its channel list at pool offset 0 (inside
+          // every pool, and the size of a non-dense slot)
+          atomicOr(p.err, DEV_ERR_CHECK);
+          km = vm = make_uint2(0u, 0u);
+        }
+        meta[x] = make_uint4(km.x, km.y, vm.x, vm.y);
+      }
+    }
+  }
+}
+
+// Issues the copies of chunk f of the pass [lo, hi) into stage `st`: token
+// tid / 8, lane tid % 8; rows from the pass's meta[].
+__device__ __forceinline__ void at_issue(const DecodeParams& p, int64_t lo, int64_t hi,
+                                         int64_t f, int st, uint8_t* smem, const AtLayout& L) {
   AtChunk ch;
-  if (!at_chunk(p.kk, lo, hi, f, ch)) return;
+  if (!at_chunk(p.kk, lo, hi, hi, f, ch)) return;
   const int i = threadIdx.x >> 3, cl = threadIdx.x & 7;
   if (i >= ch.n) return;
   const int c = p.c;
-  const int s = ch.s;
-  const int64_t t = clamp_t(p.sel[(size_t)s * p.kk + ch.j0 + i], p.T);
-  uint2 km = row_meta(p.hdrK + (size_t)s * p.n_seg, t, p.S, c);
-  uint2 vm = row_meta(p.hdrV + (size_t)s * p.n_seg, t, p.S, c);
-  if (row_end(km, c) > p.pool_check || row_end(vm, c) > p.pool_check) {
-    // outside the checked pool extent: report it and read a stand-in row of
-    // c values with its channel list at pool offset 0 (inside every pool,
-    // and the size of a non-dense slot)
-    if (cl == 0) atomicOr(p.err, DEV_ERR_CHECK);
-    km = vm = make_uint2(0u, 0u);
-  }
+  const int64_t x = (int64_t)ch.s * p.kk + ch.j0 + i - lo;
+  const uint4 m = reinterpret_cast<const uint4*>(smem + L.meta)[x];
   const uint32_t slot = smem_u32(smem + L.stages) + (uint32_t)((st * AT_CHUNK + i) * p.at_slot);
-  const bool kd = (int32_t)km.y == NO_IDX, vd = (int32_t)vm.y == NO_IDX;
+  const bool kd = (int32_t)m.y == NO_IDX, vd = (int32_t)m.w == NO_IDX;
   const int kn = kd ? D : c, vn = vd ? D : c;
-  const uint8_t* kv = p.pool + (uint64_t)km.x * 16u;
-  const uint8_t* vv = p.pool + (uint64_t)vm.x * 16u;
+  const uint8_t* kv = p.pool + (uint64_t)m.x * 16u;
+  const uint8_t* vv = p.pool + (uint64_t)m.z * 16u;
   const uint32_t vs = slot + p.at_kv + p.at_ki;
 #pragma unroll
   for (int ck = cl; ck < 16; ck += 8) {
     if (8 * ck < kn) {
       cpa16(slot + 16 * ck, kv + 16 * ck);
-      if (!kd) cpa8(slot + p.at_kv + 8 * ck, kv + 8 * (int64_t)(int32_t)km.y + 8 * ck);
+      if (!kd) cpa8(slot + p.at_kv + 8 * ck, kv + 8 * (int64_t)(int32_t)m.y + 8 * ck);
     }
     if (8 * ck < vn) {
       cpa16(vs + 16 * ck, vv + 16 * ck);
-      if (!vd) cpa8(vs + p.at_vv + 8 * ck, vv + 8 * (int64_t)(int32_t)vm.y + 8 * ck);
+      if (!vd) cpa8(vs + p.at_vv + 8 * ck, vv + 8 * (int64_t)(int32_t)m.w + 8 * ck);
     }
   }
-  if (cl == 0)
-    reinterpret_cast<uint4*>(smem + L.meta)[st * AT_CHUNK + i] = make_uint4(km.x, km.y, vm.x, vm.y);
 }
 
 template <int NST>
@@ -170,7 +205,7 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_kernel(DecodeParams p) {
   __half* Pl = reinterpret_cast<__half*>(at_smem + L.pl);
   float* qs = reinterpret_cast<float*>(at_smem + L.qs);
   float* lg = reinterpret_cast<float*>(at_smem + L.lg);
-  const uint4* meta = reinterpret_cast<const uint4*>(at_smem + L.meta);
+  uint4* meta = reinterpret_cast<uint4*>(at_smem + L.meta);
   const int64_t N = (int64_t)p.B * p.H * p.kk;
   const int64_t lo = (int64_t)blockIdx.x * p.attn_per;
   const int64_t hi = lo + p.attn_per < N ? lo + p.attn_per : N;
@@ -189,166 +224,175 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_kernel(DecodeParams p) {
   if (p.pdl_trigger) griddep_launch();
   if (lo >= N) return;
   const int nbs = (p.kk + AT_CHUNK - 1) / AT_CHUNK;
-  const int64_t f0 = (lo / p.kk) * nbs + (lo % p.kk) / AT_CHUNK;
-#pragma unroll
-  for (int n = 0; n < NST - 1; ++n) {
-    at_issue(p, lo, hi, f0 + n, n, at_smem, L);
-    cpa_commit();
-  }
   const float scale = 0.08838834764831845f;     // 1 / sqrt(128)
   const int mm = lane >> 3, r8 = lane & 7;
   const int n0 = warp * 8;                       // this warp's output channels in phase C
   float acc_h[4] = {0.f, 0.f, 0.f, 0.f}, acc_l[4] = {0.f, 0.f, 0.f, 0.f};
   int cur_s = -1;
-  for (int n = 0;; ++n) {
-    AtChunk ch;
-    if (!at_chunk(p.kk, lo, hi, f0 + n, ch)) break;
-    at_issue(p, lo, hi, f0 + n + NST - 1, (n + NST - 1) % NST, at_smem, L);
-    cpa_commit();
-    cpa_wait<NST - 1>();
+  // passes of at most AT_META positions: resolve their rows, then stream them
+  for (int64_t pa = lo; pa < hi; pa += AT_META) {
+    const int64_t pb = pa + AT_META < hi ? pa + AT_META : hi;
+    if (pa != lo) cpa_wait<0>();
+    __syncthreads();                     // the previous pass no longer reads meta[]
+    at_meta_pass(p, pa, pb, meta);
     __syncthreads();
-    const int st = n % NST;
-    if (ch.s != cur_s) {
-      cur_s = ch.s;
-      const int b = ch.s / p.H, h = ch.s % p.H;
-      const float* qt = p.qt + ((size_t)b * p.Hq + (size_t)h * g) * D;
-      for (int x = tid; x < D * gp; x += AT_THREADS) {
-        const int chn = x / gp, hh = x % gp;
-        qs[x] = hh < g ? qt[hh * D + chn] : 0.f;
-      }
-      __syncthreads();
+    const int64_t f0 = (pa / p.kk) * nbs + (pa % p.kk) / AT_CHUNK;
+#pragma unroll
+    for (int n = 0; n < NST - 1; ++n) {
+      at_issue(p, pa, pb, f0 + n, n, at_smem, L);
+      cpa_commit();
     }
-    // ---- A: logits and the V tile --------------------------------------------
-    {
-      const bool valid = tok < ch.n;
-      const uint4 mt = valid ? meta[st * AT_CHUNK + tok] : make_uint4(0u, 0u, 0u, 0u);
-      const uint8_t* slot = at_smem + L.stages + (size_t)(st * AT_CHUNK + tok) * p.at_slot;
-      const bool kd = (int32_t)mt.y == NO_IDX, vd = (int32_t)mt.w == NO_IDX;
-      const int kn = valid ? (kd ? D : c) : 0, vn = valid ? (vd ? D : c) : 0;
-      for (int h4 = 0; h4 < gp; h4 += 4) {
-        float part[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int ck = cl; ck < 16; ck += 8) {
-          if (8 * ck < kn) {
-            const uint4 kr = *reinterpret_cast<const uint4*>(slot + 16 * ck);
-            const uint2 kx = kd ? make_uint2(0u, 0u)
-                                : *reinterpret_cast<const uint2*>(slot + p.at_kv + 8 * ck);
-            float v[8];
-            h8_to_f(kr, v);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int chn = kd ? 8 * ck + e : chan_of(kx, e);
-              const float4 q4 = *reinterpret_cast<const float4*>(qs + chn * gp + h4);
-              part[0] = fmaf(q4.x, v[e], part[0]);
-              part[1] = fmaf(q4.y, v[e], part[1]);
-              part[2] = fmaf(q4.z, v[e], part[2]);
-              part[3] = fmaf(q4.w, v[e], part[3]);
+    for (int n = 0;; ++n) {
+      AtChunk ch;
+      if (!at_chunk(p.kk, pa, pb, hi, f0 + n, ch)) break;
+      at_issue(p, pa, pb, f0 + n + NST - 1, (n + NST - 1) % NST, at_smem, L);
+      cpa_commit();
+      cpa_wait<NST - 1>();
+      __syncthreads();
+      const int st = n % NST;
+      const int64_t x0 = (int64_t)ch.s * p.kk + ch.j0 - pa;   // chunk's first meta[] index
+      if (ch.s != cur_s) {
+        cur_s = ch.s;
+        const int b = ch.s / p.H, h = ch.s % p.H;
+        const float* qt = p.qt + ((size_t)b * p.Hq + (size_t)h * g) * D;
+        for (int x = tid; x < D * gp; x += AT_THREADS) {
+          const int chn = x / gp, hh = x % gp;
+          qs[x] = hh < g ? qt[hh * D + chn] : 0.f;
+        }
+        __syncthreads();
+      }
+      // ---- A: logits and the V tile --------------------------------------------
+      {
+        const bool valid = tok < ch.n;
+        const uint4 mt = valid ? meta[x0 + tok] : make_uint4(0u, 0u, 0u, 0u);
+        const uint8_t* slot = at_smem + L.stages + (size_t)(st * AT_CHUNK + tok) * p.at_slot;
+        const bool kd = (int32_t)mt.y == NO_IDX, vd = (int32_t)mt.w == NO_IDX;
+        const int kn = valid ? (kd ? D : c) : 0, vn = valid ? (vd ? D : c) : 0;
+        for (int h4 = 0; h4 < gp; h4 += 4) {
+          float part[4] = {0.f, 0.f, 0.f, 0.f};
+  #pragma unroll
+          for (int ck = cl; ck < 16; ck += 8) {
+            if (8 * ck < kn) {
+              const uint4 kr = *reinterpret_cast<const uint4*>(slot + 16 * ck);
+              const uint2 kx = kd ? make_uint2(0u, 0u)
+                                  : *reinterpret_cast<const uint2*>(slot + p.at_kv + 8 * ck);
+              float v[8];
+              h8_to_f(kr, v);
+  #pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const int chn = kd ? 8 * ck + e : chan_of(kx, e);
+                const float4 q4 = *reinterpret_cast<const float4*>(qs + chn * gp + h4);
+                part[0] = fmaf(q4.x, v[e], part[0]);
+                part[1] = fmaf(q4.y, v[e], part[1]);
+                part[2] = fmaf(q4.z, v[e], part[2]);
+                part[3] = fmaf(q4.w, v[e], part[3]);
+              }
             }
           }
+  #pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            float x = part[k];
+            x += __shfl_xor_sync(0xffffffffu, x, 1);
+            x += __shfl_xor_sync(0xffffffffu, x, 2);
+            x += __shfl_xor_sync(0xffffffffu, x, 4);
+            part[k] = x;
+          }
+          if (valid && cl == 0)
+            *reinterpret_cast<float4*>(lg + tok * gp + h4) =
+                make_float4(part[0] * scale, part[1] * scale, part[2] * scale, part[3] * scale);
         }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          float x = part[k];
-          x += __shfl_xor_sync(0xffffffffu, x, 1);
-          x += __shfl_xor_sync(0xffffffffu, x, 2);
-          x += __shfl_xor_sync(0xffffffffu, x, 4);
-          part[k] = x;
-        }
-        if (valid && cl == 0)
-          *reinterpret_cast<float4*>(lg + tok * gp + h4) =
-              make_float4(part[0] * scale, part[1] * scale, part[2] * scale, part[3] * scale);
-      }
-#pragma unroll
-      for (int ck = cl; ck < 16; ck += 8) {
-        if (8 * ck < vn) {
-          const uint8_t* vs = slot + p.at_kv + p.at_ki;
-          const uint4 vr = *reinterpret_cast<const uint4*>(vs + 16 * ck);
-          const uint2 vx = vd ? make_uint2(0u, 0u)
-                              : *reinterpret_cast<const uint2*>(vs + p.at_vv + 8 * ck);
-          const __half* hv = reinterpret_cast<const __half*>(&vr);
-          __half* vrow = Vt + tok * AT_VLD;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) vrow[vd ? 8 * ck + e : chan_of(vx, e)] = hv[e];
+  #pragma unroll
+        for (int ck = cl; ck < 16; ck += 8) {
+          if (8 * ck < vn) {
+            const uint8_t* vs = slot + p.at_kv + p.at_ki;
+            const uint4 vr = *reinterpret_cast<const uint4*>(vs + 16 * ck);
+            const uint2 vx = vd ? make_uint2(0u, 0u)
+                                : *reinterpret_cast<const uint2*>(vs + p.at_vv + 8 * ck);
+            const __half* hv = reinterpret_cast<const __half*>(&vr);
+            __half* vrow = Vt + tok * AT_VLD;
+  #pragma unroll
+            for (int e = 0; e < 8; ++e) vrow[vd ? 8 * ck + e : chan_of(vx, e)] = hv[e];
+          }
         }
       }
-    }
-    __syncthreads();
-    // ---- B: online softmax, one warp per head ----------------------------------
-    if (warp < g) {
-      const int hh = warp;
-      float mloc = -INFINITY;
-      for (int i = lane; i < ch.n; i += 32) mloc = fmaxf(mloc, lg[i * gp + hh]);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1)
-        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, off));
-      const float m_old = s_m[hh];
-      const float m_new = fmaxf(m_old, mloc);
-      const float alpha = expf(m_old - m_new);
-      float lsum = 0.f;
-      for (int i = lane; i < AT_CHUNK; i += 32) {
-        const float e = i < ch.n ? expf(lg[i * gp + hh] - m_new) : 0.f;
-        const __half hi = __float2half_rn(e);
-        Ph[hh * AT_PLD + i] = hi;
-        Pl[hh * AT_PLD + i] = __float2half_rn((e - __half2float(hi)) * 2048.f);
-        lsum += e;
+      __syncthreads();
+      // ---- B: online softmax, one warp per head ----------------------------------
+      if (warp < g) {
+        const int hh = warp;
+        float mloc = -INFINITY;
+        for (int i = lane; i < ch.n; i += 32) mloc = fmaxf(mloc, lg[i * gp + hh]);
+  #pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+          mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, off));
+        const float m_old = s_m[hh];
+        const float m_new = fmaxf(m_old, mloc);
+        const float alpha = expf(m_old - m_new);
+        float lsum = 0.f;
+        for (int i = lane; i < AT_CHUNK; i += 32) {
+          const float e = i < ch.n ? expf(lg[i * gp + hh] - m_new) : 0.f;
+          const __half hi = __float2half_rn(e);
+          Ph[hh * AT_PLD + i] = hi;
+          Pl[hh * AT_PLD + i] = __float2half_rn((e - __half2float(hi)) * 2048.f);
+          lsum += e;
+        }
+  #pragma unroll
+        for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+        if (lane == 0) {
+          s_alpha[hh] = alpha;
+          s_m[hh] = m_new;
+          s_l[hh] = fmaf(s_l[hh], alpha, lsum);
+        }
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
-      if (lane == 0) {
-        s_alpha[hh] = alpha;
-        s_m[hh] = m_new;
-        s_l[hh] = fmaf(s_l[hh], alpha, lsum);
-      }
-    }
-    __syncthreads();
-    // ---- C: o~ <- alpha o~ + P V, warp w owns channels [8w, 8w + 8) -------------
-    {
-      const int r0 = lane >> 2;
-      const float a0 = r0 < g ? s_alpha[r0] : 1.f;
-      const float a1 = r0 + 8 < g ? s_alpha[r0 + 8] : 1.f;
-      acc_h[0] *= a0;
-      acc_h[1] *= a0;
-      acc_h[2] *= a1;
-      acc_h[3] *= a1;
-      acc_l[0] *= a0;
-      acc_l[1] *= a0;
-      acc_l[2] *= a1;
-      acc_l[3] *= a1;
-      const uint32_t ph = smem_u32(Ph), pl = smem_u32(Pl), vt = smem_u32(Vt);
-      const int ksteps = (ch.n + 15) >> 4;
-      for (int ks = 0; ks < ksteps; ++ks) {
-        const int k0 = ks * 16;
-        uint32_t ah[4], al[4], bb[2];
-        const uint32_t aoff = (uint32_t)(((r8 + (mm & 1) * 8) * AT_PLD + k0 + (mm >> 1) * 8) * 2);
-        ldsm_x4(ph + aoff, ah);
-        ldsm_x4(pl + aoff, al);
-        ldsm_x2_t(vt + (uint32_t)(((k0 + (lane & 15)) * AT_VLD + n0) * 2), bb);
-        mma16816(acc_h, ah, bb[0], bb[1]);
-        mma16816(acc_l, al, bb[0], bb[1]);
-      }
-      // clear this warp's columns of the V tile for the next chunk
-      *reinterpret_cast<uint4*>(Vt + lane * AT_VLD + n0) = make_uint4(0u, 0u, 0u, 0u);
-      *reinterpret_cast<uint4*>(Vt + (lane + 32) * AT_VLD + n0) = make_uint4(0u, 0u, 0u, 0u);
-      if (ch.last) {
-        // the slice's part of this stream is done: write its partial
-        const int first = (int)(((int64_t)ch.s * p.kk) / p.attn_per);
-        const size_t pbase = ((size_t)ch.s * p.attn_mp + (blockIdx.x - first)) * g;
-        const int col = n0 + 2 * (lane & 3);
-        if (r0 < g)
-          *reinterpret_cast<float2*>(p.part_o + (pbase + r0) * D + col) =
-              make_float2(fmaf(acc_l[0], 1.f / 2048.f, acc_h[0]),
-                          fmaf(acc_l[1], 1.f / 2048.f, acc_h[1]));
-        if (r0 + 8 < g)
-          *reinterpret_cast<float2*>(p.part_o + (pbase + r0 + 8) * D + col) =
-              make_float2(fmaf(acc_l[2], 1.f / 2048.f, acc_h[2]),
-                          fmaf(acc_l[3], 1.f / 2048.f, acc_h[3]));
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc_h[e] = acc_l[e] = 0.f;
-        if (warp < g && lane == 0) {
-          p.part_ml[(pbase + warp) * 2] = s_m[warp];
-          p.part_ml[(pbase + warp) * 2 + 1] = s_l[warp];
-          s_m[warp] = -INFINITY;
-          s_l[warp] = 0.f;
+      __syncthreads();
+      // ---- C: o~ <- alpha o~ + P V, warp w owns channels [8w, 8w + 8) -------------
+      {
+        const int r0 = lane >> 2;
+        const float a0 = r0 < g ? s_alpha[r0] : 1.f;
+        const float a1 = r0 + 8 < g ? s_alpha[r0 + 8] : 1.f;
+        acc_h[0] *= a0;
+        acc_h[1] *= a0;
+        acc_h[2] *= a1;
+        acc_h[3] *= a1;
+        acc_l[0] *= a0;
+        acc_l[1] *= a0;
+        acc_l[2] *= a1;
+        acc_l[3] *= a1;
+        const uint32_t ph = smem_u32(Ph), pl = smem_u32(Pl), vt = smem_u32(Vt);
+        const int ksteps = (ch.n + 15) >> 4;
+        for (int ks = 0; ks < ksteps; ++ks) {
+          const int k0 = ks * 16;
+          uint32_t ah[4], al[4], bb[2];
+          const uint32_t aoff = (uint32_t)(((r8 + (mm & 1) * 8) * AT_PLD + k0 + (mm >> 1) * 8) * 2);
+          ldsm_x4(ph + aoff, ah);
+          ldsm_x4(pl + aoff, al);
+          ldsm_x2_t(vt + (uint32_t)(((k0 + (lane & 15)) * AT_VLD + n0) * 2), bb);
+          mma16816(acc_h, ah, bb[0], bb[1]);
+          mma16816(acc_l, al, bb[0], bb[1]);
+        }
+        // clear this warp's columns of the V tile for the next chunk
+        *reinterpret_cast<uint4*>(Vt + lane * AT_VLD + n0) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(Vt + (lane + 32) * AT_VLD + n0) = make_uint4(0u, 0u, 0u, 0u);
+        if (ch.last) {
+          // the slice's part of this stream is done: write its partial
+          const int first = (int)(((int64_t)ch.s * p.kk) / p.attn_per);
+          const size_t pbase = ((size_t)ch.s * p.attn_mp + (blockIdx.x - first)) * g;
+          const int col = n0 + 2 * (lane & 3);
+          if (r0 < g)
+            *reinterpret_cast<float2*>(p.part_o + (pbase + r0) * D + col) =
+                make_float2(fmaf(acc_l[0], 1.f / 2048.f, acc_h[0]),
+                            fmaf(acc_l[1], 1.f / 2048.f, acc_h[1]));
+          if (r0 + 8 < g)
+            *reinterpret_cast<float2*>(p.part_o + (pbase + r0 + 8) * D + col) =
+                make_float2(fmaf(acc_l[2], 1.f / 2048.f, acc_h[2]),
+                            fmaf(acc_l[3], 1.f / 2048.f, acc_h[3]));
+  #pragma unroll
+          for (int e = 0; e < 4; ++e) acc_h[e] = acc_l[e] = 0.f;
+          if (warp < g && lane == 0) {
+            p.part_ml[(pbase + warp) * 2] = s_m[warp];
+            p.part_ml[(pbase + warp) * 2 + 1] = s_l[warp];
+            s_m[warp] = -INFINITY;
+            s_l[warp] = 0.f;
+          }
         }
       }
     }

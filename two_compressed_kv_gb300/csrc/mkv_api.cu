@@ -74,7 +74,11 @@ struct mkv_ctx {
   uint64_t pool_cap = 0;
   uint64_t pool_need = 0;          // bytes of the live cache's pool (packed size + tail pad)
   uint64_t check_override = 0;     // test hook: a smaller checked pool extent (0 = none)
-  uint32_t pdl_mask = 0x1f;        // test hook: decode kernels launched with PDL (bit k)
+  // decode kernels launched with programmatic dependent launch (bit k =
+  // MKV_KERNEL_* id): the rotation, score and attention kernels gain about
+  // 1.5 us each at the 128K batch-8 shape; the clustered selection kernel
+  // and the merge lose time with it, so they are launched plainly
+  uint32_t pdl_mask = (1u << MKV_KERNEL_QROT) | (1u << MKV_KERNEL_SCORE) | (1u << MKV_KERNEL_ATTN);
 
   // compression scratch
   SegInfo* seg = nullptr;
