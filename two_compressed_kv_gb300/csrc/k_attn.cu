@@ -95,8 +95,9 @@ __host__ __device__ inline AtLayout at_layout(int g, int slot, int nst) {
 
 size_t at_smem_bytes(int g, int slot, int nst) { return at_layout(g, slot, nst).total; }
 
-// Chunk f (a 64-position block of a stream, in (stream, block) order) clipped
-// to the slice [lo, hi); false once the block starts at or after hi.
+// Chunks of a pass: the 64-position blocks of each stream's selection,
+// clipped to the pass [lo, hi) of a slice that ends at slice_hi, walked in
+// order without divisions (one per pass, in at_begin).
 struct AtChunk {
   int s;        // stream
   int j0;       // first position within the stream's selection
@@ -104,21 +105,46 @@ struct AtChunk {
   bool last;    // the slice's last chunk of this stream
 };
 
-// Chunk f clipped to the pass [lo, hi) of the slice that ends at slice_hi.
-__device__ __forceinline__ bool at_chunk(int kk, int64_t lo, int64_t hi, int64_t slice_hi,
-                                         int64_t f, AtChunk& c) {
-  const int nbs = (kk + AT_CHUNK - 1) / AT_CHUNK;
-  const int64_t s = f / nbs;
-  const int b = (int)(f - s * nbs);
-  const int64_t start = s * kk + (int64_t)AT_CHUNK * b;
-  const int64_t end = s * kk + min(AT_CHUNK * b + AT_CHUNK, kk);
-  const int64_t a = start > lo ? start : lo;
-  const int64_t e = end < hi ? end : hi;
+// Position coordinates relative to the pass start (pass length <= AT_META).
+struct AtIter {
+  int rel;         // s * kk - pass start
+  int s;
+  int b;           // block within the stream
+};
+
+__device__ __forceinline__ AtIter at_begin(int kk, int64_t lo) {
+  AtIter it;
+  it.s = (int)(lo / kk);
+  it.rel = (int)((int64_t)it.s * kk - lo);
+  it.b = -it.rel / AT_CHUNK;
+  return it;
+}
+
+__device__ __forceinline__ void at_advance(AtIter& it, int kk) {
+  if (AT_CHUNK * (it.b + 1) >= kk) {
+    ++it.s;
+    it.rel += kk;
+    it.b = 0;
+  } else {
+    ++it.b;
+  }
+}
+
+// n_pass: positions in the pass; slice_end: the slice's end relative to the
+// pass start (clamped to the int range)
+__device__ __forceinline__ bool at_get(const AtIter& it, int kk, int n_pass, int slice_end,
+                                       AtChunk& c) {
+  const int start = it.rel + AT_CHUNK * it.b;
+  const int bend = AT_CHUNK * it.b + AT_CHUNK;
+  const bool stream_end = bend >= kk;
+  const int end = it.rel + (stream_end ? kk : bend);
+  const int a = start > 0 ? start : 0;
+  const int e = end < n_pass ? end : n_pass;
   if (a >= e) return false;
-  c.s = (int)s;
-  c.j0 = (int)(a - s * kk);
-  c.n = (int)(e - a);
-  c.last = (e == slice_hi) || (e == end && b == nbs - 1);
+  c.s = it.s;
+  c.j0 = a - it.rel;
+  c.n = e - a;
+  c.last = (e == slice_end) || (e == end && stream_end);
   return true;
 }
 
@@ -162,17 +188,15 @@ __device__ __forceinline__ void at_meta_pass(const DecodeParams& p, int64_t lo, 
   }
 }
 
-// Issues the copies of chunk f of the pass [lo, hi) into stage `st`: token
-// tid / 8, lane tid % 8; rows from the pass's meta[].
-__device__ __forceinline__ void at_issue(const DecodeParams& p, int64_t lo, int64_t hi,
-                                         int64_t f, int st, uint8_t* smem, const AtLayout& L) {
-  AtChunk ch;
-  if (!at_chunk(p.kk, lo, hi, hi, f, ch)) return;
+// Issues the copies of chunk ch into stage `st` (rel_s: the chunk stream's
+// start relative to the pass): token tid / 8, lane tid % 8; rows from the
+// pass's meta[].
+__device__ __forceinline__ void at_issue(const DecodeParams& p, int rel_s, const AtChunk& ch,
+                                         int st, uint8_t* smem, const AtLayout& L) {
   const int i = threadIdx.x >> 3, cl = threadIdx.x & 7;
   if (i >= ch.n) return;
   const int c = p.c;
-  const int64_t x = (int64_t)ch.s * p.kk + ch.j0 + i - lo;
-  const uint4 m = reinterpret_cast<const uint4*>(smem + L.meta)[x];
+  const uint4 m = reinterpret_cast<const uint4*>(smem + L.meta)[ch.j0 + i + rel_s];
   const uint32_t slot = smem_u32(smem + L.stages) + (uint32_t)((st * AT_CHUNK + i) * p.at_slot);
   const bool kd = (int32_t)m.y == NO_IDX, vd = (int32_t)m.w == NO_IDX;
   const int kn = kd ? D : c, vn = vd ? D : c;
@@ -223,7 +247,6 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_kernel(DecodeParams p) {
   griddep_wait();     // the selection comes from the kernel before this one
   if (p.pdl_trigger) griddep_launch();
   if (lo >= N) return;
-  const int nbs = (p.kk + AT_CHUNK - 1) / AT_CHUNK;
   const float scale = 0.08838834764831845f;     // 1 / sqrt(128)
   const int mm = lane >> 3, r8 = lane & 7;
   const int n0 = warp * 8;                       // this warp's output channels in phase C
@@ -236,22 +259,33 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_kernel(DecodeParams p) {
     __syncthreads();                     // the previous pass no longer reads meta[]
     at_meta_pass(p, pa, pb, meta);
     __syncthreads();
-    const int64_t f0 = (pa / p.kk) * nbs + (pa % p.kk) / AT_CHUNK;
+    const int n_pass = (int)(pb - pa);
+    const int slice_end = (int)(hi - pa < 0x7fffffff ? hi - pa : 0x7fffffff);
+    AtIter cit = at_begin(p.kk, pa);     // the chunk being computed
+    AtIter iit = cit;                     // the chunk being issued
 #pragma unroll
     for (int n = 0; n < NST - 1; ++n) {
-      at_issue(p, pa, pb, f0 + n, n, at_smem, L);
+      AtChunk ich;
+      if (at_get(iit, p.kk, n_pass, slice_end, ich)) at_issue(p, iit.rel, ich, n, at_smem, L);
+      at_advance(iit, p.kk);
       cpa_commit();
     }
     for (int n = 0;; ++n) {
       AtChunk ch;
-      if (!at_chunk(p.kk, pa, pb, hi, f0 + n, ch)) break;
-      at_issue(p, pa, pb, f0 + n + NST - 1, (n + NST - 1) % NST, at_smem, L);
+      if (!at_get(cit, p.kk, n_pass, slice_end, ch)) break;
+      const int x0 = cit.rel + ch.j0;        // the chunk's first meta[] index
+      at_advance(cit, p.kk);
+      {
+        AtChunk ich;
+        if (at_get(iit, p.kk, n_pass, slice_end, ich))
+          at_issue(p, iit.rel, ich, (n + NST - 1) % NST, at_smem, L);
+        at_advance(iit, p.kk);
+      }
       cpa_commit();
       cpa_wait<NST - 1>();
       __syncthreads();
       const int st = n % NST;
-      const int64_t x0 = (int64_t)ch.s * p.kk + ch.j0 - pa;   // chunk's first meta[] index
-      if (ch.s != cur_s) {
+        if (ch.s != cur_s) {
         cur_s = ch.s;
         const int b = ch.s / p.H, h = ch.s % p.H;
         const float* qt = p.qt + ((size_t)b * p.Hq + (size_t)h * g) * D;

@@ -16,16 +16,13 @@
 //   scan     exclusive scan of the packed segment sizes -> headers, total.
 //   pack     same rotation and selection again, writes the packed payload.
 #include "mkv_internal.cuh"
+#include "tc05.cuh"
 
 namespace mkv {
 
 // ---------------------------------------------------------------------------
-// PTX helpers (sm_80+ instructions that sm_103a keeps)
+// cp.async with a source size: bytes past src_bytes are filled with zeros
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes));
 }
@@ -33,133 +30,157 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t r[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t r[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void mma16816(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};\n"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
+// ---------------------------------------------------------------------------
+// X tiles for the fifth-generation tensor cores: 128 tokens x 128 channels of
+// fp16 in the 128-byte swizzled layout, as two 16 KB atoms columns (channels
+// 0-63, 64-127); in each, token r is the 128-byte row r and its 16-byte chunk
+// c sits at chunk c ^ (r mod 8).  The same tile is a K-major operand with
+// tokens as M (the rotation X R) and an MN-major operand with channels as M
+// or N and tokens as K (the Gram X^T X).
+// ---------------------------------------------------------------------------
+constexpr int TC_T = GRAM_TILE;              // tokens per tile
+constexpr uint32_t TC_TILE = 32768;          // bytes per tile
+constexpr uint32_t TC_ATOMS = 16384;         // bytes per 64-channel half
 
-// A [rows][128] fp16 tile in shared memory: 256-byte rows of 16 chunks of 16 B,
-// chunk index XOR (row & 7) so that 8 rows at one logical chunk hit 8
-// different bank groups.
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {
-  return (uint32_t)(row * 256 + ((chunk ^ (row & 7)) << 4));
-}
-
-// Loads tokens [t0, t0+64) of a stream into a swizzled tile; rows at or past T
-// are zero-filled.
-__device__ __forceinline__ void load_tile(uint32_t tile, const __half* X, int64_t t0, int64_t T) {
-  for (int i = threadIdx.x; i < TILE_T * 16; i += blockDim.x) {
-    const int row = i >> 4, chunk = i & 15;
+// Loads tokens [t0, t0 + 128) of a stream (rows at or past t_end read as
+// zeros); 128 threads, 16 copies each.
+__device__ __forceinline__ void tc_load_tile(uint32_t tile, const __half* X, int64_t t0,
+                                             int64_t t_end) {
+#pragma unroll 4
+  for (int q = threadIdx.x; q < TC_T * 16; q += 128) {
+    const int row = q >> 4, c16 = q & 15;
     const int64_t t = t0 + row;
-    const bool ok = t < T;
-    const __half* src = X + (ok ? t : 0) * D + chunk * 8;
-    cp_async16(tile + swz(row, chunk), src, ok ? 16u : 0u);
+    const bool ok = t < t_end;
+    const __half* src = X + (ok ? t : 0) * D + c16 * 8;
+    const uint32_t dst = tile + (uint32_t)(c16 >> 3) * TC_ATOMS + (uint32_t)row * 128u +
+                         ((uint32_t)((c16 & 7) ^ (row & 7)) << 4);
+    cp_async16(dst, src, ok ? 16u : 0u);
   }
 }
 
-// ---------------------------------------------------------------------------
-// gram: partial G over one chunk of tokens.  8 warps; warp w owns the 32 x 64
-// block G[i0:i0+32, j0:j0+64].  A = X^T and B = X both come from the token-major
-// tile through ldmatrix.trans.  The tensor-core accumulators take GR_FLUSH
-// tiles at a time and are then added into a separate fp32 sum: tensor-core
-// accumulation does not round to nearest, so its error grows with the number
-// of products summed in one accumulator; flushing keeps G good to a few 1e-6
-// relative at any context length.
-// grid: (gram_chunks, BH, 2), block 256, dynamic smem 3 x 16 KB
-// ---------------------------------------------------------------------------
-constexpr int GR_STAGES = 3;
-constexpr int GR_FLUSH = 2;     // tiles (of 64 tokens) per accumulator flush
+// MN-major descriptor of a tile used with channels as M (or N): 64-channel
+// atoms 16 KB apart (leading byte offset), groups of 8 tokens 1024 B apart
+// (stride byte offset), 128-byte swizzle.  K (tokens) advances by 16 tokens
+// = 2048 B per MMA.
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(TC_ATOMS >> 4) << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+// kind::f16 instruction descriptor with both operands MN-major (bits 15, 16)
+__host__ __device__ constexpr uint32_t idesc_f16_f32_mn(int M, int N) {
+  return idesc_f16_f32(M, N) | (1u << 15) | (1u << 16);
+}
 
-__global__ void __launch_bounds__(256) gram_kernel(CompressParams p) {
-  extern __shared__ __align__(128) uint8_t gsm[];
+// Waits on an mbarrier phase with the library's bounded wait; records a
+// timeout in the status word and returns false if it gives up.
+__device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, int* err) {
+  if (mbar_wait(bar, parity)) return true;
+  atomicOr(err, DEV_ERR_TIMEOUT);
+  return false;
+}
+
+// ---------------------------------------------------------------------------
+// gram: partial G = X^T X over one chunk of tokens on the tensor cores
+// (tcgen05, fp16 operands, fp32 accumulators in tensor memory).  Tiles of 128
+// tokens are double-buffered (cp.async); thread 0 issues the 8 MMAs of a tile
+// (M = N = 128 channels, K = 16 tokens each) into one of two TMEM
+// accumulators and commits them to that accumulator's mbarrier; meanwhile
+// the 128 threads add the other accumulator into fp32 registers (thread i
+// holds row i of G).  Flushing after every tile keeps the tensor-core
+// accumulation to 128 products, so G is good to a few 1e-6 relative at any
+// context length.
+// grid: (gram_chunks, BH, 2), block 128, dynamic smem 2 tiles + alignment
+// ---------------------------------------------------------------------------
+constexpr int GT_THREADS = 128;
+constexpr size_t GT_SMEM = 2 * TC_TILE + 1024 + 16384;   // +16 KB: at most two CTAs per SM
+
+__global__ void __launch_bounds__(GT_THREADS, 1) gram_kernel(CompressParams p) {
+  extern __shared__ uint8_t gsm_raw[];
+  __shared__ uint64_t mma_done[2];
+  __shared__ uint32_t tbase_sh;
   const int chunk = blockIdx.x, s = blockIdx.y, x = blockIdx.z;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const __half* X = p.X[x] + (size_t)s * p.T * D;
   const int64_t tb = (int64_t)chunk * p.gram_chunk_tokens;
   const int64_t te = imin64(p.T, tb + p.gram_chunk_tokens);
-  const int n_tiles = te > tb ? (int)((te - tb + TILE_T - 1) / TILE_T) : 0;
-  const uint32_t base = smem_u32(gsm);
-  const int i0 = (warp & 3) * 32, j0 = (warp >> 2) * 64;
+  const int n_tiles = te > tb ? (int)((te - tb + TC_T - 1) / TC_T) : 0;
+  const uint32_t base = (smem_u32(gsm_raw) + 1023u) & ~1023u;     // 1024-byte aligned tiles
 
-  float acc[2][8][4], tot[2][8][4];
-#pragma unroll
-  for (int a = 0; a < 2; ++a)
-#pragma unroll
-    for (int b = 0; b < 8; ++b)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[a][b][e] = tot[a][b][e] = 0.f;
-
-  for (int st = 0; st < GR_STAGES - 1; ++st) {
-    if (st < n_tiles) load_tile(base + st * 16384u, X, tb + (int64_t)st * TILE_T, te);
-    cp_async_commit();
+  if (warp == 0) {
+    tmem_alloc(&tbase_sh, 256);
+    tmem_relinquish();
   }
-  const int mm = lane >> 3, r8 = lane & 7;
-  for (int it = 0; it < n_tiles; ++it) {
-    cp_async_wait<GR_STAGES - 2>();
+  if (tid == 0) {
+    mbar_init(&mma_done[0], 1);
+    mbar_init(&mma_done[1], 1);
+    mbar_init_fence();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tbase_sh;
+  const uint32_t idesc = idesc_f16_f32_mn(128, 128);
+  float tot[D];
+#pragma unroll
+  for (int j = 0; j < D; ++j) tot[j] = 0.f;
+  bool ok = true;
+
+  // adds accumulator b (its use-th completion) into tot
+  auto flush = [&](int b, int use) {
+    if (!tc_wait(&mma_done[b], (uint32_t)(use & 1), p.err)) {
+      ok = false;
+      return;
+    }
+    tc_fence_after();
+    const uint32_t ta = tbase + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * 128);
+#pragma unroll
+    for (int q = 0; q < D / 16; ++q) {
+      uint32_t r[16];
+      tmem_ld16(ta + 16 * q, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) tot[16 * q + j] += __uint_as_float(r[j]);
+    }
+  };
+
+  if (n_tiles > 0) tc_load_tile(base, X, tb, te);
+  cp_async_commit();
+  for (int it = 0; it < n_tiles && ok; ++it) {
+    const int b = it & 1;
+    // the other buffer's MMAs (tile it - 1) must be done before its smem is
+    // refilled and its accumulator read
+    if (it >= 1) flush(b ^ 1, (it - 1) >> 1);
+    tc_fence_before();
     __syncthreads();
-    const int nxt = it + GR_STAGES - 1;
-    if (nxt < n_tiles) load_tile(base + (nxt % GR_STAGES) * 16384u, X, tb + (int64_t)nxt * TILE_T, te);
+    if (it + 1 < n_tiles) tc_load_tile(base + (b ^ 1) * TC_TILE, X, tb + (int64_t)(it + 1) * TC_T, te);
     cp_async_commit();
-    const uint32_t tile = base + (it % GR_STAGES) * 16384u;
+    cp_async_wait<1>();
+    fence_proxy_async();          // the tile's generic-proxy writes, before the MMAs read it
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t tile = base + b * TC_TILE;
 #pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      const int kt0 = ks * 16;
-      uint32_t a[2][4];
-#pragma unroll
-      for (int mi = 0; mi < 2; ++mi) {
-        const int row = kt0 + (mm >> 1) * 8 + r8;
-        const int ch = (i0 + mi * 16 + (mm & 1) * 8) >> 3;
-        ldsm_x4_t(tile + swz(row, ch), a[mi]);
+      for (int k = 0; k < TC_T / 16; ++k) {
+        const uint64_t dsc = sdesc_mn_sw128(tile + (uint32_t)k * 2048u);
+        tc_mma_f16(tbase + (uint32_t)(b * 128), dsc, dsc, idesc, k > 0 ? 1u : 0u);
       }
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        uint32_t bb[4];
-        const int row = kt0 + (mm & 1) * 8 + r8;
-        const int ch = (j0 + np * 16 + (mm >> 1) * 8) >> 3;
-        ldsm_x4_t(tile + swz(row, ch), bb);
-#pragma unroll
-        for (int mi = 0; mi < 2; ++mi) {
-          mma16816(acc[mi][2 * np], a[mi], bb[0], bb[1]);
-          mma16816(acc[mi][2 * np + 1], a[mi], bb[2], bb[3]);
-        }
-      }
-    }
-    if ((it + 1) % GR_FLUSH == 0 || it + 1 == n_tiles) {
-#pragma unroll
-      for (int a = 0; a < 2; ++a)
-#pragma unroll
-        for (int b = 0; b < 8; ++b)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            tot[a][b][e] += acc[a][b][e];
-            acc[a][b][e] = 0.f;
-          }
+      tc_commit(&mma_done[b]);
     }
   }
+  if (ok && n_tiles > 0) flush((n_tiles - 1) & 1, (n_tiles - 1) >> 1);
   cp_async_wait<0>();
-  float* out = p.gram_part + (((size_t)x * p.BH + s) * p.gram_chunks + chunk) * (D * D);
-  const int g = lane >> 2, q = lane & 3;
+  float* out = p.gram_part + (((size_t)x * p.BH + s) * p.gram_chunks + chunk) * (D * D) +
+               (size_t)tid * D;
 #pragma unroll
-  for (int mi = 0; mi < 2; ++mi)
-#pragma unroll
-    for (int ni = 0; ni < 8; ++ni) {
-      const int i = i0 + mi * 16 + g, j = j0 + ni * 8 + 2 * q;
-      *reinterpret_cast<float2*>(out + i * D + j) = make_float2(tot[mi][ni][0], tot[mi][ni][1]);
-      *reinterpret_cast<float2*>(out + (i + 8) * D + j) = make_float2(tot[mi][ni][2], tot[mi][ni][3]);
-    }
+  for (int j = 0; j < D; j += 4) *reinterpret_cast<float4*>(out + j) = make_float4(tot[j], tot[j + 1], tot[j + 2], tot[j + 3]);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tbase, 256);
 }
 
 // ---------------------------------------------------------------------------
@@ -426,25 +447,104 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // ---------------------------------------------------------------------------
-// analyze (PACK = false) / pack (PACK = true).
-// One CTA covers whole segments [sg0, sg1) of one stream, in 64-token tiles.
-// Warp w computes rows 16*(w&3).. and columns 64*(w>>2).. of x~ = x R_hi + x R_lo.
-// grid: (ctas_per_stream, BH, 2), block 256, dynamic smem ~131 KB
+// Per-token top-c of one thread's 128 magnitudes (bit patterns of |x~|, which
+// order like the magnitudes), ties to the lower channel.  Bit search for the
+// c-th largest key, stopping once exactly c keys are >= the candidate; with
+// ties at the threshold the lowest channels among them are taken.  Returns
+// the 128-bit channel mask and the kept energy (sum of the kept squares in
+// channel order).
 // ---------------------------------------------------------------------------
-constexpr int XT_LD = D + 4;
-constexpr size_t AN_SMEM = 2 * 32768 + 2 * 16384 + (size_t)TILE_T * XT_LD * 4 + TILE_T * 16 +
-                           TILE_T * 4 + D * 4 + 64;
+__device__ __forceinline__ float thread_topc(const uint32_t k[D], int c, uint32_t mask[4]) {
+  if (c >= D) {
+    float kept = 0.f;
+#pragma unroll
+    for (int j = 0; j < D; ++j) {
+      const float f = __uint_as_float(k[j]);
+      kept = fmaf(f, f, kept);
+    }
+    mask[0] = mask[1] = mask[2] = mask[3] = 0xffffffffu;
+    return kept;
+  }
+  uint32_t thr = 0;
+  int cnt_ge = D;
+  for (int bit = 30; bit >= 0; --bit) {
+    const uint32_t cand = thr | (1u << bit);
+    int n0 = 0, n1 = 0, n2 = 0, n3 = 0;
+#pragma unroll
+    for (int j = 0; j < D; j += 4) {
+      n0 += k[j] >= cand;
+      n1 += k[j + 1] >= cand;
+      n2 += k[j + 2] >= cand;
+      n3 += k[j + 3] >= cand;
+    }
+    const int cnt = (n0 + n1) + (n2 + n3);
+    if (cnt >= c) {
+      thr = cand;
+      cnt_ge = cnt;
+      if (cnt == c) break;
+    }
+  }
+  int need = D;                       // keys equal to thr still taken
+  if (cnt_ge != c) {
+    int gt = 0;
+#pragma unroll
+    for (int j = 0; j < D; ++j) gt += k[j] > thr;
+    need = c - gt;
+  }
+  float kept = 0.f;
+  int eq = 0;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    uint32_t w = 0;
+#pragma unroll
+    for (int b = 0; b < 32; ++b) {
+      const uint32_t kj = k[32 * m + b];
+      const bool take = kj > thr || (kj == thr && eq < need);
+      eq += kj == thr;
+      w |= (uint32_t)take << b;
+      const float f = __uint_as_float(kj);
+      kept = take ? fmaf(f, f, kept) : kept;
+    }
+    mask[m] = w;
+  }
+  return kept;
+}
+
+// ---------------------------------------------------------------------------
+// rotate: the statistics pass (PACK = false) and the packing pass (PACK =
+// true).  One CTA (4 warps) covers whole segments [sg0, sg1) of one stream in
+// tiles of 128 tokens.  x~ = x R_hi + 2^-11 (x R_lo) on the tensor cores
+// (tcgen05, M = 128 tokens, N = 128 basis vectors, K = 128 channels; R split
+// into an fp16 part and a remainder scaled by 2^11 so that it stays a normal
+// fp16, one TMEM accumulator each); thread t then reads token t's 128 rotated
+// values from tensor memory.
+//   statistics: per token the c channels of largest |x~| (thread_topc), its
+//     kept energy and channel mask (the mask also goes to global scratch for
+//     the packing pass); per segment the column energies, the shared mask
+//     and the strategy.
+//   packing: writes the packed rows (warp per row, from the fp32 x~ tile in
+//     shared memory): the segment mask for SM, the token's stored mask for
+//     PV, every channel for dense segments.
+// grid: (ctas_per_stream, BH, 2), block 128, dynamic smem RT_SMEM
+// ---------------------------------------------------------------------------
+constexpr int RT_THREADS = 128;
+constexpr int XT_LD = D + 1;          // fp32 x~ rows: conflict-free by row and by column
+constexpr size_t RT_SMEM = 1024 + 4 * (size_t)TC_TILE + (size_t)TC_T * XT_LD * 4 + TC_T * 16 +
+                           TC_T * 4 + D * 4 + 64;
 
 template <bool PACK>
-__global__ void __launch_bounds__(256, 1) analyze_kernel(CompressParams p) {
-  extern __shared__ __align__(128) uint8_t asmem[];
-  uint8_t* Rhi = asmem;
-  uint8_t* Rlo = asmem + 32768;
-  uint8_t* Xs = asmem + 65536;                                  // 2 x 16 KB
-  float* Xt = reinterpret_cast<float*>(asmem + 65536 + 32768);  // [64][XT_LD]
-  uint32_t* tokmask = reinterpret_cast<uint32_t*>(Xt + TILE_T * XT_LD);  // [64][4]
-  float* tokkept = reinterpret_cast<float*>(tokmask + TILE_T * 4);       // [64]
-  float* colacc = tokkept + TILE_T;                                      // [128]
+__global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p) {
+  extern __shared__ uint8_t rt_raw[];
+  __shared__ uint64_t mma_bar;
+  __shared__ uint32_t tbase_sh;
+  const uint32_t raw = smem_u32(rt_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;            // tiles on 1024-byte boundaries
+  uint8_t* gbase = rt_raw + (base - raw);
+  const uint32_t Bhi = base, Blo = base + TC_TILE, Xs = base + 2 * TC_TILE;
+  float* Xt = reinterpret_cast<float*>(gbase + 4 * TC_TILE);             // [128][XT_LD]
+  uint32_t* tokmask = reinterpret_cast<uint32_t*>(Xt + TC_T * XT_LD);    // [128][4]
+  float* tokkept = reinterpret_cast<float*>(tokmask + TC_T * 4);         // [128]
+  float* colacc = tokkept + TC_T;                                        // [128]
   float* segkept = colacc + D;                                           // [1]
 
   const int x = blockIdx.z, s = blockIdx.y;
@@ -456,102 +556,103 @@ __global__ void __launch_bounds__(256, 1) analyze_kernel(CompressParams p) {
   const int64_t tb = (int64_t)sg0 * p.S;
   const int64_t te = imin64(p.T, (int64_t)sg1 * p.S);
   const __half* X = p.X[x] + (size_t)s * p.T * D;
-  const uint32_t xs_base = smem_u32(Xs);
+  const int n_tiles = (int)((te - tb + TC_T - 1) / TC_T);
 
-  // first tile in flight while R is split and transposed
-  load_tile(xs_base, X, tb, p.T);
+  if (warp == 0) {
+    tmem_alloc(&tbase_sh, 256);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(&mma_bar, 1);
+    mbar_init_fence();
+  }
+  // first tile in flight while R is split into the two B operands
+  tc_load_tile(Xs, X, tb, te);
   cp_async_commit();
   {
+    // B = R^T, K-major: row j (basis vector) holds R[0..127][j] along K
     const float* R = p.R + (size_t)sx * D * D;
-    for (int e = tid; e < D * D; e += blockDim.x) {
+    for (int e = tid; e < D * D; e += RT_THREADS) {
       const int i = e >> 7, j = e & 127;      // R[i][j]: input channel i, basis vector j
       const float r = R[e];
       const __half hi = __float2half_rn(r);
       const __half lo = __float2half_rn((r - __half2float(hi)) * 2048.f);   // kept normal
-      const uint32_t off = swz(j, i >> 3) + (i & 7) * 2;
-      *reinterpret_cast<__half*>(Rhi + off) = hi;
-      *reinterpret_cast<__half*>(Rlo + off) = lo;
+      const uint32_t off = (uint32_t)(i >> 6) * TC_ATOMS + (uint32_t)j * 128u +
+                           ((uint32_t)(((i & 63) >> 3) ^ (j & 7)) << 4) + (uint32_t)(i & 7) * 2u;
+      *reinterpret_cast<__half*>(gbase + off) = hi;
+      *reinterpret_cast<__half*>(gbase + TC_TILE + off) = lo;
     }
   }
   if (!PACK) {
-    for (int j = tid; j < D; j += blockDim.x) colacc[j] = 0.f;
+    for (int j = tid; j < D; j += RT_THREADS) colacc[j] = 0.f;
     if (tid == 0) segkept[0] = 0.f;
   }
-  const uint32_t rhi = smem_u32(Rhi), rlo = smem_u32(Rlo);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tbase_sh;
+  const uint32_t idesc = idesc_f16_f32(128, 128);
   const SegInfo* seginfo = p.seg + (size_t)sx * p.n_seg;
   const mkv_segment_header* hdr = p.hdr + (size_t)sx * p.n_seg;
-  const int m0 = (warp & 3) * 16, n0 = (warp >> 2) * 64;
-  const int mm = lane >> 3, r8 = lane & 7;
-  const int n_tiles = (int)((te - tb + TILE_T - 1) / TILE_T);
+  uint32_t* gmask = p.tokmask + (size_t)sx * p.T * 4;
+  bool ok = true;
 
-  for (int it = 0; it < n_tiles; ++it) {
-    const int64_t t0 = tb + (int64_t)it * TILE_T;
-    const int rows = (int)imin64(TILE_T, te - t0);
-    if (it + 1 < n_tiles) load_tile(xs_base + ((it + 1) & 1) * 16384u, X, t0 + TILE_T, p.T);
+  for (int it = 0; it < n_tiles && ok; ++it) {
+    const int64_t t0 = tb + (int64_t)it * TC_T;
+    const int rows = (int)imin64(TC_T, te - t0);
+    const uint32_t xt = Xs + (uint32_t)(it & 1) * TC_TILE;
+    if (it + 1 < n_tiles) tc_load_tile(Xs + (uint32_t)((it + 1) & 1) * TC_TILE, X, t0 + TC_T, te);
     cp_async_commit();
     cp_async_wait<1>();
+    fence_proxy_async();          // tile and B operands: generic-proxy writes before the MMAs
     __syncthreads();
-    const uint32_t tile = xs_base + (it & 1) * 16384u;
-    // ---- x~ tile on tensor cores -------------------------------------------
-    float acc[8][4], accl[8][4];
+    if (tid == 0) {
+      tc_fence_after();
 #pragma unroll
-    for (int ni = 0; ni < 8; ++ni)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[ni][e] = accl[ni][e] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      uint32_t a[4];
-      ldsm_x4(tile + swz(m0 + (mm & 1) * 8 + r8, 2 * ks + (mm >> 1)), a);
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        const int jr = n0 + np * 16 + (mm >> 1) * 8 + r8;
-        const uint32_t off = swz(jr, 2 * ks + (mm & 1));
-        uint32_t bh[4], bl[4];
-        ldsm_x4(rhi + off, bh);
-        ldsm_x4(rlo + off, bl);
-        mma16816(acc[2 * np], a, bh[0], bh[1]);
-        mma16816(acc[2 * np + 1], a, bh[2], bh[3]);
-        mma16816(accl[2 * np], a, bl[0], bl[1]);
-        mma16816(accl[2 * np + 1], a, bl[2], bl[3]);
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t ko = (uint32_t)(k >> 2) * TC_ATOMS + (uint32_t)(k & 3) * 32u;
+        const uint64_t a = sdesc_k_sw128(xt + ko);
+        tc_mma_f16(tbase, a, sdesc_k_sw128(Bhi + ko), idesc, k > 0 ? 1u : 0u);
+        tc_mma_f16(tbase + 128, a, sdesc_k_sw128(Blo + ko), idesc, k > 0 ? 1u : 0u);
       }
+      tc_commit(&mma_bar);
     }
+    if (!tc_wait(&mma_bar, (uint32_t)(it & 1), p.err)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    // ---- token tid's rotated values: fp32 tile row and magnitude keys --------
     {
-      const int g = lane >> 2, q = lane & 3;
-      constexpr float kLo = 1.f / 2048.f;
+      uint32_t k[D];
+      const uint32_t ta = tbase + ((uint32_t)(warp * 32) << 16);
 #pragma unroll
-      for (int ni = 0; ni < 8; ++ni) {
-        const int col = n0 + ni * 8 + 2 * q;
-        *reinterpret_cast<float2*>(Xt + (m0 + g) * XT_LD + col) =
-            make_float2(fmaf(accl[ni][0], kLo, acc[ni][0]), fmaf(accl[ni][1], kLo, acc[ni][1]));
-        *reinterpret_cast<float2*>(Xt + (m0 + g + 8) * XT_LD + col) =
-            make_float2(fmaf(accl[ni][2], kLo, acc[ni][2]), fmaf(accl[ni][3], kLo, acc[ni][3]));
+      for (int q = 0; q < D / 16; ++q) {
+        uint32_t h[16], l[16];
+        tmem_ld16(ta + 16 * q, h);
+        tmem_ld16(ta + 128 + 16 * q, l);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float v = fmaf(__uint_as_float(l[j]), 1.f / 2048.f, __uint_as_float(h[j]));
+          Xt[tid * XT_LD + 16 * q + j] = v;
+          k[16 * q + j] = __float_as_uint(v) & 0x7fffffffu;
+        }
+      }
+      if (!PACK && tid < rows) {
+        uint32_t m[4];
+        const float kept = thread_topc(k, p.c, m);
+        *reinterpret_cast<uint4*>(tokmask + 4 * tid) = make_uint4(m[0], m[1], m[2], m[3]);
+        tokkept[tid] = kept;
+        *reinterpret_cast<uint4*>(gmask + (size_t)(t0 + tid) * 4) = make_uint4(m[0], m[1], m[2], m[3]);
       }
     }
+    tc_fence_before();
     __syncthreads();
-    // ---- per-token selection (and packing) ---------------------------------
-    for (int r = warp; r < rows; r += 8) {
-      const int64_t t = t0 + r;
-      float v[4];
-      uint32_t key[4];
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        v[m] = Xt[r * XT_LD + lane + 32 * m];
-        key[m] = __float_as_uint(v[m]) & 0x7fffffffu;
-      }
-      if (!PACK) {
-        bool sel[4];
-        warp_topc(key, p.c, sel);
-        float kept = 0.f;
-#pragma unroll
-        for (int m = 0; m < 4; ++m) kept += sel[m] ? v[m] * v[m] : 0.f;
-        kept = warp_sum(kept);
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const uint32_t w = __ballot_sync(0xffffffffu, sel[m]);
-          if (lane == 0) tokmask[r * 4 + m] = w;
-        }
-        if (lane == 0) tokkept[r] = kept;
-      } else {
+    if (PACK) {
+      // ---- packed rows: warp per row --------------------------------------------
+      for (int r = warp; r < rows; r += RT_THREADS / 32) {
+        const int64_t t = t0 + r;
         const int sg = (int)(t / p.S);
         const int rl = (int)(t - (int64_t)sg * p.S);
         const SegInfo si = seginfo[sg];
@@ -562,54 +663,56 @@ __global__ void __launch_bounds__(256, 1) analyze_kernel(CompressParams p) {
         }
         uint8_t* seg = p.pool + (size_t)hdr[sg].off16 * 16u;
         const uint32_t c = (uint32_t)p.c;
+        float v[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) v[m] = Xt[r * XT_LD + lane + 32 * m];
         if (si.strategy == MKV_STRATEGY_DENSE) {
           __half* row = reinterpret_cast<__half*>(seg + 256u * rl);
 #pragma unroll
           for (int m = 0; m < 4; ++m) row[lane + 32 * m] = __float2half_rn(v[m]);
+          continue;
+        }
+        uint32_t w[4];
+        if (si.strategy == MKV_STRATEGY_SM) {
+#pragma unroll
+          for (int m = 0; m < 4; ++m) w[m] = si.mask[m];
         } else {
-          uint32_t w[4];
-          if (si.strategy == MKV_STRATEGY_SM) {
+          const uint4 g = *reinterpret_cast<const uint4*>(gmask + (size_t)t * 4);
+          w[0] = g.x;
+          w[1] = g.y;
+          w[2] = g.z;
+          w[3] = g.w;
+        }
+        __half* vrow;
+        uint8_t* irow;
+        if (si.strategy == MKV_STRATEGY_SM) {
+          vrow = reinterpret_cast<__half*>(seg + pad16(c) + 2u * c * rl);
+          irow = (rl == 0) ? seg : nullptr;
+        } else {
+          vrow = reinterpret_cast<__half*>(seg + 2u * c * rl);
+          irow = seg + 2u * c * si.rows + c * rl;
+        }
+        const uint32_t lt = (1u << lane) - 1u;
+        int before = 0;
 #pragma unroll
-            for (int m = 0; m < 4; ++m) w[m] = si.mask[m];
-          } else {
-            bool sel[4];
-            warp_topc(key, p.c, sel);
-#pragma unroll
-            for (int m = 0; m < 4; ++m) w[m] = __ballot_sync(0xffffffffu, sel[m]);
+        for (int m = 0; m < 4; ++m) {
+          if ((w[m] >> lane) & 1u) {
+            const int pos = before + __popc(w[m] & lt);
+            vrow[pos] = __float2half_rn(v[m]);
+            if (irow) irow[pos] = (uint8_t)(lane + 32 * m);
           }
-          __half* vrow;
-          uint8_t* irow;
-          if (si.strategy == MKV_STRATEGY_SM) {
-            vrow = reinterpret_cast<__half*>(seg + pad16(c) + 2u * c * rl);
-            irow = (rl == 0) ? seg : nullptr;
-          } else {
-            vrow = reinterpret_cast<__half*>(seg + 2u * c * rl);
-            irow = seg + 2u * c * si.rows + c * rl;
-          }
-          const uint32_t lt = (1u << lane) - 1u;
-          int before = 0;
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            if ((w[m] >> lane) & 1u) {
-              const int pos = before + __popc(w[m] & lt);
-              vrow[pos] = __float2half_rn(v[m]);
-              if (irow) irow[pos] = (uint8_t)(lane + 32 * m);
-            }
-            before += __popc(w[m]);
-          }
-          // zero the padding after the index bytes
-          if (si.strategy == MKV_STRATEGY_SM && rl == 0) {
-            for (uint32_t z = c + lane; z < pad16(c); z += 32) seg[z] = 0;
-          }
-          if (si.strategy == MKV_STRATEGY_PV && rl == si.rows - 1) {
-            uint8_t* ib = seg + 2u * c * si.rows;
-            for (uint32_t z = c * si.rows + lane; z < pad16(c * si.rows); z += 32) ib[z] = 0;
-          }
+          before += __popc(w[m]);
+        }
+        // zero the padding after the index bytes
+        if (si.strategy == MKV_STRATEGY_SM && rl == 0) {
+          for (uint32_t z = c + lane; z < pad16(c); z += 32) seg[z] = 0;
+        }
+        if (si.strategy == MKV_STRATEGY_PV && rl == si.rows - 1) {
+          uint8_t* ib = seg + 2u * c * si.rows;
+          for (uint32_t z = c * si.rows + lane; z < pad16(c * si.rows); z += 32) ib[z] = 0;
         }
       }
-    }
-    __syncthreads();
-    if (!PACK) {
+    } else {
       // ---- segment statistics: walk the segments that intersect this tile ----
       int64_t a = t0;
       const int64_t tend = t0 + rows;
@@ -617,17 +720,18 @@ __global__ void __launch_bounds__(256, 1) analyze_kernel(CompressParams p) {
         const int sg = (int)(a / p.S);
         const int64_t segend = imin64(p.T, (int64_t)(sg + 1) * p.S);
         const int64_t b = imin64(tend, segend);
-        if (tid < D) {
+        {
           float cacc = colacc[tid];
           for (int64_t t = a; t < b; ++t) {
             const float val = Xt[(int)(t - t0) * XT_LD + tid];
             cacc = fmaf(val, val, cacc);
           }
           colacc[tid] = cacc;
-        } else if (tid == D) {
-          float k = segkept[0];
-          for (int64_t t = a; t < b; ++t) k += tokkept[(int)(t - t0)];
-          segkept[0] = k;
+        }
+        if (tid == 0) {
+          float kk = segkept[0];
+          for (int64_t t = a; t < b; ++t) kk += tokkept[(int)(t - t0)];
+          segkept[0] = kk;
         }
         __syncthreads();
         if (b == segend) {
@@ -678,15 +782,19 @@ __global__ void __launch_bounds__(256, 1) analyze_kernel(CompressParams p) {
             }
           }
           __syncthreads();
-          if (tid < D) colacc[tid] = 0.f;
-          if (tid == D) segkept[0] = 0.f;
+          colacc[tid] = 0.f;
+          if (tid == 0) segkept[0] = 0.f;
           __syncthreads();
         }
         a = b;
       }
     }
+    __syncthreads();              // the fp32 tile is rewritten by the next tile
   }
   cp_async_wait<0>();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tbase, 256);
 }
 
 // ---------------------------------------------------------------------------
@@ -736,9 +844,11 @@ __global__ void __launch_bounds__(1024) scan_kernel(CompressParams p) {
 // launchers
 // ---------------------------------------------------------------------------
 cudaError_t launch_gram(const CompressParams& p, cudaStream_t st) {
-  const int smem = GR_STAGES * 16384;
+  cudaError_t e = cudaFuncSetAttribute(gram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)GT_SMEM);
+  if (e != cudaSuccess) return e;
   dim3 grid(p.gram_chunks, p.BH, 2);
-  gram_kernel<<<grid, 256, smem, st>>>(p);
+  gram_kernel<<<grid, GT_THREADS, GT_SMEM, st>>>(p);
   return cudaGetLastError();
 }
 
@@ -751,17 +861,17 @@ cudaError_t launch_eig(const CompressParams& p, cudaStream_t st) {
 }
 
 template <bool PACK>
-static cudaError_t launch_an(const CompressParams& p, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(analyze_kernel<PACK>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)AN_SMEM);
+static cudaError_t launch_rot(const CompressParams& p, cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(rotate_kernel<PACK>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)RT_SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(p.ctas_per_stream, p.BH, 2);
-  analyze_kernel<PACK><<<grid, 256, AN_SMEM, st>>>(p);
+  rotate_kernel<PACK><<<grid, RT_THREADS, RT_SMEM, st>>>(p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_analyze(const CompressParams& p, cudaStream_t st) { return launch_an<false>(p, st); }
-cudaError_t launch_pack(const CompressParams& p, cudaStream_t st) { return launch_an<true>(p, st); }
+cudaError_t launch_analyze(const CompressParams& p, cudaStream_t st) { return launch_rot<false>(p, st); }
+cudaError_t launch_pack(const CompressParams& p, cudaStream_t st) { return launch_rot<true>(p, st); }
 
 cudaError_t launch_scan(const CompressParams& p, cudaStream_t st) {
   scan_kernel<<<1, 1024, 0, st>>>(p);

@@ -82,6 +82,7 @@ struct mkv_ctx {
 
   // compression scratch
   SegInfo* seg = nullptr;
+  uint32_t* tokmask = nullptr;     // [2][BH][max_ctx][4] per-token channel masks
   float* gram_part = nullptr;
   unsigned long long* total_dev = nullptr;
   unsigned long long* total_host = nullptr;
@@ -192,6 +193,7 @@ void release(mkv_ctx* c) {
   }
   cudaFree(c->pool);
   cudaFree(c->seg);
+  cudaFree(c->tokmask);
   cudaFree(c->gram_part);
   cudaFree(c->total_dev);
   if (c->total_host) cudaFreeHost(c->total_host);
@@ -361,6 +363,7 @@ mkv_status mkv_create(const mkv_config* cfg, mkv_ctx** out) {
     AL(c->plan_n[i], (size_t)c->G);
   }
   AL(c->seg, 2 * BH * (size_t)c->max_seg);
+  AL(c->tokmask, 2 * BH * (size_t)cfg->max_ctx * 4);
   AL(c->gram_part, 2 * BH * (size_t)c->gram_chunks_max * D * D);
   AL(c->total_dev, 3);
   AL(c->qt, (size_t)c->B * c->Hq * D);
@@ -415,7 +418,7 @@ mkv_status mkv_compress(mkv_ctx* c, const void* k, const void* v, int64_t ctx_le
   p.tau = c->cfg.tau;
   p.n_seg = (int)ceil_div(ctx_len, p.S);
   p.gram_chunks = std::min(c->gram_chunks_max, gram_chunks_for(c->BH, ctx_len));
-  p.gram_chunk_tokens = ceil_div(ceil_div(ctx_len, p.gram_chunks), TILE_T) * TILE_T;
+  p.gram_chunk_tokens = ceil_div(ceil_div(ctx_len, p.gram_chunks), GRAM_TILE) * GRAM_TILE;
   p.gram_chunks = (int)ceil_div(ctx_len, p.gram_chunk_tokens);
   p.gram_part = c->gram_part;
   p.R = c->R[stage];
@@ -426,6 +429,7 @@ mkv_status mkv_compress(mkv_ctx* c, const void* k, const void* v, int64_t ctx_le
   p.segs_per_cta = (int)std::max<int64_t>(1, ceil_div(total_segs, want_ctas));
   p.ctas_per_stream = (int)ceil_div(p.n_seg, p.segs_per_cta);
   p.seg = c->seg;
+  p.tokmask = c->tokmask;
   p.hdr = c->hdr[stage];
   p.total = c->total_dev;
   p.pool = nullptr;
@@ -717,7 +721,7 @@ mkv_status mkv_basis_static(const void* k, const void* v, int batch, int n_kv_he
   // mkv_compress's chunk count, reduced only when the partials would not fit
   p.gram_chunks = (int)std::min<int64_t>(gram_chunks_for(p.BH, ctx_len),
                                          kBasisStaticParts / streams);
-  p.gram_chunk_tokens = ceil_div(ceil_div(ctx_len, p.gram_chunks), TILE_T) * TILE_T;
+  p.gram_chunk_tokens = ceil_div(ceil_div(ctx_len, p.gram_chunks), GRAM_TILE) * GRAM_TILE;
   p.gram_chunks = (int)ceil_div(ctx_len, p.gram_chunk_tokens);
   p.gram_part = scratch;
   p.R = basis;

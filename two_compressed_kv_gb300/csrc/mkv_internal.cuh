@@ -11,10 +11,10 @@ namespace mkv {
 
 constexpr int D = 128;                 // head dim
 constexpr int MAX_G = 16;              // query heads per KV head
+constexpr int GRAM_TILE = 128;         // tokens per tensor-core tile of the prefill kernels
 constexpr int HIST1 = 4096;            // level-1 radix digit of the score key: bits 31..20
 constexpr int HISTA = 1024;            // candidates, bits 19..10
 constexpr int HISTB = 1024;            // candidates, bits  9..0
-constexpr int TILE_T = 64;             // tokens per rotation tile
 constexpr int ATTN_MAX_CHUNK = 128;    // largest explicit attention slice (mkv_config.attn_chunk)
 
 __host__ __device__ inline int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
@@ -53,7 +53,7 @@ struct CompressParams {
   int n_seg;                 // segments per stream
   // Gram pass
   int gram_chunks;           // CTAs per stream in the Gram pass
-  int64_t gram_chunk_tokens; // tokens per Gram CTA (multiple of 64)
+  int64_t gram_chunk_tokens; // tokens per Gram CTA (multiple of GRAM_TILE)
   float* gram_part;          // [2][BH][gram_chunks][128][128]
   // basis
   float* R;                  // [2][BH][128][128]
@@ -62,6 +62,7 @@ struct CompressParams {
   int segs_per_cta;          // segments per CTA
   int ctas_per_stream;
   SegInfo* seg;              // [2][BH][n_seg]
+  uint32_t* tokmask;         // [2][BH][T][4]: per-token channel masks (statistics -> packing)
   mkv_segment_header* hdr;   // [2][BH][n_seg]
   unsigned long long* total; // device: [0] total packed bytes, [1..2] dense segments of K, V
   uint8_t* pool;
