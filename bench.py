@@ -527,12 +527,15 @@ def run_gpu(args, w: W.Workload, ws: int, rank: int, local: int):
                          f"median {per * 1e3:.0f} ms, scaled to the {w.n_kv_heads} KV heads "
                          f"of a token"}
 
+    comp_kernels = None
     side = {}
-    if rank == 0 and not args.no_side:
+    if rank == 0:
         for c in ctxs:
             c.close()
         ctxs = []
         torch.cuda.empty_cache()
+        comp_kernels = compress_kernel_ms(w, dev)
+    if rank == 0 and not args.no_side:
         for name, layers in ((W.MILLION_1M.name, 1), (W.MIXED_256K.name, 1)):
             side[name] = side_workload(W.WORKLOADS[name], layers, max(5, args.steps), dev, stream)
             torch.cuda.empty_cache()
@@ -573,11 +576,34 @@ def run_gpu(args, w: W.Workload, ws: int, rank: int, local: int):
             "ctx_tokens_per_step": tok,
         }
         line["prefill"].update(prefill_roofline(w, statistics.median(comp_ms), st0, peak))
+        line["prefill"]["kernel_ms_per_layer"] = comp_kernels
         if side:
             line["other_workloads"] = side
         print(json.dumps(line), flush=True)
     for m in ctxs:
         m.close()
+
+
+def compress_kernel_ms(w: W.Workload, dev) -> dict:
+    """Device time of each compression step for layer 0 (a fresh ctx with
+    kernel timing on; the layer is compressed twice, the second is read)."""
+    from two_compressed_kv_gb300 import mkv as M
+    cfg = M.make_config(w.batch, w.n_kv_heads, w.n_q_heads, w.ctx, w.segment, w.c, w.tau,
+                        w.top_k, flags=M.MKV_FLAG_KERNEL_TIMING, device=dev.index or 0)
+    K, V = W.draw_kv(w, layer=0, device=dev)
+    out = {}
+    with M.Mkv(cfg) as m:
+        m.compress(K, V)
+        torch.cuda.synchronize(dev)
+        for kid in range(5, 10):
+            M.mkv_kernel_time(m.ctx, kid, reset=True)
+        m.compress(K, V)
+        torch.cuda.synchronize(dev)
+        for kid, name in enumerate(M.COMPRESS_KERNEL_NAMES, start=5):
+            out[name] = M.mkv_kernel_time(m.ctx, kid)[0]
+    del K, V
+    torch.cuda.empty_cache()
+    return out
 
 
 def prefill_roofline(w: W.Workload, ms: float, st: dict, peak_gbs: float) -> dict:
@@ -675,6 +701,8 @@ def side_workload(w: W.Workload, layers: int, steps: int, dev, stream) -> dict:
     res["prefill"].update(prefill_roofline(w, statistics.median(comp), st0, peak))
     for m in ctxs:
         m.close()
+    ctxs = []
+    res["prefill"]["kernel_ms_per_layer"] = compress_kernel_ms(w, dev)
     return res
 
 

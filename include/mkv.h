@@ -125,14 +125,20 @@ typedef struct {
   int64_t kernel_launches;         /* kernels launched by this ctx since creation */
 } mkv_stats_t;
 
-/* Kernel ids for mkv_kernel_time. */
+/* Kernel ids for mkv_kernel_time: the decode kernels, then (with
+ * MKV_FLAG_KERNEL_TIMING) the compression steps. */
 enum {
   MKV_KERNEL_QROT = 0,
   MKV_KERNEL_SCORE = 1,
   MKV_KERNEL_TOPK = 2,   /* the exact top-k selection */
   MKV_KERNEL_ATTN = 3,
   MKV_KERNEL_MERGE = 4,
-  MKV_KERNEL_COUNT = 5
+  MKV_KERNEL_GRAM = 5,   /* G = X^T X partial sums */
+  MKV_KERNEL_EIG = 6,    /* basis and eigenvalues */
+  MKV_KERNEL_ANALYZE = 7,/* rotation, per-token channels, segment strategies */
+  MKV_KERNEL_LAYOUT = 8, /* offsets, headers, score-kernel partition and plan */
+  MKV_KERNEL_PACK = 9,   /* packed payload */
+  MKV_KERNEL_COUNT = 10
 };
 
 /* Checks a config without touching any GPU.  MKV_OK or MKV_ERR_INVALID_ARG. */

@@ -211,8 +211,10 @@ struct EigShared {
 };
 
 // Jacobi sweeps on A (in place), accumulating the rotations into V, until a
-// sweep rotates nothing or max_sweeps have run.  Block-wide.
-__device__ void jacobi_sweeps(float* A, float* V, int max_sweeps, EigShared& sh) {
+// sweep rotates nothing or max_sweeps have run.  A pair (p, q) is rotated
+// when |a_pq| > tol sqrt(|a_pp a_qq|); blocks and columns whose rotations
+// are all identities are left untouched.  Block-wide.
+__device__ void jacobi_sweeps(float* A, float* V, int max_sweeps, float tol, EigShared& sh) {
   const int tid = threadIdx.x;
   for (int sweep = 0; sweep < max_sweeps; ++sweep) {
     if (tid == 0) sh.rotated = 0;
@@ -223,7 +225,7 @@ __device__ void jacobi_sweeps(float* A, float* V, int max_sweeps, EigShared& sh)
         const int pp = min(a, b), qq = max(a, b);
         const float app = A[pp * LDA + pp], aqq = A[qq * LDA + qq], apq = A[pp * LDA + qq];
         float c = 1.f, s = 0.f, t = 0.f;
-        if (apq != 0.f && fabsf(apq) > 1e-7f * sqrtf(fabsf(app * aqq))) {
+        if (apq != 0.f && fabsf(apq) > tol * sqrtf(fabsf(app * aqq))) {
           const float th = (aqq - app) / (2.f * apq);
           t = (th >= 0.f ? 1.f : -1.f) / (fabsf(th) + sqrtf(1.f + th * th));
           c = 1.f / sqrtf(1.f + t * t);
@@ -239,6 +241,7 @@ __device__ void jacobi_sweeps(float* A, float* V, int max_sweeps, EigShared& sh)
       __syncthreads();
       for (int blk = tid; blk < 64 * 64; blk += EIG_THREADS) {
         const int P = blk >> 6, Q = blk & 63;
+        if (sh.sn[P] == 0.f && sh.sn[Q] == 0.f) continue;   // both rotations are identities
         const int p1 = sh.top[P], p2 = sh.bot[P];
         if (P == Q) {
           const float apq = A[p1 * LDA + p2], t = sh.tt[P];
@@ -261,8 +264,9 @@ __device__ void jacobi_sweeps(float* A, float* V, int max_sweeps, EigShared& sh)
       }
       for (int e = tid; e < D * 64; e += EIG_THREADS) {
         const int r = e >> 6, k = e & 63;
-        const int pp = sh.top[k], qq = sh.bot[k];
         const float c = sh.cs[k], s = sh.sn[k];
+        if (s == 0.f) continue;
+        const int pp = sh.top[k], qq = sh.bot[k];
         const float vp = V[r * LDA + pp], vq = V[r * LDA + qq];
         V[r * LDA + pp] = c * vp - s * vq;
         V[r * LDA + qq] = s * vp + c * vq;
@@ -351,7 +355,9 @@ __global__ void __launch_bounds__(EIG_THREADS) eig_kernel(CompressParams p) {
   }
   __syncthreads();
 
-  jacobi_sweeps(A, V, EIG_MAX_SWEEPS, sh);
+  // the first solve only has to bring A close to diagonal: the refinement
+  // below re-forms V^T G V and finishes the convergence
+  jacobi_sweeps(A, V, EIG_MAX_SWEEPS, 1e-5f, sh);
   // refinement: orthonormal V, then A = V^T G V from the original G
   newton_schulz(V, A);
   smem_matmul<false>(Gs, V, A);     // A = G V
@@ -367,7 +373,7 @@ __global__ void __launch_bounds__(EIG_THREADS) eig_kernel(CompressParams p) {
     }
   }
   __syncthreads();
-  jacobi_sweeps(Ar, V, EIG_REFINE_SWEEPS, sh);
+  jacobi_sweeps(Ar, V, EIG_REFINE_SWEEPS, 1e-7f, sh);
   if (tid < D) lam[tid] = Ar[tid * LDA + tid];
   __syncthreads();
   newton_schulz(V, W);

@@ -434,13 +434,19 @@ mkv_status mkv_compress(mkv_ctx* c, const void* k, const void* v, int64_t ctx_le
   p.total = c->total_dev;
   p.pool = nullptr;
 
-  CK(launch_gram(p, st));
-  CK(launch_eig(p, st));
-  CK(launch_analyze(p, st));
-  CK(launch_scan(p, st));
-  CK(launch_partition(p.hdr, c->BH, p.n_seg, p.c, c->G, c->stage_bytes, c->part[stage],
-                      c->cta_cnt[stage], c->plan[stage], c->plan_n[stage], st));
-  c->launches += 6;
+  mkv_status s;
+  if ((s = timed(c, MKV_KERNEL_GRAM, st, 1, [&] { return launch_gram(p, st); })) != MKV_OK) return s;
+  if ((s = timed(c, MKV_KERNEL_EIG, st, 1, [&] { return launch_eig(p, st); })) != MKV_OK) return s;
+  if ((s = timed(c, MKV_KERNEL_ANALYZE, st, 1, [&] { return launch_analyze(p, st); })) != MKV_OK)
+    return s;
+  if ((s = timed(c, MKV_KERNEL_LAYOUT, st, 3, [&] {
+         cudaError_t e = launch_scan(p, st);
+         if (e == cudaSuccess)
+           e = launch_partition(p.hdr, c->BH, p.n_seg, p.c, c->G, c->stage_bytes, c->part[stage],
+                                c->cta_cnt[stage], c->plan[stage], c->plan_n[stage], st);
+         return e;
+       })) != MKV_OK)
+    return s;
   CK(cudaMemcpyAsync(c->total_host, c->total_dev, 3 * sizeof(unsigned long long),
                      cudaMemcpyDeviceToHost, st));
   CK(cudaStreamSynchronize(st));
@@ -471,8 +477,7 @@ mkv_status mkv_compress(mkv_ctx* c, const void* k, const void* v, int64_t ctx_le
   p.pool_check = c->check_override ? std::min(c->check_override, need) : need;
   p.err = c->err;
   c->ready = false;   // the live headers may no longer match the pool
-  CK(launch_pack(p, st));
-  c->launches += 1;
+  if ((s = timed(c, MKV_KERNEL_PACK, st, 1, [&] { return launch_pack(p, st); })) != MKV_OK) return s;
   c->live = stage;
   c->pool_need = need;
   // the attention kernel's per-token slot: room for a dense row only when

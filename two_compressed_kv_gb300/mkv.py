@@ -30,8 +30,10 @@ MKV_FLAG_KERNEL_TIMING = 1
 MKV_FLAG_SCORE_TIMING = 2
 MKV_FLAG_NO_PDL = 4
 MKV_BASIS_STATIC_MAX_BYTES = 16 << 20
-MKV_KERNEL_QROT, MKV_KERNEL_SCORE, MKV_KERNEL_TOPK, MKV_KERNEL_ATTN, MKV_KERNEL_MERGE = range(5)
-KERNEL_NAMES = ["qrot", "score", "topk", "attn", "merge"]
+(MKV_KERNEL_QROT, MKV_KERNEL_SCORE, MKV_KERNEL_TOPK, MKV_KERNEL_ATTN, MKV_KERNEL_MERGE,
+ MKV_KERNEL_GRAM, MKV_KERNEL_EIG, MKV_KERNEL_ANALYZE, MKV_KERNEL_LAYOUT, MKV_KERNEL_PACK) = range(10)
+KERNEL_NAMES = ["qrot", "score", "topk", "attn", "merge"]          # decode kernels
+COMPRESS_KERNEL_NAMES = ["gram", "eig", "analyze", "layout", "pack"]  # ids 5..9
 
 
 class mkv_config(Structure):
