@@ -31,7 +31,7 @@ g = query heads per KV head.
 
 Functions whose results have no independent pin are marked "parity unpinned"
 in their docstring.  At present every function is pinned by a test in
-tests/test_oracle_pins.py.
+tests/test_oracle_pins.py (the append functions by tests/test_oracle_append.py).
 """
 from __future__ import annotations
 
@@ -397,3 +397,70 @@ def decode_layer(layer: CompressedLayer, q: np.ndarray, k: int):
             sel[b, h] = r.sel
             scores[b, h] = r.scores
     return out, sel, scores
+
+
+# ---------------------------------------------------------------------------
+# Decode-time appends (§1 "Observation & Method 2: compressed KV cache
+# management": newly generated KV stay in a GPU-side buffer, are attended in
+# later decode steps, and full segments are compressed and switched in)
+# ---------------------------------------------------------------------------
+def append_rows(X_new: np.ndarray, R: np.ndarray) -> np.ndarray:
+    """READING: a newly generated token waits in the buffer as its rotated
+    vector x R (the stream's existing basis) in fp16 with every channel kept,
+    i.e. a dense row.  Returns the stored values as [n, d] fp64."""
+    return to_fp16(rotate(X_new, R)).astype(np.float64)
+
+
+@dataclass
+class GrownStream:
+    """A compressed stream with decode-time appends.
+
+    READING: the prefill part keeps its segments (the last one possibly
+    ragged); appended tokens fill a buffer of up to S tokens; whenever the
+    buffer holds S tokens they are compressed as one segment with the
+    stream's basis, by the same steps as the prefill (compress_stream with
+    R given), and committed after the prefill part and earlier commits.
+    Token order: prefill tokens, committed segments, then the buffer."""
+    base: CompressedStream
+    committed: List[CompressedStream] = field(default_factory=list)
+    tail: Optional[np.ndarray] = None        # [n, d] fp16 tokens not yet committed
+
+    @property
+    def S(self) -> int:
+        return self.base.S
+
+    @property
+    def T(self) -> int:
+        return self.base.T + self.S * len(self.committed) + self.n_tail
+
+    @property
+    def n_tail(self) -> int:
+        return 0 if self.tail is None else self.tail.shape[0]
+
+
+def append_stream(gs: GrownStream, X_new: np.ndarray, tau: float) -> GrownStream:
+    """Adds tokens [n, d] (fp16) to the buffer, committing every full S."""
+    X_new = np.asarray(X_new)
+    d = gs.base.d
+    tail = np.zeros((0, d), dtype=X_new.dtype) if gs.tail is None else gs.tail
+    tail = np.concatenate([tail, X_new], axis=0)
+    committed = list(gs.committed)
+    while tail.shape[0] >= gs.S:
+        seg, tail = tail[:gs.S], tail[gs.S:]
+        committed.append(compress_stream(seg, gs.S, gs.base.c, tau, R=gs.base.R))
+    return GrownStream(base=gs.base, committed=committed, tail=tail)
+
+
+def grown_dense_hat(gs: GrownStream) -> np.ndarray:
+    """[T, d] fp64 of the values decode reads: the prefill part's stored
+    values, the committed segments', then the buffer's dense rows."""
+    parts = [gs.base.dense_hat()] + [cs.dense_hat() for cs in gs.committed]
+    if gs.n_tail:
+        parts.append(append_rows(gs.tail, gs.base.R))
+    return np.concatenate(parts, axis=0)
+
+
+def grown_segment_starts(T0: int, S: int, n_committed: int) -> List[int]:
+    """First token of every segment: the prefill segments at multiples of S,
+    then one committed segment per S tokens after the prefill's end."""
+    return list(range(0, T0, S)) + [T0 + i * S for i in range(n_committed)]
