@@ -484,7 +484,8 @@ mkv_status mkv_compress(mkv_ctx* c, const void* k, const void* v, int64_t ctx_le
   // the cache has dense segments
   c->at_kv = dense_k ? 256 : 2 * p.c;
   c->at_vv = dense_v ? 256 : 2 * p.c;
-  c->at_ki = c->at_vi = (int)pad16((uint32_t)p.c);
+  // channel lists are copied from the 16-byte boundary at or below their start
+  c->at_ki = c->at_vi = (int)pad16((uint32_t)p.c + 8u);
   CK(attn_shape(c->g, c->at_kv + c->at_ki + c->at_vv + c->at_vi, &c->at_stages,
                 &c->at_ctas_per_sm));
   c->T = ctx_len;
