@@ -13,10 +13,10 @@ namespace mkv {
 // attn_per positions, one slice per CTA.  A CTA walks its slice in chunks of
 // up to 64 tokens that never cross a stream boundary (chunk = the 64-position
 // blocks of a stream, clipped to the slice).  Per chunk:
-//   issue   (stages - 1 chunks ahead) one lane per token moves its K and V
-//           rows (values and channel lists, resolved for the whole pass
-//           beforehand) into the chunk's stage slot with bulk copies that
-//           complete on the stage's mbarrier;
+//   issue   (stages - 1 chunks ahead) every lane of the token's 8-lane group
+//           reads the token id and its K and V segment headers, and copies
+//           its pieces of the two packed rows (16-byte value chunks, 8-byte
+//           channel lists) into the chunk's stage slot with cp.async;
 //   A       8 lanes per token: partial logits q~_i . k^_t over the lane's
 //           stored values (q~ indexed by the stored channel), summed over the
 //           group by a fixed butterfly; V values scattered into a zeroed fp16
@@ -189,54 +189,37 @@ __device__ __forceinline__ void at_meta_pass(const DecodeParams& p, int64_t lo, 
 }
 
 // Issues the copies of chunk ch into stage `st` (rel_s: the chunk stream's
-// start relative to the pass).  Lane 0 of token i's 8-lane group moves the
-// token's rows with the bulk-copy engine: the K values, the K channel list,
-// the V values and the V channel list, each as one copy completing on the
-// stage's mbarrier.  A channel list is copied from the 16-byte boundary at or
-// below its start (a PV row's list may start 8 bytes past one); the copy
-// stays inside the segment's 16-byte padded index area.  Tokens past the
-// chunk's end arrive without bytes, so the barrier always counts 64 arrivals.
+// start relative to the pass): token tid / 8, lane tid % 8; rows from the
+// pass's meta[].
 __device__ __forceinline__ void at_issue(const DecodeParams& p, int rel_s, const AtChunk& ch,
-                                         int st, uint8_t* smem, const AtLayout& L, uint64_t* bar,
-                                         uint64_t pol) {
+                                         int st, uint8_t* smem, const AtLayout& L) {
   const int i = threadIdx.x >> 3, cl = threadIdx.x & 7;
-  if (cl != 0) return;
-  if (i >= ch.n) {
-    mbar_arrive(&bar[st]);
-    return;
-  }
-  const uint32_t c = (uint32_t)p.c;
+  if (i >= ch.n) return;
+  const int c = p.c;
   const uint4 m = reinterpret_cast<const uint4*>(smem + L.meta)[ch.j0 + i + rel_s];
-  uint8_t* slot = smem + L.stages + (size_t)(st * AT_CHUNK + i) * p.at_slot;
+  const uint32_t slot = smem_u32(smem + L.stages) + (uint32_t)((st * AT_CHUNK + i) * p.at_slot);
   const bool kd = (int32_t)m.y == NO_IDX, vd = (int32_t)m.w == NO_IDX;
-  const uint64_t k0 = (uint64_t)m.x * 16u, v0 = (uint64_t)m.z * 16u;
-  const uint32_t kvb = kd ? 256u : 2u * c, vvb = vd ? 256u : 2u * c;
-  uint64_t ka = 0, va = 0;
-  uint32_t kib = 0, vib = 0;
-  if (!kd) {
-    const uint64_t s0 = (uint64_t)((int64_t)k0 + 8 * (int64_t)(int32_t)m.y);
-    ka = s0 & ~15ull;
-    kib = pad16((uint32_t)(s0 + c - ka));
+  const int kn = kd ? D : c, vn = vd ? D : c;
+  const uint8_t* kv = p.pool + (uint64_t)m.x * 16u;
+  const uint8_t* vv = p.pool + (uint64_t)m.z * 16u;
+  const uint32_t vs = slot + p.at_kv + p.at_ki;
+#pragma unroll
+  for (int ck = cl; ck < 16; ck += 8) {
+    if (8 * ck < kn) {
+      cpa16(slot + 16 * ck, kv + 16 * ck);
+      if (!kd) cpa8(slot + p.at_kv + 8 * ck, kv + 8 * (int64_t)(int32_t)m.y + 8 * ck);
+    }
+    if (8 * ck < vn) {
+      cpa16(vs + 16 * ck, vv + 16 * ck);
+      if (!vd) cpa8(vs + p.at_vv + 8 * ck, vv + 8 * (int64_t)(int32_t)m.w + 8 * ck);
+    }
   }
-  if (!vd) {
-    const uint64_t s0 = (uint64_t)((int64_t)v0 + 8 * (int64_t)(int32_t)m.w);
-    va = s0 & ~15ull;
-    vib = pad16((uint32_t)(s0 + c - va));
-  }
-  fence_proxy_async();       // this slot's earlier generic reads, before the async writes
-  mbar_arrive_expect_tx(&bar[st], kvb + kib + vvb + vib);
-  bulk_g2s(slot, p.pool + k0, kvb, &bar[st], pol);
-  if (kib) bulk_g2s(slot + p.at_kv, p.pool + ka, kib, &bar[st], pol);
-  uint8_t* vs = slot + p.at_kv + p.at_ki;
-  bulk_g2s(vs, p.pool + v0, vvb, &bar[st], pol);
-  if (vib) bulk_g2s(vs + p.at_vv, p.pool + va, vib, &bar[st], pol);
 }
 
 template <int NST>
 __global__ void __launch_bounds__(AT_THREADS, 2) attn_kernel(DecodeParams p) {
   extern __shared__ __align__(128) uint8_t at_smem[];
   __shared__ float s_m[MAX_G], s_l[MAX_G], s_alpha[MAX_G];
-  __shared__ uint64_t stage_bar[NST];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int tok = tid >> 3, cl = tid & 7;
   const int g = p.g, gp = (g + 3) & ~3, c = p.c;
@@ -260,10 +243,6 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_kernel(DecodeParams p) {
       s_m[tid] = -INFINITY;
       s_l[tid] = 0.f;
     }
-    if (tid == 0) {
-      for (int st = 0; st < NST; ++st) mbar_init(&stage_bar[st], AT_CHUNK);
-      mbar_init_fence();
-    }
   }
   griddep_wait();     // the selection comes from the kernel before this one
   if (p.pdl_trigger) griddep_launch();
@@ -273,12 +252,10 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_kernel(DecodeParams p) {
   const int n0 = warp * 8;                       // this warp's output channels in phase C
   float acc_h[4] = {0.f, 0.f, 0.f, 0.f}, acc_l[4] = {0.f, 0.f, 0.f, 0.f};
   int cur_s = -1;
-  const uint64_t pol = policy_evict_first();
-  uint32_t parity = 0;                   // bit st: parity of stage st's next completion
-  bool ok = true;
   // passes of at most AT_META positions: resolve their rows, then stream them
-  for (int64_t pa = lo; pa < hi && ok; pa += AT_META) {
+  for (int64_t pa = lo; pa < hi; pa += AT_META) {
     const int64_t pb = pa + AT_META < hi ? pa + AT_META : hi;
+    if (pa != lo) cpa_wait<0>();
     __syncthreads();                     // the previous pass no longer reads meta[]
     at_meta_pass(p, pa, pb, meta);
     __syncthreads();
@@ -289,9 +266,9 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_kernel(DecodeParams p) {
 #pragma unroll
     for (int n = 0; n < NST - 1; ++n) {
       AtChunk ich;
-      if (at_get(iit, p.kk, n_pass, slice_end, ich))
-        at_issue(p, iit.rel, ich, n, at_smem, L, stage_bar, pol);
+      if (at_get(iit, p.kk, n_pass, slice_end, ich)) at_issue(p, iit.rel, ich, n, at_smem, L);
       at_advance(iit, p.kk);
+      cpa_commit();
     }
     for (int n = 0;; ++n) {
       AtChunk ch;
@@ -301,20 +278,13 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_kernel(DecodeParams p) {
       {
         AtChunk ich;
         if (at_get(iit, p.kk, n_pass, slice_end, ich))
-          at_issue(p, iit.rel, ich, (n + NST - 1) % NST, at_smem, L, stage_bar, pol);
+          at_issue(p, iit.rel, ich, (n + NST - 1) % NST, at_smem, L);
         at_advance(iit, p.kk);
       }
+      cpa_commit();
+      cpa_wait<NST - 1>();
+      __syncthreads();
       const int st = n % NST;
-      if (!mbar_wait(&stage_bar[st], (parity >> st) & 1u)) {
-        // a copy never landed: report, then wait (bounded) for the others
-        if (tid == 0) atomicOr(p.err, DEV_ERR_TIMEOUT);
-        ok = false;
-      }
-      parity ^= 1u << st;
-      if (__syncthreads_or(!ok)) {
-        ok = false;
-        break;
-      }
         if (ch.s != cur_s) {
         cur_s = ch.s;
         const int b = ch.s / p.H, h = ch.s % p.H;
@@ -339,8 +309,7 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_kernel(DecodeParams p) {
             if (8 * ck < kn) {
               const uint4 kr = *reinterpret_cast<const uint4*>(slot + 16 * ck);
               const uint2 kx = kd ? make_uint2(0u, 0u)
-                                  : *reinterpret_cast<const uint2*>(
-                                        slot + p.at_kv + 8 * (mt.y & 1u) + 8 * ck);
+                                  : *reinterpret_cast<const uint2*>(slot + p.at_kv + 8 * ck);
               float v[8];
               h8_to_f(kr, v);
   #pragma unroll
@@ -372,8 +341,7 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_kernel(DecodeParams p) {
             const uint8_t* vs = slot + p.at_kv + p.at_ki;
             const uint4 vr = *reinterpret_cast<const uint4*>(vs + 16 * ck);
             const uint2 vx = vd ? make_uint2(0u, 0u)
-                                : *reinterpret_cast<const uint2*>(
-                                      vs + p.at_vv + 8 * (mt.w & 1u) + 8 * ck);
+                                : *reinterpret_cast<const uint2*>(vs + p.at_vv + 8 * ck);
             const __half* hv = reinterpret_cast<const __half*>(&vr);
             __half* vrow = Vt + tok * AT_VLD;
   #pragma unroll
@@ -463,11 +431,7 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_kernel(DecodeParams p) {
       }
     }
   }
-  if (!ok) {
-    // after a timeout, stages may still have copies landing: wait for them
-    // (bounded) before the shared memory is given up
-    for (int st = 0; st < NST; ++st) mbar_wait(&stage_bar[st], (parity >> st) & 1u);
-  }
+  cpa_wait<0>();
 }
 
 // Slices that cover stream s's selection: the first one and how many.

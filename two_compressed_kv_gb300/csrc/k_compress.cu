@@ -453,22 +453,28 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // ---------------------------------------------------------------------------
-// Per-token top-c of one thread's 128 magnitudes (bit patterns of |x~|, which
-// order like the magnitudes), ties to the lower channel.  Bit search for the
-// c-th largest key, stopping once exactly c keys are >= the candidate; with
-// ties at the threshold the lowest channels among them are taken.  Returns
-// the 128-bit channel mask and the kept energy (sum of the kept squares in
-// channel order).
+// Per-token top-c of 128 magnitudes held by a pair of lanes (64 each: lane
+// 2k has channels 0..63, lane 2k+1 channels 64..127), ties to the lower
+// channel.  Bit search on the magnitudes' bit patterns (non-negative floats
+// order like their bits), the pair's counts combined by a shuffle whose mask
+// is the pair alone (pairs leave the loop at different steps), stopping once
+// exactly c keys are >= the candidate; with ties at the threshold the lowest
+// channels among them are taken, lane 2k's before lane 2k+1's.  Returns this
+// lane's 64 mask bits and its part of the kept energy (sum of the kept
+// squares in channel order).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float thread_topc(const uint32_t k[D], int c, uint32_t mask[4]) {
+__device__ __forceinline__ float pair_topc(const uint32_t k[64], int c, uint32_t mask[2]) {
+  const int lane = threadIdx.x & 31;
+  const unsigned pm = 3u << (lane & ~1);        // this lane and its partner
+  const bool upper = lane & 1;
   if (c >= D) {
     float kept = 0.f;
 #pragma unroll
-    for (int j = 0; j < D; ++j) {
+    for (int j = 0; j < 64; ++j) {
       const float f = __uint_as_float(k[j]);
       kept = fmaf(f, f, kept);
     }
-    mask[0] = mask[1] = mask[2] = mask[3] = 0xffffffffu;
+    mask[0] = mask[1] = 0xffffffffu;
     return kept;
   }
   uint32_t thr = 0;
@@ -477,35 +483,42 @@ __device__ __forceinline__ float thread_topc(const uint32_t k[D], int c, uint32_
     const uint32_t cand = thr | (1u << bit);
     int n0 = 0, n1 = 0, n2 = 0, n3 = 0;
 #pragma unroll
-    for (int j = 0; j < D; j += 4) {
+    for (int j = 0; j < 64; j += 4) {
       n0 += k[j] >= cand;
       n1 += k[j + 1] >= cand;
       n2 += k[j + 2] >= cand;
       n3 += k[j + 3] >= cand;
     }
-    const int cnt = (n0 + n1) + (n2 + n3);
+    int cnt = (n0 + n1) + (n2 + n3);
+    cnt += __shfl_xor_sync(pm, cnt, 1);
     if (cnt >= c) {
       thr = cand;
       cnt_ge = cnt;
       if (cnt == c) break;
     }
   }
-  int need = D;                       // keys equal to thr still taken
+  int take_eq = 64;                    // keys equal to thr that this lane still takes
   if (cnt_ge != c) {
-    int gt = 0;
+    int gt = 0, eq = 0;
 #pragma unroll
-    for (int j = 0; j < D; ++j) gt += k[j] > thr;
-    need = c - gt;
+    for (int j = 0; j < 64; ++j) {
+      gt += k[j] > thr;
+      eq += k[j] == thr;
+    }
+    const int gt_all = gt + __shfl_xor_sync(pm, gt, 1);
+    const int eq_lower = __shfl_sync(pm, eq, lane & ~1);   // equal keys of channels 0..63
+    const int need = c - gt_all;
+    take_eq = upper ? need - min(need, eq_lower) : min(need, eq);
   }
   float kept = 0.f;
   int eq = 0;
 #pragma unroll
-  for (int m = 0; m < 4; ++m) {
+  for (int m = 0; m < 2; ++m) {
     uint32_t w = 0;
 #pragma unroll
     for (int b = 0; b < 32; ++b) {
       const uint32_t kj = k[32 * m + b];
-      const bool take = kj > thr || (kj == thr && eq < need);
+      const bool take = kj > thr || (kj == thr && eq < take_eq);
       eq += kj == thr;
       w |= (uint32_t)take << b;
       const float f = __uint_as_float(kj);
@@ -518,23 +531,26 @@ __device__ __forceinline__ float thread_topc(const uint32_t k[D], int c, uint32_
 
 // ---------------------------------------------------------------------------
 // rotate: the statistics pass (PACK = false) and the packing pass (PACK =
-// true).  One CTA (4 warps) covers whole segments [sg0, sg1) of one stream in
+// true).  One CTA (8 warps) covers whole segments [sg0, sg1) of one stream in
 // tiles of 128 tokens.  x~ = x R_hi + 2^-11 (x R_lo) on the tensor cores
 // (tcgen05, M = 128 tokens, N = 128 basis vectors, K = 128 channels; R split
 // into an fp16 part and a remainder scaled by 2^11 so that it stays a normal
-// fp16, one TMEM accumulator each); thread t then reads token t's 128 rotated
-// values from tensor memory.
-//   statistics: per token the c channels of largest |x~| (thread_topc), its
-//     kept energy and channel mask (the mask also goes to global scratch for
-//     the packing pass); per segment the column energies, the shared mask
-//     and the strategy.
-//   packing: writes the packed rows (warp per row, from the fp32 x~ tile in
-//     shared memory): the segment mask for SM, the token's stored mask for
-//     PV, every channel for dense segments.
-// grid: (ctas_per_stream, BH, 2), block 128, dynamic smem RT_SMEM
+// fp16, one TMEM accumulator each).  Warps w and w + 4 read TMEM lanes
+// 32 (w mod 4) .. +31 (one token each), channels 0..63 and 64..127, into an
+// fp32 tile in shared memory.
+//   statistics: per token the c channels of largest |x~| (pair_topc: two
+//     lanes per token), its kept energy and channel mask (the mask also goes
+//     to global scratch for the packing pass); per segment the column
+//     energies and the kept energy, stored for the strategy kernel.
+//   packing: writes the packed rows, warp per row, with the segment data and
+//     the tokens' stored masks staged in shared memory first: the segment
+//     mask for SM, the token's mask for PV, every channel for dense segments.
+// grid: (ctas_per_stream, BH, 2), block 256, dynamic smem RT_SMEM
 // ---------------------------------------------------------------------------
-constexpr int RT_THREADS = 128;
+constexpr int RT_THREADS = 256;
+constexpr int RT_WARPS = RT_THREADS / 32;
 constexpr int XT_LD = D + 1;          // fp32 x~ rows: conflict-free by row and by column
+constexpr int RT_MAXSEG = TC_T / 16 + 1;   // segments a tile can touch (S >= 16)
 constexpr size_t RT_SMEM = 1024 + 4 * (size_t)TC_TILE + (size_t)TC_T * XT_LD * 4 + TC_T * 16 +
                            TC_T * 4 + D * 4 + 64;
 
@@ -543,6 +559,8 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
   extern __shared__ uint8_t rt_raw[];
   __shared__ uint64_t mma_bar;
   __shared__ uint32_t tbase_sh;
+  __shared__ SegInfo seg_sh[RT_MAXSEG];
+  __shared__ uint32_t off_sh[RT_MAXSEG];
   const uint32_t raw = smem_u32(rt_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;            // tiles on 1024-byte boundaries
   uint8_t* gbase = rt_raw + (base - raw);
@@ -573,7 +591,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
     mbar_init_fence();
   }
   // first tile in flight while R is split into the two B operands
-  tc_load_tile(Xs, X, tb, te);
+  if (tid < 128) tc_load_tile(Xs, X, tb, te);
   cp_async_commit();
   {
     // B = R^T, K-major: row j (basis vector) holds R[0..127][j] along K
@@ -590,7 +608,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
     }
   }
   if (!PACK) {
-    for (int j = tid; j < D; j += RT_THREADS) colacc[j] = 0.f;
+    if (tid < D) colacc[tid] = 0.f;
     if (tid == 0) segkept[0] = 0.f;
   }
   tc_fence_before();
@@ -598,8 +616,6 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
   tc_fence_after();
   const uint32_t tbase = tbase_sh;
   const uint32_t idesc = idesc_f16_f32(128, 128);
-  const SegInfo* seginfo = p.seg + (size_t)sx * p.n_seg;
-  const mkv_segment_header* hdr = p.hdr + (size_t)sx * p.n_seg;
   uint32_t* gmask = p.tokmask + (size_t)sx * p.T * 4;
   bool ok = true;
 
@@ -607,7 +623,8 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
     const int64_t t0 = tb + (int64_t)it * TC_T;
     const int rows = (int)imin64(TC_T, te - t0);
     const uint32_t xt = Xs + (uint32_t)(it & 1) * TC_TILE;
-    if (it + 1 < n_tiles) tc_load_tile(Xs + (uint32_t)((it + 1) & 1) * TC_TILE, X, t0 + TC_T, te);
+    if (it + 1 < n_tiles && tid < 128)
+      tc_load_tile(Xs + (uint32_t)((it + 1) & 1) * TC_TILE, X, t0 + TC_T, te);
     cp_async_commit();
     cp_async_wait<1>();
     fence_proxy_async();          // tile and B operands: generic-proxy writes before the MMAs
@@ -623,51 +640,101 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
       }
       tc_commit(&mma_bar);
     }
+    // segment data (packing) while the MMAs run
+    const int sgf = (int)(t0 / p.S);
+    if (PACK) {
+      const int nsg = (int)((t0 + rows - 1) / p.S) - sgf + 1;
+      if (tid < nsg) {
+        const size_t e = (size_t)sx * p.n_seg + sgf + tid;
+        seg_sh[tid] = p.seg[e];
+        off_sh[tid] = p.hdr[e].off16;
+      }
+      if (tid < rows)
+        *reinterpret_cast<uint4*>(tokmask + 4 * tid) =
+            *reinterpret_cast<const uint4*>(gmask + (size_t)(t0 + tid) * 4);
+    }
     if (!tc_wait(&mma_bar, (uint32_t)(it & 1), p.err)) {
       ok = false;
       break;
     }
     tc_fence_after();
-    // ---- token tid's rotated values: fp32 tile row and magnitude keys --------
     {
-      uint32_t k[D];
-      const uint32_t ta = tbase + ((uint32_t)(warp * 32) << 16);
+      // warps w and w + 4: token 32 (w mod 4) + lane, channels 64 (w / 4) ..
+      const int tok = 32 * (warp & 3) + lane, c0 = 64 * (warp >> 2);
+      const uint32_t ta = tbase + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)c0;
 #pragma unroll
-      for (int q = 0; q < D / 16; ++q) {
+      for (int q = 0; q < 4; ++q) {
         uint32_t h[16], l[16];
         tmem_ld16(ta + 16 * q, h);
         tmem_ld16(ta + 128 + 16 * q, l);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float v = fmaf(__uint_as_float(l[j]), 1.f / 2048.f, __uint_as_float(h[j]));
-          Xt[tid * XT_LD + 16 * q + j] = v;
-          k[16 * q + j] = __float_as_uint(v) & 0x7fffffffu;
-        }
-      }
-      if (!PACK && tid < rows) {
-        uint32_t m[4];
-        const float kept = thread_topc(k, p.c, m);
-        *reinterpret_cast<uint4*>(tokmask + 4 * tid) = make_uint4(m[0], m[1], m[2], m[3]);
-        tokkept[tid] = kept;
-        *reinterpret_cast<uint4*>(gmask + (size_t)(t0 + tid) * 4) = make_uint4(m[0], m[1], m[2], m[3]);
+        for (int j = 0; j < 16; ++j)
+          Xt[tok * XT_LD + c0 + 16 * q + j] =
+              fmaf(__uint_as_float(l[j]), 1.f / 2048.f, __uint_as_float(h[j]));
       }
     }
     tc_fence_before();
     __syncthreads();
-    if (PACK) {
+    if (!PACK) {
+      // ---- per-token channels: two lanes per token -----------------------------
+      const int tok = tid >> 1, half = tid & 1;
+      uint32_t k[64];
+#pragma unroll
+      for (int j = 0; j < 64; ++j)
+        k[j] = __float_as_uint(Xt[tok * XT_LD + 64 * half + j]) & 0x7fffffffu;
+      uint32_t m[2];
+      float kept = pair_topc(k, p.c, m);
+      kept += __shfl_xor_sync(0xffffffffu, kept, 1);     // channels 0..63 first, then 64..127
+      if (tok < rows) {
+        *reinterpret_cast<uint2*>(tokmask + 4 * tok + 2 * half) = make_uint2(m[0], m[1]);
+        *reinterpret_cast<uint2*>(gmask + (size_t)(t0 + tok) * 4 + 2 * half) = make_uint2(m[0], m[1]);
+        if (!half) tokkept[tok] = kept;
+      }
+      __syncthreads();
+      // ---- per segment: column energies and kept energy, for the strategy -------
+      int64_t a = t0;
+      const int64_t tend = t0 + rows;
+      while (a < tend) {
+        const int sg = (int)(a / p.S);
+        const int64_t segend = imin64(p.T, (int64_t)(sg + 1) * p.S);
+        const int64_t b = imin64(tend, segend);
+        if (tid < D) {
+          float cacc = colacc[tid];
+          for (int64_t t = a; t < b; ++t) {
+            const float val = Xt[(int)(t - t0) * XT_LD + tid];
+            cacc = fmaf(val, val, cacc);
+          }
+          if (b == segend) {
+            p.colE[((size_t)sx * p.n_seg + sg) * D + tid] = cacc;
+            cacc = 0.f;
+          }
+          colacc[tid] = cacc;
+        } else if (tid == D) {
+          float kk = segkept[0];
+          for (int64_t t = a; t < b; ++t) kk += tokkept[(int)(t - t0)];
+          if (b == segend) {
+            p.segK[(size_t)sx * p.n_seg + sg] = kk;
+            kk = 0.f;
+          }
+          segkept[0] = kk;
+        }
+        a = b;
+      }
+    } else {
       // ---- packed rows: warp per row --------------------------------------------
-      for (int r = warp; r < rows; r += RT_THREADS / 32) {
+      for (int r = warp; r < rows; r += RT_WARPS) {
         const int64_t t = t0 + r;
         const int sg = (int)(t / p.S);
         const int rl = (int)(t - (int64_t)sg * p.S);
-        const SegInfo si = seginfo[sg];
-        if ((uint64_t)hdr[sg].off16 * 16u + si.size > p.pool_check) {
+        const SegInfo& si = seg_sh[sg - sgf];
+        const uint32_t off16 = off_sh[sg - sgf];
+        if ((uint64_t)off16 * 16u + si.size > p.pool_check) {
           // the segment would end past the checked pool extent: report, skip
           if (lane == 0) atomicOr(p.err, DEV_ERR_CHECK);
           continue;
         }
-        uint8_t* seg = p.pool + (size_t)hdr[sg].off16 * 16u;
+        uint8_t* seg = p.pool + (size_t)off16 * 16u;
         const uint32_t c = (uint32_t)p.c;
         float v[4];
 #pragma unroll
@@ -683,11 +750,8 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
 #pragma unroll
           for (int m = 0; m < 4; ++m) w[m] = si.mask[m];
         } else {
-          const uint4 g = *reinterpret_cast<const uint4*>(gmask + (size_t)t * 4);
-          w[0] = g.x;
-          w[1] = g.y;
-          w[2] = g.z;
-          w[3] = g.w;
+#pragma unroll
+          for (int m = 0; m < 4; ++m) w[m] = tokmask[4 * r + m];
         }
         __half* vrow;
         uint8_t* irow;
@@ -718,89 +782,74 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
           for (uint32_t z = c * si.rows + lane; z < pad16(c * si.rows); z += 32) ib[z] = 0;
         }
       }
-    } else {
-      // ---- segment statistics: walk the segments that intersect this tile ----
-      int64_t a = t0;
-      const int64_t tend = t0 + rows;
-      while (a < tend) {
-        const int sg = (int)(a / p.S);
-        const int64_t segend = imin64(p.T, (int64_t)(sg + 1) * p.S);
-        const int64_t b = imin64(tend, segend);
-        {
-          float cacc = colacc[tid];
-          for (int64_t t = a; t < b; ++t) {
-            const float val = Xt[(int)(t - t0) * XT_LD + tid];
-            cacc = fmaf(val, val, cacc);
-          }
-          colacc[tid] = cacc;
-        }
-        if (tid == 0) {
-          float kk = segkept[0];
-          for (int64_t t = a; t < b; ++t) kk += tokkept[(int)(t - t0)];
-          segkept[0] = kk;
-        }
-        __syncthreads();
-        if (b == segend) {
-          if (warp == 0) {
-            float cv[4];
-            uint32_t key[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-              cv[m] = colacc[lane + 32 * m];
-              key[m] = __float_as_uint(cv[m]) & 0x7fffffffu;
-            }
-            const float etot = warp_sum(cv[0] + cv[1] + cv[2] + cv[3]);
-            bool sel[4];
-            warp_topc(key, p.c, sel);
-            float smk = 0.f;
-#pragma unroll
-            for (int m = 0; m < 4; ++m) smk += sel[m] ? cv[m] : 0.f;
-            smk = warp_sum(smk);
-            uint32_t w[4];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) w[m] = __ballot_sync(0xffffffffu, sel[m]);
-            if (lane == 0) {
-              const int rws = (int)(segend - (int64_t)sg * p.S);
-              const float fsm = etot > 0.f ? smk / etot : 1.f;
-              const float fpv = etot > 0.f ? segkept[0] / etot : 1.f;
-              uint32_t best = segment_bytes(MKV_STRATEGY_DENSE, rws, p.c);
-              int strat = MKV_STRATEGY_DENSE;
-              const uint32_t cpv = segment_bytes(MKV_STRATEGY_PV, rws, p.c);
-              const uint32_t csm = segment_bytes(MKV_STRATEGY_SM, rws, p.c);
-              if (fpv >= p.tau && cpv <= best) {
-                best = cpv;
-                strat = MKV_STRATEGY_PV;
-              }
-              if (fsm >= p.tau && csm <= best) {
-                best = csm;
-                strat = MKV_STRATEGY_SM;
-              }
-              SegInfo si;
-              si.size = best;
-              si.strategy = (uint8_t)strat;
-              si.pad = 0;
-              si.rows = (uint16_t)rws;
-#pragma unroll
-              for (int m = 0; m < 4; ++m) si.mask[m] = w[m];
-              si.f_sm = fsm;
-              si.f_pv = fpv;
-              p.seg[(size_t)sx * p.n_seg + sg] = si;
-            }
-          }
-          __syncthreads();
-          colacc[tid] = 0.f;
-          if (tid == 0) segkept[0] = 0.f;
-          __syncthreads();
-        }
-        a = b;
-      }
     }
-    __syncthreads();              // the fp32 tile is rewritten by the next tile
+    __syncthreads();              // the fp32 tile and staged data are rewritten by the next tile
   }
   cp_async_wait<0>();
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tbase, 256);
+}
+
+// ---------------------------------------------------------------------------
+// strategy: one warp per segment (all segments of all streams).  From the
+// segment's column energies and kept energy: e_tot, the shared mask (top-c
+// column energies, ties to the lower channel), f_SM, f_PV, and the cheapest
+// strategy whose fraction reaches tau (dense always allowed; cost ties
+// resolve SM, PV, dense).
+// grid: ceil(2 BH n_seg / 8), block 256
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) strategy_kernel(CompressParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t e = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int64_t n = (int64_t)2 * p.BH * p.n_seg;
+  if (e >= n) return;
+  const int sg = (int)(e % p.n_seg);
+  float cv[4];
+  uint32_t key[4];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    cv[m] = p.colE[(size_t)e * D + lane + 32 * m];
+    key[m] = __float_as_uint(cv[m]) & 0x7fffffffu;
+  }
+  const float etot = warp_sum(cv[0] + cv[1] + cv[2] + cv[3]);
+  bool sel[4];
+  warp_topc(key, p.c, sel);
+  float smk = 0.f;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) smk += sel[m] ? cv[m] : 0.f;
+  smk = warp_sum(smk);
+  uint32_t w[4];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) w[m] = __ballot_sync(0xffffffffu, sel[m]);
+  if (lane == 0) {
+    const int rws = (int)(imin64(p.T, (int64_t)(sg + 1) * p.S) - (int64_t)sg * p.S);
+    const float kept = p.segK[e];
+    const float fsm = etot > 0.f ? smk / etot : 1.f;
+    const float fpv = etot > 0.f ? kept / etot : 1.f;
+    uint32_t best = segment_bytes(MKV_STRATEGY_DENSE, rws, p.c);
+    int strat = MKV_STRATEGY_DENSE;
+    const uint32_t cpv = segment_bytes(MKV_STRATEGY_PV, rws, p.c);
+    const uint32_t csm = segment_bytes(MKV_STRATEGY_SM, rws, p.c);
+    if (fpv >= p.tau && cpv <= best) {
+      best = cpv;
+      strat = MKV_STRATEGY_PV;
+    }
+    if (fsm >= p.tau && csm <= best) {
+      best = csm;
+      strat = MKV_STRATEGY_SM;
+    }
+    SegInfo si;
+    si.size = best;
+    si.strategy = (uint8_t)strat;
+    si.pad = 0;
+    si.rows = (uint16_t)rws;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) si.mask[m] = w[m];
+    si.f_sm = fsm;
+    si.f_pv = fpv;
+    p.seg[e] = si;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -876,7 +925,13 @@ static cudaError_t launch_rot(const CompressParams& p, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_analyze(const CompressParams& p, cudaStream_t st) { return launch_rot<false>(p, st); }
+cudaError_t launch_analyze(const CompressParams& p, cudaStream_t st) {
+  cudaError_t e = launch_rot<false>(p, st);
+  if (e != cudaSuccess) return e;
+  const int64_t n = (int64_t)2 * p.BH * p.n_seg;
+  strategy_kernel<<<(unsigned)((n + 7) / 8), 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
 cudaError_t launch_pack(const CompressParams& p, cudaStream_t st) { return launch_rot<true>(p, st); }
 
 cudaError_t launch_scan(const CompressParams& p, cudaStream_t st) {

@@ -83,6 +83,8 @@ struct mkv_ctx {
   // compression scratch
   SegInfo* seg = nullptr;
   uint32_t* tokmask = nullptr;     // [2][BH][max_ctx][4] per-token channel masks
+  float* colE = nullptr;           // [2][BH][max_seg][128] column energies per segment
+  float* segK = nullptr;           // [2][BH][max_seg] kept energy per segment
   float* gram_part = nullptr;
   unsigned long long* total_dev = nullptr;
   unsigned long long* total_host = nullptr;
@@ -194,6 +196,8 @@ void release(mkv_ctx* c) {
   cudaFree(c->pool);
   cudaFree(c->seg);
   cudaFree(c->tokmask);
+  cudaFree(c->colE);
+  cudaFree(c->segK);
   cudaFree(c->gram_part);
   cudaFree(c->total_dev);
   if (c->total_host) cudaFreeHost(c->total_host);
@@ -364,6 +368,8 @@ mkv_status mkv_create(const mkv_config* cfg, mkv_ctx** out) {
   }
   AL(c->seg, 2 * BH * (size_t)c->max_seg);
   AL(c->tokmask, 2 * BH * (size_t)cfg->max_ctx * 4);
+  AL(c->colE, 2 * BH * (size_t)c->max_seg * D);
+  AL(c->segK, 2 * BH * (size_t)c->max_seg);
   AL(c->gram_part, 2 * BH * (size_t)c->gram_chunks_max * D * D);
   AL(c->total_dev, 3);
   AL(c->qt, (size_t)c->B * c->Hq * D);
@@ -430,6 +436,8 @@ mkv_status mkv_compress(mkv_ctx* c, const void* k, const void* v, int64_t ctx_le
   p.ctas_per_stream = (int)ceil_div(p.n_seg, p.segs_per_cta);
   p.seg = c->seg;
   p.tokmask = c->tokmask;
+  p.colE = c->colE;
+  p.segK = c->segK;
   p.hdr = c->hdr[stage];
   p.total = c->total_dev;
   p.pool = nullptr;
@@ -484,8 +492,7 @@ mkv_status mkv_compress(mkv_ctx* c, const void* k, const void* v, int64_t ctx_le
   // the cache has dense segments
   c->at_kv = dense_k ? 256 : 2 * p.c;
   c->at_vv = dense_v ? 256 : 2 * p.c;
-  // channel lists are copied from the 16-byte boundary at or below their start
-  c->at_ki = c->at_vi = (int)pad16((uint32_t)p.c + 8u);
+  c->at_ki = c->at_vi = (int)pad16((uint32_t)p.c);
   CK(attn_shape(c->g, c->at_kv + c->at_ki + c->at_vv + c->at_vi, &c->at_stages,
                 &c->at_ctas_per_sm));
   c->T = ctx_len;

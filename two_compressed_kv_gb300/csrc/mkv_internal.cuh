@@ -63,6 +63,8 @@ struct CompressParams {
   int ctas_per_stream;
   SegInfo* seg;              // [2][BH][n_seg]
   uint32_t* tokmask;         // [2][BH][T][4]: per-token channel masks (statistics -> packing)
+  float* colE;               // [2][BH][n_seg][128]: column energies per segment
+  float* segK;               // [2][BH][n_seg]: kept energy of per-token top-c per segment
   mkv_segment_header* hdr;   // [2][BH][n_seg]
   unsigned long long* total; // device: [0] total packed bytes, [1..2] dense segments of K, V
   uint8_t* pool;
