@@ -191,6 +191,34 @@ mkv_status mkv_decode(mkv_ctx* ctx, const void* q, float* out, int32_t* sel,
  * unknown bits. */
 mkv_status mkv_set_flags(mkv_ctx* ctx, uint32_t flags);
 
+/* Decode-time appends (§1 "Observation & Method 2": newly generated KV are
+ * kept in a GPU-side buffer and used by the following decode steps; once a
+ * segment's worth has accumulated it is compressed and switched into the
+ * compressed cache without blocking decode).
+ * Adds n tokens to every stream; they become tokens T .. T + n - 1 of later
+ * decodes (T = prefill tokens + tokens appended so far).  Each token is
+ * rotated into its stream's existing K / V basis and kept as an fp16 row with
+ * every channel (a dense row) in a buffer of up to `segment` tokens per
+ * stream.  Whenever the buffer is full its tokens are compressed as one
+ * segment -- the stream's basis, the per-token top-c, the strategy rule and
+ * the packing of mkv_compress -- and appended after the cache's segments
+ * (a ragged last prefill segment stays as it is; committed segments start at
+ * the prefill's end and hold `segment` tokens each).
+ *   k, v: device fp16 [B][H][n][128], contiguous; read by the call's work on
+ *         `stream`, so they must stay valid until it has run.
+ *   n >= 1; the context after the call must not exceed max_ctx (room for
+ *   appends exists only when mkv_compress was given fewer than max_ctx
+ *   tokens).
+ * Asynchronous on `stream`, no host synchronisation, except when a commit
+ * might not fit the pool's spare room: the pool then grows once (one
+ * synchronisation of `stream`, one allocation, a copy of the packed bytes).
+ * Later decodes must run on the same stream or after it.  A new
+ * mkv_compress drops all appended tokens.
+ * MKV_ERR_STATE before any mkv_compress; MKV_ERR_INVALID_ARG for NULL
+ * pointers, n < 1 or max_ctx exceeded (nothing is appended then). */
+mkv_status mkv_append(mkv_ctx* ctx, const void* k, const void* v, int32_t n,
+                      mkv_stream_t stream);
+
 /* Frees everything the ctx owns.  NULL is allowed.  Synchronises the device. */
 void mkv_free(mkv_ctx* ctx);
 
@@ -203,7 +231,9 @@ const char* mkv_last_error_string(void);
 /* Counters of the current cache (synchronous; copies headers to the host). */
 mkv_status mkv_stats(const mkv_ctx* ctx, mkv_stats_t* out);
 
-/* Copies one compressed stream to host buffers (synchronous).
+/* Copies one compressed stream to host buffers (synchronous).  Its segments
+ * are the prefill's followed by those committed by mkv_append (n_segments
+ * from mkv_stats); tokens still in the append buffer are not exported.
  *   which: 0 = K, 1 = V.
  *   basis:   host float[128*128] or NULL; R row-major, R[r*128 + j] = entry r of
  *            basis vector j.

@@ -15,7 +15,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmkv.so")
-SOURCES = ["mkv_api.cu", "k_compress.cu", "k_score.cu", "k_select.cu", "k_attn.cu", "k_checks.cu"]
+SOURCES = ["mkv_api.cu", "k_compress.cu", "k_score.cu", "k_select.cu", "k_attn.cu", "k_checks.cu",
+           "k_append.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O3",
          "--expt-relaxed-constexpr", "-I", os.path.join(HERE, "..", "include")]

@@ -39,12 +39,26 @@ constexpr int AT_PLD = 72;          // halves per P row (144 B)
 
 constexpr int32_t NO_IDX = (int32_t)0x80000000;
 
-// Row of token t in one stream: pool offset of its stored values / 16, and
-// the byte distance / 8 from the values to the row's channel list (the
-// segment mask for SM, the row's own indices for PV; NO_IDX for dense rows).
-__device__ __forceinline__ uint2 row_meta(const mkv_segment_header* hdr, int64_t t, int S, int c) {
-  const int64_t sg = t / S;
-  const uint32_t r = (uint32_t)(t - sg * S);
+// Row of token t in stream s: pool offset of its stored values / 16, and the
+// byte distance / 8 from the values to the row's channel list (the segment
+// mask for SM, the row's own indices for PV; NO_IDX for dense rows).  Tokens
+// before T0 sit in the prefill segments, tokens from T0 to T_packed in the
+// committed ones, later tokens in the tail (dense rows at tail16).
+__device__ __forceinline__ uint2 row_meta(const DecodeParams& p, const mkv_segment_header* hdr,
+                                          int s, int64_t t, uint32_t tail16) {
+  const int S = p.S, c = p.c;
+  if (t >= p.T_packed)
+    return make_uint2(tail16 + (uint32_t)(((int64_t)s * S + (t - p.T_packed)) * 16), (uint32_t)NO_IDX);
+  int64_t sg;
+  uint32_t r;
+  if (t < p.T0) {
+    sg = t / S;
+    r = (uint32_t)(t - sg * S);
+  } else {
+    const int64_t u = t - p.T0, q = u / S;
+    sg = p.nseg0 + q;
+    r = (uint32_t)(u - q * S);
+  }
   const mkv_segment_header hd = hdr[sg];
   const uint32_t c2 = 2u * (uint32_t)c;
   if (hd.strategy == MKV_STRATEGY_SM) {
@@ -173,8 +187,8 @@ __device__ __forceinline__ void at_meta_pass(const DecodeParams& p, int64_t lo, 
       const int x = x0 + u * AT_THREADS;
       if (x < n) {
         const int64_t tt = clamp_t((int32_t)t[u], p.T);
-        uint2 km = row_meta(p.hdrK + (size_t)sidx[u] * p.n_seg, tt, p.S, p.c);
-        uint2 vm = row_meta(p.hdrV + (size_t)sidx[u] * p.n_seg, tt, p.S, p.c);
+        uint2 km = row_meta(p, p.hdrK + (size_t)sidx[u] * p.n_seg, sidx[u], tt, p.tail_k16);
+        uint2 vm = row_meta(p, p.hdrV + (size_t)sidx[u] * p.n_seg, sidx[u], tt, p.tail_v16);
         if (row_end(km, p.c) > p.pool_check || row_end(vm, p.c) > p.pool_check) {
           // outside the checked pool extent: report it and read a stand-in
           // row of c values with its channel list at pool offset 0 (inside

@@ -55,7 +55,30 @@ __global__ void __launch_bounds__(QR_THREADS) qrot_kernel(DecodeParams p) {
   }
   psum[hq][j] = mine;
   __syncthreads();
-  if (tid < D) p.qbar[(size_t)s * D + j] = ((psum[0][j] + psum[1][j]) + psum[2][j]) + psum[3][j];
+  const int n_tail = (int)(p.T - p.T_packed);
+  if (tid < D) {
+    const float qb = ((psum[0][j] + psum[1][j]) + psum[2][j]) + psum[3][j];
+    p.qbar[(size_t)s * D + j] = qb;
+    qs[0][j] = qb;
+  }
+  if (n_tail > 0) {
+    // scores of the tail's tokens (dense rotated rows) and their histogram
+    __syncthreads();
+    const __half* rows = reinterpret_cast<const __half*>(p.pool + (uint64_t)p.tail_k16 * 16u) +
+                         (size_t)s * p.S * D;
+    for (int t = tid; t < n_tail; t += QR_THREADS) {
+      const __half2* r2 = reinterpret_cast<const __half2*>(rows + (size_t)t * D);
+      float acc = 0.f;
+#pragma unroll 8
+      for (int x = 0; x < D / 2; ++x) {
+        const float2 f = __half22float2(r2[x]);
+        acc = fmaf(f.x, qs[0][2 * x], acc);
+        acc = fmaf(f.y, qs[0][2 * x + 1], acc);
+      }
+      p.scores[(size_t)s * p.Tp + p.T_packed + t] = acc;
+      atomicAdd(&p.hist[(size_t)s * HIST1 + (f2key(acc) >> 20)], 1u);
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -332,7 +355,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
         }
         const int s = s_cur;
         const int sl = s - s_first;
-        float* out = p.scores + (size_t)s * p.Tp + (int64_t)(sg - s * p.n_seg) * p.S;
+        float* out = p.scores + (size_t)s * p.Tp + seg_start(sg - s * p.n_seg, p.S, p.nseg0, p.T0);
         // the common case reads q_bar and counts into this CTA's shared copies;
         // keeping the two cases apart lets both compile to shared-memory
         // loads and atomics instead of generic ones
@@ -399,30 +422,55 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
 }
 
 // ---------------------------------------------------------------------------
-// partition of the K segments over the score kernel's CTAs (compression time):
-// CTA i starts at the first segment whose payload starts at or after
-// i * total / G bytes of the K payload.
+// partition of the K segments over the score kernel's CTAs (compression time
+// and after each commit): CTA i starts at the first segment (in stream,
+// segment order) whose cumulative size before it reaches i * total / G.
+// prefix[] receives the cumulative sizes (one CTA of 1024 threads).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) partition_kernel(const mkv_segment_header* hdrK,
                                                          int n_streams, int n_seg, int c, int G,
-                                                         int32_t* part, int32_t* cta_cnt) {
+                                                         int32_t* part, int32_t* cta_cnt,
+                                                         int64_t* prefix) {
+  __shared__ unsigned long long wsum[32];
   const int64_t n = (int64_t)n_streams * n_seg;
-  const mkv_segment_header last = hdrK[n - 1];
-  const uint64_t first = (uint64_t)hdrK[0].off16 * 16u;
-  const uint64_t total =
-      (uint64_t)last.off16 * 16u + segment_bytes(last.strategy, last.rows, c) - first;
-  for (int s = threadIdx.x; s < n_streams; s += blockDim.x) cta_cnt[s] = 0;
-  for (int i = threadIdx.x; i <= G; i += blockDim.x) {
-    const uint64_t target = (uint64_t)(((double)i / (double)G) * (double)total);
-    int64_t lo = 0, hi = n;   // first segment whose start >= target
-    while (lo < hi) {
-      const int64_t mid = (lo + hi) >> 1;
-      if ((uint64_t)hdrK[mid].off16 * 16u - first >= target) hi = mid; else lo = mid + 1;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t per = (n + 1023) / 1024;
+  const int64_t lo = imin64(n, tid * per), hi = imin64(n, lo + per);
+  unsigned long long mine = 0;
+  for (int64_t e = lo; e < hi; ++e) {
+    const mkv_segment_header h = hdrK[e];
+    mine += segment_bytes(h.strategy, h.rows, c);
+  }
+  unsigned long long inc = mine;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const unsigned long long o = __shfl_up_sync(0xffffffffu, inc, off);
+    if (lane >= off) inc += o;
+  }
+  if (lane == 31) wsum[warp] = inc;
+  __syncthreads();
+  unsigned long long acc = inc - mine;
+  for (int w = 0; w < warp; ++w) acc += wsum[w];
+  for (int64_t e = lo; e < hi; ++e) {
+    prefix[e] = (int64_t)acc;
+    const mkv_segment_header h = hdrK[e];
+    acc += segment_bytes(h.strategy, h.rows, c);
+  }
+  if (tid == 1023) prefix[n] = (int64_t)acc;
+  for (int s = tid; s < n_streams; s += blockDim.x) cta_cnt[s] = 0;
+  __syncthreads();
+  const int64_t total = prefix[n];
+  for (int i = tid; i <= G; i += blockDim.x) {
+    const int64_t target = (int64_t)(((double)i / (double)G) * (double)total);
+    int64_t a = 0, b = n;   // first segment whose cumulative start >= target
+    while (a < b) {
+      const int64_t mid = (a + b) >> 1;
+      if (prefix[mid] >= target) b = mid; else a = mid + 1;
     }
-    part[i] = (int32_t)(i == 0 ? 0 : (i == G ? n : lo));
+    part[i] = (int32_t)(i == 0 ? 0 : (i == G ? n : a));
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < G; i += blockDim.x) {
+  for (int i = tid; i < G; i += blockDim.x) {
     const int a = part[i], b = part[i + 1];
     if (a >= b) continue;
     for (int s = a / n_seg; s <= (b - 1) / n_seg; ++s) atomicAdd(&cta_cnt[s], 1);
@@ -431,9 +479,10 @@ __global__ void __launch_bounds__(1024) partition_kernel(const mkv_segment_heade
 
 // ---------------------------------------------------------------------------
 // plan: the score kernel's stages for CTA i (one warp per CTA, compression
-// time).  Whole segments are grouped in order while the stage's line-aligned
-// span stays within stage_bytes (at least one segment per stage) and it holds
-// at most SC_MAX_SEGS segments.  A stage never has more entries than its CTA
+// time).  Whole segments are grouped in order while each starts where the
+// previous one ends in the pool (committed segments do not), the stage's
+// line-aligned span stays within stage_bytes (at least one segment per stage)
+// and it holds at most SC_MAX_SEGS segments.  A stage never has more entries than its CTA
 // has segments, so CTA i's plan fits in plan[part[i] .. part[i + 1]).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ StagePlan make_stage(int seg0, int nseg, uint64_t off0, uint64_t end) {
@@ -462,8 +511,8 @@ __global__ void __launch_bounds__(32) plan_kernel(const mkv_segment_header* hdrK
     for (int j = 0; j < nb; ++j) {
       const uint64_t sj = __shfl_sync(0xffffffffu, st, j);
       const uint64_t ej = __shfl_sync(0xffffffffu, se, j);
-      if (nseg > 0 && (nseg == SC_MAX_SEGS || ((ej + 127u) & ~127ull) - (off0 & ~127ull) >
-                                                  (uint64_t)stage_bytes + 128u)) {
+      if (nseg > 0 && (nseg == SC_MAX_SEGS || sj != end ||
+                       ((ej + 127u) & ~127ull) - (off0 & ~127ull) > (uint64_t)stage_bytes + 128u)) {
         if (lane == 0) plan[a + k] = make_stage(seg0, nseg, off0, end);
         ++k;
         seg0 = base + j;
@@ -522,8 +571,8 @@ cudaError_t prepare_decode_kernels() {
 
 cudaError_t launch_partition(const mkv_segment_header* hdrK, int n_streams, int n_seg, int c,
                              int G, int stage_bytes, int32_t* part, int32_t* cta_cnt,
-                             StagePlan* plan, int32_t* plan_n, cudaStream_t st) {
-  partition_kernel<<<1, 1024, 0, st>>>(hdrK, n_streams, n_seg, c, G, part, cta_cnt);
+                             StagePlan* plan, int32_t* plan_n, int64_t* prefix, cudaStream_t st) {
+  partition_kernel<<<1, 1024, 0, st>>>(hdrK, n_streams, n_seg, c, G, part, cta_cnt, prefix);
   plan_kernel<<<G, 32, 0, st>>>(hdrK, c, stage_bytes, part, plan, plan_n);
   return cudaGetLastError();
 }

@@ -102,6 +102,20 @@ struct mkv_ctx {
   float* part_o = nullptr;
   float* part_ml = nullptr;
 
+  // decode-time appends (tokens after the prefill)
+  int64_t T0 = 0;                  // prefill tokens
+  int nseg0 = 0;                   // prefill segments per stream
+  int n_commit = 0;                // committed segments per stream
+  int tail_len = 0;                // tokens waiting in the tail
+  uint64_t tail_bytes = 0;         // rotated tail rows in the pool (K then V), 0: no appends
+  uint64_t tail_off = 0;           // their byte offset in the pool
+  uint64_t packed_bound = 0;       // upper bound of the packed bytes' end (host)
+  uint64_t* packed_end = nullptr;  // the packed bytes' end (device, moved by commits)
+  __half* tail_x = nullptr;        // [2][BH][S][128] tail tokens as given
+  mkv_segment_header* hdr_commit = nullptr;   // [2][BH] headers of one commit
+  int64_t* kprefix = nullptr;      // [BH * max_seg + 1] cumulative K segment sizes
+  int at_stages_dense = 2, at_ctas_dense = 1; // attention shape with room for dense rows
+
   int64_t decode_calls = 0;
   int64_t launches = 0;
   KernelTimer timers[MKV_KERNEL_COUNT];
@@ -212,6 +226,10 @@ void release(mkv_ctx* c) {
   cudaFree(c->err);
   cudaFree(c->part_o);
   cudaFree(c->part_ml);
+  cudaFree(c->packed_end);
+  cudaFree(c->tail_x);
+  cudaFree(c->hdr_commit);
+  cudaFree(c->kprefix);
   for (auto& t : c->timers) {
     for (auto& e : t.pending) {
       cudaEventDestroy(e.first);
@@ -220,6 +238,11 @@ void release(mkv_ctx* c) {
     for (auto& e : t.spare) cudaEventDestroy(e);
   }
   delete c;
+}
+
+// Packed bytes of one commit if every new segment were dense.
+uint64_t commit_worst(const mkv_ctx* c) {
+  return 2ull * c->BH * segment_bytes(MKV_STRATEGY_DENSE, c->cfg.segment, c->cfg.c);
 }
 
 int gram_chunks_for(int BH, int64_t T) {
@@ -315,7 +338,8 @@ mkv_status mkv_create(const mkv_config* cfg, mkv_ctx** out) {
   c->Hq = cfg->n_q_heads;
   c->g = c->Hq / c->H;
   c->BH = c->B * c->H;
-  c->max_seg = ceil_div(cfg->max_ctx, cfg->segment);
+  // a ragged prefill plus committed segments can need one segment more
+  c->max_seg = ceil_div(cfg->max_ctx, cfg->segment) + 1;
   c->kk_max = (int)std::min<int64_t>(cfg->top_k, cfg->max_ctx);
   c->gram_chunks_max = gram_chunks_for(c->BH, cfg->max_ctx);
   c->Tp_max = ceil_div(cfg->max_ctx, 16) * 16;
@@ -381,6 +405,10 @@ mkv_status mkv_create(const mkv_config* cfg, mkv_ctx** out) {
   AL(c->state, BH);
   AL(c->sel, BH * (size_t)c->kk_max);
   AL(c->err, 1);
+  AL(c->packed_end, 1);
+  AL(c->tail_x, 2 * BH * (size_t)cfg->segment * D);
+  AL(c->hdr_commit, 2 * BH);
+  AL(c->kprefix, BH * (size_t)c->max_seg + 1);
   AL(c->part_o, BH * (size_t)c->attn_mp * c->g * D);
   AL(c->part_ml, BH * (size_t)c->attn_mp * c->g * 2);
 #undef AL
@@ -451,7 +479,8 @@ mkv_status mkv_compress(mkv_ctx* c, const void* k, const void* v, int64_t ctx_le
          cudaError_t e = launch_scan(p, st);
          if (e == cudaSuccess)
            e = launch_partition(p.hdr, c->BH, p.n_seg, p.c, c->G, c->stage_bytes, c->part[stage],
-                                c->cta_cnt[stage], c->plan[stage], c->plan_n[stage], st);
+                                c->cta_cnt[stage], c->plan[stage], c->plan_n[stage], c->kprefix,
+                                st);
          return e;
        })) != MKV_OK)
     return s;
@@ -468,8 +497,14 @@ mkv_status mkv_compress(mkv_ctx* c, const void* k, const void* v, int64_t ctx_le
     g_last_error = "packed cache exceeds max_pool_bytes";
     return MKV_ERR_OOM;
   }
-  // the score kernel copies whole 128-byte lines: 256 bytes of tail padding
-  const uint64_t need = total + 256;
+  // the score kernel copies whole 128-byte lines: 256 bytes of padding after
+  // the packed bytes.  When tokens can still be appended, room for two
+  // commits (every segment dense) and the rotated tail follow.
+  const bool appendable = ctx_len < c->cfg.max_ctx;
+  const uint64_t tail_bytes = appendable ? 2ull * c->BH * p.S * D * 2 : 0;
+  const uint64_t reserve = appendable ? 2 * commit_worst(c) : 0;
+  const uint64_t tail_off = (total + 256 + reserve + 255) & ~255ull;
+  const uint64_t need = appendable ? tail_off + tail_bytes : total + 256;
   if (need > c->pool_cap) {
     uint8_t* np = nullptr;
     cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&np), need);
@@ -486,8 +521,17 @@ mkv_status mkv_compress(mkv_ctx* c, const void* k, const void* v, int64_t ctx_le
   p.err = c->err;
   c->ready = false;   // the live headers may no longer match the pool
   if ((s = timed(c, MKV_KERNEL_PACK, st, 1, [&] { return launch_pack(p, st); })) != MKV_OK) return s;
+  CK(cudaMemcpyAsync(c->packed_end, c->total_dev, sizeof(uint64_t), cudaMemcpyDeviceToDevice,
+                     st));
   c->live = stage;
   c->pool_need = need;
+  c->T0 = ctx_len;
+  c->nseg0 = p.n_seg;
+  c->n_commit = 0;
+  c->tail_len = 0;
+  c->tail_bytes = tail_bytes;
+  c->tail_off = tail_off;
+  c->packed_bound = total;
   // the attention kernel's per-token slot: room for a dense row only when
   // the cache has dense segments
   c->at_kv = dense_k ? 256 : 2 * p.c;
@@ -495,6 +539,7 @@ mkv_status mkv_compress(mkv_ctx* c, const void* k, const void* v, int64_t ctx_le
   c->at_ki = c->at_vi = (int)pad16((uint32_t)p.c);
   CK(attn_shape(c->g, c->at_kv + c->at_ki + c->at_vv + c->at_vi, &c->at_stages,
                 &c->at_ctas_per_sm));
+  CK(attn_shape(c->g, 256 + c->at_ki + 256 + c->at_vi, &c->at_stages_dense, &c->at_ctas_dense));
   c->T = ctx_len;
   c->n_seg = p.n_seg;
   c->ready = true;
@@ -518,6 +563,11 @@ mkv_status mkv_decode(mkv_ctx* c, const void* q, float* out, int32_t* sel, mkv_s
   p.c = c->cfg.c;
   p.n_seg = c->n_seg;
   p.kk = (int)std::min<int64_t>(c->cfg.top_k, c->T);
+  p.T0 = c->T0;
+  p.nseg0 = c->nseg0;
+  p.T_packed = c->T0 + (int64_t)c->n_commit * p.S;
+  p.tail_k16 = (uint32_t)(c->tail_off >> 4);
+  p.tail_v16 = (uint32_t)((c->tail_off + c->tail_bytes / 2) >> 4);
   p.q = static_cast<const __half*>(q);
   p.RK = c->R[c->live];
   p.RV = c->R[c->live] + (size_t)c->BH * D * D;
@@ -545,18 +595,20 @@ mkv_status mkv_decode(mkv_ctx* c, const void* q, float* out, int32_t* sel, mkv_s
   p.err = c->err;
   {
     const int64_t N = (int64_t)c->BH * p.kk;
-    const int64_t P = (int64_t)c->G * c->at_ctas_per_sm;
+    // appended tokens are dense rows (the tail) or may sit in dense segments
+    const bool appended = c->T > c->T0;
+    const int64_t P = (int64_t)c->G * (appended ? c->at_ctas_dense : c->at_ctas_per_sm);
     p.attn_per = c->attn_per_fixed
                      ? c->attn_per_fixed
                      : std::max({ceil_div(N, P), kMinSlice, ceil_div(p.kk, c->attn_mp - 1)});
     p.attn_ctas = (int)ceil_div(N, p.attn_per);
     p.attn_mp = c->attn_mp;
-    p.at_kv = c->at_kv;
+    p.at_kv = appended ? 256 : c->at_kv;
     p.at_ki = c->at_ki;
-    p.at_vv = c->at_vv;
+    p.at_vv = appended ? 256 : c->at_vv;
     p.at_vi = c->at_vi;
-    p.at_slot = c->at_kv + c->at_ki + c->at_vv + c->at_vi;
-    p.at_stages = c->at_stages;
+    p.at_slot = p.at_kv + p.at_ki + p.at_vv + p.at_vi;
+    p.at_stages = appended ? c->at_stages_dense : c->at_stages;
   }
   p.part_o = c->part_o;
   p.part_ml = c->part_ml;
@@ -573,6 +625,139 @@ mkv_status mkv_decode(mkv_ctx* c, const void* q, float* out, int32_t* sel, mkv_s
   if ((s = timed(c, MKV_KERNEL_ATTN, st, 1, [&] { return launch_attn(p, st); })) != MKV_OK) return s;
   if ((s = timed(c, MKV_KERNEL_MERGE, st, 1, [&] { return launch_merge(p, st); })) != MKV_OK) return s;
   c->decode_calls += 1;
+  return MKV_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Moves the packed bytes and the tail to a larger pool when the next commit
+// might not fit before the tail.  Synchronises the stream (decode kernels
+// may still read the old pool).
+mkv_status grow_pool(mkv_ctx* c, cudaStream_t st) {
+  uint64_t end = 0;
+  CK(cudaMemcpyAsync(&end, c->packed_end, sizeof(uint64_t), cudaMemcpyDeviceToHost, st));
+  CK(cudaStreamSynchronize(st));
+  c->packed_bound = end;
+  const uint64_t worst = commit_worst(c);
+  if (end + 256 + worst <= c->tail_off) return MKV_OK;
+  const uint64_t tail_off = (end + 256 + 4 * worst + 255) & ~255ull;
+  const uint64_t need = tail_off + c->tail_bytes;
+  if (c->cfg.max_pool_bytes && need > c->cfg.max_pool_bytes) {
+    g_last_error = "appended segments exceed max_pool_bytes";
+    return MKV_ERR_OOM;
+  }
+  uint8_t* np = nullptr;
+  cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&np), need);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_fail(e, "cudaMalloc(pool)");
+  }
+  CK(cudaMemcpyAsync(np, c->pool, end, cudaMemcpyDeviceToDevice, st));
+  CK(cudaMemcpyAsync(np + tail_off, c->pool + c->tail_off, c->tail_bytes, cudaMemcpyDeviceToDevice,
+                     st));
+  CK(cudaStreamSynchronize(st));
+  CK(cudaFree(c->pool));
+  c->pool = np;
+  c->pool_cap = need;
+  c->pool_need = need;
+  c->tail_off = tail_off;
+  return MKV_OK;
+}
+
+// Compresses the full tail (S tokens per stream) into one new segment per
+// stream with the streams' bases, places the segments after the packed
+// bytes, and switches to headers and score plans that include them.
+mkv_status commit_tail(mkv_ctx* c, cudaStream_t st) {
+  if (c->packed_bound + 256 + commit_worst(c) > c->tail_off) {
+    mkv_status s = grow_pool(c, st);
+    if (s != MKV_OK) return s;
+  }
+  const int stage = 1 - c->live;
+  CompressParams p;
+  memset(&p, 0, sizeof(p));
+  p.X[0] = c->tail_x;
+  p.X[1] = c->tail_x + (size_t)c->BH * c->cfg.segment * D;
+  p.BH = c->BH;
+  p.T = c->cfg.segment;
+  p.S = c->cfg.segment;
+  p.c = c->cfg.c;
+  p.tau = c->cfg.tau;
+  p.n_seg = 1;
+  p.R = c->R[c->live];
+  p.segs_per_cta = 1;
+  p.ctas_per_stream = 1;
+  p.seg = c->seg;
+  p.tokmask = c->tokmask;
+  p.colE = c->colE;
+  p.segK = c->segK;
+  p.hdr = c->hdr_commit;
+  p.pool = c->pool;
+  p.pool_check = c->check_override ? std::min(c->check_override, c->tail_off) : c->tail_off;
+  p.err = c->err;
+  p.packed_end = c->packed_end;
+  CK(launch_analyze(p, st));
+  CK(launch_commit_scan(p, st));
+  CK(launch_pack(p, st));
+  CK(launch_grow_headers(c->hdr[c->live], c->n_seg, c->hdr_commit, 2 * c->BH, c->hdr[stage], st));
+  CK(cudaMemcpyAsync(c->R[stage], c->R[c->live], 2 * (size_t)c->BH * D * D * sizeof(float),
+                     cudaMemcpyDeviceToDevice, st));
+  CK(cudaMemcpyAsync(c->lam[stage], c->lam[c->live], 2 * (size_t)c->BH * D * sizeof(float),
+                     cudaMemcpyDeviceToDevice, st));
+  CK(launch_partition(c->hdr[stage], c->BH, c->n_seg + 1, c->cfg.c, c->G, c->stage_bytes,
+                      c->part[stage], c->cta_cnt[stage], c->plan[stage], c->plan_n[stage],
+                      c->kprefix, st));
+  c->launches += 7;
+  c->live = stage;
+  c->n_seg += 1;
+  c->n_commit += 1;
+  c->tail_len = 0;
+  c->packed_bound += commit_worst(c);
+  return MKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mkv_status mkv_append(mkv_ctx* c, const void* k, const void* v, int32_t n, mkv_stream_t stream) {
+  if (!c || !k || !v || n < 1) return MKV_ERR_INVALID_ARG;
+  if (!c->ready) return MKV_ERR_STATE;
+  if (c->T + n > c->cfg.max_ctx || c->tail_bytes == 0) {
+    g_last_error = "mkv_append: the context would exceed max_ctx";
+    return MKV_ERR_INVALID_ARG;
+  }
+  CK(cudaSetDevice(c->cfg.device));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int S = c->cfg.segment;
+  int64_t first = 0;
+  while (first < n) {
+    const int take = (int)std::min<int64_t>(n - first, S - c->tail_len);
+    AppendParams a;
+    a.k = static_cast<const __half*>(k);
+    a.v = static_cast<const __half*>(v);
+    a.n_total = n;
+    a.first = first;
+    a.n = take;
+    a.tail_len = c->tail_len;
+    a.BH = c->BH;
+    a.S = S;
+    a.R = c->R[c->live];
+    a.pool = c->pool;
+    a.tail_k = c->tail_off;
+    a.tail_v = c->tail_off + c->tail_bytes / 2;
+    a.tail_x = c->tail_x;
+    CK(launch_append(a, st));
+    c->launches += 1;
+    c->tail_len += take;
+    c->T += take;
+    first += take;
+    if (c->tail_len == S) {
+      mkv_status s = commit_tail(c, st);
+      if (s != MKV_OK) return s;
+    }
+  }
   return MKV_OK;
 }
 
@@ -615,22 +800,38 @@ mkv_status mkv_export(const mkv_ctx* c, int b, int h, int which, float* basis, f
   std::vector<mkv_segment_header> hd(c->n_seg);
   CK(cudaMemcpy(hd.data(), c->hdr[c->live] + sx * c->n_seg, c->n_seg * sizeof(mkv_segment_header),
                 cudaMemcpyDeviceToHost));
+  // the prefill segments are contiguous; each committed segment is exported
+  // after them, in order
   const uint64_t first = (uint64_t)hd[0].off16 * 16u;
-  const mkv_segment_header& last = hd[c->n_seg - 1];
-  const uint64_t end = (uint64_t)last.off16 * 16u + segment_bytes(last.strategy, last.rows, c->cfg.c);
-  const uint64_t bytes = end - first;
+  const mkv_segment_header& last0 = hd[c->nseg0 - 1];
+  const uint64_t end0 = (uint64_t)last0.off16 * 16u + segment_bytes(last0.strategy, last0.rows, c->cfg.c);
+  uint64_t bytes = end0 - first;
+  for (int i = c->nseg0; i < c->n_seg; ++i) bytes += segment_bytes(hd[i].strategy, hd[i].rows, c->cfg.c);
   if (payload) {
     if (*payload_bytes < bytes) {
       *payload_bytes = bytes;
       return MKV_ERR_INVALID_ARG;
     }
-    CK(cudaMemcpy(payload, c->pool + first, bytes, cudaMemcpyDeviceToHost));
+    uint8_t* out = static_cast<uint8_t*>(payload);
+    CK(cudaMemcpy(out, c->pool + first, end0 - first, cudaMemcpyDeviceToHost));
+    uint64_t at = end0 - first;
+    for (int i = c->nseg0; i < c->n_seg; ++i) {
+      const uint64_t sz = segment_bytes(hd[i].strategy, hd[i].rows, c->cfg.c);
+      CK(cudaMemcpy(out + at, c->pool + (uint64_t)hd[i].off16 * 16u, sz, cudaMemcpyDeviceToHost));
+      at += sz;
+    }
   }
   *payload_bytes = bytes;
   if (headers) {
+    uint64_t at = end0 - first;
     for (int i = 0; i < c->n_seg; ++i) {
       headers[i] = hd[i];
-      headers[i].off16 = hd[i].off16 - (uint32_t)(first >> 4);
+      if (i < c->nseg0) {
+        headers[i].off16 = hd[i].off16 - (uint32_t)(first >> 4);
+      } else {
+        headers[i].off16 = (uint32_t)(at >> 4);
+        at += segment_bytes(hd[i].strategy, hd[i].rows, c->cfg.c);
+      }
     }
   }
   return MKV_OK;

@@ -70,7 +70,33 @@ struct CompressParams {
   uint8_t* pool;
   uint64_t pool_check;       // pack writes must end within this many pool bytes
   int* err;                  // device status word
+  uint64_t* packed_end;      // commit: device running end of the packed bytes (scan base)
 };
+
+// Decode-time append: rotates n new tokens per stream into the stream's K and
+// V bases and stores them, fp16, as rows [tail_len, tail_len + n) of the tail
+// (dense rotated rows in the pool, original tokens in tail_x).
+struct AppendParams {
+  const __half* k;           // [B][H][n_total][128]: this call's new tokens
+  const __half* v;
+  int64_t n_total;           // tokens per stream in k and v
+  int64_t first;             // first of them to store
+  int n;                     // tokens stored by this launch
+  int tail_len;              // rows already in the tail
+  int BH, S;
+  const float* R;            // [2][BH][128][128] live bases
+  uint8_t* pool;
+  uint64_t tail_k, tail_v;   // byte offsets of the rotated tail regions
+  __half* tail_x;            // [2][BH][S][128] original tokens
+};
+cudaError_t launch_append(const AppendParams& a, cudaStream_t st);
+// headers of one committed segment per stream: offsets from *packed_end on
+// (which then moves past them)
+cudaError_t launch_commit_scan(const CompressParams& p, cudaStream_t st);
+// out[2][BH][n_old + 1] = old[2][BH][n_old] with seg_new[2][BH] appended per stream
+cudaError_t launch_grow_headers(const mkv_segment_header* old, int n_old,
+                                const mkv_segment_header* seg_new, int n_streams2,
+                                mkv_segment_header* out, cudaStream_t st);
 
 cudaError_t launch_gram(const CompressParams& p, cudaStream_t st);
 cudaError_t launch_eig(const CompressParams& p, cudaStream_t st);
@@ -105,8 +131,16 @@ struct DecodeParams {
   int B, H, Hq, g;
   int64_t T;
   int64_t Tp;                      // row stride of scores / candidates: T rounded up to 16
-  int S, c, n_seg;
+  int S, c, n_seg;                 // n_seg: segments per stream, prefill ones then committed ones
   int kk;                          // min(top_k, T)
+  // decode-time appends: tokens [0, T0) are the prefill (segments 0 .. nseg0 - 1
+  // at multiples of S, the last possibly ragged); committed segments of S
+  // tokens follow from T0; tokens [T_packed, T) wait in the tail, stored as
+  // dense rotated rows at pool offset tail_k16 (K) / tail_v16 (V), in 16-byte
+  // units, S rows per stream
+  int64_t T0, T_packed;
+  int nseg0;
+  uint32_t tail_k16, tail_v16;
   const __half* q;                 // [B][Hq][128]
   const float* RK;                 // [BH][128][128]
   const float* RV;                 // [BH][128][128]
@@ -152,6 +186,12 @@ struct DecodeParams {
   int pdl_trigger;                 // kernels let their dependents start early
 };
 
+// First token of segment sg of a stream (prefill segments at multiples of S,
+// committed segments of S tokens after the prefill's T0 tokens).
+__host__ __device__ inline int64_t seg_start(int sg, int S, int nseg0, int64_t T0) {
+  return sg < nseg0 ? (int64_t)sg * S : T0 + (int64_t)(sg - nseg0) * S;
+}
+
 // bits of the device status word (0 = ok), set with atomicOr
 constexpr int DEV_ERR_TIMEOUT = 1;   // a bounded wait gave up
 constexpr int DEV_ERR_CHECK = 2;     // an access fell outside the checked pool extent
@@ -171,7 +211,7 @@ void score_stage_plan(int S, int c, int* stage_bytes, int* n_stages);
 // once per compression); plan holds n_streams * n_seg entries
 cudaError_t launch_partition(const mkv_segment_header* hdrK, int n_streams, int n_seg, int c,
                              int G, int stage_bytes, int32_t* part, int32_t* cta_cnt,
-                             StagePlan* plan, int32_t* plan_n, cudaStream_t st);
+                             StagePlan* plan, int32_t* plan_n, int64_t* prefix, cudaStream_t st);
 cudaError_t launch_qrot(const DecodeParams& p, cudaStream_t st);
 cudaError_t launch_score(const DecodeParams& p, cudaStream_t st);
 // the selection launch (one cluster of sel_R CTAs per stream)

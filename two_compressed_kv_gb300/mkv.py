@@ -88,6 +88,7 @@ def _load():
         "mkv_check_device": (c_int, [P]),
         "mkv_basis_static": (c_int, [P, P, c_int, c_int, c_int64, P, P, P]),
         "mkv_debug_wait_test": (c_int, [P, c_uint64, P]),
+        "mkv_append": (c_int, [P, P, P, c_int32, P]),
         "mkv_set_flags": (c_int, [P, c_uint32]),
         "mkv_debug_set_pdl": (c_int, [P, c_uint32]),
         "mkv_debug_set_check_extent": (c_int, [P, c_uint64]),
@@ -180,6 +181,15 @@ def mkv_decode(ctx, q, out, sel=None, stream=None) -> None:
     po = _dptr(out, torch.float32, "out", q.shape)
     ps = None if sel is None else _dptr(sel, torch.int32, "sel")
     _check(_lib.mkv_decode(ctx, pq, po, ps, _stream_ptr(stream, q.device)), "mkv_decode")
+
+
+def mkv_append(ctx, k, v, stream=None) -> None:
+    """k, v: fp16 [B][H][n][128] new tokens of every stream."""
+    import torch
+    pk = _dptr(k, torch.float16, "k")
+    pv = _dptr(v, torch.float16, "v", k.shape)
+    _check(_lib.mkv_append(ctx, pk, pv, int(k.shape[2]), _stream_ptr(stream, k.device)),
+           "mkv_append")
 
 
 def mkv_decode_raw(ctx, q_ptr: int, out_ptr: int, sel_ptr: int = 0, stream_ptr: int = 0) -> int:
@@ -294,6 +304,10 @@ class Mkv:
         mkv_compress(self.ctx, k, v, k.shape[2], stream)
         self.T = k.shape[2]
 
+    def append(self, k, v, stream=None):
+        mkv_append(self.ctx, k, v, stream)
+        self.T += k.shape[2]
+
     def decode(self, q, out=None, sel=None, stream=None):
         import torch
         if out is None:
@@ -302,7 +316,7 @@ class Mkv:
         return out
 
     def n_segments(self) -> int:
-        return -(-self.T // self.cfg.segment)
+        return int(mkv_stats(self.ctx)["n_segments"])
 
     def export(self, b, h, which):
         return mkv_export(self.ctx, b, h, which, self.n_segments())
