@@ -41,8 +41,8 @@ from typing import List, Optional
 
 import numpy as np
 
-SM, PV, DENSE = 0, 1, 2
-STRATEGY_NAMES = {SM: "SM", PV: "PV", DENSE: "D"}
+SM, PV, DENSE, PVB = 0, 1, 2, 3
+STRATEGY_NAMES = {SM: "SM", PV: "PV", DENSE: "D", PVB: "PVB"}
 HEADER_DTYPE = np.dtype([("off16", "<u4"), ("strategy", "u1"), ("rsv", "u1"), ("rows", "<u2")])
 
 
@@ -142,28 +142,40 @@ def segment_stats(Xt_seg: np.ndarray, P_seg: np.ndarray, c: int) -> SegmentStats
 def segment_cost(strategy: int, rows: int, c: int, d: int = 128) -> int:
     """Packed bytes of one segment (READING: the cost that "cheapest" means).
 
-    SM: c uint8 channel indices padded to 16 B, then rows x c fp16 values.
-    PV: rows x c fp16 values, then rows x c uint8 indices padded to 16 B.
-    D : rows x d fp16 values."""
+    SM : c uint8 channel indices padded to 16 B, then rows x c fp16 values.
+    PV : rows x c fp16 values, then rows x c uint8 indices padded to 16 B.
+    D  : rows x d fp16 values.
+    PVB: rows x c fp16 values, then one 16-byte channel bitmask per row
+         (READING of the pages' open "suitable strategy": the per-vector
+         selection with its channels as a bitmask, cheaper than c index bytes
+         when c > 16)."""
     if strategy == SM:
         return pad16(c) + 2 * c * rows
     if strategy == PV:
         return 2 * c * rows + pad16(c * rows)
     if strategy == DENSE:
         return 2 * d * rows
+    if strategy == PVB:
+        return 2 * c * rows + 16 * rows
     raise ValueError(strategy)
 
 
-def choose_strategy(f_sm: float, f_pv: float, rows: int, c: int, tau: float, d: int = 128) -> int:
+def choose_strategy(f_sm: float, f_pv: float, rows: int, c: int, tau: float, d: int = 128,
+                    bitmask_pv: bool = False) -> int:
     """The cheapest strategy whose retained fraction is >= tau; dense is always
-    allowed; equal costs resolve in the order SM, PV, D (READING)."""
+    allowed; equal costs resolve in the order SM, PV, PVB, D (READING).  PVB
+    (per-vector channels as a bitmask) is a candidate only when bitmask_pv;
+    it keeps exactly PV's channels, so it is eligible whenever PV is."""
+    order = {SM: 0, PV: 1, PVB: 2, DENSE: 3}
     cands = []
     if f_sm >= tau:
-        cands.append((segment_cost(SM, rows, c, d), SM))
+        cands.append((segment_cost(SM, rows, c, d), order[SM], SM))
     if f_pv >= tau:
-        cands.append((segment_cost(PV, rows, c, d), PV))
-    cands.append((segment_cost(DENSE, rows, c, d), DENSE))
-    return min(cands)[1]
+        cands.append((segment_cost(PV, rows, c, d), order[PV], PV))
+        if bitmask_pv:
+            cands.append((segment_cost(PVB, rows, c, d), order[PVB], PVB))
+    cands.append((segment_cost(DENSE, rows, c, d), order[DENSE], DENSE))
+    return min(cands)[2]
 
 
 @dataclass
@@ -183,7 +195,7 @@ class CompressedStream:
         s = self.segs[t // self.S]
         if s.strategy == SM:
             return s.mask
-        if s.strategy == PV:
+        if s.strategy in (PV, PVB):
             return self.P[t]
         return np.arange(self.d)
 
@@ -205,7 +217,7 @@ class CompressedStream:
 
 
 def compress_stream(X: np.ndarray, S: int, c: int, tau: float,
-                    R: Optional[np.ndarray] = None) -> CompressedStream:
+                    R: Optional[np.ndarray] = None, bitmask_pv: bool = False) -> CompressedStream:
     """Steps 1-4 for one stream.  `R` (an orthonormal basis) replaces step 1
     when given; the parity tests use that to check the steps that follow a
     basis produced elsewhere (a basis is only unique up to column signs and
@@ -222,7 +234,7 @@ def compress_stream(X: np.ndarray, S: int, c: int, tau: float,
     tau = float(np.float32(tau))            # the threshold is an fp32 value (READING)
     for (a, b) in segment_bounds(T, S):
         st = segment_stats(Xt[a:b], P[a:b], c)
-        st.strategy = choose_strategy(st.f_sm, st.f_pv, b - a, c, tau, d)
+        st.strategy = choose_strategy(st.f_sm, st.f_pv, b - a, c, tau, d, bitmask_pv)
         cs.segs.append(st)
     return cs
 
@@ -230,6 +242,25 @@ def compress_stream(X: np.ndarray, S: int, c: int, tau: float,
 # ---------------------------------------------------------------------------
 # Packed layout (§1 Observation & Method 2: sparse KV packed dense)
 # ---------------------------------------------------------------------------
+def channel_bitmask(P: np.ndarray) -> np.ndarray:
+    """16-byte little-endian channel bitmask of each row of channel lists P
+    ([rows, c]): bit j % 32 of 32-bit word j // 32 is set for every channel j
+    in the row."""
+    rows = P.shape[0]
+    words = np.zeros((rows, 4), dtype=np.uint64)
+    for r in range(rows):
+        for j in P[r]:
+            words[r, int(j) // 32] |= np.uint64(1) << np.uint64(int(j) % 32)
+    return words.astype("<u4").view(np.uint8).reshape(rows, 16)
+
+
+def bitmask_channels(mask16: np.ndarray) -> np.ndarray:
+    """Ascending channels whose bits are set in one 16-byte bitmask."""
+    words = np.frombuffer(np.ascontiguousarray(mask16).tobytes(), dtype="<u4")
+    return np.array([32 * w + b for w in range(4) for b in range(32)
+                     if (int(words[w]) >> b) & 1], dtype=np.int64)
+
+
 def pack_stream(cs: CompressedStream):
     """(headers, payload bytes) of one stream.
 
@@ -255,6 +286,10 @@ def pack_stream(cs: CompressedStream):
             idx = np.zeros(pad16(c * rows), dtype=np.uint8)
             idx[:c * rows] = P.reshape(-1)
             blob = vals.astype("<f2").tobytes() + idx.tobytes()
+        elif s.strategy == PVB:
+            P = cs.P[a:b]
+            vals = np.take_along_axis(q16[a:b], P, axis=1)
+            blob = vals.astype("<f2").tobytes() + channel_bitmask(P).tobytes()
         else:
             blob = q16[a:b].astype("<f2").tobytes()
         assert len(blob) == segment_cost(s.strategy, rows, c, d)
@@ -290,6 +325,14 @@ def unpack_stream(hdr: np.ndarray, payload: bytes, T: int, S: int, c: int, d: in
             out[r, idx] = vals
         elif st == DENSE:
             out[a:b] = seg.view("<f2").reshape(rows, d).astype(np.float64)
+        elif st == PVB:
+            vals = seg[:2 * c * rows].view("<f2").reshape(rows, c).astype(np.float64)
+            masks = seg[2 * c * rows:].reshape(rows, 16)
+            for r in range(rows):
+                ch = bitmask_channels(masks[r])
+                if len(ch) != c:
+                    raise ValueError(f"segment {si} row {r}: bitmask holds {len(ch)} channels")
+                out[a + r, ch] = vals[r]
         else:
             raise ValueError(f"segment {si}: bad strategy {st}")
     return out

@@ -353,7 +353,7 @@ def _mut_ties_high(mp):
 
 
 def _mut_most_retained(mp):
-    def f(f_sm, f_pv, rows, c, tau, d=128):
+    def f(f_sm, f_pv, rows, c, tau, d=128, bitmask_pv=False):
         return O.PV if f_pv >= tau else (O.SM if f_sm >= tau else O.DENSE)
     mp.setattr(O, "choose_strategy", f)
 
