@@ -370,7 +370,7 @@ def gathered_bytes(m, M, sel: np.ndarray, w: W.Workload) -> float:
                 hdr = M.mkv_export_headers(m.ctx, b, h, x, m.n_segments())
                 segs = sel[b, h] // w.segment
                 st = hdr["strategy"][segs]
-                row = np.where(st == 0, 2 * c, np.where(st == 1, 3 * c, 256))
+                row = np.select([st == 0, st == 1, st == 3], [2 * c, 3 * c, 2 * c + 16], 256)
                 total += int(row.sum())
                 sm_segs = np.unique(segs[st == 0])
                 total += len(sm_segs) * ((c + 15) // 16 * 16)
@@ -539,6 +539,11 @@ def run_gpu(args, w: W.Workload, ws: int, rank: int, local: int):
         for name, layers in ((W.MILLION_1M.name, 1), (W.MIXED_256K.name, 1)):
             side[name] = side_workload(W.WORKLOADS[name], layers, max(5, args.steps), dev, stream)
             torch.cuda.empty_cache()
+        # the headline shape with bitmask-indexed per-vector segments (4 layers)
+        from two_compressed_kv_gb300 import mkv as M
+        side[w.name + "+bitmask-pv"] = side_workload(w, 4, max(5, args.steps), dev, stream,
+                                                     M.MKV_FLAG_BITMASK_PV)
+        torch.cuda.empty_cache()
 
     if rank == 0:
         cfgd = workload_config(w, L, score_bytes)
@@ -629,13 +634,13 @@ def prefill_roofline(w: W.Workload, ms: float, st: dict, peak_gbs: float) -> dic
             "tensor_frac_of_measured_bf16": (tfs / tf_peak) if tf_peak else None}
 
 
-def side_workload(w: W.Workload, layers: int, steps: int, dev, stream) -> dict:
+def side_workload(w: W.Workload, layers: int, steps: int, dev, stream, flags: int = 0) -> dict:
     """One more workload, timed like the headline (CUDA-graph replays of a
     decode of every layer, 3 warm-up steps, CUDA events on the launching
     stream) plus its mkv_compress time per layer."""
     from two_compressed_kv_gb300 import mkv as M
     cfg = M.make_config(w.batch, w.n_kv_heads, w.n_q_heads, w.ctx, w.segment, w.c, w.tau,
-                        w.top_k, flags=0, device=dev.index or 0)
+                        w.top_k, flags=flags, device=dev.index or 0)
     ctxs, qs, outs, comp = [], [], [], []
     for layer in range(layers):
         K, V = W.draw_kv(w, layer=layer, device=dev)
@@ -675,8 +680,8 @@ def side_workload(w: W.Workload, layers: int, steps: int, dev, stream) -> dict:
     for m in ctxs:
         if M.mkv_check_device(m.ctx) != M.MKV_OK:
             raise RuntimeError("a device-side check fired during the timed region")
-    kt = kernel_times(ctxs, step, M.MKV_FLAG_KERNEL_TIMING, 5, dev)
-    s_ms, s_n = kernel_times(ctxs, step, M.MKV_FLAG_SCORE_TIMING, 5, dev)["score"]
+    kt = kernel_times(ctxs, step, flags | M.MKV_FLAG_KERNEL_TIMING, 5, dev, flags)
+    s_ms, s_n = kernel_times(ctxs, step, flags | M.MKV_FLAG_SCORE_TIMING, 5, dev, flags)["score"]
     kk = min(w.top_k, w.ctx)
     sel0 = torch.empty(w.batch, w.n_kv_heads, kk, dtype=torch.int32, device=dev)
     M.mkv_decode(ctxs[0].ctx, qs[0], outs[0], sel0, stream)
@@ -697,7 +702,10 @@ def side_workload(w: W.Workload, layers: int, steps: int, dev, stream) -> dict:
                        "unit": "prefill-tokens/s per layer (K and V)",
                        "ms_per_layer_median": statistics.median(comp)},
            "kernel_us_per_layer_standalone": {k: v[0] / max(1, v[1]) * 1e3 for k, v in kt.items()},
-           "strategies_K": st0["strategy_count"][0], "strategies_V": st0["strategy_count"][1]}
+           "strategies_K": st0["strategy_count"][0], "strategies_V": st0["strategy_count"][1],
+           "payload_bytes_K": st0["payload_bytes"][0], "payload_bytes_V": st0["payload_bytes"][1]}
+    if flags & M.MKV_FLAG_BITMASK_PV:
+        res["config"]["strategies"] = "SM, PV, PVB (bitmask-indexed per-vector), D"
     res["prefill"].update(prefill_roofline(w, statistics.median(comp), st0, peak))
     for m in ctxs:
         m.close()

@@ -59,7 +59,9 @@ typedef enum {
 enum {
   MKV_STRATEGY_SM = 0,    /* segment-shared mask of c channels */
   MKV_STRATEGY_PV = 1,    /* per-vector top-c channels (values + uint8 indices) */
-  MKV_STRATEGY_DENSE = 2  /* all 128 channels */
+  MKV_STRATEGY_DENSE = 2, /* all 128 channels */
+  MKV_STRATEGY_PVB = 3    /* per-vector top-c channels (values + a 16-byte channel
+                             bitmask per row); only with MKV_FLAG_BITMASK_PV */
 };
 
 #define MKV_HEAD_DIM 128
@@ -75,7 +77,14 @@ enum {
  * copies of packed keys) overlap that kernel's tail.  Timing flags imply this
  * flag, since an event between two kernels separates them. */
 #define MKV_FLAG_NO_PDL 4u
-#define MKV_FLAGS_ALL (MKV_FLAG_KERNEL_TIMING | MKV_FLAG_SCORE_TIMING | MKV_FLAG_NO_PDL)
+/* Adds MKV_STRATEGY_PVB to the strategies mkv_compress (and the commits of
+ * mkv_append) may choose: the per-vector channels of PV, encoded as a 16-byte
+ * bitmask per row instead of c index bytes (cheaper whenever c > 16; on an
+ * equal cost PV is kept).  A variant the paper leaves open ("a suitable
+ * compression strategy" per segment). */
+#define MKV_FLAG_BITMASK_PV 8u
+#define MKV_FLAGS_ALL \
+  (MKV_FLAG_KERNEL_TIMING | MKV_FLAG_SCORE_TIMING | MKV_FLAG_NO_PDL | MKV_FLAG_BITMASK_PV)
 
 typedef struct {
   int32_t batch;          /* B >= 1 */
@@ -116,7 +125,7 @@ typedef struct {
 typedef struct {
   int64_t ctx_len;                 /* T of the current cache (0 if none) */
   int64_t n_segments;              /* per stream */
-  int64_t strategy_count[2][3];    /* [K, V][SM, PV, DENSE] over all streams */
+  int64_t strategy_count[2][4];    /* [K, V][SM, PV, DENSE, PVB] over all streams */
   uint64_t payload_bytes[2];       /* packed bytes of all K, all V streams */
   uint64_t header_bytes;           /* bytes of all segment headers */
   uint64_t uncompressed_bytes;     /* 2 * B * H * T * 128 * 2 */
@@ -148,6 +157,9 @@ mkv_status mkv_validate_config(const mkv_config* cfg);
  *   SM:    pad16(c) + rows * 2c      (uint8 mask, then fp16 values per row)
  *   PV:    rows * 2c + pad16(rows*c) (fp16 values per row, then uint8 indices)
  *   DENSE: rows * 256
+ *   PVB:   rows * 2c + rows * 16     (fp16 values per row, then a bitmask per
+ *                                     row: bit j % 32 of little-endian word
+ *                                     j / 32 for channel j)
  * Returns 0 for an invalid argument. */
 uint64_t mkv_segment_bytes(int strategy, int rows, int c);
 

@@ -111,10 +111,10 @@ def check_basis(X: np.ndarray, R: np.ndarray, lam: np.ndarray, report: dict):
 
 
 def compare_compressed(X: np.ndarray, R: np.ndarray, hdr: np.ndarray, payload: bytes,
-                       S: int, c: int, tau: float, report: dict):
+                       S: int, c: int, tau: float, report: dict, bitmask_pv: bool = False):
     """Packed stream from the library vs the oracle's steps 2-4 given the
     library's basis.  Returns the oracle's CompressedStream."""
-    cs = O.compress_stream(X, S, c, tau, R=R.astype(np.float64))
+    cs = O.compress_stream(X, S, c, tau, R=R.astype(np.float64), bitmask_pv=bitmask_pv)
     buf = np.frombuffer(payload, dtype=np.uint8)
     q16 = O.to_fp16(cs.Xt)
     tau32 = float(np.float32(tau))
@@ -164,8 +164,12 @@ def compare_compressed(X: np.ndarray, R: np.ndarray, hdr: np.ndarray, payload: b
                         f"segment {si}")
         else:
             gv = gseg[:2 * c * rows].view("<f2").reshape(rows, c)
-            gidx = gseg[2 * c * rows:2 * c * rows + c * rows].reshape(rows, c).astype(np.int64)
-            assert not gseg[2 * c * rows + c * rows:].any(), f"segment {si}: nonzero padding"
+            if st == O.PVB:
+                masks = gseg[2 * c * rows:].reshape(rows, 16)
+                gidx = np.stack([O.bitmask_channels(masks[r]) for r in range(rows)])
+            else:
+                gidx = gseg[2 * c * rows:2 * c * rows + c * rows].reshape(rows, c).astype(np.int64)
+                assert not gseg[2 * c * rows + c * rows:].any(), f"segment {si}: nonzero padding"
             for r in range(rows):
                 P = cs.P[a + r]
                 if not np.array_equal(gidx[r], P):

@@ -64,11 +64,11 @@ int main(void) {
 
 
 def test_segment_bytes_match_oracle_layout(M):
-    for st in (0, 1, 2):
+    for st in (0, 1, 2, 3):
         for c in range(8, 129, 8):
             for rows in (1, 2, 7, 16, 44, 64, 128, 255, 256):
                 assert M.mkv_segment_bytes(st, rows, c) == O.segment_cost(st, rows, c)
-    assert M.mkv_segment_bytes(3, 10, 8) == 0
+    assert M.mkv_segment_bytes(4, 10, 8) == 0
     assert M.mkv_segment_bytes(0, 0, 8) == 0
 
 
@@ -85,7 +85,7 @@ def test_validate_config(M):
            dict(segment=72), dict(segment=272), dict(c=4), dict(c=36), dict(c=136),
            dict(tau=0.0), dict(tau=1.5), dict(tau=float("nan")), dict(top_k=0),
            dict(max_ctx=0), dict(batch=0), dict(attn_chunk=4), dict(attn_chunk=12),
-           dict(flags=8), dict(device=-1), dict(attn_chunk=136)]
+           dict(flags=16), dict(device=-1), dict(attn_chunk=136)]
     for b in bad:
         assert M.mkv_validate_config(_cfg(M, **b)) == M.MKV_ERR_INVALID_ARG, b
     for good in [dict(segment=16), dict(segment=256), dict(c=8), dict(c=128), dict(tau=1.0),

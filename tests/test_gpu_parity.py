@@ -25,9 +25,9 @@ def M():
     return mkv
 
 
-def run_gpu(M, w, K, V, q, attn_chunk=0, max_ctx=None):
+def run_gpu(M, w, K, V, q, attn_chunk=0, max_ctx=None, flags=0):
     cfg = M.make_config(w.batch, w.n_kv_heads, w.n_q_heads, max_ctx or K.shape[2], w.segment,
-                        w.c, w.tau, w.top_k, attn_chunk=attn_chunk)
+                        w.c, w.tau, w.top_k, attn_chunk=attn_chunk, flags=flags)
     m = M.Mkv(cfg)
     m.compress(K.to(DEV), V.to(DEV))
     kk = min(w.top_k, K.shape[2])
@@ -37,7 +37,8 @@ def run_gpu(M, w, K, V, q, attn_chunk=0, max_ctx=None):
     return m, out.cpu().numpy(), sel.cpu().numpy()
 
 
-def check_streams(w, K, V, q, m, out, sel, streams, basis=True, oracle_packed=True):
+def check_streams(w, K, V, q, m, out, sel, streams, basis=True, oracle_packed=True,
+                  bitmask_pv=False):
     rep = {}
     g = w.group
     T = K.shape[2]
@@ -49,8 +50,8 @@ def check_streams(w, K, V, q, m, out, sel, streams, basis=True, oracle_packed=Tr
         if basis:
             check_basis(Kn, RK, lamK, rep)
             check_basis(Vn, RV, lamV, rep)
-        ck = compare_compressed(Kn, RK, hk, pk, w.segment, w.c, w.tau, rep)
-        cv = compare_compressed(Vn, RV, hv, pv, w.segment, w.c, w.tau, rep)
+        ck = compare_compressed(Kn, RK, hk, pk, w.segment, w.c, w.tau, rep, bitmask_pv)
+        cv = compare_compressed(Vn, RV, hv, pv, w.segment, w.c, w.tau, rep, bitmask_pv)
         Kh = O.unpack_stream(hk, pk, T, w.segment, w.c)
         Vh = O.unpack_stream(hv, pv, T, w.segment, w.c)
         qn = q[b, h * g:(h + 1) * g].cpu().numpy()
@@ -158,6 +159,53 @@ def test_edge_cases(M, name):
     rep = check_streams(w, K, V, q, m, out, sel, all_streams(w), basis=False)
     _near_tie_budget(rep)
     m.close()
+
+
+# ---------------------------------------------------------------------------
+# Bitmask-indexed per-vector segments (MKV_FLAG_BITMASK_PV)
+# ---------------------------------------------------------------------------
+PVB_CASES = {
+    "mixed-regimes-c48": dict(ctx=900, segment=64, c=48, tau=0.9, mixed_regimes=True),
+    "c40-ragged": dict(ctx=700, segment=64, c=40, tau=0.93),
+    "c16-tie-to-PV": dict(ctx=400, segment=32, c=16, tau=0.6),
+    "c8-PV-cheaper": dict(ctx=300, segment=32, c=8, tau=0.4),
+    "g7-S16": dict(n_kv_heads=1, n_q_heads=7, ctx=333, segment=16, c=40, tau=0.93),
+}
+
+
+@pytest.mark.parametrize("name", list(PVB_CASES))
+def test_bitmask_pv_segments(M, name):
+    w = W.small_workload("pvb-" + name, **PVB_CASES[name])
+    K, V = W.draw_kv(w)
+    q = W.draw_queries(w, K)
+    m, out, sel = run_gpu(M, w, K, V, q, flags=M.MKV_FLAG_BITMASK_PV)
+    rep = check_streams(w, K, V, q, m, out, sel, all_streams(w), basis=False, bitmask_pv=True)
+    _near_tie_budget(rep)
+    counts = m.stats()["strategy_count"]
+    if w.c > 16:
+        assert counts[0][M.MKV_STRATEGY_PV] + counts[1][M.MKV_STRATEGY_PV] == 0
+        assert counts[1][M.MKV_STRATEGY_PVB] > 0
+    else:
+        assert counts[0][M.MKV_STRATEGY_PVB] + counts[1][M.MKV_STRATEGY_PVB] == 0
+    m.close()
+
+
+def test_bitmask_pv_full_size_headline_stream(M):
+    """The 128K batch-8 layer with bitmask PV segments (V is mostly per-vector
+    there): sampled streams against the oracle, all selections valid."""
+    w = W.HEADLINE_128K
+    K, V = W.draw_kv(w, layer=0, device=DEV)
+    q = W.draw_queries(w, K)
+    m, out, sel = run_gpu(M, w, K, V, q, flags=M.MKV_FLAG_BITMASK_PV)
+    st = m.stats()
+    assert st["strategy_count"][1][M.MKV_STRATEGY_PVB] > 0
+    rep = check_streams(w, K, V, q, m, out, sel, [(0, 0), (5, 3)], basis=False,
+                        bitmask_pv=True)
+    _near_tie_budget(rep)
+    assert (np.diff(sel, axis=2) > 0).all() and np.isfinite(out).all()
+    m.close()
+    del K, V
+    torch.cuda.empty_cache()
 
 
 def test_zero_and_constant_streams(M):

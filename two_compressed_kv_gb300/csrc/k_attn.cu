@@ -38,6 +38,15 @@ constexpr int AT_VLD = 136;         // halves per V tile row (272 B: ldmatrix wi
 constexpr int AT_PLD = 72;          // halves per P row (144 B)
 
 constexpr int32_t NO_IDX = (int32_t)0x80000000;
+// channel-list field of a PVB row: this flag plus the distance / 8 to the
+// row's 16-byte bitmask (SM distances are negative, PV ones below 2^28)
+constexpr uint32_t PVB_FLAG = 0x10000000u;
+
+__device__ __forceinline__ bool is_pvb(uint32_t y) { return (int32_t)y > 0 && (y & PVB_FLAG); }
+// byte distance from a row's values to its channel list (SM, PV, PVB rows)
+__device__ __forceinline__ int64_t list_dist(uint32_t y) {
+  return 8 * (int64_t)(is_pvb(y) ? (int32_t)(y & ~PVB_FLAG) : (int32_t)y);
+}
 
 // Row of token t in stream s: pool offset of its stored values / 16, and the
 // byte distance / 8 from the values to the row's channel list (the segment
@@ -69,6 +78,10 @@ __device__ __forceinline__ uint2 row_meta(const DecodeParams& p, const mkv_segme
     const uint32_t dv = c2 * r;
     return make_uint2(hd.off16 + dv / 16u, (uint32_t)c * (2u * hd.rows - r) / 8u);
   }
+  if (hd.strategy == MKV_STRATEGY_PVB) {
+    const uint32_t dv = c2 * r;
+    return make_uint2(hd.off16 + dv / 16u, PVB_FLAG | ((c2 * (hd.rows - r) + 16u * r) / 8u));
+  }
   return make_uint2(hd.off16 + 16u * r, (uint32_t)NO_IDX);
 }
 
@@ -77,7 +90,7 @@ __device__ __forceinline__ uint64_t row_end(const uint2& m, int c) {
   const uint64_t v0 = (uint64_t)m.x * 16u;
   if ((int32_t)m.y == NO_IDX) return v0 + 256u;
   const uint64_t vend = v0 + 2u * (uint32_t)c;
-  const uint64_t iend = (uint64_t)((int64_t)v0 + 8 * (int64_t)(int32_t)m.y) + (uint32_t)c;
+  const uint64_t iend = (uint64_t)((int64_t)v0 + list_dist(m.y)) + (is_pvb(m.y) ? 16u : (uint32_t)c);
   return vend > iend ? vend : iend;
 }
 
@@ -217,17 +230,21 @@ __device__ __forceinline__ void at_issue(const DecodeParams& p, int rel_s, const
   const uint8_t* kv = p.pool + (uint64_t)m.x * 16u;
   const uint8_t* vv = p.pool + (uint64_t)m.z * 16u;
   const uint32_t vs = slot + p.at_kv + p.at_ki;
+  const bool kb = is_pvb(m.y), vb = is_pvb(m.w);
 #pragma unroll
   for (int ck = cl; ck < 16; ck += 8) {
     if (8 * ck < kn) {
       cpa16(slot + 16 * ck, kv + 16 * ck);
-      if (!kd) cpa8(slot + p.at_kv + 8 * ck, kv + 8 * (int64_t)(int32_t)m.y + 8 * ck);
+      if (!kd && !kb) cpa8(slot + p.at_kv + 8 * ck, kv + list_dist(m.y) + 8 * ck);
     }
     if (8 * ck < vn) {
       cpa16(vs + 16 * ck, vv + 16 * ck);
-      if (!vd) cpa8(vs + p.at_vv + 8 * ck, vv + 8 * (int64_t)(int32_t)m.w + 8 * ck);
+      if (!vd && !vb) cpa8(vs + p.at_vv + 8 * ck, vv + list_dist(m.w) + 8 * ck);
     }
   }
+  // PVB rows: the 16-byte bitmask in place of the channel list
+  if (cl == 0 && kb) cpa16(slot + p.at_kv, kv + list_dist(m.y));
+  if (cl == 0 && vb) cpa16(vs + p.at_vv, vv + list_dist(m.w));
 }
 
 template <int NST>
@@ -315,9 +332,49 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_kernel(DecodeParams p) {
         const uint4 mt = valid ? meta[x0 + tok] : make_uint4(0u, 0u, 0u, 0u);
         const uint8_t* slot = at_smem + L.stages + (size_t)(st * AT_CHUNK + tok) * p.at_slot;
         const bool kd = (int32_t)mt.y == NO_IDX, vd = (int32_t)mt.w == NO_IDX;
-        const int kn = valid ? (kd ? D : c) : 0, vn = valid ? (vd ? D : c) : 0;
+        const bool kb = valid && is_pvb(mt.y), vb = valid && is_pvb(mt.w);
+        const int kn = valid && !kb ? (kd ? D : c) : 0, vn = valid && !vb ? (vd ? D : c) : 0;
+        const uint8_t* vs = slot + p.at_kv + p.at_ki;
+        // PVB rows: lane cl owns channels [16 cl, 16 cl + 16) of the bitmask;
+        // its values follow those of the group's lower lanes (prefix count,
+        // computed by every lane so that the shuffles stay uniform)
+        uint32_t kbits = 0u, vbits = 0u;
+        if (kb) kbits = (*reinterpret_cast<const uint32_t*>(slot + p.at_kv + 4 * (cl >> 1)) >>
+                         (16 * (cl & 1))) & 0xffffu;
+        if (vb) vbits = (*reinterpret_cast<const uint32_t*>(vs + p.at_vv + 4 * (cl >> 1)) >>
+                         (16 * (cl & 1))) & 0xffffu;
+        int kpre = __popc(kbits), vpre = __popc(vbits);
+        {
+          int ki = kpre, vi = vpre;
+#pragma unroll
+          for (int off = 1; off < 8; off <<= 1) {
+            const int ky = __shfl_up_sync(0xffffffffu, ki, off, 8);
+            const int vy = __shfl_up_sync(0xffffffffu, vi, off, 8);
+            if (cl >= off) {
+              ki += ky;
+              vi += vy;
+            }
+          }
+          kpre = ki - kpre;
+          vpre = vi - vpre;
+        }
         for (int h4 = 0; h4 < gp; h4 += 4) {
           float part[4] = {0.f, 0.f, 0.f, 0.f};
+          {
+            uint32_t b = kbits;
+            int i = kpre;
+            while (b) {
+              const int chn = 16 * cl + __ffs(b) - 1;
+              b &= b - 1u;
+              const float v = __half2float(*reinterpret_cast<const __half*>(slot + 2 * i));
+              ++i;
+              const float4 q4 = *reinterpret_cast<const float4*>(qs + chn * gp + h4);
+              part[0] = fmaf(q4.x, v, part[0]);
+              part[1] = fmaf(q4.y, v, part[1]);
+              part[2] = fmaf(q4.z, v, part[2]);
+              part[3] = fmaf(q4.w, v, part[3]);
+            }
+          }
   #pragma unroll
           for (int ck = cl; ck < 16; ck += 8) {
             if (8 * ck < kn) {
@@ -349,10 +406,20 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_kernel(DecodeParams p) {
             *reinterpret_cast<float4*>(lg + tok * gp + h4) =
                 make_float4(part[0] * scale, part[1] * scale, part[2] * scale, part[3] * scale);
         }
+        {
+          uint32_t b = vbits;
+          int i = vpre;
+          __half* vrow = Vt + tok * AT_VLD;
+          while (b) {
+            const int chn = 16 * cl + __ffs(b) - 1;
+            b &= b - 1u;
+            vrow[chn] = *reinterpret_cast<const __half*>(vs + 2 * i);
+            ++i;
+          }
+        }
   #pragma unroll
         for (int ck = cl; ck < 16; ck += 8) {
           if (8 * ck < vn) {
-            const uint8_t* vs = slot + p.at_kv + p.at_ki;
             const uint4 vr = *reinterpret_cast<const uint4*>(vs + 16 * ck);
             const uint2 vx = vd ? make_uint2(0u, 0u)
                                 : *reinterpret_cast<const uint2*>(vs + p.at_vv + 8 * ck);

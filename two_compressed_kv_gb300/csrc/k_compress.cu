@@ -758,6 +758,12 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
         if (si.strategy == MKV_STRATEGY_SM) {
           vrow = reinterpret_cast<__half*>(seg + pad16(c) + 2u * c * rl);
           irow = (rl == 0) ? seg : nullptr;
+        } else if (si.strategy == MKV_STRATEGY_PVB) {
+          vrow = reinterpret_cast<__half*>(seg + 2u * c * rl);
+          irow = nullptr;
+          if (lane == 0)
+            *reinterpret_cast<uint4*>(seg + 2u * c * si.rows + 16u * rl) =
+                make_uint4(w[0], w[1], w[2], w[3]);
         } else {
           vrow = reinterpret_cast<__half*>(seg + 2u * c * rl);
           irow = seg + 2u * c * si.rows + c * rl;
@@ -831,6 +837,12 @@ __global__ void __launch_bounds__(256) strategy_kernel(CompressParams p) {
     int strat = MKV_STRATEGY_DENSE;
     const uint32_t cpv = segment_bytes(MKV_STRATEGY_PV, rws, p.c);
     const uint32_t csm = segment_bytes(MKV_STRATEGY_SM, rws, p.c);
+    const uint32_t cpb = segment_bytes(MKV_STRATEGY_PVB, rws, p.c);
+    // cost ties resolve SM, PV, PVB, dense: later checks win ties
+    if (p.bitmask_pv && fpv >= p.tau && cpb <= best) {
+      best = cpb;
+      strat = MKV_STRATEGY_PVB;
+    }
     if (fpv >= p.tau && cpv <= best) {
       best = cpv;
       strat = MKV_STRATEGY_PV;

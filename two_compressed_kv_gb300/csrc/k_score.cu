@@ -127,6 +127,39 @@ struct StageMeta {
 // q_bar (a broadcast).  q_bar values come from the segment's gathered mask
 // (SM), q_bar indexed by the stored channel (PV) or q_bar itself (dense).
 // Four independent accumulators, summed in a fixed order.
+// PVB rows: the c stored values in channel order and the row's 128-bit
+// channel bitmask; value i belongs to the i-th set bit.  Chunks are taken in
+// order (no rotation) and the bits walked with find-first-set.
+template <int CPR>
+__device__ __forceinline__ float row_dot_bitmask(const uint8_t* base, int rows, int row,
+                                                 const float* qsrc) {
+  constexpr uint32_t C = 8u * CPR;
+  const uint8_t* rowp = base + 2u * C * row;
+  const uint4 mk = *reinterpret_cast<const uint4*>(base + 2u * C * (uint32_t)rows + 16u * row);
+  uint32_t cur = mk.x, nxt1 = mk.y, nxt2 = mk.z, nxt3 = mk.w;
+  int wbase = 0;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+  for (int k = 0; k < CPR; ++k) {
+    float v[8];
+    h8_to_f(*reinterpret_cast<const uint4*>(rowp + 16 * k), v);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      while (cur == 0u && wbase < 96) {   // at most three words to skip
+        cur = nxt1;
+        nxt1 = nxt2;
+        nxt2 = nxt3;
+        nxt3 = 0u;
+        wbase += 32;
+      }
+      const int ch = wbase + __ffs(cur) - 1;
+      cur &= cur - 1u;
+      acc[e & 3] = fmaf(v[e], qsrc[ch & 127], acc[e & 3]);
+    }
+  }
+  return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+}
+
 template <int STRAT, int CPR>
 __device__ __forceinline__ float row_dot(const uint8_t* base, int rows, int row, int lane,
                                          const float* qsrc, const float* qm) {
@@ -193,7 +226,9 @@ __device__ __forceinline__ void score_block(const uint8_t* base, int rows, int r
                                             uint32_t* hs, uint64_t pol) {
   const int row = r0 + lane;
   if (row < rows) {
-    const float sc = row_dot<STRAT, CPR>(base, rows, row, lane, qsrc, qm);
+    float sc;
+    if constexpr (STRAT == MKV_STRATEGY_PVB) sc = row_dot_bitmask<CPR>(base, rows, row, qsrc);
+    else sc = row_dot<STRAT, CPR>(base, rows, row, lane, qsrc, qm);
     st_f32_hint(out + row, sc, pol);
     atomicAdd(&hs[f2key(sc) >> 20], 1u);
   }
@@ -372,6 +407,9 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
           } else if (strat == MKV_STRATEGY_PV) {
             score_block<MKV_STRATEGY_PV, CPR>(base, rows, blk * 32, lane, qsrc, qm[warp], out, hs,
                                               pol);
+          } else if (strat == MKV_STRATEGY_PVB) {
+            score_block<MKV_STRATEGY_PVB, CPR>(base, rows, blk * 32, lane, qsrc, qm[warp], out, hs,
+                                               pol);
           } else {
             score_block<MKV_STRATEGY_DENSE, 16>(base, rows, blk * 32, lane, qsrc, qm[warp], out,
                                                 hs, pol);

@@ -295,7 +295,7 @@ const char* mkv_last_error_string(void) { return g_last_error.c_str(); }
 
 uint64_t mkv_segment_bytes(int strategy, int rows, int c) {
   if (rows < 1 || rows > 65535 || c < 1 || c > MKV_HEAD_DIM) return 0;
-  if (strategy < MKV_STRATEGY_SM || strategy > MKV_STRATEGY_DENSE) return 0;
+  if (strategy < MKV_STRATEGY_SM || strategy > MKV_STRATEGY_PVB) return 0;
   return segment_bytes(strategy, rows, c);
 }
 
@@ -466,6 +466,7 @@ mkv_status mkv_compress(mkv_ctx* c, const void* k, const void* v, int64_t ctx_le
   p.tokmask = c->tokmask;
   p.colE = c->colE;
   p.segK = c->segK;
+  p.bitmask_pv = (c->cfg.flags & MKV_FLAG_BITMASK_PV) != 0u;
   p.hdr = c->hdr[stage];
   p.total = c->total_dev;
   p.pool = nullptr;
@@ -697,6 +698,7 @@ mkv_status commit_tail(mkv_ctx* c, cudaStream_t st) {
   p.pool_check = c->check_override ? std::min(c->check_override, c->tail_off) : c->tail_off;
   p.err = c->err;
   p.packed_end = c->packed_end;
+  p.bitmask_pv = (c->cfg.flags & MKV_FLAG_BITMASK_PV) != 0u;
   CK(launch_analyze(p, st));
   CK(launch_commit_scan(p, st));
   CK(launch_pack(p, st));
@@ -777,7 +779,7 @@ mkv_status mkv_stats(const mkv_ctx* c, mkv_stats_t* out) {
   for (size_t i = 0; i < n; ++i) {
     const int x = (int)(i / ((size_t)c->BH * c->n_seg));
     const int st = h[i].strategy;
-    if (st >= 0 && st < 3) out->strategy_count[x][st] += 1;
+    if (st >= 0 && st < 4) out->strategy_count[x][st] += 1;
     out->payload_bytes[x] += segment_bytes(st, h[i].rows, c->cfg.c);
   }
   out->header_bytes = n * sizeof(mkv_segment_header);

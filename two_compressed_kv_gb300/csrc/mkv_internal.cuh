@@ -24,6 +24,7 @@ __host__ __device__ inline uint32_t segment_bytes(int strategy, int rows, int c)
   switch (strategy) {
     case MKV_STRATEGY_SM: return pad16((uint32_t)c) + 2u * (uint32_t)c * (uint32_t)rows;
     case MKV_STRATEGY_PV: return 2u * (uint32_t)c * (uint32_t)rows + pad16((uint32_t)c * (uint32_t)rows);
+    case MKV_STRATEGY_PVB: return (2u * (uint32_t)c + 16u) * (uint32_t)rows;
     default: return 256u * (uint32_t)rows;
   }
 }
@@ -71,6 +72,7 @@ struct CompressParams {
   uint64_t pool_check;       // pack writes must end within this many pool bytes
   int* err;                  // device status word
   uint64_t* packed_end;      // commit: device running end of the packed bytes (scan base)
+  int bitmask_pv;            // PVB is a candidate strategy
 };
 
 // Decode-time append: rotates n new tokens per stream into the stream's K and

@@ -25,10 +25,11 @@ MKV_ERR_CUDA = 4
 MKV_ERR_DEVICE_CHECK = 5
 MKV_ERR_TIMEOUT = 6
 
-MKV_STRATEGY_SM, MKV_STRATEGY_PV, MKV_STRATEGY_DENSE = 0, 1, 2
+MKV_STRATEGY_SM, MKV_STRATEGY_PV, MKV_STRATEGY_DENSE, MKV_STRATEGY_PVB = 0, 1, 2, 3
 MKV_FLAG_KERNEL_TIMING = 1
 MKV_FLAG_SCORE_TIMING = 2
 MKV_FLAG_NO_PDL = 4
+MKV_FLAG_BITMASK_PV = 8
 MKV_BASIS_STATIC_MAX_BYTES = 16 << 20
 (MKV_KERNEL_QROT, MKV_KERNEL_SCORE, MKV_KERNEL_TOPK, MKV_KERNEL_ATTN, MKV_KERNEL_MERGE,
  MKV_KERNEL_GRAM, MKV_KERNEL_EIG, MKV_KERNEL_ANALYZE, MKV_KERNEL_LAYOUT, MKV_KERNEL_PACK) = range(10)
@@ -50,7 +51,7 @@ class mkv_segment_header(Structure):
 
 class mkv_stats_t(Structure):
     _fields_ = [("ctx_len", c_int64), ("n_segments", c_int64),
-                ("strategy_count", (c_int64 * 3) * 2), ("payload_bytes", c_uint64 * 2),
+                ("strategy_count", (c_int64 * 4) * 2), ("payload_bytes", c_uint64 * 2),
                 ("header_bytes", c_uint64), ("uncompressed_bytes", c_uint64),
                 ("pool_capacity", c_uint64), ("decode_calls", c_int64),
                 ("kernel_launches", c_int64)]
@@ -202,7 +203,7 @@ def mkv_stats(ctx) -> dict:
     _check(_lib.mkv_stats(ctx, ctypes.byref(st)), "mkv_stats")
     return {
         "ctx_len": st.ctx_len, "n_segments": st.n_segments,
-        "strategy_count": [[st.strategy_count[x][i] for i in range(3)] for x in range(2)],
+        "strategy_count": [[st.strategy_count[x][i] for i in range(4)] for x in range(2)],
         "payload_bytes": [st.payload_bytes[0], st.payload_bytes[1]],
         "header_bytes": st.header_bytes, "uncompressed_bytes": st.uncompressed_bytes,
         "pool_capacity": st.pool_capacity, "decode_calls": st.decode_calls,
