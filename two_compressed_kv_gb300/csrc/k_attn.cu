@@ -94,6 +94,12 @@ __device__ __forceinline__ uint64_t row_end(const uint2& m, int c) {
   return vend > iend ? vend : iend;
 }
 
+// Slot of channel ch in the staged q~ table.  The lanes of a token read
+// channels that lie about 8 values apart in a sorted channel list, so their
+// high bits differ; placing channel ch at slot 16 (ch mod 8) + ch / 8 puts the
+// 16-byte entries (g <= 4) of such channels in different bank groups.
+__device__ __forceinline__ int q_slot(int ch) { return ((ch & 7) << 4) | (ch >> 3); }
+
 __device__ __forceinline__ int chan_of(const uint2& x, int e) {
   return (int)(((e < 4 ? x.x : x.y) >> (8 * (e & 3))) & 0x7fu);
 }
@@ -322,7 +328,7 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_kernel(DecodeParams p) {
         const float* qt = p.qt + ((size_t)b * p.Hq + (size_t)h * g) * D;
         for (int x = tid; x < D * gp; x += AT_THREADS) {
           const int chn = x / gp, hh = x % gp;
-          qs[x] = hh < g ? qt[hh * D + chn] : 0.f;
+          qs[q_slot(chn) * gp + hh] = hh < g ? qt[hh * D + chn] : 0.f;
         }
         __syncthreads();
       }
@@ -337,14 +343,17 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_kernel(DecodeParams p) {
         const uint8_t* vs = slot + p.at_kv + p.at_ki;
         // PVB rows: lane cl owns channels [16 cl, 16 cl + 16) of the bitmask;
         // its values follow those of the group's lower lanes (prefix count,
-        // computed by every lane so that the shuffles stay uniform)
+        // taken by every lane of a warp that holds a PVB row, so that the
+        // shuffles stay warp-uniform)
         uint32_t kbits = 0u, vbits = 0u;
-        if (kb) kbits = (*reinterpret_cast<const uint32_t*>(slot + p.at_kv + 4 * (cl >> 1)) >>
-                         (16 * (cl & 1))) & 0xffffu;
-        if (vb) vbits = (*reinterpret_cast<const uint32_t*>(vs + p.at_vv + 4 * (cl >> 1)) >>
-                         (16 * (cl & 1))) & 0xffffu;
-        int kpre = __popc(kbits), vpre = __popc(vbits);
-        {
+        int kpre = 0, vpre = 0;
+        if (__any_sync(0xffffffffu, kb || vb)) {
+          if (kb) kbits = (*reinterpret_cast<const uint32_t*>(slot + p.at_kv + 4 * (cl >> 1)) >>
+                           (16 * (cl & 1))) & 0xffffu;
+          if (vb) vbits = (*reinterpret_cast<const uint32_t*>(vs + p.at_vv + 4 * (cl >> 1)) >>
+                           (16 * (cl & 1))) & 0xffffu;
+          kpre = __popc(kbits);
+          vpre = __popc(vbits);
           int ki = kpre, vi = vpre;
 #pragma unroll
           for (int off = 1; off < 8; off <<= 1) {
@@ -368,7 +377,7 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_kernel(DecodeParams p) {
               b &= b - 1u;
               const float v = __half2float(*reinterpret_cast<const __half*>(slot + 2 * i));
               ++i;
-              const float4 q4 = *reinterpret_cast<const float4*>(qs + chn * gp + h4);
+              const float4 q4 = *reinterpret_cast<const float4*>(qs + q_slot(chn) * gp + h4);
               part[0] = fmaf(q4.x, v, part[0]);
               part[1] = fmaf(q4.y, v, part[1]);
               part[2] = fmaf(q4.z, v, part[2]);
@@ -386,7 +395,7 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_kernel(DecodeParams p) {
   #pragma unroll
               for (int e = 0; e < 8; ++e) {
                 const int chn = kd ? 8 * ck + e : chan_of(kx, e);
-                const float4 q4 = *reinterpret_cast<const float4*>(qs + chn * gp + h4);
+                const float4 q4 = *reinterpret_cast<const float4*>(qs + q_slot(chn) * gp + h4);
                 part[0] = fmaf(q4.x, v[e], part[0]);
                 part[1] = fmaf(q4.y, v[e], part[1]);
                 part[2] = fmaf(q4.z, v[e], part[2]);
