@@ -58,15 +58,15 @@ __device__ __forceinline__ uint2 row_meta(const DecodeParams& p, const mkv_segme
   const int S = p.S, c = p.c;
   if (t >= p.T_packed)
     return make_uint2(tail16 + (uint32_t)(((int64_t)s * S + (t - p.T_packed)) * 16), (uint32_t)NO_IDX);
-  int64_t sg;
-  uint32_t r;
+  // t < T <= 2^31 - 1: 32-bit division
+  uint32_t sg, r;
   if (t < p.T0) {
-    sg = t / S;
-    r = (uint32_t)(t - sg * S);
+    sg = (uint32_t)t / (uint32_t)S;
+    r = (uint32_t)t - sg * (uint32_t)S;
   } else {
-    const int64_t u = t - p.T0, q = u / S;
-    sg = p.nseg0 + q;
-    r = (uint32_t)(u - q * S);
+    const uint32_t u = (uint32_t)(t - p.T0), q = u / (uint32_t)S;
+    sg = (uint32_t)p.nseg0 + q;
+    r = u - q * (uint32_t)S;
   }
   const mkv_segment_header hd = hdr[sg];
   const uint32_t c2 = 2u * (uint32_t)c;
@@ -187,6 +187,9 @@ __device__ __forceinline__ bool at_get(const AtIter& it, int kk, int n_pass, int
 __device__ __forceinline__ void at_meta_pass(const DecodeParams& p, int64_t lo, int64_t hi,
                                              uint4* meta) {
   const int n = (int)(hi - lo);
+  // stream of position lo + x: s0 + (r0 + x) / kk, with r0 + x < kk + AT_META
+  const int s0 = (int)(lo / p.kk);
+  const uint32_t r0 = (uint32_t)(lo - (int64_t)s0 * p.kk);
   for (int x0 = threadIdx.x; x0 < n; x0 += 4 * AT_THREADS) {
     int64_t t[4];
     int sidx[4];
@@ -196,9 +199,8 @@ __device__ __forceinline__ void at_meta_pass(const DecodeParams& p, int64_t lo, 
       sidx[u] = 0;
       t[u] = 0;
       if (x < n) {
-        const int64_t pos = lo + x;
-        sidx[u] = (int)(pos / p.kk);
-        t[u] = p.sel[pos];
+        sidx[u] = s0 + (int)((r0 + (uint32_t)x) / (uint32_t)p.kk);
+        t[u] = p.sel[lo + x];
       }
     }
 #pragma unroll
