@@ -359,6 +359,37 @@ def kernel_times(ctxs, step, flags: int, n: int, dev, base_flags: int = 0) -> di
             M.mkv_set_flags(m.ctx, base_flags)
 
 
+def fused_step_ms(ctxs, qs, outs, steps: int, dev, stream) -> float:
+    """Device time of one step decoded with mkv_decode_layers (all layers, up
+    to 64 per call, one launch of each decode kernel per call), timed like the
+    headline: CUDA-graph replays, 3 warm-up steps, CUDA events."""
+    from two_compressed_kv_gb300 import mkv as M
+    groups = [range(i, min(i + M.MKV_MAX_FUSED_LAYERS, len(ctxs)))
+              for i in range(0, len(ctxs), M.MKV_MAX_FUSED_LAYERS)]
+
+    def fstep():
+        for gr in groups:
+            M.mkv_decode_layers([ctxs[i].ctx for i in gr], [qs[i] for i in gr],
+                                [outs[i] for i in gr])
+
+    fstep()
+    torch.cuda.synchronize(dev)
+    graphs = capture_steps(fstep, steps + 3, dev)
+    for g in graphs[:3]:
+        g.replay()
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for g in graphs[3:]:
+        g.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    for m in ctxs:
+        if M.mkv_check_device(m.ctx) != M.MKV_OK:
+            raise RuntimeError("a device-side check fired during the fused timing")
+    return ev0.elapsed_time(ev1) / steps
+
+
 def gathered_bytes(m, M, sel: np.ndarray, w: W.Workload) -> float:
     """Bytes of the K and V rows (plus shared masks) that the selected tokens
     read, counted from the packed layout of every stream."""
@@ -465,6 +496,7 @@ def run_gpu(args, w: W.Workload, ws: int, rank: int, local: int):
         launches = sum(m.stats()["kernel_launches"] for m in ctxs) - launches0
     units_step = L * w.batch * w.ctx
     ms_step, value = _job_value(ev0.elapsed_time(ev1), args.steps, units_step, ws, dev)
+    fused_ms = fused_step_ms(ctxs, qs, outs, args.steps, dev, stream) if use_graph else None
 
     # per-kernel device time: the same steps again, with events around every
     # kernel (which launches them one after another), then around the score
@@ -536,7 +568,8 @@ def run_gpu(args, w: W.Workload, ws: int, rank: int, local: int):
         torch.cuda.empty_cache()
         comp_kernels = compress_kernel_ms(w, dev)
     if rank == 0 and not args.no_side:
-        for name, layers in ((W.MILLION_1M.name, 1), (W.MIXED_256K.name, 1)):
+        for name, layers in ((W.MILLION_1M.name, 1), (W.MIXED_256K.name, 1),
+                             (W.LAYER_32K.name, 32)):
             side[name] = side_workload(W.WORKLOADS[name], layers, max(5, args.steps), dev, stream)
             torch.cuda.empty_cache()
         # the headline shape with bitmask-indexed per-vector segments (4 layers)
@@ -580,6 +613,12 @@ def run_gpu(args, w: W.Workload, ws: int, rank: int, local: int):
                             "strategies_V": st0["strategy_count"][1]},
             "ctx_tokens_per_step": tok,
         }
+        if fused_ms:
+            line["fused_layers"] = {
+                "api": f"mkv_decode_layers (all {L} layers in one call: one launch of each "
+                       f"decode kernel per step)",
+                "ms_per_step": fused_ms, "value": ws * tok / (fused_ms / 1e3), "unit": UNIT,
+                "hbm_frac_of_measured": alg_layer * L / (fused_ms / 1e3) / 1e9 / peak}
         line["prefill"].update(prefill_roofline(w, statistics.median(comp_ms), st0, peak))
         line["prefill"]["kernel_ms_per_layer"] = comp_kernels
         if side:
@@ -680,6 +719,7 @@ def side_workload(w: W.Workload, layers: int, steps: int, dev, stream, flags: in
     for m in ctxs:
         if M.mkv_check_device(m.ctx) != M.MKV_OK:
             raise RuntimeError("a device-side check fired during the timed region")
+    fused_ms = fused_step_ms(ctxs, qs, outs, steps, dev, stream) if layers > 1 else None
     kt = kernel_times(ctxs, step, flags | M.MKV_FLAG_KERNEL_TIMING, 5, dev, flags)
     s_ms, s_n = kernel_times(ctxs, step, flags | M.MKV_FLAG_SCORE_TIMING, 5, dev, flags)["score"]
     kk = min(w.top_k, w.ctx)
@@ -704,6 +744,12 @@ def side_workload(w: W.Workload, layers: int, steps: int, dev, stream, flags: in
            "kernel_us_per_layer_standalone": {k: v[0] / max(1, v[1]) * 1e3 for k, v in kt.items()},
            "strategies_K": st0["strategy_count"][0], "strategies_V": st0["strategy_count"][1],
            "payload_bytes_K": st0["payload_bytes"][0], "payload_bytes_V": st0["payload_bytes"][1]}
+    if fused_ms:
+        res["fused_layers"] = {"api": f"mkv_decode_layers ({layers} layers in one call)",
+                               "ms_per_step": fused_ms,
+                               "value": layers * w.batch * w.ctx / (fused_ms / 1e3),
+                               "hbm_frac_of_measured":
+                                   alg * layers / (fused_ms / 1e3) / 1e9 / peak}
     if flags & M.MKV_FLAG_BITMASK_PV:
         res["config"]["strategies"] = "SM, PV, PVB (bitmask-indexed per-vector), D"
     res["prefill"].update(prefill_roofline(w, statistics.median(comp), st0, peak))

@@ -198,6 +198,28 @@ mkv_status mkv_compress(mkv_ctx* ctx, const void* k, const void* v, int64_t ctx_
 mkv_status mkv_decode(mkv_ctx* ctx, const void* q, float* out, int32_t* sel,
                       mkv_stream_t stream);
 
+/* Largest n of mkv_decode_layers. */
+#define MKV_MAX_FUSED_LAYERS 64
+
+/* mkv_decode of n ctxs (e.g. the attention layers of a model, or the layers
+ * of several requests of one shape) with one launch of each decode kernel
+ * over all of them, so that the GPU stays full between layers (an interface
+ * addition with no counterpart in the paper).  The result for ctx i is
+ * exactly (bit for bit) that of mkv_decode(ctxs[i], q[i], out[i], sel[i]).
+ *   ctxs: host array of n distinct ctxs, all created with the same batch,
+ *         heads, segment, c, top_k and device, and in the same state (same
+ *         context length, the same number of appended tokens).
+ *   q, out: host arrays of n device pointers, laid out as in mkv_decode.
+ *   sel: NULL, or a host array of n device pointers (each may be NULL).
+ *   1 <= n <= MKV_MAX_FUSED_LAYERS.
+ * Asynchronous on `stream`; no host synchronisation, no allocation.  The
+ * per-kernel timing flags do not apply (nothing is timed).
+ * MKV_ERR_INVALID_ARG for NULL arrays or pointers, n out of range, a ctx
+ * repeated, or ctxs whose shape or state differ (nothing is launched then);
+ * MKV_ERR_STATE if a ctx has no compressed cache. */
+mkv_status mkv_decode_layers(mkv_ctx* const* ctxs, int n, const void* const* q,
+                             float* const* out, int32_t* const* sel, mkv_stream_t stream);
+
 /* Replaces the ctx's MKV_FLAG_* bits (e.g. to time the kernels of a few
  * decode steps).  Host only; applies to later calls.  MKV_ERR_INVALID_ARG for
  * unknown bits. */

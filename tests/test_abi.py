@@ -145,3 +145,16 @@ def test_debug_hooks_reject_bad_arguments_without_gpu(M):
     assert M.lib.mkv_debug_wait_test(fake, 10, None) == M.MKV_ERR_INVALID_ARG
     assert M.lib.mkv_debug_wait_test(fake, 3_000_000_000, None) == M.MKV_ERR_INVALID_ARG
     assert M.lib.mkv_debug_set_check_extent(None, 0) == M.MKV_ERR_INVALID_ARG
+
+
+def test_decode_layers_rejects_bad_arguments_without_gpu(M):
+    """Argument checks of mkv_decode_layers run before any CUDA call."""
+    ok = M.MKV_ERR_INVALID_ARG
+    assert M.mkv_decode_layers_raw(None, 1, [1], [1]) == ok
+    assert M.mkv_decode_layers_raw([None], 1, [1], [1]) == ok
+    assert M.mkv_decode_layers_raw([1], 1, None, [1]) == ok
+    assert M.mkv_decode_layers_raw([1], 1, [1], None) == ok
+    assert M.mkv_decode_layers_raw([1], 0, [1], [1]) == ok
+    assert M.mkv_decode_layers_raw([1] * 65, 65, [1] * 65, [1] * 65) == ok
+    assert M.MKV_MAX_FUSED_LAYERS == 64
+

@@ -256,7 +256,7 @@ __device__ __forceinline__ void at_issue(const DecodeParams& p, int rel_s, const
 }
 
 template <int NST>
-__global__ void __launch_bounds__(AT_THREADS, 2) attn_kernel(DecodeParams p) {
+__device__ __forceinline__ void attn_kernel_body(const DecodeParams& p) {
   extern __shared__ __align__(128) uint8_t at_smem[];
   __shared__ float s_m[MAX_G], s_l[MAX_G], s_alpha[MAX_G];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -526,6 +526,14 @@ __global__ void __launch_bounds__(AT_THREADS, 2) attn_kernel(DecodeParams p) {
   cpa_wait<0>();
 }
 
+// one layer (parameters by value), and several layers in one launch (layer = blockIdx.z)
+template <int NST>
+__global__ void __launch_bounds__(AT_THREADS, 2) attn_kernel(DecodeParams p) { attn_kernel_body<NST>(p); }
+template <int NST>
+__global__ void __launch_bounds__(AT_THREADS, 2) attn_kernel_layers(const __grid_constant__ LayerParams lp) {
+  attn_kernel_body<NST>(lp.p[blockIdx.z]);
+}
+
 // Slices that cover stream s's selection: the first one and how many.
 __device__ __forceinline__ int at_first_part(const DecodeParams& p, int s) {
   return (int)(((int64_t)s * p.kk) / p.attn_per);
@@ -545,7 +553,7 @@ constexpr int MG_THREADS = 128;
 constexpr int MG_ROWS = 32;
 constexpr int MG_LD = MG_ROWS + 1;
 
-__global__ void __launch_bounds__(MG_THREADS) merge_kernel(DecodeParams p) {
+__device__ __forceinline__ void merge_kernel_body(const DecodeParams& p) {
   extern __shared__ __align__(16) float wsm[];     // [parts][g] weights
   __shared__ float Rt[D * MG_LD];                  // Rt[j][rr] = R_V[32q + rr][j]
   __shared__ __align__(16) float ot[MAX_G][D];
@@ -612,6 +620,12 @@ __global__ void __launch_bounds__(MG_THREADS) merge_kernel(DecodeParams p) {
   }
 }
 
+// one layer (parameters by value), and several layers in one launch (layer = blockIdx.z)
+__global__ void __launch_bounds__(MG_THREADS) merge_kernel(DecodeParams p) { merge_kernel_body(p); }
+__global__ void __launch_bounds__(MG_THREADS) merge_kernel_layers(const __grid_constant__ LayerParams lp) {
+  merge_kernel_body(lp.p[blockIdx.z]);
+}
+
 cudaError_t attn_shape(int g, int slot, int* stages, int* ctas_per_sm) {
   // four stages when two CTAs still fit an SM, else fewer
   int nst = 2;
@@ -637,29 +651,38 @@ cudaError_t prepare_attn_kernels() {
   // the largest carve-up attn_shape can choose: two stages of dense rows
   // (256 + 128 bytes of K and of V per token) and 16 heads
   const int mx = (int)at_smem_bytes(MAX_G, 768, 2);
-  cudaError_t e = cudaFuncSetAttribute(attn_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(attn_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(attn_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+  const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  cudaError_t e = cudaFuncSetAttribute(attn_kernel<2>, a, mx);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_kernel<3>, a, mx);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_kernel<4>, a, mx);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_kernel_layers<2>, a, mx);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_kernel_layers<3>, a, mx);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_kernel_layers<4>, a, mx);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(merge_kernel_layers, a, 48 * 1024 + 4 * 1024);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              48 * 1024 + 4 * 1024);
+  return cudaFuncSetAttribute(merge_kernel, a, 48 * 1024 + 4 * 1024);
 }
 
-cudaError_t launch_attn(const DecodeParams& p, cudaStream_t st) {
+cudaError_t launch_attn(const DecodeParams& p, cudaStream_t st, const LayerParams* lp, int n) {
   const size_t smem = at_smem_bytes(p.g, p.at_slot, p.at_stages);
-  const dim3 grid(p.attn_ctas), block(AT_THREADS);
+  const dim3 grid(p.attn_ctas, 1, n), block(AT_THREADS);
   const bool pdl = ((p.pdl >> MKV_KERNEL_ATTN) & 1) != 0;
+  if (lp) {
+    if (p.at_stages >= 4) return launch_kernel(attn_kernel_layers<4>, grid, block, smem, st, pdl, 0, *lp);
+    if (p.at_stages == 3) return launch_kernel(attn_kernel_layers<3>, grid, block, smem, st, pdl, 0, *lp);
+    return launch_kernel(attn_kernel_layers<2>, grid, block, smem, st, pdl, 0, *lp);
+  }
   if (p.at_stages >= 4) return launch_kernel(attn_kernel<4>, grid, block, smem, st, pdl, 0, p);
   if (p.at_stages == 3) return launch_kernel(attn_kernel<3>, grid, block, smem, st, pdl, 0, p);
   return launch_kernel(attn_kernel<2>, grid, block, smem, st, pdl, 0, p);
 }
 
-cudaError_t launch_merge(const DecodeParams& p, cudaStream_t st) {
-  return launch_kernel(merge_kernel, dim3(p.B * p.H, D / MG_ROWS), dim3(MG_THREADS),
-                       sizeof(float) * (size_t)p.attn_mp * p.g, st,
-                       ((p.pdl >> MKV_KERNEL_MERGE) & 1) != 0, 0, p);
+cudaError_t launch_merge(const DecodeParams& p, cudaStream_t st, const LayerParams* lp, int n) {
+  const dim3 grid(p.B * p.H, D / MG_ROWS, n);
+  const size_t smem = sizeof(float) * (size_t)p.attn_mp * p.g;
+  const bool pdl = ((p.pdl >> MKV_KERNEL_MERGE) & 1) != 0;
+  if (lp) return launch_kernel(merge_kernel_layers, grid, dim3(MG_THREADS), smem, st, pdl, 0, *lp);
+  return launch_kernel(merge_kernel, grid, dim3(MG_THREADS), smem, st, pdl, 0, p);
 }
 
 }  // namespace mkv

@@ -23,7 +23,7 @@ namespace mkv {
 // ---------------------------------------------------------------------------
 constexpr int QR_THREADS = 512;
 
-__global__ void __launch_bounds__(QR_THREADS) qrot_kernel(DecodeParams p) {
+__device__ __forceinline__ void qrot_kernel_body(const DecodeParams& p) {
   extern __shared__ __align__(16) float Rs[];   // [128][128]
   __shared__ float qs[MAX_G][D];
   __shared__ float psum[4][D];
@@ -79,6 +79,12 @@ __global__ void __launch_bounds__(QR_THREADS) qrot_kernel(DecodeParams p) {
       atomicAdd(&p.hist[(size_t)s * HIST1 + (f2key(acc) >> 20)], 1u);
     }
   }
+}
+
+// one layer (parameters by value), and several layers in one launch (layer = blockIdx.z)
+__global__ void __launch_bounds__(QR_THREADS) qrot_kernel(DecodeParams p) { qrot_kernel_body(p); }
+__global__ void __launch_bounds__(QR_THREADS) qrot_kernel_layers(const __grid_constant__ LayerParams lp) {
+  qrot_kernel_body(lp.p[blockIdx.z]);
 }
 
 // ---------------------------------------------------------------------------
@@ -237,7 +243,7 @@ __device__ __forceinline__ void score_block(const uint8_t* base, int rows, int r
 // CPR = c / 8 is a template parameter of the whole kernel (one instantiation
 // per c), so the per-item dispatch is only on the segment's strategy.
 template <int CPR>
-__global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
+__device__ __forceinline__ void score_kernel_body(const DecodeParams& p) {
   extern __shared__ __align__(128) uint8_t stage_mem[];
   __shared__ uint64_t full_bar[SC_MAX_STAGES], empty_bar[SC_MAX_STAGES];
   __shared__ StageMeta meta[SC_MAX_STAGES];
@@ -459,6 +465,14 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) {
   }
 }
 
+// one layer (parameters by value), and several layers in one launch (layer = blockIdx.z)
+template <int CPR>
+__global__ void __launch_bounds__(SC_THREADS, 1) score_kernel(DecodeParams p) { score_kernel_body<CPR>(p); }
+template <int CPR>
+__global__ void __launch_bounds__(SC_THREADS, 1) score_kernel_layers(const __grid_constant__ LayerParams lp) {
+  score_kernel_body<CPR>(lp.p[blockIdx.z]);
+}
+
 // ---------------------------------------------------------------------------
 // partition of the K segments over the score kernel's CTAs (compression time
 // and after each commit): CTA i starts at the first segment (in stream,
@@ -588,9 +602,14 @@ void score_stage_plan(int S, int c, int* stage_bytes, int* n_stages) {
 cudaError_t prepare_score_kernels() {
   cudaError_t e = cudaFuncSetAttribute(qrot_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, D * D * 4);
   if (e != cudaSuccess) return e;
-#define MKV_SCORE_ATTR(N)                                                                   \
-  e = cudaFuncSetAttribute(score_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
-                           227 * 1024 - SC_STATIC_SMEM);                                  \
+  e = cudaFuncSetAttribute(qrot_kernel_layers, cudaFuncAttributeMaxDynamicSharedMemorySize, D * D * 4);
+  if (e != cudaSuccess) return e;
+#define MKV_SCORE_ATTR(N)                                                                        \
+  e = cudaFuncSetAttribute(score_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,        \
+                           227 * 1024 - SC_STATIC_SMEM);                                       \
+  if (e != cudaSuccess) return e;                                                               \
+  e = cudaFuncSetAttribute(score_kernel_layers<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                           227 * 1024 - SC_STATIC_SMEM);                                       \
   if (e != cudaSuccess) return e;
   MKV_SCORE_ATTR(1) MKV_SCORE_ATTR(2) MKV_SCORE_ATTR(3) MKV_SCORE_ATTR(4) MKV_SCORE_ATTR(5)
   MKV_SCORE_ATTR(6) MKV_SCORE_ATTR(7) MKV_SCORE_ATTR(8) MKV_SCORE_ATTR(9) MKV_SCORE_ATTR(10)
@@ -615,17 +634,25 @@ cudaError_t launch_partition(const mkv_segment_header* hdrK, int n_streams, int 
   return cudaGetLastError();
 }
 
-cudaError_t launch_qrot(const DecodeParams& p, cudaStream_t st) {
-  return launch_kernel(qrot_kernel, dim3(p.B * p.H), dim3(QR_THREADS), (size_t)D * D * 4, st,
-                       ((p.pdl >> MKV_KERNEL_QROT) & 1) != 0, 0, p);
+cudaError_t launch_qrot(const DecodeParams& p, cudaStream_t st, const LayerParams* lp, int n) {
+  const bool pdl = ((p.pdl >> MKV_KERNEL_QROT) & 1) != 0;
+  if (lp)
+    return launch_kernel(qrot_kernel_layers, dim3(p.B * p.H, 1, n), dim3(QR_THREADS),
+                         (size_t)D * D * 4, st, pdl, 0, *lp);
+  return launch_kernel(qrot_kernel, dim3(p.B * p.H), dim3(QR_THREADS), (size_t)D * D * 4, st, pdl,
+                       0, p);
 }
 
-cudaError_t launch_score(const DecodeParams& p, cudaStream_t st) {
+cudaError_t launch_score(const DecodeParams& p, cudaStream_t st, const LayerParams* lp, int n) {
   const size_t smem = sc_slot(p.stage_bytes) * p.n_stages;
   const bool pdl = ((p.pdl >> MKV_KERNEL_SCORE) & 1) != 0;
   switch (p.c >> 3) {
-#define MKV_SCORE_CASE(N) \
-  case N: return launch_kernel(score_kernel<N>, dim3(p.G), dim3(SC_THREADS), smem, st, pdl, 0, p);
+#define MKV_SCORE_CASE(N)                                                                       \
+  case N:                                                                                       \
+    if (lp)                                                                                     \
+      return launch_kernel(score_kernel_layers<N>, dim3(p.G, 1, n), dim3(SC_THREADS), smem, st, \
+                           pdl, 0, *lp);                                                        \
+    return launch_kernel(score_kernel<N>, dim3(p.G), dim3(SC_THREADS), smem, st, pdl, 0, p);
     MKV_SCORE_CASE(1) MKV_SCORE_CASE(2) MKV_SCORE_CASE(3) MKV_SCORE_CASE(4) MKV_SCORE_CASE(5)
     MKV_SCORE_CASE(6) MKV_SCORE_CASE(7) MKV_SCORE_CASE(8) MKV_SCORE_CASE(9) MKV_SCORE_CASE(10)
     MKV_SCORE_CASE(11) MKV_SCORE_CASE(12) MKV_SCORE_CASE(13) MKV_SCORE_CASE(14)

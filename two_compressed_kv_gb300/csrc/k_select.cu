@@ -105,7 +105,7 @@ struct SelGeom {
   }
 };
 
-__global__ void __launch_bounds__(SEL_THREADS, 1) select_kernel(DecodeParams p) {
+__device__ __forceinline__ void select_kernel_body(const DecodeParams& p) {
   namespace cg = cooperative_groups;
   cg::cluster_group cl = cg::this_cluster();
   extern __shared__ __align__(16) uint8_t sel_dyn[];
@@ -391,6 +391,12 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) select_kernel(DecodeParams p) 
   }
 }
 
+// one layer (parameters by value), and several layers in one launch (layer = blockIdx.z)
+__global__ void __launch_bounds__(SEL_THREADS, 1) select_kernel(DecodeParams p) { select_kernel_body(p); }
+__global__ void __launch_bounds__(SEL_THREADS, 1) select_kernel_layers(const __grid_constant__ LayerParams lp) {
+  select_kernel_body(lp.p[blockIdx.z]);
+}
+
 int select_cluster_size(int n_streams, int64_t T, int G) {
   int R = 1;
   while (R < 8 && (int64_t)n_streams * R * 2 <= G && T / (2 * R) >= 4096) R *= 2;
@@ -398,13 +404,20 @@ int select_cluster_size(int n_streams, int64_t T, int G) {
 }
 
 cudaError_t prepare_select_kernels() {
+  const cudaError_t e = cudaFuncSetAttribute(select_kernel_layers,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SEL_SMEM);
+  if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)SEL_SMEM);
 }
 
-cudaError_t launch_topk(const DecodeParams& p, cudaStream_t st) {
+cudaError_t launch_topk(const DecodeParams& p, cudaStream_t st, const LayerParams* lp, int n) {
+  const bool pdl = ((p.pdl >> MKV_KERNEL_TOPK) & 1) != 0;
+  if (lp)
+    return launch_kernel(select_kernel_layers, dim3(p.sel_R, p.B * p.H, n), dim3(SEL_THREADS),
+                         SEL_SMEM, st, pdl, p.sel_R, *lp);
   return launch_kernel(select_kernel, dim3(p.sel_R, p.B * p.H, 1), dim3(SEL_THREADS), SEL_SMEM,
-                       st, ((p.pdl >> MKV_KERNEL_TOPK) & 1) != 0, p.sel_R, p);
+                       st, pdl, p.sel_R, p);
 }
 
 }  // namespace mkv

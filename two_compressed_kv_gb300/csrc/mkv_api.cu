@@ -547,12 +547,31 @@ mkv_status mkv_compress(mkv_ctx* c, const void* k, const void* v, int64_t ctx_le
   return MKV_OK;
 }
 
-mkv_status mkv_decode(mkv_ctx* c, const void* q, float* out, int32_t* sel, mkv_stream_t stream) {
-  if (!c || !q || !out) return MKV_ERR_INVALID_ARG;
-  if (!c->ready) return MKV_ERR_STATE;
-  CK(cudaSetDevice(c->cfg.device));
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  DecodeParams p;
+}  // extern "C"
+
+namespace {
+
+// Attention launch shape: per-token slots holding value rows of at_kv (K)
+// and at_vv (V) bytes, `stages` ring stages, `ctas_per_sm` resident CTAs.
+void set_attn_shape(const mkv_ctx* c, DecodeParams& p, int at_kv, int at_vv, int stages,
+                    int ctas_per_sm) {
+  const int64_t N = (int64_t)c->BH * p.kk;
+  const int64_t P = (int64_t)c->G * ctas_per_sm;
+  p.attn_per = c->attn_per_fixed
+                   ? c->attn_per_fixed
+                   : std::max({ceil_div(N, P), kMinSlice, ceil_div(p.kk, c->attn_mp - 1)});
+  p.attn_ctas = (int)ceil_div(N, p.attn_per);
+  p.attn_mp = c->attn_mp;
+  p.at_kv = at_kv;
+  p.at_ki = c->at_ki;
+  p.at_vv = at_vv;
+  p.at_vi = c->at_vi;
+  p.at_slot = p.at_kv + p.at_ki + p.at_vv + p.at_vi;
+  p.at_stages = stages;
+}
+
+// Decode parameters of one ctx (compressed) for q, out and sel.
+void fill_decode(mkv_ctx* c, const void* q, float* out, int32_t* sel, DecodeParams& p) {
   memset(&p, 0, sizeof(p));
   p.B = c->B;
   p.H = c->H;
@@ -595,21 +614,11 @@ mkv_status mkv_decode(mkv_ctx* c, const void* q, float* out, int32_t* sel, mkv_s
   p.sel_user = sel;
   p.err = c->err;
   {
-    const int64_t N = (int64_t)c->BH * p.kk;
     // appended tokens are dense rows (the tail) or may sit in dense segments
     const bool appended = c->T > c->T0;
-    const int64_t P = (int64_t)c->G * (appended ? c->at_ctas_dense : c->at_ctas_per_sm);
-    p.attn_per = c->attn_per_fixed
-                     ? c->attn_per_fixed
-                     : std::max({ceil_div(N, P), kMinSlice, ceil_div(p.kk, c->attn_mp - 1)});
-    p.attn_ctas = (int)ceil_div(N, p.attn_per);
-    p.attn_mp = c->attn_mp;
-    p.at_kv = appended ? 256 : c->at_kv;
-    p.at_ki = c->at_ki;
-    p.at_vv = appended ? 256 : c->at_vv;
-    p.at_vi = c->at_vi;
-    p.at_slot = p.at_kv + p.at_ki + p.at_vv + p.at_vi;
-    p.at_stages = appended ? c->at_stages_dense : c->at_stages;
+    set_attn_shape(c, p, appended ? 256 : c->at_kv, appended ? 256 : c->at_vv,
+                   appended ? c->at_stages_dense : c->at_stages,
+                   appended ? c->at_ctas_dense : c->at_ctas_per_sm);
   }
   p.part_o = c->part_o;
   p.part_ml = c->part_ml;
@@ -619,6 +628,19 @@ mkv_status mkv_decode(mkv_ctx* c, const void* q, float* out, int32_t* sel, mkv_s
       (c->cfg.flags & (MKV_FLAG_KERNEL_TIMING | MKV_FLAG_SCORE_TIMING | MKV_FLAG_NO_PDL)) == 0u;
   p.pdl = pdl_on ? (c->pdl_mask & 0x1f) : 0;
   p.pdl_trigger = (c->pdl_mask & 0x100) ? 0 : 1;
+}
+
+}  // namespace
+
+extern "C" {
+
+mkv_status mkv_decode(mkv_ctx* c, const void* q, float* out, int32_t* sel, mkv_stream_t stream) {
+  if (!c || !q || !out) return MKV_ERR_INVALID_ARG;
+  if (!c->ready) return MKV_ERR_STATE;
+  CK(cudaSetDevice(c->cfg.device));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  DecodeParams p;
+  fill_decode(c, q, out, sel, p);
   mkv_status s;
   if ((s = timed(c, MKV_KERNEL_QROT, st, 1, [&] { return launch_qrot(p, st); })) != MKV_OK) return s;
   if ((s = timed(c, MKV_KERNEL_SCORE, st, 1, [&] { return launch_score(p, st); })) != MKV_OK) return s;
@@ -626,6 +648,70 @@ mkv_status mkv_decode(mkv_ctx* c, const void* q, float* out, int32_t* sel, mkv_s
   if ((s = timed(c, MKV_KERNEL_ATTN, st, 1, [&] { return launch_attn(p, st); })) != MKV_OK) return s;
   if ((s = timed(c, MKV_KERNEL_MERGE, st, 1, [&] { return launch_merge(p, st); })) != MKV_OK) return s;
   c->decode_calls += 1;
+  return MKV_OK;
+}
+
+mkv_status mkv_decode_layers(mkv_ctx* const* ctxs, int n, const void* const* q, float* const* out,
+                             int32_t* const* sel, mkv_stream_t stream) {
+  if (!ctxs || !q || !out || n < 1 || n > MKV_MAX_FUSED_LAYERS) return MKV_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i) {
+    if (!ctxs[i] || !q[i] || !out[i]) return MKV_ERR_INVALID_ARG;
+    for (int j = 0; j < i; ++j)
+      if (ctxs[j] == ctxs[i]) {
+        g_last_error = "mkv_decode_layers: a ctx appears twice";
+        return MKV_ERR_INVALID_ARG;
+      }
+  }
+  for (int i = 0; i < n; ++i)
+    if (!ctxs[i]->ready) return MKV_ERR_STATE;
+  mkv_ctx* c0 = ctxs[0];
+  for (int i = 1; i < n; ++i) {
+    const mkv_ctx* c = ctxs[i];
+    if (c->cfg.device != c0->cfg.device || c->T != c0->T || c->T0 != c0->T0 ||
+        c->n_commit != c0->n_commit || c->n_seg != c0->n_seg || c->cfg.c != c0->cfg.c ||
+        c->cfg.segment != c0->cfg.segment || c->attn_per_fixed != c0->attn_per_fixed) {
+      g_last_error = "mkv_decode_layers: the ctxs differ in device, shape or state";
+      return MKV_ERR_INVALID_ARG;
+    }
+  }
+  CK(cudaSetDevice(c0->cfg.device));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  LayerParams lp;
+  for (int i = 0; i < n; ++i) fill_decode(ctxs[i], q[i], out[i], sel ? sel[i] : nullptr, lp.p[i]);
+  // every launch-shape field must agree with layer 0 (the launch uses p[0])
+  const DecodeParams& a = lp.p[0];
+  for (int i = 1; i < n; ++i) {
+    const DecodeParams& b = lp.p[i];
+    if (b.B != a.B || b.H != a.H || b.Hq != a.Hq || b.g != a.g || b.T != a.T || b.Tp != a.Tp ||
+        b.S != a.S || b.c != a.c || b.n_seg != a.n_seg || b.kk != a.kk || b.T0 != a.T0 ||
+        b.T_packed != a.T_packed || b.nseg0 != a.nseg0 || b.G != a.G ||
+        b.stage_bytes != a.stage_bytes || b.n_stages != a.n_stages || b.sel_R != a.sel_R ||
+        b.attn_mp != a.attn_mp || b.at_ki != a.at_ki || b.at_vi != a.at_vi) {
+      g_last_error = "mkv_decode_layers: the ctxs differ in shape";
+      return MKV_ERR_INVALID_ARG;
+    }
+  }
+  // one attention shape for all layers: the widest per-token slot of any
+  int kv = 0, vv = 0;
+  for (int i = 0; i < n; ++i) {
+    kv = std::max(kv, lp.p[i].at_kv);
+    vv = std::max(vv, lp.p[i].at_vv);
+  }
+  int stages = a.at_stages, ctas = 1;
+  CK(attn_shape(a.g, kv + a.at_ki + vv + a.at_vi, &stages, &ctas));
+  for (int i = 0; i < n; ++i) {
+    set_attn_shape(ctxs[i], lp.p[i], kv, vv, stages, ctas);
+    lp.p[i].pdl = lp.p[0].pdl;
+    lp.p[i].pdl_trigger = lp.p[0].pdl_trigger;
+  }
+  const DecodeParams& p = lp.p[0];
+  CK(launch_qrot(p, st, &lp, n));
+  CK(launch_score(p, st, &lp, n));
+  CK(launch_topk(p, st, &lp, n));
+  CK(launch_attn(p, st, &lp, n));
+  CK(launch_merge(p, st, &lp, n));
+  c0->launches += 5;
+  for (int i = 0; i < n; ++i) ctxs[i]->decode_calls += 1;
   return MKV_OK;
 }
 

@@ -214,15 +214,31 @@ void score_stage_plan(int S, int c, int* stage_bytes, int* n_stages);
 cudaError_t launch_partition(const mkv_segment_header* hdrK, int n_streams, int n_seg, int c,
                              int G, int stage_bytes, int32_t* part, int32_t* cta_cnt,
                              StagePlan* plan, int32_t* plan_n, int64_t* prefix, cudaStream_t st);
-cudaError_t launch_qrot(const DecodeParams& p, cudaStream_t st);
-cudaError_t launch_score(const DecodeParams& p, cudaStream_t st);
+// Decode parameters of several layers decoded by one launch of each decode
+// kernel (layer l = blockIdx.z), passed by value as a __grid_constant__
+// kernel parameter.  All layers share every launch-shape field of p[0].
+constexpr int MAX_FUSED_LAYERS = MKV_MAX_FUSED_LAYERS;
+struct LayerParams {
+  DecodeParams p[MAX_FUSED_LAYERS];
+};
+static_assert(sizeof(LayerParams) <= 32000, "layer parameters must fit the kernel parameter space");
+
+// Decode launches: one layer with p, or layers lp->p[0 .. n) (p == lp->p[0])
+// in one launch when lp is given.
+cudaError_t launch_qrot(const DecodeParams& p, cudaStream_t st, const LayerParams* lp = nullptr,
+                        int n = 1);
+cudaError_t launch_score(const DecodeParams& p, cudaStream_t st, const LayerParams* lp = nullptr,
+                         int n = 1);
 // the selection launch (one cluster of sel_R CTAs per stream)
-cudaError_t launch_topk(const DecodeParams& p, cudaStream_t st);
+cudaError_t launch_topk(const DecodeParams& p, cudaStream_t st, const LayerParams* lp = nullptr,
+                        int n = 1);
 // CTAs per stream for the selection: up to 8 while the grid fits G SMs twice
 int select_cluster_size(int n_streams, int64_t T, int G);
-cudaError_t launch_attn(const DecodeParams& p, cudaStream_t st);
+cudaError_t launch_attn(const DecodeParams& p, cudaStream_t st, const LayerParams* lp = nullptr,
+                        int n = 1);
 // attention kernel shape for a slot size: stages and resident CTAs per SM
 cudaError_t attn_shape(int g, int slot, int* stages, int* ctas_per_sm);
-cudaError_t launch_merge(const DecodeParams& p, cudaStream_t st);
+cudaError_t launch_merge(const DecodeParams& p, cudaStream_t st, const LayerParams* lp = nullptr,
+                         int n = 1);
 
 }  // namespace mkv

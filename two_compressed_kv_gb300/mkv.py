@@ -80,6 +80,7 @@ def _load():
         "mkv_create": (c_int, [POINTER(mkv_config), POINTER(P)]),
         "mkv_compress": (c_int, [P, P, P, c_int64, P]),
         "mkv_decode": (c_int, [P, P, P, P, P]),
+        "mkv_decode_layers": (c_int, [P, c_int, P, P, P, P]),
         "mkv_free": (None, [P]),
         "mkv_status_string": (c_char_p, [c_int]),
         "mkv_last_error_string": (c_char_p, []),
@@ -182,6 +183,40 @@ def mkv_decode(ctx, q, out, sel=None, stream=None) -> None:
     po = _dptr(out, torch.float32, "out", q.shape)
     ps = None if sel is None else _dptr(sel, torch.int32, "sel")
     _check(_lib.mkv_decode(ctx, pq, po, ps, _stream_ptr(stream, q.device)), "mkv_decode")
+
+
+MKV_MAX_FUSED_LAYERS = 64
+
+
+def mkv_decode_layers(ctxs, qs, outs, sels=None, stream=None) -> None:
+    """mkv_decode of several ctxs (same shape and state) in one launch per
+    decode kernel.  ctxs: ctx handles; qs, outs (and sels, or None): one
+    tensor per ctx, as for mkv_decode."""
+    import torch
+    n = len(ctxs)
+    if len(qs) != n or len(outs) != n or (sels is not None and len(sels) != n):
+        raise ValueError("ctxs, qs, outs and sels must have the same length")
+    devs = {t.device for t in list(qs) + list(outs) + list(sels or []) if t is not None}
+    if len(devs) > 1:
+        raise ValueError("all tensors of one call must be on one device")
+    arr = lambda vals: (c_void_p * max(1, n))(*vals)
+    pc = arr([c if isinstance(c, int) else getattr(c, "value", c) for c in ctxs])
+    pq = arr([_dptr(q, torch.float16, "q") for q in qs])
+    po = arr([_dptr(o, torch.float32, "out", q.shape) for o, q in zip(outs, qs)])
+    ps = None if sels is None else arr([None if t is None else _dptr(t, torch.int32, "sel")
+                                        for t in sels])
+    dev = qs[0].device if n else None
+    with torch.cuda.device(dev):
+        _check(_lib.mkv_decode_layers(pc, n, pq, po, ps, _stream_ptr(stream, dev)),
+               "mkv_decode_layers")
+
+
+def mkv_decode_layers_raw(ctxs, n: int, q_ptrs, out_ptrs, sel_ptrs=None, stream_ptr: int = 0) -> int:
+    """Pointer-level call (no checks beyond the library's own); returns the status.
+    Any of the arrays may be None (a NULL array)."""
+    arr = lambda vals: None if vals is None else (c_void_p * max(1, len(vals)))(*vals)
+    return _lib.mkv_decode_layers(arr(ctxs), n, arr(q_ptrs), arr(out_ptrs), arr(sel_ptrs),
+                                  stream_ptr or None)
 
 
 def mkv_append(ctx, k, v, stream=None) -> None:
