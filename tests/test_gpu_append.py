@@ -45,8 +45,9 @@ def _library_hat(m, b, h, x, T0, S, c, n_commit):
                                        (100, [64, 200, 130, 50])],
                          ids=["ragged-prefill", "aligned-prefill", "pool-growth"])
 def test_appends_across_segment_boundaries(M, T0, pieces):
-    """pool-growth: 7 commits, more than the room mkv_compress reserves (2),
-    so the pool is moved to a larger allocation during the appends."""
+    """pool-growth: 6 commits (444 appended tokens, S = 64), more than the room
+    mkv_compress reserves (2), so the pool is moved to a larger allocation
+    during the appends."""
     S, c, tau, k = 64, 40, 0.85, 96
     w = W.small_workload(f"append-{T0}", n_kv_heads=2, n_q_heads=8, ctx=T0 + sum(pieces),
                          segment=S, c=c, tau=tau, top_k=k, seed=41)
