@@ -274,6 +274,29 @@ def test_energy_identity():
         assert math.isclose(s.e_tot, float((X[a:b].astype(np.float64) ** 2).sum()), rel_tol=1e-12)
 
 
+def check_gqa_closed_form():
+    """Query head i attends with KV head i // g, pinned without restating the
+    rule: when every V row of KV head h equals one vector a_h, each query
+    head's output is a_(i // g) whatever its weights (they sum to one), and
+    another mapping (i mod H) would return the other vector for head 1."""
+    T, H, g = 64, 2, 3
+    rng = np.random.default_rng(5)
+    K = rng.standard_normal((1, H, T, 128)).astype(np.float16)
+    a = np.stack([rng.standard_normal(128), 3.0 + rng.standard_normal(128)])
+    V = np.broadcast_to(a[None, :, None, :], (1, H, T, 128)).astype(np.float16)
+    q = rng.standard_normal((1, H * g, 128)).astype(np.float16)
+    layer = O.compress_layer(K, np.ascontiguousarray(V), 32, 40, 0.85)
+    out, _, _ = O.decode_layer(layer, q, 16)
+    a16 = a.astype(np.float16).astype(np.float64)
+    for i in range(H * g):
+        assert np.abs(out[0, i] - a16[i // g]).max() <= 2e-2, i
+    assert np.abs(out[0, 1] - a16[1 % H]).max() > 1.0
+
+
+def test_gqa_mapping_closed_form():
+    check_gqa_closed_form()
+
+
 def test_gqa_head_mapping():
     """Query head i attends with KV head i // g (g = Hq / H)."""
     w = W.small_workload("gqa", ctx=96, n_kv_heads=2, n_q_heads=6)
@@ -413,9 +436,29 @@ def _mut_empty_segment_unkept(mp):
     mp.setattr(O, "segment_stats", f)
 
 
+def _mut_gqa_interleaved(mp):
+    """query head i attends with KV head i mod H instead of i // g"""
+    def wrong(layer, q, k):
+        B, Hq, d = q.shape
+        kk = min(k, layer.T)
+        out = np.zeros((B, Hq, d))
+        sel = np.zeros((B, layer.H, kk), dtype=np.int64)
+        scores = np.zeros((B, layer.H, layer.T))
+        for b in range(B):
+            for h in range(layer.H):
+                heads = np.arange(h, Hq, layer.H)
+                ck, cv = layer.K[b][h], layer.V[b][h]
+                r = O.decode_stream(q[b, heads], ck.R, cv.R, ck.dense_hat(), cv.dense_hat(), k)
+                out[b, heads] = r.out
+                sel[b, h] = r.sel
+                scores[b, h] = r.scores
+        return out, sel, scores
+    mp.setattr(O, "decode_layer", wrong)
+
+
 MUTATIONS = [_mut_rotate_transposed, _mut_ties_high, _mut_most_retained, _mut_topk_ties_high,
              _mut_no_scale, _mut_sign_flipped, _mut_ascending, _mut_stats_drop_pad,
-             _mut_empty_segment_unkept]
+             _mut_empty_segment_unkept, _mut_gqa_interleaved]
 
 
 @pytest.mark.parametrize("mutation", MUTATIONS, ids=[m.__name__ for m in MUTATIONS])
@@ -424,7 +467,7 @@ def test_pins_catch_planted_mistake(mutation, monkeypatch):
     rng = np.random.default_rng(5)
     Xr = (rng.standard_normal((300, 16)) * np.exp(-np.arange(16) / 4)).astype(np.float16)
     checks = [check_hand_case, check_basis_closed_forms, check_costs_and_choice,
-              lambda: check_basis_invariants(Xr), check_zero_energy]
+              lambda: check_basis_invariants(Xr), check_zero_energy, check_gqa_closed_form]
     caught = 0
     for chk in checks:
         try:
