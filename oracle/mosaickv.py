@@ -481,8 +481,10 @@ class GrownStream:
         return 0 if self.tail is None else self.tail.shape[0]
 
 
-def append_stream(gs: GrownStream, X_new: np.ndarray, tau: float) -> GrownStream:
-    """Adds tokens [n, d] (fp16) to the buffer, committing every full S."""
+def append_stream(gs: GrownStream, X_new: np.ndarray, tau: float,
+                  bitmask_pv: bool = False) -> GrownStream:
+    """Adds tokens [n, d] (fp16) to the buffer, committing every full S.
+    A commit uses the strategy set of the prefill (bitmask_pv as there)."""
     X_new = np.asarray(X_new)
     d = gs.base.d
     tail = np.zeros((0, d), dtype=X_new.dtype) if gs.tail is None else gs.tail
@@ -490,7 +492,8 @@ def append_stream(gs: GrownStream, X_new: np.ndarray, tau: float) -> GrownStream
     committed = list(gs.committed)
     while tail.shape[0] >= gs.S:
         seg, tail = tail[:gs.S], tail[gs.S:]
-        committed.append(compress_stream(seg, gs.S, gs.base.c, tau, R=gs.base.R))
+        committed.append(compress_stream(seg, gs.S, gs.base.c, tau, R=gs.base.R,
+                                         bitmask_pv=bitmask_pv))
     return GrownStream(base=gs.base, committed=committed, tail=tail)
 
 

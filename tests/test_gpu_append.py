@@ -41,18 +41,22 @@ def _library_hat(m, b, h, x, T0, S, c, n_commit):
     return R.astype(np.float64), np.concatenate(parts, axis=0)
 
 
-@pytest.mark.parametrize("T0,pieces", [(300, [5, 59, 1, 70, 65]), (256, [5, 59, 1, 70, 65]),
-                                       (100, [64, 200, 130, 50])],
-                         ids=["ragged-prefill", "aligned-prefill", "pool-growth"])
-def test_appends_across_segment_boundaries(M, T0, pieces):
+@pytest.mark.parametrize("T0,pieces,bitmask", [(300, [5, 59, 1, 70, 65], False),
+                                               (256, [5, 59, 1, 70, 65], False),
+                                               (100, [64, 200, 130, 50], False),
+                                               (256, [5, 59, 1, 70, 65], True)],
+                         ids=["ragged-prefill", "aligned-prefill", "pool-growth", "bitmask-pv"])
+def test_appends_across_segment_boundaries(M, T0, pieces, bitmask):
     """pool-growth: 6 commits (444 appended tokens, S = 64), more than the room
     mkv_compress reserves (2), so the pool is moved to a larger allocation
-    during the appends."""
+    during the appends.  bitmask-pv: MKV_FLAG_BITMASK_PV, mixed regimes, so
+    that commits include bitmask-indexed per-vector segments."""
     S, c, tau, k = 64, 40, 0.85, 96
     w = W.small_workload(f"append-{T0}", n_kv_heads=2, n_q_heads=8, ctx=T0 + sum(pieces),
-                         segment=S, c=c, tau=tau, top_k=k, seed=41)
+                         segment=S, c=c, tau=tau, top_k=k, seed=41, mixed_regimes=bitmask)
     K, V = W.draw_kv(w)
-    cfg = M.make_config(w.batch, w.n_kv_heads, w.n_q_heads, w.ctx, S, c, tau, k)
+    cfg = M.make_config(w.batch, w.n_kv_heads, w.n_q_heads, w.ctx, S, c, tau, k,
+                        flags=M.MKV_FLAG_BITMASK_PV if bitmask else 0)
     m = M.Mkv(cfg)
     m.compress(K[:, :, :T0].contiguous().to(DEV), V[:, :, :T0].contiguous().to(DEV))
     g = w.group
@@ -61,14 +65,15 @@ def test_appends_across_segment_boundaries(M, T0, pieces):
     for h in range(2):
         for x, X in ((0, K), (1, V)):
             R = m.export(0, h, x)[0].astype(np.float64)
-            base = O.compress_stream(X[0, h, :T0].numpy(), S, c, tau, R=R)
+            base = O.compress_stream(X[0, h, :T0].numpy(), S, c, tau, R=R, bitmask_pv=bitmask)
             grown[(h, x)] = O.GrownStream(base=base)
     T = T0
     for step, n in enumerate(pieces):
         m.append(K[:, :, T:T + n].contiguous().to(DEV), V[:, :, T:T + n].contiguous().to(DEV))
         for key in grown:
             X = K if key[1] == 0 else V
-            grown[key] = O.append_stream(grown[key], X[0, key[0], T:T + n].numpy(), tau)
+            grown[key] = O.append_stream(grown[key], X[0, key[0], T:T + n].numpy(), tau,
+                                         bitmask_pv=bitmask)
         T += n
         q = W.draw_queries(w, K[:, :, :T], step=step)
         kk = min(k, T)
@@ -113,9 +118,11 @@ def test_appends_across_segment_boundaries(M, T0, pieces):
     n_commit = len(grown[(0, 0)].committed)
     assert n_commit == sum(pieces) // S
     nseg0 = -(-T0 // S)
+    n_pvb = 0
     for h in range(2):
         for x, X in ((0, K), (1, V)):
             R, _, hdr, pay = m.export(0, h, x)
+            n_pvb += int((hdr[nseg0:nseg0 + n_commit]["strategy"] == O.PVB).sum())
             buf = np.frombuffer(pay, dtype=np.uint8)
             for i in range(n_commit):
                 hd = hdr[nseg0 + i:nseg0 + i + 1].copy()
@@ -123,8 +130,10 @@ def test_appends_across_segment_boundaries(M, T0, pieces):
                 hd[0]["off16"] = 0
                 t0 = T0 + i * S
                 compare_compressed(X[0, h, t0:t0 + S].numpy(), R, hd, buf[off:].tobytes(), S, c,
-                                   tau, rep)
-    assert_budgets(f"appends T0={T0} commits={n_commit}", rep)
+                                   tau, rep, bitmask)
+    assert_budgets(f"appends T0={T0} commits={n_commit}" + (" bitmask" if bitmask else ""), rep)
+    if bitmask:
+        assert n_pvb > 0, "no committed segment used the bitmask strategy"
     # a repeated decode is bit-identical
     q = W.draw_queries(w, K, step=99)
     o1 = m.decode(q.to(DEV)).cpu()

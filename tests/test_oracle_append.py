@@ -108,8 +108,8 @@ def _planted(monkeypatch, which):
     if which == "fresh_basis":
         orig = O.compress_stream
 
-        def commit_fresh(X, S, c, tau, R=None):
-            return orig(X, S, c, tau, R=None if X.shape[0] == S else R)
+        def commit_fresh(X, S, c, tau, R=None, **kw):
+            return orig(X, S, c, tau, R=None if X.shape[0] == S else R, **kw)
         monkeypatch.setattr(O, "compress_stream", commit_fresh)
     elif which == "unrotated_tail":
         monkeypatch.setattr(O, "append_rows",
@@ -125,7 +125,7 @@ def _planted(monkeypatch, which):
     elif which == "late_commit":
         orig_append = O.append_stream
 
-        def late(gs, X_new, tau):
+        def late(gs, X_new, tau, bitmask_pv=False):
             tail = X_new if gs.tail is None else np.concatenate([gs.tail, X_new])
             committed = list(gs.committed)
             while tail.shape[0] > gs.S:
@@ -149,3 +149,30 @@ def test_planted_mistakes_are_caught(monkeypatch, which):
         except AssertionError:
             failed += 1
     assert failed >= 1, f"planted mistake {which} passed every pin"
+
+
+def test_bitmask_commits_follow_the_prefill_rule():
+    """With bitmask-indexed per-vector segments enabled, a committed segment
+    is compressed by the same rule as the prefill: here (aligned prefill) the
+    grown stream decodes exactly like compressing all tokens with bitmask PV
+    and the same basis (fitted to the prefill only), and the committed
+    segment is a PVB one (its per-token outliers keep tau per vector but not
+    under one shared mask, and c = 40 > 16 makes PVB cheaper than PV)."""
+    rng = np.random.default_rng(9)
+    d, T, S = 128, 96, 32
+    Q, _ = np.linalg.qr(rng.standard_normal((d, d)))
+    Z = rng.standard_normal((T, d)) * np.where(rng.random((T, d)) < 0.05, 20.0, 1.0)
+    X = (Z @ Q).astype(np.float16)
+    _, R = O.basis(X[:64])
+    gs = O.GrownStream(base=O.compress_stream(X[:64], S, 40, 0.8, R=R, bitmask_pv=True))
+    gs = O.append_stream(gs, X[64:75], 0.8, bitmask_pv=True)
+    gs = O.append_stream(gs, X[75:96], 0.8, bitmask_pv=True)
+    whole = O.compress_stream(X, S, 40, 0.8, R=R, bitmask_pv=True)
+    assert len(gs.committed) == 1 and gs.n_tail == 0
+    assert gs.committed[0].segs[0].strategy == whole.segs[2].strategy == O.PVB
+    assert np.array_equal(O.grown_dense_hat(gs), whole.dense_hat())
+    # without the flag the same tokens commit as a PV segment
+    plain = O.append_stream(O.GrownStream(base=O.compress_stream(X[:64], S, 40, 0.8, R=R)),
+                            X[64:96], 0.8)
+    assert plain.committed[0].segs[0].strategy == O.PV
+
