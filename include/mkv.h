@@ -320,7 +320,7 @@ mkv_status mkv_debug_wait_test(mkv_ctx* ctx, uint64_t limit_ns, mkv_stream_t str
  * launched with programmatic dependent launch when no flag disables it.  Bit
  * k (k = MKV_KERNEL_* id) enables it for kernel k; bit 8 keeps the kernels
  * from signalling early (the next kernel then starts when they end).
- * Default 0x0b (the rotation, score and attention kernels).  Results do not
+ * Default 0x03 (the rotation and score kernels).  Results do not
  * depend on it.  MKV_ERR_INVALID_ARG for other bits. */
 mkv_status mkv_debug_set_pdl(mkv_ctx* ctx, uint32_t mask);
 mkv_status mkv_debug_set_check_extent(mkv_ctx* ctx, uint64_t bytes);

@@ -78,7 +78,7 @@ struct mkv_ctx {
   // MKV_KERNEL_* id): the rotation, score and attention kernels gain about
   // 1.5 us each at the 128K batch-8 shape; the clustered selection kernel
   // and the merge lose time with it, so they are launched plainly
-  uint32_t pdl_mask = (1u << MKV_KERNEL_QROT) | (1u << MKV_KERNEL_SCORE) | (1u << MKV_KERNEL_ATTN);
+  uint32_t pdl_mask = (1u << MKV_KERNEL_QROT) | (1u << MKV_KERNEL_SCORE);
 
   // compression scratch
   SegInfo* seg = nullptr;
