@@ -723,10 +723,12 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
       }
     } else {
       // ---- packed rows: warp per row --------------------------------------------
+      // row r of the tile is row lr0 + r past the start of segment sgf (32-bit)
+      const int lr0 = (int)(t0 - (int64_t)sgf * p.S);
       for (int r = warp; r < rows; r += RT_WARPS) {
-        const int64_t t = t0 + r;
-        const int sg = (int)(t / p.S);
-        const int rl = (int)(t - (int64_t)sg * p.S);
+        const int q = (lr0 + r) / p.S;
+        const int sg = sgf + q;
+        const int rl = lr0 + r - q * p.S;
         const SegInfo& si = seg_sh[sg - sgf];
         const uint32_t off16 = off_sh[sg - sgf];
         if ((uint64_t)off16 * 16u + si.size > p.pool_check) {
