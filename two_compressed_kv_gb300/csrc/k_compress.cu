@@ -453,28 +453,28 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // ---------------------------------------------------------------------------
-// Per-token top-c of 128 magnitudes held by a pair of lanes (64 each: lane
-// 2k has channels 0..63, lane 2k+1 channels 64..127), ties to the lower
-// channel.  Bit search on the magnitudes' bit patterns (non-negative floats
-// order like their bits), the pair's counts combined by a shuffle whose mask
-// is the pair alone (pairs leave the loop at different steps), stopping once
+// Per-token top-c of 128 magnitudes held by a group of four lanes (32 each:
+// lane 4k + i has channels 32 i .. 32 i + 31), ties to the lower channel.
+// Bit search on the magnitudes' bit patterns (non-negative floats order like
+// their bits), the group's counts combined by shuffles whose mask is the
+// group alone (groups leave the loop at different steps), stopping once
 // exactly c keys are >= the candidate; with ties at the threshold the lowest
-// channels among them are taken, lane 2k's before lane 2k+1's.  Returns this
-// lane's 64 mask bits and its part of the kept energy (sum of the kept
+// channels among them are taken, lower lanes' before higher lanes'.  Returns
+// this lane's 32 mask bits and its part of the kept energy (sum of the kept
 // squares in channel order).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float pair_topc(const uint32_t k[64], int c, uint32_t mask[2]) {
+__device__ __forceinline__ float quad_topc(const uint32_t k[32], int c, uint32_t& mask) {
   const int lane = threadIdx.x & 31;
-  const unsigned pm = 3u << (lane & ~1);        // this lane and its partner
-  const bool upper = lane & 1;
+  const unsigned gm = 15u << (lane & ~3);       // the four lanes of this token
+  const int sub = lane & 3;
   if (c >= D) {
     float kept = 0.f;
 #pragma unroll
-    for (int j = 0; j < 64; ++j) {
+    for (int j = 0; j < 32; ++j) {
       const float f = __uint_as_float(k[j]);
       kept = fmaf(f, f, kept);
     }
-    mask[0] = mask[1] = 0xffffffffu;
+    mask = 0xffffffffu;
     return kept;
   }
   uint32_t thr = 0;
@@ -483,62 +483,67 @@ __device__ __forceinline__ float pair_topc(const uint32_t k[64], int c, uint32_t
     const uint32_t cand = thr | (1u << bit);
     int n0 = 0, n1 = 0, n2 = 0, n3 = 0;
 #pragma unroll
-    for (int j = 0; j < 64; j += 4) {
+    for (int j = 0; j < 32; j += 4) {
       n0 += k[j] >= cand;
       n1 += k[j + 1] >= cand;
       n2 += k[j + 2] >= cand;
       n3 += k[j + 3] >= cand;
     }
     int cnt = (n0 + n1) + (n2 + n3);
-    cnt += __shfl_xor_sync(pm, cnt, 1);
+    cnt += __shfl_xor_sync(gm, cnt, 1);
+    cnt += __shfl_xor_sync(gm, cnt, 2);
     if (cnt >= c) {
       thr = cand;
       cnt_ge = cnt;
       if (cnt == c) break;
     }
   }
-  int take_eq = 64;                    // keys equal to thr that this lane still takes
+  int take_eq = 32;                    // keys equal to thr that this lane still takes
   if (cnt_ge != c) {
     int gt = 0, eq = 0;
 #pragma unroll
-    for (int j = 0; j < 64; ++j) {
+    for (int j = 0; j < 32; ++j) {
       gt += k[j] > thr;
       eq += k[j] == thr;
     }
-    const int gt_all = gt + __shfl_xor_sync(pm, gt, 1);
-    const int eq_lower = __shfl_sync(pm, eq, lane & ~1);   // equal keys of channels 0..63
+    int gt_all = gt + __shfl_xor_sync(gm, gt, 1);
+    gt_all += __shfl_xor_sync(gm, gt_all, 2);
+    // equal keys of the lower lanes of the group (lower channels)
+    int eq_incl = eq;
+    int o = __shfl_up_sync(gm, eq_incl, 1, 4);
+    if (sub >= 1) eq_incl += o;
+    o = __shfl_up_sync(gm, eq_incl, 2, 4);
+    if (sub >= 2) eq_incl += o;
+    const int eq_before = eq_incl - eq;
     const int need = c - gt_all;
-    take_eq = upper ? need - min(need, eq_lower) : min(need, eq);
+    take_eq = min(eq, max(0, need - eq_before));
   }
   float kept = 0.f;
   int eq = 0;
+  uint32_t w = 0;
 #pragma unroll
-  for (int m = 0; m < 2; ++m) {
-    uint32_t w = 0;
-#pragma unroll
-    for (int b = 0; b < 32; ++b) {
-      const uint32_t kj = k[32 * m + b];
-      const bool take = kj > thr || (kj == thr && eq < take_eq);
-      eq += kj == thr;
-      w |= (uint32_t)take << b;
-      const float f = __uint_as_float(kj);
-      kept = take ? fmaf(f, f, kept) : kept;
-    }
-    mask[m] = w;
+  for (int b = 0; b < 32; ++b) {
+    const uint32_t kj = k[b];
+    const bool take = kj > thr || (kj == thr && eq < take_eq);
+    eq += kj == thr;
+    w |= (uint32_t)take << b;
+    const float f = __uint_as_float(kj);
+    kept = take ? fmaf(f, f, kept) : kept;
   }
+  mask = w;
   return kept;
 }
 
 // ---------------------------------------------------------------------------
 // rotate: the statistics pass (PACK = false) and the packing pass (PACK =
-// true).  One CTA (8 warps) covers whole segments [sg0, sg1) of one stream in
+// true).  One CTA (16 warps) covers whole segments [sg0, sg1) of one stream in
 // tiles of 128 tokens.  x~ = x R_hi + 2^-11 (x R_lo) on the tensor cores
 // (tcgen05, M = 128 tokens, N = 128 basis vectors, K = 128 channels; R split
 // into an fp16 part and a remainder scaled by 2^11 so that it stays a normal
 // fp16, one TMEM accumulator each).  Warps w and w + 4 read TMEM lanes
 // 32 (w mod 4) .. +31 (one token each), channels 0..63 and 64..127, into an
 // fp32 tile in shared memory.
-//   statistics: per token the c channels of largest |x~| (pair_topc: two
+//   statistics: per token the c channels of largest |x~| (quad_topc: four
 //     lanes per token), its kept energy and channel mask (the mask also goes
 //     to global scratch for the packing pass); per segment the column
 //     energies and the kept energy, stored for the strategy kernel.
@@ -547,7 +552,7 @@ __device__ __forceinline__ float pair_topc(const uint32_t k[64], int c, uint32_t
 //     mask for SM, the token's mask for PV, every channel for dense segments.
 // grid: (ctas_per_stream, BH, 2), block 256, dynamic smem RT_SMEM
 // ---------------------------------------------------------------------------
-constexpr int RT_THREADS = 256;
+constexpr int RT_THREADS = 512;
 constexpr int RT_WARPS = RT_THREADS / 32;
 constexpr int XT_LD = D + 1;          // fp32 x~ rows: conflict-free by row and by column
 constexpr int RT_MAXSEG = TC_T / 16 + 1;   // segments a tile can touch (S >= 16)
@@ -659,11 +664,12 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
     }
     tc_fence_after();
     {
-      // warps w and w + 4: token 32 (w mod 4) + lane, channels 64 (w / 4) ..
-      const int tok = 32 * (warp & 3) + lane, c0 = 64 * (warp >> 2);
+      // warp w: token 32 (w mod 4) + lane (its TMEM lane quarter), channels
+      // 32 (w / 4) .. 32 (w / 4) + 31
+      const int tok = 32 * (warp & 3) + lane, c0 = 32 * (warp >> 2);
       const uint32_t ta = tbase + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)c0;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < 2; ++q) {
         uint32_t h[16], l[16];
         tmem_ld16(ta + 16 * q, h);
         tmem_ld16(ta + 128 + 16 * q, l);
@@ -677,19 +683,21 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
     tc_fence_before();
     __syncthreads();
     if (!PACK) {
-      // ---- per-token channels: two lanes per token -----------------------------
-      const int tok = tid >> 1, half = tid & 1;
-      uint32_t k[64];
+      // ---- per-token channels: four lanes per token ----------------------------
+      const int tok = tid >> 2, quarter = tid & 3;
+      uint32_t k[32];
 #pragma unroll
-      for (int j = 0; j < 64; ++j)
-        k[j] = __float_as_uint(Xt[tok * XT_LD + 64 * half + j]) & 0x7fffffffu;
-      uint32_t m[2];
-      float kept = pair_topc(k, p.c, m);
-      kept += __shfl_xor_sync(0xffffffffu, kept, 1);     // channels 0..63 first, then 64..127
+      for (int j = 0; j < 32; ++j)
+        k[j] = __float_as_uint(Xt[tok * XT_LD + 32 * quarter + j]) & 0x7fffffffu;
+      uint32_t m;
+      float kept = quad_topc(k, p.c, m);
+      // the group's parts in channel order: (0 + 1) + (2 + 3)
+      kept += __shfl_xor_sync(0xffffffffu, kept, 1);
+      kept += __shfl_xor_sync(0xffffffffu, kept, 2);
       if (tok < rows) {
-        *reinterpret_cast<uint2*>(tokmask + 4 * tok + 2 * half) = make_uint2(m[0], m[1]);
-        *reinterpret_cast<uint2*>(gmask + (size_t)(t0 + tok) * 4 + 2 * half) = make_uint2(m[0], m[1]);
-        if (!half) tokkept[tok] = kept;
+        tokmask[4 * tok + quarter] = m;
+        gmask[(size_t)(t0 + tok) * 4 + quarter] = m;
+        if (!quarter) tokkept[tok] = kept;
       }
       __syncthreads();
       // ---- per segment: column energies and kept energy, for the strategy -------
