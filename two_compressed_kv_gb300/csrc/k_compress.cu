@@ -193,9 +193,9 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gram_kernel(CompressParams p) {
 // set by the fp32 rounding of the products (about sqrt(n) eps_32 of ||G||).
 // Eigenvalues are sorted descending (ties to the lower index), and each
 // column's largest-magnitude entry is made positive (ties to the lower row).
-// grid: 2 * BH, block 512, dynamic smem 3 x 128 x 129 floats
+// grid: 2 * BH, block 1024, dynamic smem 3 x 128 x 129 floats
 // ---------------------------------------------------------------------------
-constexpr int EIG_THREADS = 512;
+constexpr int EIG_THREADS = 1024;
 constexpr int LDA = D + 1;
 constexpr int EIG_MAX_SWEEPS = 16;
 constexpr int EIG_REFINE_SWEEPS = 6;
