@@ -16,6 +16,7 @@
 //   scan     exclusive scan of the packed segment sizes -> headers, total.
 //   pack     same rotation and selection again, writes the packed payload.
 #include "mkv_internal.cuh"
+#include "block_scan.cuh"
 #include "tc05.cuh"
 
 namespace mkv {
@@ -879,41 +880,50 @@ __global__ void __launch_bounds__(256) strategy_kernel(CompressParams p) {
 // segment headers and the total packed size.  One CTA.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) scan_kernel(CompressParams p) {
+  // steps of 8192 consecutive segments, thread tid taking segments 8 tid ..
+  // 8 tid + 7 of the step (the 8-byte head of each segment record: size,
+  // strategy, rows), a block-wide exclusive scan per step and a running carry
   const int64_t n = (int64_t)2 * p.BH * p.n_seg;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t per = (n + 1023) / 1024;
-  const int64_t lo = imin64(n, tid * per), hi = imin64(n, lo + per);
-  unsigned long long mine = 0;
-  for (int64_t e = lo; e < hi; ++e) mine += p.seg[e].size;
-  unsigned long long inc = mine;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const unsigned long long o = __shfl_up_sync(0xffffffffu, inc, off);
-    if (lane >= off) inc += o;
-  }
-  __shared__ unsigned long long ws[32];
-  if (lane == 31) ws[warp] = inc;
-  __syncthreads();
-  unsigned long long wb = 0;
-  for (int w = 0; w < warp; ++w) wb += ws[w];
-  unsigned long long off = wb + inc - mine;
+  const int tid = threadIdx.x;
+  const int64_t per_x = (int64_t)p.BH * p.n_seg;
+  __shared__ unsigned long long ws[65];
   __shared__ unsigned int n_dense[2];
   if (tid < 2) n_dense[tid] = 0u;
-  __syncthreads();
-  const int64_t per_x = (int64_t)p.BH * p.n_seg;
-  for (int64_t e = lo; e < hi; ++e) {
-    const SegInfo si = p.seg[e];
-    if (si.strategy == MKV_STRATEGY_DENSE) atomicAdd(&n_dense[e >= per_x ? 1 : 0], 1u);
-    mkv_segment_header h;
-    h.off16 = (uint32_t)(off >> 4);
-    h.strategy = si.strategy;
-    h.reserved = 0;
-    h.rows = si.rows;
-    p.hdr[e] = h;
-    off += si.size;
+  unsigned long long carry = 0;     // bytes of all earlier steps (same in every thread)
+  unsigned int dense_lo = 0, dense_hi = 0;
+  for (int64_t s0 = 0; s0 < n; s0 += 8192) {
+    const int64_t e0 = s0 + 8 * (int64_t)tid;
+    uint2 hd[8];                     // x: size, y: strategy | rows << 16
+    unsigned long long mine = 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      hd[u] = e0 + u < n ? *reinterpret_cast<const uint2*>(&p.seg[e0 + u]) : make_uint2(0u, 0u);
+      mine += hd[u].x;
+    }
+    unsigned long long tot;
+    unsigned long long off = carry + block_excl_scan64(mine, ws, tot);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (e0 + u < n) {
+        const uint32_t strat = hd[u].y & 0xffu;
+        if (strat == MKV_STRATEGY_DENSE) {
+          if (e0 + u >= per_x) ++dense_hi; else ++dense_lo;
+        }
+        mkv_segment_header h;
+        h.off16 = (uint32_t)(off >> 4);
+        h.strategy = (uint8_t)strat;
+        h.reserved = 0;
+        h.rows = (uint16_t)(hd[u].y >> 16);
+        p.hdr[e0 + u] = h;
+        off += hd[u].x;
+      }
+    }
+    carry += tot;
   }
+  if (dense_lo) atomicAdd(&n_dense[0], dense_lo);
+  if (dense_hi) atomicAdd(&n_dense[1], dense_hi);
   __syncthreads();
-  if (tid == 1023) p.total[0] = wb + inc;
+  if (tid == 0) p.total[0] = carry;
   if (tid < 2) p.total[1 + tid] = n_dense[tid];
 }
 

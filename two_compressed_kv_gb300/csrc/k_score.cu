@@ -10,6 +10,7 @@
 // floating-point sum runs in a fixed order, so a decode is bit-for-bit
 // repeatable.  This file also holds the compression-time partition of the
 // score work (partition and plan kernels).
+#include "block_scan.cuh"
 #include "decode_common.cuh"
 
 namespace mkv {
@@ -483,32 +484,36 @@ __global__ void __launch_bounds__(1024) partition_kernel(const mkv_segment_heade
                                                          int n_streams, int n_seg, int c, int G,
                                                          int32_t* part, int32_t* cta_cnt,
                                                          int64_t* prefix) {
-  __shared__ unsigned long long wsum[32];
+  __shared__ unsigned long long wsum[65];
   const int64_t n = (int64_t)n_streams * n_seg;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t per = (n + 1023) / 1024;
-  const int64_t lo = imin64(n, tid * per), hi = imin64(n, lo + per);
-  unsigned long long mine = 0;
-  for (int64_t e = lo; e < hi; ++e) {
-    const mkv_segment_header h = hdrK[e];
-    mine += segment_bytes(h.strategy, h.rows, c);
-  }
-  unsigned long long inc = mine;
+  const int tid = threadIdx.x;
+  // steps of 8192 consecutive segments, thread tid taking 8 tid .. 8 tid + 7
+  // of the step (coalesced loads), a block-wide exclusive scan per step and
+  // a running carry
+  unsigned long long carry = 0;
+  for (int64_t s0 = 0; s0 < n; s0 += 8192) {
+    const int64_t e0 = s0 + 8 * (int64_t)tid;
+    uint32_t sz[8];
+    unsigned long long mine = 0;
 #pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const unsigned long long o = __shfl_up_sync(0xffffffffu, inc, off);
-    if (lane >= off) inc += o;
+    for (int u = 0; u < 8; ++u) {
+      sz[u] = 0u;
+      if (e0 + u < n) {
+        const mkv_segment_header h = hdrK[e0 + u];
+        sz[u] = segment_bytes(h.strategy, h.rows, c);
+      }
+      mine += sz[u];
+    }
+    unsigned long long tot;
+    unsigned long long acc = carry + block_excl_scan64(mine, wsum, tot);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (e0 + u < n) prefix[e0 + u] = (int64_t)acc;
+      acc += sz[u];
+    }
+    carry += tot;
   }
-  if (lane == 31) wsum[warp] = inc;
-  __syncthreads();
-  unsigned long long acc = inc - mine;
-  for (int w = 0; w < warp; ++w) acc += wsum[w];
-  for (int64_t e = lo; e < hi; ++e) {
-    prefix[e] = (int64_t)acc;
-    const mkv_segment_header h = hdrK[e];
-    acc += segment_bytes(h.strategy, h.rows, c);
-  }
-  if (tid == 1023) prefix[n] = (int64_t)acc;
+  if (tid == 0) prefix[n] = (int64_t)carry;
   for (int s = tid; s < n_streams; s += blockDim.x) cta_cnt[s] = 0;
   __syncthreads();
   const int64_t total = prefix[n];
