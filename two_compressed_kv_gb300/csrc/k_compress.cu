@@ -454,85 +454,78 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // ---------------------------------------------------------------------------
+// 32 x 32 bit-matrix transpose in registers: on entry w[r] bit c is entry
+// (r, c), on exit w[c] bit r.  Five stages of block swaps (16, 8, 4, 2, 1).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void transpose32(uint32_t w[32]) {
+#pragma unroll
+  for (int sft = 16, lvl = 0; sft >= 1; sft >>= 1, ++lvl) {
+    const uint32_t m = lvl == 0 ? 0x0000ffffu
+                     : lvl == 1 ? 0x00ff00ffu
+                     : lvl == 2 ? 0x0f0f0f0fu
+                     : lvl == 3 ? 0x33333333u
+                                : 0x55555555u;
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+      if (r & sft) continue;
+      const uint32_t t = ((w[r] >> sft) ^ w[r + sft]) & m;
+      w[r + sft] ^= t;
+      w[r] ^= t << sft;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Per-token top-c of 128 magnitudes held by a group of four lanes (32 each:
 // lane 4k + i has channels 32 i .. 32 i + 31), ties to the lower channel.
-// Bit search on the magnitudes' bit patterns (non-negative floats order like
-// their bits), the group's counts combined by shuffles whose mask is the
-// group alone (groups leave the loop at different steps), stopping once
-// exactly c keys are >= the candidate; with ties at the threshold the lowest
-// channels among them are taken, lower lanes' before higher lanes'.  Returns
-// this lane's 32 mask bits and its part of the kept energy (sum of the kept
-// squares in channel order).
+// The magnitudes' bit patterns (non-negative floats order like their bits)
+// are transposed into bit planes; a radix select from the top bit keeps, per
+// lane, the set A of keys that match the threshold's bits so far and the set
+// G of keys already above it, with group counts (shuffles whose mask is the
+// group alone: groups leave the loop at different steps).  It stops once G
+// and A hold exactly c keys; otherwise A ends as the keys equal to the
+// threshold, of which the lowest channels are taken, lower lanes' first.
+// Returns this lane's 32 mask bits; the kept energy is summed by the caller.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float quad_topc(const uint32_t k[32], int c, uint32_t& mask) {
+__device__ __forceinline__ uint32_t quad_topc(uint32_t w[32], int c) {
   const int lane = threadIdx.x & 31;
   const unsigned gm = 15u << (lane & ~3);       // the four lanes of this token
   const int sub = lane & 3;
-  if (c >= D) {
-    float kept = 0.f;
+  if (c >= D) return 0xffffffffu;
+  transpose32(w);                               // w[b] bit j: bit b of key j
+  uint32_t A = 0xffffffffu, G = 0u;
+  int nG = 0, nA = D;                           // group counts of G and A
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const float f = __uint_as_float(k[j]);
-      kept = fmaf(f, f, kept);
+  for (int b = 30; b >= 0; --b) {
+    const uint32_t ones = A & w[b];
+    int n1 = __popc(ones);
+    n1 += __shfl_xor_sync(gm, n1, 1);
+    n1 += __shfl_xor_sync(gm, n1, 2);
+    if (nG + n1 >= c) {
+      A = ones;
+      nA = n1;
+    } else {
+      G |= ones;
+      nG += n1;
+      A &= ~w[b];
+      nA -= n1;
     }
-    mask = 0xffffffffu;
-    return kept;
+    if (nG + nA == c) break;
   }
-  uint32_t thr = 0;
-  int cnt_ge = D;
-  for (int bit = 30; bit >= 0; --bit) {
-    const uint32_t cand = thr | (1u << bit);
-    int n0 = 0, n1 = 0, n2 = 0, n3 = 0;
-#pragma unroll
-    for (int j = 0; j < 32; j += 4) {
-      n0 += k[j] >= cand;
-      n1 += k[j + 1] >= cand;
-      n2 += k[j + 2] >= cand;
-      n3 += k[j + 3] >= cand;
-    }
-    int cnt = (n0 + n1) + (n2 + n3);
-    cnt += __shfl_xor_sync(gm, cnt, 1);
-    cnt += __shfl_xor_sync(gm, cnt, 2);
-    if (cnt >= c) {
-      thr = cand;
-      cnt_ge = cnt;
-      if (cnt == c) break;
-    }
+  // take all of G and the lowest (c - nG) keys of A, lower lanes first
+  const int na = __popc(A);
+  int incl = na;
+  int o = __shfl_up_sync(gm, incl, 1, 4);
+  if (sub >= 1) incl += o;
+  o = __shfl_up_sync(gm, incl, 2, 4);
+  if (sub >= 2) incl += o;
+  const int take = min(na, max(0, (c - nG) - (incl - na)));
+  uint32_t t = 0u, a = A;
+  for (int q = 0; q < take; ++q) {
+    t |= a & (0u - a);
+    a &= a - 1u;
   }
-  int take_eq = 32;                    // keys equal to thr that this lane still takes
-  if (cnt_ge != c) {
-    int gt = 0, eq = 0;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      gt += k[j] > thr;
-      eq += k[j] == thr;
-    }
-    int gt_all = gt + __shfl_xor_sync(gm, gt, 1);
-    gt_all += __shfl_xor_sync(gm, gt_all, 2);
-    // equal keys of the lower lanes of the group (lower channels)
-    int eq_incl = eq;
-    int o = __shfl_up_sync(gm, eq_incl, 1, 4);
-    if (sub >= 1) eq_incl += o;
-    o = __shfl_up_sync(gm, eq_incl, 2, 4);
-    if (sub >= 2) eq_incl += o;
-    const int eq_before = eq_incl - eq;
-    const int need = c - gt_all;
-    take_eq = min(eq, max(0, need - eq_before));
-  }
-  float kept = 0.f;
-  int eq = 0;
-  uint32_t w = 0;
-#pragma unroll
-  for (int b = 0; b < 32; ++b) {
-    const uint32_t kj = k[b];
-    const bool take = kj > thr || (kj == thr && eq < take_eq);
-    eq += kj == thr;
-    w |= (uint32_t)take << b;
-    const float f = __uint_as_float(kj);
-    kept = take ? fmaf(f, f, kept) : kept;
-  }
-  mask = w;
-  return kept;
+  return G | t;
 }
 
 // ---------------------------------------------------------------------------
@@ -686,12 +679,18 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
     if (!PACK) {
       // ---- per-token channels: four lanes per token ----------------------------
       const int tok = tid >> 2, quarter = tid & 3;
+      const float* xrow = Xt + tok * XT_LD + 32 * quarter;
       uint32_t k[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        k[j] = __float_as_uint(Xt[tok * XT_LD + 32 * quarter + j]) & 0x7fffffffu;
-      uint32_t m;
-      float kept = quad_topc(k, p.c, m);
+      for (int j = 0; j < 32; ++j) k[j] = __float_as_uint(xrow[j]) & 0x7fffffffu;
+      const uint32_t m = quad_topc(k, p.c);
+      // this lane's kept energy, in channel order
+      float kept = 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float f = xrow[j];
+        kept = ((m >> j) & 1u) ? fmaf(f, f, kept) : kept;
+      }
       // the group's parts in channel order: (0 + 1) + (2 + 3)
       kept += __shfl_xor_sync(0xffffffffu, kept, 1);
       kept += __shfl_xor_sync(0xffffffffu, kept, 2);
