@@ -548,6 +548,7 @@ __device__ __forceinline__ uint32_t quad_topc(uint32_t w[32], int c) {
 // ---------------------------------------------------------------------------
 constexpr int RT_THREADS = 512;
 constexpr int RT_WARPS = RT_THREADS / 32;
+static_assert(RT_THREADS == 4 * D, "four lanes per token and four column partial sums");
 constexpr int XT_LD = D + 1;          // fp32 x~ rows: conflict-free by row and by column
 constexpr int RT_MAXSEG = TC_T / 16 + 1;   // segments a tile can touch (S >= 16)
 constexpr size_t RT_SMEM = 1024 + 4 * (size_t)TC_TILE + (size_t)TC_T * XT_LD * 4 + TC_T * 16 +
@@ -560,6 +561,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
   __shared__ uint32_t tbase_sh;
   __shared__ SegInfo seg_sh[RT_MAXSEG];
   __shared__ uint32_t off_sh[RT_MAXSEG];
+  __shared__ float colpart[RT_THREADS / D][D];   // column-energy partial sums
   const uint32_t raw = smem_u32(rt_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;            // tiles on 1024-byte boundaries
   uint8_t* gbase = rt_raw + (base - raw);
@@ -707,26 +709,42 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
         const int sg = (int)(a / p.S);
         const int64_t segend = imin64(p.T, (int64_t)(sg + 1) * p.S);
         const int64_t b = imin64(tend, segend);
-        if (tid < D) {
-          float cacc = colacc[tid];
-          for (int64_t t = a; t < b; ++t) {
-            const float val = Xt[(int)(t - t0) * XT_LD + tid];
-            cacc = fmaf(val, val, cacc);
+        const int r0 = (int)(a - t0), r1 = (int)(b - t0);
+        // every thread: column tid mod 128 over rows r0 + part, r0 + part + 4, ...
+        // (part = tid / 128); warp 4 also sums the tokens' kept energies
+        {
+          const int col = tid & (D - 1), part = tid >> 7;
+          float q = 0.f;
+          for (int r = r0 + part; r < r1; r += RT_THREADS / D) {
+            const float val = Xt[r * XT_LD + col];
+            q = fmaf(val, val, q);
           }
+          colpart[part][col] = q;
+        }
+        float kq = 0.f;
+        if (warp == 4) {
+          for (int r = r0 + lane; r < r1; r += 32) kq += tokkept[r];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, o);
+        }
+        __syncthreads();
+        if (tid < D) {
+          float cacc = colacc[tid] + ((colpart[0][tid] + colpart[1][tid]) +
+                                      (colpart[2][tid] + colpart[3][tid]));
           if (b == segend) {
             p.colE[((size_t)sx * p.n_seg + sg) * D + tid] = cacc;
             cacc = 0.f;
           }
           colacc[tid] = cacc;
-        } else if (tid == D) {
-          float kk = segkept[0];
-          for (int64_t t = a; t < b; ++t) kk += tokkept[(int)(t - t0)];
+        } else if (tid == 4 * 32) {
+          float kk = segkept[0] + kq;
           if (b == segend) {
             p.segK[(size_t)sx * p.n_seg + sg] = kk;
             kk = 0.f;
           }
           segkept[0] = kk;
         }
+        __syncthreads();          // colpart is rewritten by the next piece
         a = b;
       }
     } else {
