@@ -209,14 +209,30 @@ struct EigShared {
   float cs[64], sn[64], tt[64];
   int top[64], bot[64];
   int rotated;
+  float floor;
 };
 
 // Jacobi sweeps on A (in place), accumulating the rotations into V, until a
 // sweep rotates nothing or max_sweeps have run.  A pair (p, q) is rotated
-// when |a_pq| > tol sqrt(|a_pp a_qq|); blocks and columns whose rotations
-// are all identities are left untouched.  Block-wide.
-__device__ void jacobi_sweeps(float* A, float* V, int max_sweeps, float tol, EigShared& sh) {
+// when |a_pq| > tol sqrt(|a_pp a_qq|) and |a_pq| > floor_rel max_i |a_ii|
+// (floor_rel = 0: no floor); blocks and columns whose rotations are all
+// identities are left untouched.  Block-wide.
+__device__ void jacobi_sweeps(float* A, float* V, int max_sweeps, float tol, float floor_rel,
+                              EigShared& sh) {
   const int tid = threadIdx.x;
+  float floor_abs = 0.f;
+  if (floor_rel > 0.f) {
+    // the largest diagonal entry (warp 0), read by every thread
+    if (tid < 32) {
+      float mx = 0.f;
+      for (int i = tid; i < D; i += 32) mx = fmaxf(mx, fabsf(A[i * LDA + i]));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      if (tid == 0) sh.floor = floor_rel * mx;
+    }
+    __syncthreads();
+    floor_abs = sh.floor;
+  }
   for (int sweep = 0; sweep < max_sweeps; ++sweep) {
     if (tid == 0) sh.rotated = 0;
     __syncthreads();
@@ -226,7 +242,7 @@ __device__ void jacobi_sweeps(float* A, float* V, int max_sweeps, float tol, Eig
         const int pp = min(a, b), qq = max(a, b);
         const float app = A[pp * LDA + pp], aqq = A[qq * LDA + qq], apq = A[pp * LDA + qq];
         float c = 1.f, s = 0.f, t = 0.f;
-        if (apq != 0.f && fabsf(apq) > tol * sqrtf(fabsf(app * aqq))) {
+        if (apq != 0.f && fabsf(apq) > tol * sqrtf(fabsf(app * aqq)) && fabsf(apq) > floor_abs) {
           const float th = (aqq - app) / (2.f * apq);
           t = (th >= 0.f ? 1.f : -1.f) / (fabsf(th) + sqrtf(1.f + th * th));
           c = 1.f / sqrtf(1.f + t * t);
@@ -356,9 +372,10 @@ __global__ void __launch_bounds__(EIG_THREADS) eig_kernel(CompressParams p) {
   }
   __syncthreads();
 
-  // the first solve only has to bring A close to diagonal: the refinement
-  // below re-forms V^T G V and finishes the convergence
-  jacobi_sweeps(A, V, EIG_MAX_SWEEPS, 1e-5f, sh);
+  // the first solve only has to bring A close to diagonal (pairs at or
+  // below 1e-6 of the largest diagonal entry are left): the refinement below
+  // re-forms V^T G V and finishes the convergence
+  jacobi_sweeps(A, V, EIG_MAX_SWEEPS, 1e-5f, 1e-6f, sh);
   // refinement: orthonormal V, then A = V^T G V from the original G
   newton_schulz(V, A);
   smem_matmul<false>(Gs, V, A);     // A = G V
@@ -374,7 +391,7 @@ __global__ void __launch_bounds__(EIG_THREADS) eig_kernel(CompressParams p) {
     }
   }
   __syncthreads();
-  jacobi_sweeps(Ar, V, EIG_REFINE_SWEEPS, 1e-7f, sh);
+  jacobi_sweeps(Ar, V, EIG_REFINE_SWEEPS, 1e-7f, 0.f, sh);
   if (tid < D) lam[tid] = Ar[tid * LDA + tid];
   __syncthreads();
   newton_schulz(V, W);
