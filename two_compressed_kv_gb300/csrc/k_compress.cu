@@ -197,6 +197,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gram_kernel(CompressParams p) {
 // grid: 2 * BH, block 1024, dynamic smem 3 x 128 x 129 floats
 // ---------------------------------------------------------------------------
 constexpr int EIG_THREADS = 1024;
+static_assert(EIG_THREADS % 64 == 0, "a thread's blocks share one column rotation");
 constexpr int LDA = D + 1;
 constexpr int EIG_MAX_SWEEPS = 16;
 constexpr int EIG_REFINE_SWEEPS = 6;
@@ -256,9 +257,15 @@ __device__ void jacobi_sweeps(float* A, float* V, int max_sweeps, float tol, flo
         sh.bot[tid] = qq;
       }
       __syncthreads();
+      // EIG_THREADS is a multiple of 64: every block (P, Q) and V column pair
+      // of this thread has Q = tid mod 64, so its rotation is read once
+      const int Q = tid & 63;
+      const float cQ = sh.cs[Q], sQ = sh.sn[Q];
+      const int q1 = sh.top[Q], q2 = sh.bot[Q];
       for (int blk = tid; blk < 64 * 64; blk += EIG_THREADS) {
-        const int P = blk >> 6, Q = blk & 63;
-        if (sh.sn[P] == 0.f && sh.sn[Q] == 0.f) continue;   // both rotations are identities
+        const int P = blk >> 6;
+        const float sP = sh.sn[P];
+        if (sP == 0.f && sQ == 0.f) continue;   // both rotations are identities
         const int p1 = sh.top[P], p2 = sh.bot[P];
         if (P == Q) {
           const float apq = A[p1 * LDA + p2], t = sh.tt[P];
@@ -267,8 +274,7 @@ __device__ void jacobi_sweeps(float* A, float* V, int max_sweeps, float tol, flo
           A[p1 * LDA + p2] = 0.f;
           A[p2 * LDA + p1] = 0.f;
         } else {
-          const int q1 = sh.top[Q], q2 = sh.bot[Q];
-          const float cP = sh.cs[P], sP = sh.sn[P], cQ = sh.cs[Q], sQ = sh.sn[Q];
+          const float cP = sh.cs[P];
           const float b11 = A[p1 * LDA + q1], b12 = A[p1 * LDA + q2];
           const float b21 = A[p2 * LDA + q1], b22 = A[p2 * LDA + q2];
           const float u11 = cP * b11 - sP * b21, u12 = cP * b12 - sP * b22;
@@ -279,14 +285,13 @@ __device__ void jacobi_sweeps(float* A, float* V, int max_sweeps, float tol, flo
           A[p2 * LDA + q2] = sQ * u21 + cQ * u22;
         }
       }
-      for (int e = tid; e < D * 64; e += EIG_THREADS) {
-        const int r = e >> 6, k = e & 63;
-        const float c = sh.cs[k], s = sh.sn[k];
-        if (s == 0.f) continue;
-        const int pp = sh.top[k], qq = sh.bot[k];
-        const float vp = V[r * LDA + pp], vq = V[r * LDA + qq];
-        V[r * LDA + pp] = c * vp - s * vq;
-        V[r * LDA + qq] = s * vp + c * vq;
+      if (sQ != 0.f) {
+        // V columns of rotation Q, rows tid / 64, tid / 64 + EIG_THREADS / 64, ...
+        for (int r = tid >> 6; r < D; r += EIG_THREADS / 64) {
+          const float vp = V[r * LDA + q1], vq = V[r * LDA + q2];
+          V[r * LDA + q1] = cQ * vp - sQ * vq;
+          V[r * LDA + q2] = sQ * vp + cQ * vq;
+        }
       }
       __syncthreads();
     }
