@@ -556,25 +556,35 @@ __device__ __forceinline__ uint32_t quad_topc(uint32_t w[32], int c) {
 // tiles of 128 tokens.  x~ = x R_hi + 2^-11 (x R_lo) on the tensor cores
 // (tcgen05, M = 128 tokens, N = 128 basis vectors, K = 128 channels; R split
 // into an fp16 part and a remainder scaled by 2^11 so that it stays a normal
-// fp16, one TMEM accumulator each).  Warps w and w + 4 read TMEM lanes
-// 32 (w mod 4) .. +31 (one token each), channels 0..63 and 64..127, into an
-// fp32 tile in shared memory.
-//   statistics: per token the c channels of largest |x~| (quad_topc: four
-//     lanes per token), its kept energy and channel mask (the mask also goes
-//     to global scratch for the packing pass); per segment the column
-//     energies and the kept energy, stored for the strategy kernel.
-//   packing: writes the packed rows, warp per row, with the segment data and
-//     the tokens' stored masks staged in shared memory first: the segment
-//     mask for SM, the token's mask for PV, every channel for dense segments.
-// grid: (ctas_per_stream, BH, 2), block 256, dynamic smem RT_SMEM
+// fp16, one TMEM accumulator each).  Warp w reads TMEM lanes 32 (w mod 4)
+// .. +31 (one token each), channels 32 (w / 4) .. +31.
+//   statistics: the readback goes to an fp32 tile in shared memory; per token
+//     the c channels of largest |x~| (quad_topc: four lanes per token), its
+//     kept energy and channel mask (the mask also goes to global scratch for
+//     the packing pass); per segment the column energies and the kept energy,
+//     stored for the strategy kernel.
+//   packing: with the segment data and the tokens' stored masks staged in
+//     shared memory, each thread compacts its 32 channels of one token from
+//     the readback registers into a shared-memory image of the packed row
+//     (values, and index bytes for PV): the segment mask for SM, the token's
+//     mask for PV, every channel for dense segments.  The images are then
+//     written out in aligned 16- and 8-byte pieces (c is a multiple of 8, so
+//     every packed value row starts on 16 bytes and every index row on 8).
+// grid: (ctas_per_stream, BH, 2), block 512, dynamic smem rt_smem(PACK)
 // ---------------------------------------------------------------------------
 constexpr int RT_THREADS = 512;
-constexpr int RT_WARPS = RT_THREADS / 32;
 static_assert(RT_THREADS == 4 * D, "four lanes per token and four column partial sums");
 constexpr int XT_LD = D + 1;          // fp32 x~ rows: conflict-free by row and by column
 constexpr int RT_MAXSEG = TC_T / 16 + 1;   // segments a tile can touch (S >= 16)
-constexpr size_t RT_SMEM = 1024 + 4 * (size_t)TC_TILE + (size_t)TC_T * XT_LD * 4 + TC_T * 16 +
-                           TC_T * 4 + D * 4 + 64;
+constexpr int ST_V = 2 * D + 16;      // staged value row bytes (16-byte pieces, banks spread)
+constexpr int ST_I = D + 8;           // staged index row bytes (8-byte pieces)
+// statistics: the fp32 tile; packing: the staged value and index rows
+constexpr size_t rt_smem(bool pack) {
+  return 1024 + 4 * (size_t)TC_TILE +
+         (pack ? (size_t)TC_T * (ST_V + ST_I) : (size_t)TC_T * XT_LD * 4) + TC_T * 16 + TC_T * 4 +
+         D * 4 + 64;
+}
+static_assert(rt_smem(false) <= 227 * 1024 && rt_smem(true) <= 227 * 1024, "shared memory");
 
 template <bool PACK>
 __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p) {
@@ -584,12 +594,16 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
   __shared__ SegInfo seg_sh[RT_MAXSEG];
   __shared__ uint32_t off_sh[RT_MAXSEG];
   __shared__ float colpart[RT_THREADS / D][D];   // column-energy partial sums
+  __shared__ uint32_t rowinfo[TC_T];             // packing: segment slot << 16 | row in segment
   const uint32_t raw = smem_u32(rt_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;            // tiles on 1024-byte boundaries
   uint8_t* gbase = rt_raw + (base - raw);
   const uint32_t Bhi = base, Blo = base + TC_TILE, Xs = base + 2 * TC_TILE;
   float* Xt = reinterpret_cast<float*>(gbase + 4 * TC_TILE);             // [128][XT_LD]
-  uint32_t* tokmask = reinterpret_cast<uint32_t*>(Xt + TC_T * XT_LD);    // [128][4]
+  uint8_t* stv = gbase + 4 * TC_TILE;                                     // [128][ST_V]
+  uint8_t* sti = stv + TC_T * ST_V;                                       // [128][ST_I]
+  uint32_t* tokmask = reinterpret_cast<uint32_t*>(
+      PACK ? sti + TC_T * ST_I : reinterpret_cast<uint8_t*>(Xt + TC_T * XT_LD));   // [128][4]
   float* tokkept = reinterpret_cast<float*>(tokmask + TC_T * 4);         // [128]
   float* colacc = tokkept + TC_T;                                        // [128]
   float* segkept = colacc + D;                                           // [1]
@@ -665,6 +679,8 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
     }
     // segment data (packing) while the MMAs run
     const int sgf = (int)(t0 / p.S);
+    // row r of the tile is row lr0 + r past the start of segment sgf (32-bit)
+    const int lr0 = (int)(t0 - (int64_t)sgf * p.S);
     if (PACK) {
       const int nsg = (int)((t0 + rows - 1) / p.S) - sgf + 1;
       if (tid < nsg) {
@@ -676,12 +692,71 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
         *reinterpret_cast<uint4*>(tokmask + 4 * tid) =
             *reinterpret_cast<const uint4*>(gmask + (size_t)(t0 + tid) * 4);
     }
-    if (!tc_wait(&mma_bar, (uint32_t)(it & 1), p.err)) {
+    // one decision for the whole block (and the staged segment data visible)
+    if (__syncthreads_or(!tc_wait(&mma_bar, (uint32_t)(it & 1), p.err))) {
       ok = false;
       break;
     }
     tc_fence_after();
-    {
+    if (PACK) {
+      // ---- compaction: thread = (token, 32 channels) -----------------------------
+      const int tok = 32 * (warp & 3) + lane, qt = warp >> 2, c0 = 32 * qt;
+      const uint32_t ta = tbase + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)c0;
+      const bool live = tok < rows;
+      int strat = MKV_STRATEGY_DENSE, pos = 0;
+      uint32_t m = 0xffffffffu;
+      uint8_t* sm_idx = nullptr;     // SM index bytes of a segment's first row go straight out
+      if (live) {
+        const int q = (lr0 + tok) / p.S;
+        const int rl = lr0 + tok - q * p.S;
+        const SegInfo& si = seg_sh[q];
+        strat = si.strategy;
+        if (strat != MKV_STRATEGY_DENSE) {
+          const uint32_t* mw = strat == MKV_STRATEGY_SM ? si.mask : tokmask + 4 * tok;
+          m = mw[qt];
+          for (int z = 0; z < qt; ++z) pos += __popc(mw[z]);
+        }
+        if (qt == 0) rowinfo[tok] = ((uint32_t)q << 16) | (uint32_t)rl;
+        if (strat == MKV_STRATEGY_SM && rl == 0 &&
+            (uint64_t)off_sh[q] * 16u + si.size <= p.pool_check)
+          sm_idx = p.pool + (size_t)off_sh[q] * 16u;
+      }
+      __half* vrow = reinterpret_cast<__half*>(stv + tok * ST_V);
+      uint8_t* irow = strat == MKV_STRATEGY_PV ? sti + tok * ST_I : nullptr;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        uint32_t h[16], l[16];
+        __syncwarp();
+        tmem_ld16(ta + 16 * q, h);
+        tmem_ld16(ta + 128 + 16 * q, l);
+        tmem_ld_wait();
+        __half2 hv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          hv[j] = __floats2half2_rn(fmaf(__uint_as_float(l[2 * j]), 1.f / 2048.f, __uint_as_float(h[2 * j])),
+                                    fmaf(__uint_as_float(l[2 * j + 1]), 1.f / 2048.f,
+                                         __uint_as_float(h[2 * j + 1])));
+        if (live) {
+          if (strat == MKV_STRATEGY_DENSE) {
+            uint4* dst = reinterpret_cast<uint4*>(stv + tok * ST_V + 2 * (c0 + 16 * q));
+            const uint32_t* hw = reinterpret_cast<const uint32_t*>(hv);
+            dst[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            dst[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+          } else {
+            const uint32_t mm = m >> (16 * q);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              if ((mm >> j) & 1u) {
+                vrow[pos] = (j & 1) ? __high2half(hv[j >> 1]) : __low2half(hv[j >> 1]);
+                if (irow) irow[pos] = (uint8_t)(c0 + 16 * q + j);
+                if (sm_idx) sm_idx[pos] = (uint8_t)(c0 + 16 * q + j);
+                ++pos;
+              }
+            }
+          }
+        }
+      }
+    } else {
       // warp w: token 32 (w mod 4) + lane (its TMEM lane quarter), channels
       // 32 (w / 4) .. 32 (w / 4) + 31
       const int tok = 32 * (warp & 3) + lane, c0 = 32 * (warp >> 2);
@@ -770,72 +845,45 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
         a = b;
       }
     } else {
-      // ---- packed rows: warp per row --------------------------------------------
-      // row r of the tile is row lr0 + r past the start of segment sgf (32-bit)
-      const int lr0 = (int)(t0 - (int64_t)sgf * p.S);
-      for (int r = warp; r < rows; r += RT_WARPS) {
-        const int q = (lr0 + r) / p.S;
-        const int sg = sgf + q;
-        const int rl = lr0 + r - q * p.S;
-        const SegInfo& si = seg_sh[sg - sgf];
-        const uint32_t off16 = off_sh[sg - sgf];
+      // ---- copy-out: (row, 16-byte piece) per item ------------------------------
+      const uint32_t c = (uint32_t)p.c;
+      for (int item = tid; item < rows * 16; item += RT_THREADS) {
+        const int r = item >> 4, k = item & 15;
+        const uint32_t ri = rowinfo[r];
+        const int q = (int)(ri >> 16);
+        const uint32_t rl = ri & 0xffffu;
+        const SegInfo& si = seg_sh[q];
+        const uint32_t off16 = off_sh[q];
         if ((uint64_t)off16 * 16u + si.size > p.pool_check) {
           // the segment would end past the checked pool extent: report, skip
-          if (lane == 0) atomicOr(p.err, DEV_ERR_CHECK);
+          if (k == 0) atomicOr(p.err, DEV_ERR_CHECK);
           continue;
         }
         uint8_t* seg = p.pool + (size_t)off16 * 16u;
-        const uint32_t c = (uint32_t)p.c;
-        float v[4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) v[m] = Xt[r * XT_LD + lane + 32 * m];
-        if (si.strategy == MKV_STRATEGY_DENSE) {
-          __half* row = reinterpret_cast<__half*>(seg + 256u * rl);
-#pragma unroll
-          for (int m = 0; m < 4; ++m) row[lane + 32 * m] = __float2half_rn(v[m]);
+        const int strat = si.strategy;
+        const uint32_t srows = si.rows;
+        if (strat == MKV_STRATEGY_DENSE) {
+          *reinterpret_cast<uint4*>(seg + 256u * rl + 16u * k) =
+              *reinterpret_cast<const uint4*>(stv + r * ST_V + 16 * k);
           continue;
         }
-        uint32_t w[4];
-        if (si.strategy == MKV_STRATEGY_SM) {
-#pragma unroll
-          for (int m = 0; m < 4; ++m) w[m] = si.mask[m];
-        } else {
-#pragma unroll
-          for (int m = 0; m < 4; ++m) w[m] = tokmask[4 * r + m];
+        if ((uint32_t)k < (c >> 3)) {
+          const uint32_t voff = (strat == MKV_STRATEGY_SM ? pad16(c) : 0u) + 2u * c * rl;
+          *reinterpret_cast<uint4*>(seg + voff + 16u * k) =
+              *reinterpret_cast<const uint4*>(stv + r * ST_V + 16 * k);
+          if (strat == MKV_STRATEGY_PV)
+            *reinterpret_cast<uint2*>(seg + 2u * c * srows + c * rl + 8u * k) =
+                *reinterpret_cast<const uint2*>(sti + r * ST_I + 8 * k);
         }
-        __half* vrow;
-        uint8_t* irow;
-        if (si.strategy == MKV_STRATEGY_SM) {
-          vrow = reinterpret_cast<__half*>(seg + pad16(c) + 2u * c * rl);
-          irow = (rl == 0) ? seg : nullptr;
-        } else if (si.strategy == MKV_STRATEGY_PVB) {
-          vrow = reinterpret_cast<__half*>(seg + 2u * c * rl);
-          irow = nullptr;
-          if (lane == 0)
-            *reinterpret_cast<uint4*>(seg + 2u * c * si.rows + 16u * rl) =
-                make_uint4(w[0], w[1], w[2], w[3]);
-        } else {
-          vrow = reinterpret_cast<__half*>(seg + 2u * c * rl);
-          irow = seg + 2u * c * si.rows + c * rl;
-        }
-        const uint32_t lt = (1u << lane) - 1u;
-        int before = 0;
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          if ((w[m] >> lane) & 1u) {
-            const int pos = before + __popc(w[m] & lt);
-            vrow[pos] = __float2half_rn(v[m]);
-            if (irow) irow[pos] = (uint8_t)(lane + 32 * m);
-          }
-          before += __popc(w[m]);
-        }
-        // zero the padding after the index bytes
-        if (si.strategy == MKV_STRATEGY_SM && rl == 0) {
-          for (uint32_t z = c + lane; z < pad16(c); z += 32) seg[z] = 0;
-        }
-        if (si.strategy == MKV_STRATEGY_PV && rl == si.rows - 1) {
-          uint8_t* ib = seg + 2u * c * si.rows;
-          for (uint32_t z = c * si.rows + lane; z < pad16(c * si.rows); z += 32) ib[z] = 0;
+        if (k == 0) {
+          if (strat == MKV_STRATEGY_PVB)
+            *reinterpret_cast<uint4*>(seg + 2u * c * srows + 16u * rl) =
+                *reinterpret_cast<const uint4*>(tokmask + 4 * r);
+          // zero padding after the index bytes (c and c * rows are multiples of 8)
+          if (strat == MKV_STRATEGY_SM && rl == 0 && (c & 15u))
+            *reinterpret_cast<uint2*>(seg + c) = make_uint2(0u, 0u);
+          if (strat == MKV_STRATEGY_PV && rl == srows - 1 && ((c * srows) & 15u))
+            *reinterpret_cast<uint2*>(seg + 3u * c * srows) = make_uint2(0u, 0u);
         }
       }
     }
@@ -989,10 +1037,11 @@ cudaError_t launch_eig(const CompressParams& p, cudaStream_t st) {
 template <bool PACK>
 static cudaError_t launch_rot(const CompressParams& p, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(rotate_kernel<PACK>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)RT_SMEM);
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)rt_smem(PACK));
   if (e != cudaSuccess) return e;
   dim3 grid(p.ctas_per_stream, p.BH, 2);
-  rotate_kernel<PACK><<<grid, RT_THREADS, RT_SMEM, st>>>(p);
+  rotate_kernel<PACK><<<grid, RT_THREADS, rt_smem(PACK), st>>>(p);
   return cudaGetLastError();
 }
 
