@@ -27,6 +27,9 @@ namespace mkv {
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes));
 }
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(dst), "l"(src));
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
@@ -581,18 +584,36 @@ constexpr int ST_I = D + 8;           // staged index row bytes (8-byte pieces)
 // statistics: the fp32 tile; packing: the staged value and index rows
 constexpr size_t rt_smem(bool pack) {
   return 1024 + 4 * (size_t)TC_TILE +
-         (pack ? (size_t)TC_T * (ST_V + ST_I) : (size_t)TC_T * XT_LD * 4) + TC_T * 16 + TC_T * 4 +
-         D * 4 + 64;
+         (pack ? (size_t)TC_T * (ST_V + ST_I) + 2 * TC_T * 16 : (size_t)TC_T * XT_LD * 4) +
+         TC_T * 16 + TC_T * 4 + D * 4 + 64;
 }
 static_assert(rt_smem(false) <= 227 * 1024 && rt_smem(true) <= 227 * 1024, "shared memory");
+
+// The 16 MMAs of one tile: x~ hi part into columns tacc .. +127, lo part
+// into tacc + 128 .. +255; committed to bar.  One thread.
+__device__ __forceinline__ void rt_issue_mma(uint32_t xt, uint32_t Bhi, uint32_t Blo, uint32_t tacc,
+                                             uint64_t* bar) {
+  const uint32_t idesc = idesc_f16_f32(128, 128);
+  tc_fence_after();
+#pragma unroll
+  for (int k = 0; k < D / 16; ++k) {
+    const uint32_t ko = (uint32_t)(k >> 2) * TC_ATOMS + (uint32_t)(k & 3) * 32u;
+    const uint64_t a = sdesc_k_sw128(xt + ko);
+    tc_mma_f16(tacc, a, sdesc_k_sw128(Bhi + ko), idesc, k > 0 ? 1u : 0u);
+    tc_mma_f16(tacc + 128, a, sdesc_k_sw128(Blo + ko), idesc, k > 0 ? 1u : 0u);
+  }
+  tc_commit(bar);
+}
 
 template <bool PACK>
 __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p) {
   extern __shared__ uint8_t rt_raw[];
-  __shared__ uint64_t mma_bar;
+  __shared__ uint64_t mma_bar[2];
   __shared__ uint32_t tbase_sh;
-  __shared__ SegInfo seg_sh[RT_MAXSEG];
-  __shared__ uint32_t off_sh[RT_MAXSEG];
+  // packing: segment data of three tiles (the current one, the next, and the
+  // one being loaded)
+  __shared__ __align__(16) SegInfo seg3[3][RT_MAXSEG];
+  __shared__ __align__(8) mkv_segment_header hdr3[3][RT_MAXSEG];
   __shared__ float colpart[RT_THREADS / D][D];   // column-energy partial sums
   __shared__ uint32_t rowinfo[TC_T];             // packing: segment slot << 16 | row in segment
   const uint32_t raw = smem_u32(rt_raw);
@@ -602,9 +623,10 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
   float* Xt = reinterpret_cast<float*>(gbase + 4 * TC_TILE);             // [128][XT_LD]
   uint8_t* stv = gbase + 4 * TC_TILE;                                     // [128][ST_V]
   uint8_t* sti = stv + TC_T * ST_V;                                       // [128][ST_I]
+  // statistics: [128][4]; packing: [3][128][4] (three tiles, like the segment data)
   uint32_t* tokmask = reinterpret_cast<uint32_t*>(
-      PACK ? sti + TC_T * ST_I : reinterpret_cast<uint8_t*>(Xt + TC_T * XT_LD));   // [128][4]
-  float* tokkept = reinterpret_cast<float*>(tokmask + TC_T * 4);         // [128]
+      PACK ? sti + TC_T * ST_I : reinterpret_cast<uint8_t*>(Xt + TC_T * XT_LD));
+  float* tokkept = reinterpret_cast<float*>(tokmask + (PACK ? 3 : 1) * TC_T * 4);   // [128]
   float* colacc = tokkept + TC_T;                                        // [128]
   float* segkept = colacc + D;                                           // [1]
 
@@ -619,16 +641,48 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
   const __half* X = p.X[x] + (size_t)s * p.T * D;
   const int n_tiles = (int)((te - tb + TC_T - 1) / TC_T);
 
+  uint32_t* gmask = p.tokmask + (size_t)sx * p.T * 4;
+  // packing: tile j's token masks and segment data into buffer j mod 3, in
+  // the same cp.async group as its X tile (threads 0..127)
+  auto load_meta = [&](int j) {
+    const int64_t t0j = tb + (int64_t)j * TC_T;
+    const int rowsj = (int)imin64(TC_T, te - t0j);
+    const int sgfj = (int)(t0j / p.S);
+    const int nsgj = (int)((t0j + rowsj - 1) / p.S) - sgfj + 1;
+    const int mbj = j % 3;
+    const bool live = tid < rowsj;
+    cp_async16(smem_u32(tokmask + (mbj * TC_T + tid) * 4),
+               gmask + (size_t)(live ? t0j + tid : t0j) * 4, live ? 16u : 0u);
+    if (tid < nsgj) {
+      const size_t e = (size_t)sx * p.n_seg + sgfj + tid;
+      const uint8_t* src = reinterpret_cast<const uint8_t*>(p.seg + e);
+      cp_async16(smem_u32(&seg3[mbj][tid]), src, 16u);
+      cp_async16(smem_u32(&seg3[mbj][tid]) + 16u, src + 16, 16u);
+      cp_async8(smem_u32(&hdr3[mbj][tid]), p.hdr + e);
+    }
+  };
+
+  // two TMEM accumulator pairs: the MMAs of tile it + 1 run while tile it is
+  // read back
   if (warp == 0) {
-    tmem_alloc(&tbase_sh, 256);
+    tmem_alloc(&tbase_sh, 512);
     tmem_relinquish();
   }
   if (tid == 0) {
-    mbar_init(&mma_bar, 1);
+    mbar_init(&mma_bar[0], 1);
+    mbar_init(&mma_bar[1], 1);
     mbar_init_fence();
   }
-  // first tile in flight while R is split into the two B operands
-  if (tid < 128) tc_load_tile(Xs, X, tb, te);
+  // tiles 0 and 1 in flight while R is split into the two B operands
+  if (tid < 128) {
+    tc_load_tile(Xs, X, tb, te);
+    if (PACK) load_meta(0);
+  }
+  cp_async_commit();
+  if (n_tiles > 1 && tid < 128) {
+    tc_load_tile(Xs + TC_TILE, X, tb + TC_T, te);
+    if (PACK) load_meta(1);
+  }
   cp_async_commit();
   {
     // B = R^T, K-major: row j (basis vector) holds R[0..127][j] along K
@@ -648,60 +702,51 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
     if (tid < D) colacc[tid] = 0.f;
     if (tid == 0) segkept[0] = 0.f;
   }
+  cp_async_wait<1>();             // tile 0
+  fence_proxy_async();            // tile and B operands: generic-proxy writes before the MMAs
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = tbase_sh;
-  const uint32_t idesc = idesc_f16_f32(128, 128);
-  uint32_t* gmask = p.tokmask + (size_t)sx * p.T * 4;
+  if (tid == 0) rt_issue_mma(Xs, Bhi, Blo, tbase, &mma_bar[0]);
   bool ok = true;
 
   for (int it = 0; it < n_tiles && ok; ++it) {
     const int64_t t0 = tb + (int64_t)it * TC_T;
     const int rows = (int)imin64(TC_T, te - t0);
-    const uint32_t xt = Xs + (uint32_t)(it & 1) * TC_TILE;
-    if (it + 1 < n_tiles && tid < 128)
-      tc_load_tile(Xs + (uint32_t)((it + 1) & 1) * TC_TILE, X, t0 + TC_T, te);
-    cp_async_commit();
-    cp_async_wait<1>();
-    fence_proxy_async();          // tile and B operands: generic-proxy writes before the MMAs
-    __syncthreads();
-    if (tid == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int k = 0; k < D / 16; ++k) {
-        const uint32_t ko = (uint32_t)(k >> 2) * TC_ATOMS + (uint32_t)(k & 3) * 32u;
-        const uint64_t a = sdesc_k_sw128(xt + ko);
-        tc_mma_f16(tbase, a, sdesc_k_sw128(Bhi + ko), idesc, k > 0 ? 1u : 0u);
-        tc_mma_f16(tbase + 128, a, sdesc_k_sw128(Blo + ko), idesc, k > 0 ? 1u : 0u);
-      }
-      tc_commit(&mma_bar);
+    const int b = it & 1;
+    const int mb = it % 3;
+    const SegInfo* seg_sh = seg3[mb];
+    const mkv_segment_header* hdr_sh = hdr3[mb];
+    const uint32_t* tmask = tokmask + (PACK ? mb * TC_T * 4 : 0);
+    if (it + 1 < n_tiles) {
+      // tile it + 1 (and its segment data) landed: its MMAs into the other pair
+      cp_async_wait<0>();
+      fence_proxy_async();
+      __syncthreads();
+      if (tid == 0)
+        rt_issue_mma(Xs + (uint32_t)(b ^ 1) * TC_TILE, Bhi, Blo, tbase + (uint32_t)(b ^ 1) * 256u,
+                     &mma_bar[b ^ 1]);
     }
-    // segment data (packing) while the MMAs run
     const int sgf = (int)(t0 / p.S);
     // row r of the tile is row lr0 + r past the start of segment sgf (32-bit)
     const int lr0 = (int)(t0 - (int64_t)sgf * p.S);
-    if (PACK) {
-      const int nsg = (int)((t0 + rows - 1) / p.S) - sgf + 1;
-      if (tid < nsg) {
-        const size_t e = (size_t)sx * p.n_seg + sgf + tid;
-        seg_sh[tid] = p.seg[e];
-        off_sh[tid] = p.hdr[e].off16;
-      }
-      if (tid < rows)
-        *reinterpret_cast<uint4*>(tokmask + 4 * tid) =
-            *reinterpret_cast<const uint4*>(gmask + (size_t)(t0 + tid) * 4);
-    }
-    // one decision for the whole block (and the staged segment data visible)
-    if (__syncthreads_or(!tc_wait(&mma_bar, (uint32_t)(it & 1), p.err))) {
+    // one decision for the whole block
+    if (__syncthreads_or(!tc_wait(&mma_bar[b], (uint32_t)((it >> 1) & 1), p.err))) {
       ok = false;
       break;
     }
     tc_fence_after();
+    // X buffer b is free: tile it + 2 in flight from here
+    if (it + 2 < n_tiles && tid < 128) {
+      tc_load_tile(Xs + (uint32_t)b * TC_TILE, X, t0 + 2 * TC_T, te);
+      if (PACK) load_meta(it + 2);
+    }
+    cp_async_commit();
     if (PACK) {
       // ---- compaction: thread = (token, 32 channels) -----------------------------
       const int tok = 32 * (warp & 3) + lane, qt = warp >> 2, c0 = 32 * qt;
-      const uint32_t ta = tbase + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)c0;
+      const uint32_t ta = tbase + (uint32_t)b * 256u + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)c0;
       const bool live = tok < rows;
       int strat = MKV_STRATEGY_DENSE, pos = 0;
       uint32_t m = 0xffffffffu;
@@ -712,14 +757,14 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
         const SegInfo& si = seg_sh[q];
         strat = si.strategy;
         if (strat != MKV_STRATEGY_DENSE) {
-          const uint32_t* mw = strat == MKV_STRATEGY_SM ? si.mask : tokmask + 4 * tok;
+          const uint32_t* mw = strat == MKV_STRATEGY_SM ? si.mask : tmask + 4 * tok;
           m = mw[qt];
           for (int z = 0; z < qt; ++z) pos += __popc(mw[z]);
         }
         if (qt == 0) rowinfo[tok] = ((uint32_t)q << 16) | (uint32_t)rl;
         if (strat == MKV_STRATEGY_SM && rl == 0 &&
-            (uint64_t)off_sh[q] * 16u + si.size <= p.pool_check)
-          sm_idx = p.pool + (size_t)off_sh[q] * 16u;
+            (uint64_t)hdr_sh[q].off16 * 16u + si.size <= p.pool_check)
+          sm_idx = p.pool + (size_t)hdr_sh[q].off16 * 16u;
       }
       __half* vrow = reinterpret_cast<__half*>(stv + tok * ST_V);
       uint8_t* irow = strat == MKV_STRATEGY_PV ? sti + tok * ST_I : nullptr;
@@ -760,7 +805,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
       // warp w: token 32 (w mod 4) + lane (its TMEM lane quarter), channels
       // 32 (w / 4) .. 32 (w / 4) + 31
       const int tok = 32 * (warp & 3) + lane, c0 = 32 * (warp >> 2);
-      const uint32_t ta = tbase + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)c0;
+      const uint32_t ta = tbase + (uint32_t)b * 256u + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)c0;
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         uint32_t h[16], l[16];
@@ -853,7 +898,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
         const int q = (int)(ri >> 16);
         const uint32_t rl = ri & 0xffffu;
         const SegInfo& si = seg_sh[q];
-        const uint32_t off16 = off_sh[q];
+        const uint32_t off16 = hdr_sh[q].off16;
         if ((uint64_t)off16 * 16u + si.size > p.pool_check) {
           // the segment would end past the checked pool extent: report, skip
           if (k == 0) atomicOr(p.err, DEV_ERR_CHECK);
@@ -878,7 +923,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
         if (k == 0) {
           if (strat == MKV_STRATEGY_PVB)
             *reinterpret_cast<uint4*>(seg + 2u * c * srows + 16u * rl) =
-                *reinterpret_cast<const uint4*>(tokmask + 4 * r);
+                *reinterpret_cast<const uint4*>(tmask + 4 * r);
           // zero padding after the index bytes (c and c * rows are multiples of 8)
           if (strat == MKV_STRATEGY_SM && rl == 0 && (c & 15u))
             *reinterpret_cast<uint2*>(seg + c) = make_uint2(0u, 0u);
@@ -892,7 +937,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
   cp_async_wait<0>();
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tbase, 256);
+  if (warp == 0) tmem_dealloc(tbase, 512);
 }
 
 // ---------------------------------------------------------------------------
