@@ -197,11 +197,15 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gram_kernel(CompressParams p) {
 // set by the fp32 rounding of the products (about sqrt(n) eps_32 of ||G||).
 // Eigenvalues are sorted descending (ties to the lower index), and each
 // column's largest-magnitude entry is made positive (ties to the lower row).
-// grid: 2 * BH, block 1024, dynamic smem 3 x 128 x 129 floats
+// During the sweeps A keeps only its upper triangle (entry (i, j) at
+// (min, max)) and V is held column-major, so that a rotation of two columns
+// of V moves whole rows of 16-byte vectors.
+// grid: 2 * BH, block 1024, dynamic smem 2 x 128 x 129 + 128 x 132 floats
 // ---------------------------------------------------------------------------
 constexpr int EIG_THREADS = 1024;
 static_assert(EIG_THREADS % 64 == 0, "a thread's blocks share one column rotation");
 constexpr int LDA = D + 1;
+constexpr int LDV = D + 4;            // column-major V: 16-byte aligned columns
 constexpr int EIG_MAX_SWEEPS = 16;
 constexpr int EIG_REFINE_SWEEPS = 6;
 
@@ -210,19 +214,32 @@ __device__ __forceinline__ int rr_player(int pos, int round) {
 }
 
 struct EigShared {
-  float cs[64], sn[64], tt[64];
+  float cs[64], sn[64];
   int top[64], bot[64];
   int rotated;
   float floor;
 };
 
-// Jacobi sweeps on A (in place), accumulating the rotations into V, until a
+__device__ __forceinline__ int upper(int i, int j) { return i < j ? i * LDA + j : j * LDA + i; }
+
+// Jacobi sweeps on the upper triangle of A (in place), accumulating the
+// rotations into the column-major Vt (column k of V at Vt + k LDV), until a
 // sweep rotates nothing or max_sweeps have run.  A pair (p, q) is rotated
 // when |a_pq| > tol sqrt(|a_pp a_qq|) and |a_pq| > floor_rel max_i |a_ii|
 // (floor_rel = 0: no floor); blocks and columns whose rotations are all
 // identities are left untouched.  Block-wide.
-__device__ void jacobi_sweeps(float* A, float* V, int max_sweeps, float tol, float floor_rel,
+//
+// A round's 64 rotations split A into 64 x 64 blocks of 2 x 2.  The thread
+// that computes rotation P also updates the diagonal block (P, P); by
+// symmetry only the 2016 off-diagonal blocks (P, Q), Q = P + d (mod 64),
+// d = 1 .. 31, and d = 32 for P < 32, are formed: warp w takes P = w and
+// P = w + 32, lane l the offset d = l (lane 0: d = 32 for P = w only), so
+// that a warp's accesses share their row and spread over the banks.  Thread
+// t updates rows 4 (t / 64) .. +3 and 4 (t / 64 + 16) .. +3 of the two
+// columns of V that rotation t mod 64 mixes.
+__device__ void jacobi_sweeps(float* A, float* Vt, int max_sweeps, float tol, float floor_rel,
                               EigShared& sh) {
+  static_assert(EIG_THREADS == 1024, "two blocks and two row groups of V per thread");
   const int tid = threadIdx.x;
   float floor_abs = 0.f;
   if (floor_rel > 0.f) {
@@ -237,6 +254,8 @@ __device__ void jacobi_sweeps(float* A, float* V, int max_sweeps, float tol, flo
     __syncthreads();
     floor_abs = sh.floor;
   }
+  const int w = tid >> 5, l = tid & 31;
+  const int R = tid & 63, g = tid >> 6;
   for (int sweep = 0; sweep < max_sweeps; ++sweep) {
     if (tid == 0) sh.rotated = 0;
     __syncthreads();
@@ -245,55 +264,57 @@ __device__ void jacobi_sweeps(float* A, float* V, int max_sweeps, float tol, flo
         int a = rr_player(tid, round), b = rr_player(D - 1 - tid, round);
         const int pp = min(a, b), qq = max(a, b);
         const float app = A[pp * LDA + pp], aqq = A[qq * LDA + qq], apq = A[pp * LDA + qq];
-        float c = 1.f, s = 0.f, t = 0.f;
+        float c = 1.f, s = 0.f;
         if (apq != 0.f && fabsf(apq) > tol * sqrtf(fabsf(app * aqq)) && fabsf(apq) > floor_abs) {
           const float th = (aqq - app) / (2.f * apq);
-          t = (th >= 0.f ? 1.f : -1.f) / (fabsf(th) + sqrtf(1.f + th * th));
+          const float t = (th >= 0.f ? 1.f : -1.f) / (fabsf(th) + sqrtf(1.f + th * th));
           c = 1.f / sqrtf(1.f + t * t);
           s = t * c;
           sh.rotated = 1;
+          // the diagonal block: no other update of this round touches it
+          A[pp * LDA + pp] = app - t * apq;
+          A[qq * LDA + qq] = aqq + t * apq;
+          A[pp * LDA + qq] = 0.f;
         }
         sh.cs[tid] = c;
         sh.sn[tid] = s;
-        sh.tt[tid] = t;
         sh.top[tid] = pp;
         sh.bot[tid] = qq;
       }
       __syncthreads();
-      // EIG_THREADS is a multiple of 64: every block (P, Q) and V column pair
-      // of this thread has Q = tid mod 64, so its rotation is read once
-      const int Q = tid & 63;
-      const float cQ = sh.cs[Q], sQ = sh.sn[Q];
-      const int q1 = sh.top[Q], q2 = sh.bot[Q];
-      for (int blk = tid; blk < 64 * 64; blk += EIG_THREADS) {
-        const int P = blk >> 6;
-        const float sP = sh.sn[P];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int P = w + 32 * k;
+        if (k == 1 && l == 0) break;   // (w + 32, w) is lane 0's block (w, w + 32)
+        const int Q = (P + (l == 0 ? 32 : l)) & 63;
+        const float sP = sh.sn[P], sQ = sh.sn[Q];
         if (sP == 0.f && sQ == 0.f) continue;   // both rotations are identities
-        const int p1 = sh.top[P], p2 = sh.bot[P];
-        if (P == Q) {
-          const float apq = A[p1 * LDA + p2], t = sh.tt[P];
-          A[p1 * LDA + p1] -= t * apq;
-          A[p2 * LDA + p2] += t * apq;
-          A[p1 * LDA + p2] = 0.f;
-          A[p2 * LDA + p1] = 0.f;
-        } else {
-          const float cP = sh.cs[P];
-          const float b11 = A[p1 * LDA + q1], b12 = A[p1 * LDA + q2];
-          const float b21 = A[p2 * LDA + q1], b22 = A[p2 * LDA + q2];
-          const float u11 = cP * b11 - sP * b21, u12 = cP * b12 - sP * b22;
-          const float u21 = sP * b11 + cP * b21, u22 = sP * b12 + cP * b22;
-          A[p1 * LDA + q1] = cQ * u11 - sQ * u12;
-          A[p1 * LDA + q2] = sQ * u11 + cQ * u12;
-          A[p2 * LDA + q1] = cQ * u21 - sQ * u22;
-          A[p2 * LDA + q2] = sQ * u21 + cQ * u22;
-        }
+        const float cP = sh.cs[P], cQ = sh.cs[Q];
+        const int p1 = sh.top[P], p2 = sh.bot[P], q1 = sh.top[Q], q2 = sh.bot[Q];
+        const int i11 = upper(p1, q1), i12 = upper(p1, q2), i21 = upper(p2, q1), i22 = upper(p2, q2);
+        const float b11 = A[i11], b12 = A[i12], b21 = A[i21], b22 = A[i22];
+        const float u11 = cP * b11 - sP * b21, u12 = cP * b12 - sP * b22;
+        const float u21 = sP * b11 + cP * b21, u22 = sP * b12 + cP * b22;
+        A[i11] = cQ * u11 - sQ * u12;
+        A[i12] = sQ * u11 + cQ * u12;
+        A[i21] = cQ * u21 - sQ * u22;
+        A[i22] = sQ * u21 + cQ * u22;
       }
-      if (sQ != 0.f) {
-        // V columns of rotation Q, rows tid / 64, tid / 64 + EIG_THREADS / 64, ...
-        for (int r = tid >> 6; r < D; r += EIG_THREADS / 64) {
-          const float vp = V[r * LDA + q1], vq = V[r * LDA + q2];
-          V[r * LDA + q1] = cQ * vp - sQ * vq;
-          V[r * LDA + q2] = sQ * vp + cQ * vq;
+      {
+        const float sR = sh.sn[R];
+        if (sR != 0.f) {
+          const float cR = sh.cs[R];
+          float4* vp = reinterpret_cast<float4*>(Vt + sh.top[R] * LDV);
+          float4* vq = reinterpret_cast<float4*>(Vt + sh.bot[R] * LDV);
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int r4 = g + 16 * k;
+            const float4 x = vp[r4], y = vq[r4];
+            vp[r4] = make_float4(cR * x.x - sR * y.x, cR * x.y - sR * y.y, cR * x.z - sR * y.z,
+                                 cR * x.w - sR * y.w);
+            vq[r4] = make_float4(sR * x.x + cR * y.x, sR * x.y + cR * y.y, sR * x.z + cR * y.z,
+                                 sR * x.w + cR * y.w);
+          }
         }
       }
       __syncthreads();
@@ -302,6 +323,27 @@ __device__ void jacobi_sweeps(float* A, float* V, int max_sweeps, float tol, flo
     __syncthreads();
     if (!any) break;
   }
+}
+
+// V between its row-major (row stride LDA) and column-major (column stride
+// LDV) forms, in place through registers.  Block-wide.
+template <bool TO_COLUMNS>
+__device__ void v_relayout(float* V) {
+  const int tid = threadIdx.x;
+  float v[D * D / EIG_THREADS];
+#pragma unroll
+  for (int k = 0; k < D * D / EIG_THREADS; ++k) {
+    const int e = tid + k * EIG_THREADS, r = e >> 7, c = e & 127;
+    v[k] = TO_COLUMNS ? V[r * LDA + c] : V[c * LDV + r];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < D * D / EIG_THREADS; ++k) {
+    const int e = tid + k * EIG_THREADS, r = e >> 7, c = e & 127;
+    if (TO_COLUMNS) V[c * LDV + r] = v[k];
+    else V[r * LDA + c] = v[k];
+  }
+  __syncthreads();
 }
 
 // C = op(X) Y for 128 x 128 matrices in shared memory (row stride LDA), with
@@ -348,8 +390,8 @@ __device__ void newton_schulz(float* V, float* W) {
 __global__ void __launch_bounds__(EIG_THREADS) eig_kernel(CompressParams p) {
   extern __shared__ __align__(16) float esm[];
   float* A = esm;
-  float* V = esm + D * LDA;
-  float* Gs = esm + 2 * D * LDA;
+  float* V = esm + D * LDA;          // row-major (LDA) or, during the sweeps, column-major (LDV)
+  float* Gs = V + D * LDV;
   __shared__ EigShared sh;
   __shared__ float lam[D];
   __shared__ int rank[D];
@@ -362,7 +404,7 @@ __global__ void __launch_bounds__(EIG_THREADS) eig_kernel(CompressParams p) {
     for (int c = 0; c < p.gram_chunks; ++c) a += part[(size_t)c * D * D + e];
     const int i = e >> 7, j = e & 127;
     A[i * LDA + j] = a;
-    V[i * LDA + j] = (i == j) ? 1.f : 0.f;
+    V[i * LDV + j] = (i == j) ? 1.f : 0.f;   // column-major for the sweeps
   }
   __syncthreads();
   // symmetrise: each (i, j), i < j, pair is owned by one thread; keep G
@@ -384,6 +426,7 @@ __global__ void __launch_bounds__(EIG_THREADS) eig_kernel(CompressParams p) {
   // below 1e-6 of the largest diagonal entry are left): the refinement below
   // re-forms V^T G V and finishes the convergence
   jacobi_sweeps(A, V, EIG_MAX_SWEEPS, 1e-5f, 1e-6f, sh);
+  v_relayout<false>(V);
   // refinement: orthonormal V, then A = V^T G V from the original G
   newton_schulz(V, A);
   smem_matmul<false>(Gs, V, A);     // A = G V
@@ -399,7 +442,9 @@ __global__ void __launch_bounds__(EIG_THREADS) eig_kernel(CompressParams p) {
     }
   }
   __syncthreads();
+  v_relayout<true>(V);
   jacobi_sweeps(Ar, V, EIG_REFINE_SWEEPS, 1e-7f, 0.f, sh);
+  v_relayout<false>(V);
   if (tid < D) lam[tid] = Ar[tid * LDA + tid];
   __syncthreads();
   newton_schulz(V, W);
@@ -1072,7 +1117,7 @@ cudaError_t launch_gram(const CompressParams& p, cudaStream_t st) {
 }
 
 cudaError_t launch_eig(const CompressParams& p, cudaStream_t st) {
-  const int smem = 3 * D * LDA * (int)sizeof(float);
+  const int smem = (2 * D * LDA + D * LDV) * (int)sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(eig_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   eig_kernel<<<2 * p.BH, EIG_THREADS, smem, st>>>(p);
