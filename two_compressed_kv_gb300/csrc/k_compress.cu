@@ -525,16 +525,25 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // ---------------------------------------------------------------------------
 // 32 x 32 bit-matrix transpose in registers: on entry w[r] bit c is entry
-// (r, c), on exit w[c] bit r.  Five stages of block swaps (16, 8, 4, 2, 1).
+// (r, c), on exit w[c] bit r.  Block swaps of 16 and 8 (one byte transpose
+// by byte permutes), then of 4, 2 and 1.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void transpose32(uint32_t w[32]) {
+  // the 16- and 8-bit levels together: in each group w[r], w[r + 8],
+  // w[r + 16], w[r + 24] byte j of word i trades places with byte i of word j
 #pragma unroll
-  for (int sft = 16, lvl = 0; sft >= 1; sft >>= 1, ++lvl) {
-    const uint32_t m = lvl == 0 ? 0x0000ffffu
-                     : lvl == 1 ? 0x00ff00ffu
-                     : lvl == 2 ? 0x0f0f0f0fu
-                     : lvl == 3 ? 0x33333333u
-                                : 0x55555555u;
+  for (int r = 0; r < 8; ++r) {
+    const uint32_t lo01 = __byte_perm(w[r], w[r + 8], 0x5140), hi01 = __byte_perm(w[r], w[r + 8], 0x7362);
+    const uint32_t lo23 = __byte_perm(w[r + 16], w[r + 24], 0x5140);
+    const uint32_t hi23 = __byte_perm(w[r + 16], w[r + 24], 0x7362);
+    w[r] = __byte_perm(lo01, lo23, 0x5410);
+    w[r + 8] = __byte_perm(lo01, lo23, 0x7632);
+    w[r + 16] = __byte_perm(hi01, hi23, 0x5410);
+    w[r + 24] = __byte_perm(hi01, hi23, 0x7632);
+  }
+#pragma unroll
+  for (int sft = 4, lvl = 0; sft >= 1; sft >>= 1, ++lvl) {
+    const uint32_t m = lvl == 0 ? 0x0f0f0f0fu : lvl == 1 ? 0x33333333u : 0x55555555u;
 #pragma unroll
     for (int r = 0; r < 32; ++r) {
       if (r & sft) continue;
@@ -833,16 +842,31 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
             dst[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
             dst[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
           } else {
-            const uint32_t mm = m >> (16 * q);
+            // each kept channel's slot from a prefix count: independent stores
+            const uint32_t mm = (m >> (16 * q)) & 0xffffu;
+            const int ch0 = c0 + 16 * q;
+            if (irow) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              if ((mm >> j) & 1u) {
-                vrow[pos] = (j & 1) ? __high2half(hv[j >> 1]) : __low2half(hv[j >> 1]);
-                if (irow) irow[pos] = (uint8_t)(c0 + 16 * q + j);
-                if (sm_idx) sm_idx[pos] = (uint8_t)(c0 + 16 * q + j);
-                ++pos;
+              for (int j = 0; j < 16; ++j) {
+                if ((mm >> j) & 1u) {
+                  const int pj = pos + __popc(mm & ((1u << j) - 1u));
+                  vrow[pj] = (j & 1) ? __high2half(hv[j >> 1]) : __low2half(hv[j >> 1]);
+                  irow[pj] = (uint8_t)(ch0 + j);
+                }
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                if ((mm >> j) & 1u)
+                  vrow[pos + __popc(mm & ((1u << j) - 1u))] =
+                      (j & 1) ? __high2half(hv[j >> 1]) : __low2half(hv[j >> 1]);
               }
             }
+            if (sm_idx) {
+              for (uint32_t a = mm, n = 0; a; a &= a - 1u, ++n)
+                sm_idx[pos + n] = (uint8_t)(ch0 + __ffs(a) - 1);
+            }
+            pos += __popc(mm);
           }
         }
       }
@@ -935,10 +959,10 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
         a = b;
       }
     } else {
-      // ---- copy-out: (row, 16-byte piece) per item ------------------------------
+      // ---- copy-out: four threads per row, 16-byte pieces k = sub, sub + 4, ... ----
       const uint32_t c = (uint32_t)p.c;
-      for (int item = tid; item < rows * 16; item += RT_THREADS) {
-        const int r = item >> 4, k = item & 15;
+      const int r = tid >> 2, sub = tid & 3;
+      if (r < rows) {
         const uint32_t ri = rowinfo[r];
         const int q = (int)(ri >> 16);
         const uint32_t rl = ri & 0xffffu;
@@ -946,34 +970,37 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
         const uint32_t off16 = hdr_sh[q].off16;
         if ((uint64_t)off16 * 16u + si.size > p.pool_check) {
           // the segment would end past the checked pool extent: report, skip
-          if (k == 0) atomicOr(p.err, DEV_ERR_CHECK);
-          continue;
-        }
-        uint8_t* seg = p.pool + (size_t)off16 * 16u;
-        const int strat = si.strategy;
-        const uint32_t srows = si.rows;
-        if (strat == MKV_STRATEGY_DENSE) {
-          *reinterpret_cast<uint4*>(seg + 256u * rl + 16u * k) =
-              *reinterpret_cast<const uint4*>(stv + r * ST_V + 16 * k);
-          continue;
-        }
-        if ((uint32_t)k < (c >> 3)) {
-          const uint32_t voff = (strat == MKV_STRATEGY_SM ? pad16(c) : 0u) + 2u * c * rl;
-          *reinterpret_cast<uint4*>(seg + voff + 16u * k) =
-              *reinterpret_cast<const uint4*>(stv + r * ST_V + 16 * k);
-          if (strat == MKV_STRATEGY_PV)
-            *reinterpret_cast<uint2*>(seg + 2u * c * srows + c * rl + 8u * k) =
-                *reinterpret_cast<const uint2*>(sti + r * ST_I + 8 * k);
-        }
-        if (k == 0) {
-          if (strat == MKV_STRATEGY_PVB)
-            *reinterpret_cast<uint4*>(seg + 2u * c * srows + 16u * rl) =
-                *reinterpret_cast<const uint4*>(tmask + 4 * r);
-          // zero padding after the index bytes (c and c * rows are multiples of 8)
-          if (strat == MKV_STRATEGY_SM && rl == 0 && (c & 15u))
-            *reinterpret_cast<uint2*>(seg + c) = make_uint2(0u, 0u);
-          if (strat == MKV_STRATEGY_PV && rl == srows - 1 && ((c * srows) & 15u))
-            *reinterpret_cast<uint2*>(seg + 3u * c * srows) = make_uint2(0u, 0u);
+          if (sub == 0) atomicOr(p.err, DEV_ERR_CHECK);
+        } else {
+          uint8_t* seg = p.pool + (size_t)off16 * 16u;
+          const int strat = si.strategy;
+          const uint32_t srows = si.rows;
+          const uint4* src = reinterpret_cast<const uint4*>(stv + r * ST_V);
+          if (strat == MKV_STRATEGY_DENSE) {
+            uint4* dst = reinterpret_cast<uint4*>(seg + 256u * rl);
+#pragma unroll
+            for (int k = sub; k < 16; k += 4) dst[k] = src[k];
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(
+                seg + (strat == MKV_STRATEGY_SM ? pad16(c) : 0u) + 2u * c * rl);
+            const int nck = (int)(c >> 3);
+            for (int k = sub; k < nck; k += 4) dst[k] = src[k];
+            if (strat == MKV_STRATEGY_PV) {
+              uint2* idst = reinterpret_cast<uint2*>(seg + 2u * c * srows + c * rl);
+              const uint2* isrc = reinterpret_cast<const uint2*>(sti + r * ST_I);
+              for (int k = sub; k < nck; k += 4) idst[k] = isrc[k];
+            }
+            if (sub == 0) {
+              if (strat == MKV_STRATEGY_PVB)
+                *reinterpret_cast<uint4*>(seg + 2u * c * srows + 16u * rl) =
+                    *reinterpret_cast<const uint4*>(tmask + 4 * r);
+              // zero padding after the index bytes (c and c * rows are multiples of 8)
+              if (strat == MKV_STRATEGY_SM && rl == 0 && (c & 15u))
+                *reinterpret_cast<uint2*>(seg + c) = make_uint2(0u, 0u);
+              if (strat == MKV_STRATEGY_PV && rl == srows - 1 && ((c * srows) & 15u))
+                *reinterpret_cast<uint2*>(seg + 3u * c * srows) = make_uint2(0u, 0u);
+            }
+          }
         }
       }
     }
