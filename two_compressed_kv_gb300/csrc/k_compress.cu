@@ -631,7 +631,12 @@ __device__ __forceinline__ uint32_t quad_topc(uint32_t w[32], int c) {
 // ---------------------------------------------------------------------------
 constexpr int RT_THREADS = 512;
 static_assert(RT_THREADS == 4 * D, "four lanes per token and four column partial sums");
-constexpr int XT_LD = D + 1;          // fp32 x~ rows: conflict-free by row and by column
+// fp32 x~ rows: channel ch at column ch + 8 (ch / 32), row stride 161 (= 1 mod
+// 32): conflict-free by column, by row, and for the four lanes of a token
+// that read its four 32-channel quarters at once
+constexpr int XT_LD = D + 3 * 8 + 9;
+static_assert(XT_LD % 32 == 1, "row stride");
+__device__ __forceinline__ int xt_col(int ch) { return ch + 8 * (ch >> 5); }
 constexpr int RT_MAXSEG = TC_T / 16 + 1;   // segments a tile can touch (S >= 16)
 constexpr int ST_V = 2 * D + 16;      // staged value row bytes (16-byte pieces, banks spread)
 constexpr int ST_I = D + 8;           // staged index row bytes (8-byte pieces)
@@ -883,7 +888,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-          Xt[tok * XT_LD + c0 + 16 * q + j] =
+          Xt[tok * XT_LD + xt_col(c0) + 16 * q + j] =
               fmaf(__uint_as_float(l[j]), 1.f / 2048.f, __uint_as_float(h[j]));
       }
     }
@@ -892,7 +897,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
     if (!PACK) {
       // ---- per-token channels: four lanes per token ----------------------------
       const int tok = tid >> 2, quarter = tid & 3;
-      const float* xrow = Xt + tok * XT_LD + 32 * quarter;
+      const float* xrow = Xt + tok * XT_LD + xt_col(32 * quarter);
       uint32_t k[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) k[j] = __float_as_uint(xrow[j]) & 0x7fffffffu;
@@ -927,7 +932,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
           const int col = tid & (D - 1), part = tid >> 7;
           float q = 0.f;
           for (int r = r0 + part; r < r1; r += RT_THREADS / D) {
-            const float val = Xt[r * XT_LD + col];
+            const float val = Xt[r * XT_LD + xt_col(col)];
             q = fmaf(val, val, q);
           }
           colpart[part][col] = q;
