@@ -704,10 +704,11 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
   // packing: tile j's token masks and segment data into buffer j mod 3, in
   // the same cp.async group as its X tile (threads 0..127)
   auto load_meta = [&](int j) {
-    const int64_t t0j = tb + (int64_t)j * TC_T;
+    const int offj = j * TC_T;                      // past the CTA's first token (32-bit)
+    const int64_t t0j = tb + offj;
     const int rowsj = (int)imin64(TC_T, te - t0j);
-    const int sgfj = (int)(t0j / p.S);
-    const int nsgj = (int)((t0j + rowsj - 1) / p.S) - sgfj + 1;
+    const int sgfj = sg0 + offj / p.S;
+    const int nsgj = sg0 + (offj + rowsj - 1) / p.S - sgfj + 1;
     const int mbj = j % 3;
     const bool live = tid < rowsj;
     cp_async16(smem_u32(tokmask + (mbj * TC_T + tid) * 4),
@@ -787,9 +788,10 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
         rt_issue_mma(Xs + (uint32_t)(b ^ 1) * TC_TILE, Bhi, Blo, tbase + (uint32_t)(b ^ 1) * 256u,
                      &mma_bar[b ^ 1]);
     }
-    const int sgf = (int)(t0 / p.S);
-    // row r of the tile is row lr0 + r past the start of segment sgf (32-bit)
-    const int lr0 = (int)(t0 - (int64_t)sgf * p.S);
+    // row r of the tile is row lr0 + r past the start of segment sgf (32-bit:
+    // a CTA covers whole segments from sg0 on)
+    const int sgf = sg0 + (it * TC_T) / p.S;
+    const int lr0 = it * TC_T - (sgf - sg0) * p.S;
     // one decision for the whole block
     if (__syncthreads_or(!tc_wait(&mma_bar[b], (uint32_t)((it >> 1) & 1), p.err))) {
       ok = false;
@@ -919,13 +921,13 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
       }
       __syncthreads();
       // ---- per segment: column energies and kept energy, for the strategy -------
-      int64_t a = t0;
-      const int64_t tend = t0 + rows;
-      while (a < tend) {
-        const int sg = (int)(a / p.S);
-        const int64_t segend = imin64(p.T, (int64_t)(sg + 1) * p.S);
-        const int64_t b = imin64(tend, segend);
-        const int r0 = (int)(a - t0), r1 = (int)(b - t0);
+      // pieces of the tile by segment, in tile rows: segment sgf + q ends at
+      // row (q + 1) S - lr0, or at the end of the stream
+      const bool at_end = t0 + rows == p.T;
+      for (int q = 0, r0 = 0, qend = p.S - lr0; r0 < rows; ++q, r0 = qend, qend += p.S) {
+        const int r1 = min(rows, qend);
+        const int sg = sgf + q;
+        const bool complete = r1 == qend || (r1 == rows && at_end);
         // every thread: column tid mod 128 over rows r0 + part, r0 + part + 4, ...
         // (part = tid / 128); warp 4 also sums the tokens' kept energies
         {
@@ -947,21 +949,20 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
         if (tid < D) {
           float cacc = colacc[tid] + ((colpart[0][tid] + colpart[1][tid]) +
                                       (colpart[2][tid] + colpart[3][tid]));
-          if (b == segend) {
+          if (complete) {
             p.colE[((size_t)sx * p.n_seg + sg) * D + tid] = cacc;
             cacc = 0.f;
           }
           colacc[tid] = cacc;
         } else if (tid == 4 * 32) {
           float kk = segkept[0] + kq;
-          if (b == segend) {
+          if (complete) {
             p.segK[(size_t)sx * p.n_seg + sg] = kk;
             kk = 0.f;
           }
           segkept[0] = kk;
         }
         __syncthreads();          // colpart is rewritten by the next piece
-        a = b;
       }
     } else {
       // ---- copy-out: four threads per row, 16-byte pieces k = sub, sub + 4, ... ----
