@@ -795,24 +795,23 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
     const mkv_segment_header* hdr_sh = hdr3[mb];
     const uint32_t* tmask = tokmask + (PACK ? mb * TC_T * 4 : 0);
     if (it + 1 < n_tiles) {
-      // tile it + 1 (and its segment data) landed: its MMAs into the other pair
-      cp_async_wait<0>();
+      cp_async_wait<0>();         // this thread's part of tile it + 1 (and its segment data)
       fence_proxy_async();
-      __syncthreads();
-      if (tid == 0)
-        rt_issue_mma(Xs + (uint32_t)(b ^ 1) * TC_TILE, Bhi, Blo, tbase + (uint32_t)(b ^ 1) * 256u,
-                     &mma_bar[b ^ 1]);
     }
     // row r of the tile is row lr0 + r past the start of segment sgf (32-bit:
     // a CTA covers whole segments from sg0 on)
     const int sgf = sg0 + (it * TC_T) / p.S;
     const int lr0 = it * TC_T - (sgf - sg0) * p.S;
-    // one decision for the whole block
+    // one decision for the whole block; past it tile it + 1 has landed and
+    // the previous tile's shared-memory reads are done
     if (__syncthreads_or(!tc_wait(&mma_bar[b], (uint32_t)((it >> 1) & 1), p.err))) {
       ok = false;
       break;
     }
     tc_fence_after();
+    if (it + 1 < n_tiles && tid == 0)   // tile it + 1's MMAs into the other pair
+      rt_issue_mma(Xs + (uint32_t)(b ^ 1) * TC_TILE, Bhi, Blo, tbase + (uint32_t)(b ^ 1) * 256u,
+                   &mma_bar[b ^ 1]);
     // X buffer b is free: tile it + 2 in flight from here
     if (it + 2 < n_tiles && tid < 128) {
       tc_load_tile(Xs + (uint32_t)b * TC_TILE, X, t0 + 2 * TC_T, te);
@@ -1025,7 +1024,8 @@ __global__ void __launch_bounds__(RT_THREADS, 1) rotate_kernel(CompressParams p)
         }
       }
     }
-    __syncthreads();              // the fp32 tile and staged data are rewritten by the next tile
+    // the fp32 tile and staged data are rewritten only past the next tile's
+    // first barrier
   }
   cp_async_wait<0>();
   tc_fence_before();
