@@ -203,7 +203,6 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gram_kernel(CompressParams p) {
 // grid: 2 * BH, block 1024, dynamic smem 2 x 128 x 129 + 128 x 132 floats
 // ---------------------------------------------------------------------------
 constexpr int EIG_THREADS = 1024;
-static_assert(EIG_THREADS % 64 == 0, "a thread's blocks share one column rotation");
 constexpr int LDA = D + 1;
 constexpr int LDV = D + 4;            // column-major V: 16-byte aligned columns
 constexpr int EIG_MAX_SWEEPS = 16;
